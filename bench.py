@@ -1,0 +1,379 @@
+"""Benchmark of the metered KV-cache decode step on GB300.
+
+Default workload: the full 28-layer Qwen2.5-7B-shaped decode (28 query / 4 KV
+heads, d = 128, batch 16 x 4096 context, bf16 synthetic K/V/q, dithered INT8
+with the Tier B certificate at delta_req = 1e-2).  One step = for every layer:
+append the step's token (write path: quantize + witness) and run the fused
+metered split-KV decode + merge.  Metric: attended-KV-tokens/s, one attended
+token being one (sequence, layer, position) read across all KV heads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload qwen_28l|qwen_1l|sweep:<mistral|yi>:<B>:<S>] [--scheme ...]
+
+--impl reference times the CPU oracle (the slow float64 statement of the same
+computation) on this host's cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload  # noqa: E402
+
+BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144}
+DISTINCT_LAYERS = 4        # prefill K/V sets generated on the host; layer l uses set l % 4
+METRIC = "metered decode attended-KV-tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen_28l")
+    ap.add_argument("--scheme", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def workload_of(name, scheme):
+    if name.startswith("sweep:"):
+        _, model, b, s = name.split(":")
+        w = sweep_workload(model, int(b), int(s))
+    else:
+        w = WORKLOADS[name]
+    if scheme:
+        w = w.with_(scheme=scheme)
+    return w
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def config_of(w, args, n_splits, world):
+    return {"workload": f"{w.name}: {w.n_layers} layers, {w.n_q_heads}q/{w.n_kv_heads}kv heads, d=128, "
+                        f"batch {w.batch} x {w.context} context per GPU, {w.scheme}",
+            "model": w.name, "global_batch": w.batch * world, "seq_len": w.context, "layers": w.n_layers,
+            "scheme": w.scheme, "delta_req": w.delta_req, "n_splits": n_splits,
+            "parallelism": f"replicas x{world} (independent sequence shards)",
+            "l2": "inputs larger than L2: every step reads the whole cache "
+                  f"({w.n_layers * w.batch * w.n_kv_heads * w.context * BYTES_PER_TOK_HEAD[w.scheme] / 1e9:.2f} GB)",
+            "prefill_data": f"{DISTINCT_LAYERS} generated K/V sets reused across layers"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    def __init__(self, device_index=0):
+        self.idx = device_index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        self.th.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(w):
+    """Per-launch DRAM bytes of the decode split kernel from the committed ncu summary, if it was
+    taken on the current kernel source (null otherwise)."""
+    src = os.path.join(ROOT, "kv_cache_quantization_witcert_gb300", "csrc", "decode.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"decode_{w.scheme}_{w.name}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", txt)
+    t = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != digest:
+        return None
+    return float(t.group(1))
+
+
+# ----------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def cpu_oracle_rate(w, seconds):
+    """Oracle decode of (sequence, KV head) groups of one layer, repeated for about `seconds`."""
+    from oracle import meter, quant
+    from oracle.philox import dither
+    os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
+    wl = w.with_(batch=1)
+    K, V = gen_kv(wl, 0)
+    q = gen_q(wl, 0, 0)
+    S = w.context
+    dl = meter.delta_loc(w.delta_req, w.n_layers, w.n_q_heads, w.steps)
+    groups = 0
+    t0 = time.perf_counter()
+    h = 0
+    while True:
+        pos = np.arange(S)
+        k, v = K[0, :, h % w.n_kv_heads], V[0, :, h % w.n_kv_heads]
+        if w.scheme == "int8_dither":
+            _, ks, kh, _ = quant.write_int8_dither(k, dither(w.seed, 0, h, pos, 0))
+            _, _, vh, _ = quant.write_int8_dither(v, dither(w.seed, 0, h, pos, 1))
+            kss = ks.astype(np.float64)
+        elif w.scheme == "fp8_e4m3":
+            kh, vh, kss = quant.write_fp8(k)[1], quant.write_fp8(v)[1], None
+        else:
+            kh = k.astype(np.float64)
+            vh = quant.write_kivi2_v(v)[3]
+            kss = None
+        wst = quant.witness_stored(quant.witness(k - kh)).astype(np.float64)
+        js = slice((h % w.n_kv_heads) * w.group, (h % w.n_kv_heads + 1) * w.group)
+        meter.decode_ref(q[0, js], kh, vh, wst, kss, None, dl)
+        groups += 1
+        h += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    # one attended token = one (sequence, layer, position) across all KV heads
+    tokens = groups * S / w.n_kv_heads
+    cores = len(os.sched_getaffinity(0))
+    return tokens / el, cores, f"{groups} (sequence, KV head) groups of one layer at S={S}, write + decode, {el:.1f} s"
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    rates = []
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for k in range(args.warmup + args.steps):
+        r, cores, sample = cpu_oracle_rate(w, per_step)
+        if k >= args.warmup:
+            rates.append(r)
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args, None, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import torch
+
+    import kv_cache_quantization_witcert_gb300 as wc
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = w.with_(seed=w.seed + rank)           # each rank holds its own shard of sequences
+    dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    total = args.warmup + args.steps
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, args.steps // 2)
+    n_app = total + e2e_steps + 1
+    cache = wc.Cache(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.batch, wl.context + n_app, wl.scheme,
+                     dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0)
+    stream = torch.cuda.current_stream()
+
+    # prefill every layer (untimed)
+    sets = {}
+    for layer in range(wl.n_layers):
+        sid = layer % DISTINCT_LAYERS
+        if sid not in sets:
+            K, V = gen_kv(wl, sid)
+            sets[sid] = (torch.from_numpy(K).to(dev, dt), torch.from_numpy(V).to(dev, dt))
+        cache.witcert_write(layer, *sets[sid])
+    del sets
+    torch.cuda.synchronize()
+
+    # per-step inputs resident in HBM: appended token and queries of every layer
+    def step_inputs(step, device=True):
+        ks, vs, qs = [], [], []
+        for layer in range(wl.n_layers):
+            k, v = gen_append_kv(wl, layer % DISTINCT_LAYERS, step % 8)
+            ks.append(k)
+            vs.append(v)
+            qs.append(gen_q(wl, layer % DISTINCT_LAYERS, step % 8))
+        arr = [np.stack(ks), np.stack(vs), np.stack(qs)]
+        return [torch.from_numpy(a).to(dt) for a in arr]
+
+    host_inputs = [step_inputs(s) for s in range(8)]
+    dev_inputs = [[t.to(dev) for t in hi] for hi in host_inputs]
+    out = torch.empty((wl.n_layers, wl.batch, wl.n_q_heads, 128), dtype=torch.float32, device=dev)
+    mtr = torch.empty((wl.n_layers, 4, wl.batch, wl.n_q_heads), dtype=torch.float32, device=dev)
+
+    def one_step(inp):
+        K1, V1, Q = inp
+        for layer in range(wl.n_layers):
+            cache.witcert_write(layer, K1[layer], V1[layer])
+            cache.witcert_decode(layer, Q[layer], wl.delta_req, out[layer], mtr[layer, 0], mtr[layer, 1],
+                                 mtr[layer, 2], mtr[layer, 3])
+
+    lens = []
+    for s in range(args.warmup):
+        one_step(dev_inputs[s % 8])
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    cache.witcert_set_profiling(True)
+    s_len0 = cache.witcert_length(0)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.steps):
+        one_step(dev_inputs[(args.warmup + s) % 8])
+    ev1.record(stream)
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    st = cache.witcert_stats()
+    cache.witcert_set_profiling(False)
+    clk = clocks.stop()
+    attended = sum(wl.batch * (s_len0 + 1 + s) for s in range(args.steps)) * wl.n_layers
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, attended], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        ms, attended = float(mx[0]), float(sm[1])
+    value = attended / (ms / 1e3)
+
+    # roofline of the dominant kernel (decode split kernel), timed by the library's events
+    n_launch = st["decode_kernel_launches"]
+    avg_ms = st["decode_kernel_ms"] / max(1, n_launch)
+    avg_S = s_len0 + 1 + (args.steps - 1) / 2.0
+    alg_bytes = wl.batch * wl.n_kv_heads * avg_S * BYTES_PER_TOK_HEAD[wl.scheme]
+    achieved = alg_bytes / (avg_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = recorded_traffic(wl)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    pinned = [[t.pin_memory() for t in hi] for hi in host_inputs]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    mtr_h = torch.empty(mtr.shape, dtype=mtr.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned[0])
+    d2h = out_h.numel() * 4 + mtr_h.numel() * 4
+    barrier()
+    l0 = cache.witcert_length(0)
+    t0 = time.perf_counter()
+    for s in range(e2e_steps):
+        inp = [t.to(dev, non_blocking=True) for t in pinned[s % 8]]
+        one_step(inp)
+        out_h.copy_(out, non_blocking=True)
+        mtr_h.copy_(mtr, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_tokens = sum(wl.batch * (l0 + 1 + s) for s in range(e2e_steps)) * wl.n_layers
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s, e2e_tokens], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        e2e_s, e2e_tokens = float(mx[0]), float(sm[1])
+
+    cpu = None
+    if rank == 0 and world == 1:
+        r, cores, sample = cpu_oracle_rate(w, args.cpu_seconds)
+        cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32 (int8 codes)",
+                "data": "synthetic (seeded numpy; bf16 N(0,1) K/V/q, x50 outlier RoPE pair, planted keys)",
+                "config": config_of(wl, args, f"auto ({st['last_n_splits']})", world),
+                "hbm_gbs_decode": achieved, "bytes_per_attended_token": wl.n_kv_heads * BYTES_PER_TOK_HEAD[wl.scheme],
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                             "kernel": "decode_split_kernel", "avg_launch_ms": avg_ms, "launches": n_launch,
+                             "alg_bytes_per_launch": alg_bytes},
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "gpu_launches": 3 * wl.n_layers * args.steps,
+                "clocks": clk,
+                "device_errors": st["device_errors"], "int8_clamps": st["int8_clamps"]}
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = workload_of(args.workload, args.scheme)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * witcert.h — C ABI of the GB300 metered KV-cache decode library.
+ *
+ * The method is WitCert ("WitCert: Sound Runtime Risk Observability and Gating
+ * for KV-Cache Quantization").  Citations below name its pages:
+ *   [summary]   technical summary page: witness paragraph with Lemma 1,
+ *               Theorem 2, the Tier B paragraph, the implementation
+ *               paragraph, the closing improvements list (TV bound);
+ *   [Lean page] paperswithlean.com page: Approach, Figure 2 and Figure 5.
+ *
+ * Conventions for every call:
+ *   - Pointers documented as "device" must be CUDA device pointers (or managed
+ *     memory) on the device that was current when the cache was created;
+ *     "host" pointers are ordinary host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on that stream unless stated otherwise.
+ *   - The caller owns all buffers it passes; the cache owns its own device
+ *     pools, its pinned host backing store and its internal side stream.
+ *   - Errors are returned as witcert_status codes; nothing throws across the
+ *     ABI.  witcert_last_error() gives a thread-local message for the last
+ *     failing call on the calling thread.
+ *   - A cache is used from one host thread at a time.
+ *   - head_dim is 128; the KV-head group size Hq/Hkv is at most 8.
+ */
+#ifndef WITCERT_H
+#define WITCERT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WITCERT_OK = 0,
+  WITCERT_EINVAL = -1,     /* bad argument or configuration */
+  WITCERT_ENOMEM = -2,     /* device or pinned host allocation failed */
+  WITCERT_ECUDA = -3,      /* a CUDA runtime call or kernel launch failed */
+  WITCERT_ETIMEDOUT = -4,  /* a bounded wait ran out (host deadline or device spin limit) */
+  WITCERT_EPAGEIN = -5,    /* gate page-in could not complete (pool exhausted, injected fault) */
+  WITCERT_ESTATE = -6      /* call not valid in the cache's current state */
+} witcert_status;
+
+typedef enum {
+  WITCERT_INT8_DITHER = 0, /* subtractively dithered INT8, per-(token, 32-channel) fp16 scales [summary, Tier B] */
+  WITCERT_FP8_E4M3 = 1,    /* black-box raw cast to OCP E4M3, no scale [summary, gate results] */
+  WITCERT_KIVI2 = 2        /* KIVI-style asymmetric 2-bit: K per channel over 16 tokens, V per token per 32 channels */
+} witcert_scheme;
+
+typedef enum {
+  WITCERT_F32 = 0,         /* float32 K, V and q */
+  WITCERT_BF16 = 1         /* bfloat16 K, V and q */
+} witcert_dtype;
+
+typedef struct {
+  int n_layers;            /* L in delta_loc = delta_req / (L*H*T) */
+  int n_q_heads;           /* Hq (H in delta_loc) */
+  int n_kv_heads;          /* Hkv; Hq must be a multiple, Hq/Hkv <= 8 */
+  int head_dim;            /* must be 128 */
+  int batch;               /* sequences held by the cache (all share one length per layer) */
+  int max_tokens;          /* capacity per sequence per layer */
+  witcert_scheme scheme;   /* fixed for the cache's lifetime */
+  witcert_dtype kv_dtype;  /* dtype of K, V and q passed to write/decode, and of the backing store */
+  uint64_t seed;           /* Philox key of the dither stream (INT8 scheme) */
+  int total_steps;         /* T in delta_loc: decode steps per request */
+  int n_splits;            /* KV splits per (sequence, KV head) in decode; 0 = choose from the SM count */
+  int max_repair_blocks;   /* capacity of the exact-key pool in 16-token blocks; 0 disables the gate
+                              and the pinned backing store */
+} witcert_config;
+
+typedef struct witcert_cache witcert_cache;
+
+typedef struct {
+  uint64_t cells_triggered;   /* (sequence, query head) cells whose meter exceeded tau */
+  uint64_t blocks_selected;   /* distinct (layer, sequence, KV head, block) picked for repair */
+  uint64_t blocks_paged_in;   /* blocks copied from the backing store into the exact pool */
+  uint64_t bytes_paged_in;    /* host-to-device bytes moved by page-in */
+  uint64_t blocks_dropped;    /* selected but not repaired because the pool was full */
+  uint64_t gate_calls;
+} witcert_gate_counters;
+
+typedef struct {
+  uint64_t tokens_written;    /* token x KV head rows written, all layers */
+  uint64_t decode_calls;
+  uint64_t int8_clamps;       /* INT8 codes clamped to [-128, 127] (expected 0) */
+  uint64_t device_errors;     /* spin limits hit inside kernels (expected 0) */
+  double decode_kernel_ms;    /* summed split-kernel time while profiling is on */
+  uint64_t decode_kernel_launches;
+  int last_n_splits;          /* KV splits used by the most recent decode */
+} witcert_stats_t;
+
+/* Create a cache.  Allocates the compressed store, the witness store, the
+ * split scratch and, when max_repair_blocks > 0, the exact-key pool and a
+ * pinned, device-mapped host backing store of exact keys.  Memory is zeroed.
+ * Synchronous.  Returns EINVAL for unsupported shapes, ENOMEM on allocation
+ * failure (nothing is leaked). */
+witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out);
+
+/* Free everything the cache owns.  Synchronizes the device first. */
+witcert_status witcert_destroy(witcert_cache* cache);
+
+/* Write path [summary, implementation paragraph (the write side keeps a
+ * witness per token and head); Tier B paragraph for the dithered quantizer;
+ * witness paragraph for w_{t,b} = ||r_{t,b}||].  Appends n_tok tokens to every sequence of
+ * `layer` at positions len..len+n_tok-1, where len is the layer's current
+ * length.  K and V are device arrays [batch][n_tok][n_kv_heads][128] of
+ * kv_dtype, contiguous; keys are post-RoPE.  Stores codes and scales, and the
+ * key witness of 16 bands (band b = dims 4b..4b+3 and 64+4b..64+4b+3, whole
+ * RoPE pairs of the rotate-half layout) as fp16 rounded up.  With the gate
+ * enabled it also writes the exact keys into the pinned backing store.
+ * EINVAL if layer is out of range or the capacity would be exceeded. */
+witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, const void* V,
+                             int n_tok, void* stream);
+
+/* Fused metered split-KV decode [summary, implementation paragraph (output
+ * and meter produced by one kernel reading the cache once, with the
+ * certificate terms merged across KV splits by log-sum-exp); Theorem 2
+ * (Tier A); Tier B paragraph; improvements list (TV aggregation)].
+ * q: device [batch][n_q_heads][128] of kv_dtype, post-RoPE.  Query head j
+ * reads KV head j / (Hq/Hkv).  Attends to all len tokens of `layer`.
+ * Outputs (device, caller-owned, float32):
+ *   out     [batch][n_q_heads][128]  attention output
+ *   meter_a [batch][n_q_heads]       min(1, (A^2-1)/2), A = sum_t p~_t exp(eps_t),
+ *                                    eps_t = (1/sqrt d) sum_b ||q_b|| w_{t,b}
+ *   meter_b [batch][n_q_heads]       same with c_t = u_t = sqrt(2 s2_t log(2S/delta_loc)),
+ *                                    s2_t = (1/d) sum_c q_c^2 s_{c,t}^2/12,
+ *                                    delta_loc = delta_req/(L*Hq*T); NaN unless INT8_DITHER
+ *   raw_a, raw_b                      the unclamped (A^2-1)/2 of each tier
+ * Meters are rounded upward (never below the exact value of the formula).
+ * Any meter pointer may be NULL; if all four are NULL the meter work is
+ * compiled out and `out` is bit-identical to the metered run's.
+ * With the gate enabled, per-16-token-block risks of the gate's tier
+ * (Tier B for INT8_DITHER, Tier A otherwise) are kept for witcert_gate.
+ * Waits (on the device) for a pending gate of this layer.  An empty layer
+ * (len 0) yields zero output and zero meters.  EINVAL on bad arguments. */
+witcert_status witcert_decode(witcert_cache* cache, int layer, const void* q, double delta_req,
+                              float* out, float* meter_a, float* meter_b, float* raw_a,
+                              float* raw_b, void* stream);
+
+/* Meter-driven gate [summary, implementation paragraph (exact blocks come
+ * back from host memory once the meter passes a threshold); Lean page,
+ * Figure 2 (repair works on whole blocks and clears their witnesses) and
+ * Figure 5 (repairs accumulate and persist)].  Uses the block
+ * risks of the layer's last decode: a (sequence, query head) cell whose
+ * unclamped meter exceeds tau has its unrepaired blocks ranked by risk
+ * (largest first, ties to the lower block) and takes the shortest prefix that
+ * leaves remaining risk <= sqrt(1+2 tau)-1; the union over a KV head's query
+ * heads is paged in from the pinned backing store into the exact-key pool,
+ * marked repaired (persistently) and its witnesses zeroed.  Runs on the
+ * cache's side stream after the work already queued on `stream`; later
+ * writes and decodes of this layer wait for it on the device.  Repairs affect
+ * decodes issued after this call.  ESTATE if the gate is disabled or the
+ * layer has not been decoded since its last write. */
+witcert_status witcert_gate(witcert_cache* cache, int layer, float tau, void* stream);
+
+/* Gate counters, summed over all gate calls.  Waits for outstanding gate work
+ * with a host deadline of `timeout_ms` (ETIMEDOUT if it runs out). */
+witcert_status witcert_gate_stats(witcert_cache* cache, witcert_gate_counters* out, int timeout_ms);
+
+/* Library counters.  Synchronizes the device. */
+witcert_status witcert_stats(witcert_cache* cache, witcert_stats_t* out);
+
+/* Turn per-launch CUDA-event timing of the decode split kernel on (1) or off (0). */
+witcert_status witcert_set_profiling(witcert_cache* cache, int on);
+
+/* Current length of `layer` (host, synchronous, no device work). */
+witcert_status witcert_length(const witcert_cache* cache, int layer, int* len);
+
+/* What witcert_export copies out (layouts below). */
+typedef enum {
+  WITCERT_X_K_CODES = 0, WITCERT_X_V_CODES = 1, WITCERT_X_K_SCALES = 2, WITCERT_X_V_SCALES = 3,
+  WITCERT_X_V_ZEROS = 4, WITCERT_X_KIVI_K_SCALE = 5, WITCERT_X_KIVI_K_ZERO = 6,
+  WITCERT_X_WITNESS = 7, WITCERT_X_SLOTS = 8, WITCERT_X_BLOCK_RISK = 9
+} witcert_export_kind;
+
+/* Cache contents in a canonical layout, for inspection and tests.  Writes
+ * into a caller-owned device buffer of `bytes` bytes (EINVAL if too small):
+ *   WITCERT_X_K_CODES, V_CODES  uint8 [batch][len][n_kv_heads][128]
+ *                               (INT8: two's-complement int8; FP8: E4M3 bits;
+ *                               KIVI: 0..3, keys of an unfinished block 0)
+ *   WITCERT_X_K_SCALES, V_SCALES fp16 [batch][len][n_kv_heads][4] (INT8; KIVI V scales)
+ *   WITCERT_X_V_ZEROS           fp16 [batch][len][n_kv_heads][4] (KIVI)
+ *   WITCERT_X_KIVI_K_SCALE, _ZERO fp16 [batch][nblk][n_kv_heads][128] (KIVI, full blocks)
+ *   WITCERT_X_WITNESS           fp16 [batch][len][n_kv_heads][16]
+ *   WITCERT_X_SLOTS             int32 [batch][n_kv_heads][nblk] (-1 = not repaired)
+ *   WITCERT_X_BLOCK_RISK        float [batch][n_q_heads][nblk] (last decode; gate enabled)
+ * nblk = ceil(len/16).  Asynchronous on `stream`. */
+witcert_status witcert_export(witcert_cache* cache, int layer, witcert_export_kind what,
+                              void* dst, size_t bytes, void* stream);
+
+/* The dither stream xi the INT8 writer and decoder regenerate [summary, Tier B
+ * paragraph: the decoder recomputes the same dither instead of storing it], for tests:
+ * Philox4x32-10 (Salmon et al., SC'11) with key (seed mod 2^32, seed div 2^32)
+ * and counter (t, (c/4) | tensor<<16, kv_head | layer<<16, 0); channel c takes
+ * output word c mod 4, xi = (u >> 8) * 2^-24 - 1/2.  Writes float32
+ * [n][128] for positions t0..t0+n-1 to device `out`.  tensor 0 = K, 1 = V. */
+witcert_status witcert_dither(uint64_t seed, int layer, int kv_head, int t0, int n, int tensor,
+                              float* out, void* stream);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* witcert_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WITCERT_H */

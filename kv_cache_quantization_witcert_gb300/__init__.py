@@ -1,0 +1,135 @@
+"""Python binding of libwitcert (GB300 metered KV-cache decode).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  Function names follow
+the C ABI (include/witcert.h): witcert_create / write / decode / gate / ...
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (BF16, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER, KIVI2,  # noqa: F401
+                   SCHEMES, WitcertError, check, load)
+
+__all__ = ["Cache", "witcert_dither", "WitcertError", "load", "SCHEMES"]
+
+_TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+class Cache:
+    """One WitCert cache: compressed K/V store, witnesses, optional gate state."""
+
+    def __init__(self, n_layers, n_q_heads, n_kv_heads, batch, max_tokens, scheme="int8_dither",
+                 dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0):
+        lib = load()
+        self.dtype = dtype
+        self.cfg = _lib.witcert_config(n_layers, n_q_heads, n_kv_heads, 128, batch, max_tokens,
+                                       SCHEMES[scheme] if isinstance(scheme, str) else scheme,
+                                       BF16 if dtype == torch.bfloat16 else F32, seed, total_steps, n_splits,
+                                       max_repair_blocks)
+        self.scheme = scheme
+        h = ctypes.c_void_p()
+        check(lib.witcert_create(ctypes.byref(self.cfg), ctypes.byref(h)), "witcert_create")
+        self._h = h
+
+    # ------------------------------------------------------------------ ABI calls
+    def witcert_write(self, layer, K, V, stream=None):
+        assert K.is_contiguous() and V.is_contiguous() and K.dtype == self.dtype and V.dtype == self.dtype
+        n_tok = K.shape[1]
+        check(load().witcert_write(self._h, layer, _ptr(K), _ptr(V), n_tok, _stream_ptr(stream)), "witcert_write")
+
+    def witcert_decode(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
+                       stream=None):
+        assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
+        check(load().witcert_decode(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
+                                    _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
+              "witcert_decode")
+
+    def witcert_gate(self, layer, tau, stream=None):
+        check(load().witcert_gate(self._h, layer, float(tau), _stream_ptr(stream)), "witcert_gate")
+
+    def witcert_gate_stats(self, timeout_ms=10000):
+        s = _lib.witcert_gate_counters()
+        check(load().witcert_gate_stats(self._h, ctypes.byref(s), timeout_ms), "witcert_gate_stats")
+        return {f: getattr(s, f) for f, _ in s._fields_}
+
+    def witcert_stats(self):
+        s = _lib.witcert_stats_t()
+        check(load().witcert_stats(self._h, ctypes.byref(s)), "witcert_stats")
+        return {f: getattr(s, f) for f, _ in s._fields_}
+
+    def witcert_set_profiling(self, on):
+        check(load().witcert_set_profiling(self._h, int(bool(on))), "witcert_set_profiling")
+
+    def witcert_length(self, layer):
+        n = ctypes.c_int()
+        check(load().witcert_length(self._h, layer, ctypes.byref(n)), "witcert_length")
+        return n.value
+
+    def witcert_export(self, layer, what, dst, stream=None):
+        check(load().witcert_export(self._h, layer, what, _ptr(dst), dst.numel() * dst.element_size(),
+                                    _stream_ptr(stream)), "witcert_export")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            check(load().witcert_destroy(self._h), "witcert_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------------ conveniences (allocation + the calls above)
+    def decode(self, layer, q, delta_req, meters=True, stream=None):
+        B, Hq = q.shape[0], q.shape[1]
+        out = torch.empty((B, Hq, 128), dtype=torch.float32, device=q.device)
+        if not meters:
+            self.witcert_decode(layer, q, delta_req, out, stream=stream)
+            return out, None
+        m = torch.empty((4, B, Hq), dtype=torch.float32, device=q.device)
+        self.witcert_decode(layer, q, delta_req, out, m[0], m[1], m[2], m[3], stream=stream)
+        return out, {"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3]}
+
+    def export(self, layer, what, stream=None):
+        B, Hkv, Hq = self.cfg.batch, self.cfg.n_kv_heads, self.cfg.n_q_heads
+        S = self.witcert_length(layer)
+        nblk = (S + 15) // 16
+        dev = torch.device("cuda", torch.cuda.current_device())
+        shapes = {
+            _lib.X_K_CODES: ((B, S, Hkv, 128), torch.uint8), _lib.X_V_CODES: ((B, S, Hkv, 128), torch.uint8),
+            _lib.X_K_SCALES: ((B, S, Hkv, 4), torch.float16), _lib.X_V_SCALES: ((B, S, Hkv, 4), torch.float16),
+            _lib.X_V_ZEROS: ((B, S, Hkv, 4), torch.float16),
+            _lib.X_KIVI_K_SCALE: ((B, nblk, Hkv, 128), torch.float16),
+            _lib.X_KIVI_K_ZERO: ((B, nblk, Hkv, 128), torch.float16),
+            _lib.X_WITNESS: ((B, S, Hkv, 16), torch.float16), _lib.X_SLOTS: ((B, Hkv, nblk), torch.int32),
+            _lib.X_BLOCK_RISK: ((B, Hq, nblk), torch.float32),
+        }
+        shape, dt = shapes[what]
+        dst = torch.empty(shape, dtype=dt, device=dev)
+        if dst.numel():
+            self.witcert_export(layer, what, dst, stream=stream)
+        return dst
+
+
+def witcert_dither(seed, layer, kv_head, t0, n, tensor, out=None, stream=None):
+    """Device dither xi [n, 128] float32 (see witcert_dither in include/witcert.h)."""
+    if out is None:
+        out = torch.empty((n, 128), dtype=torch.float32, device="cuda")
+    check(load().witcert_dither(seed, layer, kv_head, t0, n, tensor, _ptr(out), _stream_ptr(stream)),
+          "witcert_dither")
+    return out

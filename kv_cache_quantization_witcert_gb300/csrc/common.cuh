@@ -1,0 +1,206 @@
+// Device-side building blocks shared by the write, decode, gate and export kernels.
+//
+// Cache layout in HBM.  For every (layer, sequence, KV head) the cache is one
+// contiguous stream of 16-token blocks; a block holds everything a decode
+// needs for those 16 tokens, so one bulk copy stages it:
+//
+//   INT8_DITHER (4864 B = 16 x 304):  K codes 2048 | V codes 2048 | K scales 128 | V scales 128 | witness 512
+//   FP8_E4M3    (4608 B = 16 x 288):  K codes 2048 | V codes 2048 | witness 512
+//   KIVI2       (2304 B = 16 x 144):  K codes 512 | K scale,zero 512 | V codes 512 | V scale,zero 256 | witness 512
+//
+// Codes are stored in "fragment order": the byte a lane of a warp needs for
+// the A operand of mma.m16n8k16 sits where one 16-byte shared-memory load per
+// lane fetches it without bank conflicts.  The index functions below are the
+// single definition of that order; export kernels invert them.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+namespace witcert {
+
+constexpr int kD = 128;
+constexpr int kBlk = 16;
+constexpr int kBands = 16;
+constexpr int kGroupCh = 32;
+constexpr int kGroups = 4;
+constexpr int kMaxGroupHeads = 8;
+
+enum SchemeId : int { kInt8 = 0, kFp8 = 1, kKivi = 2 };
+
+struct Int8Layout { static constexpr int KC = 0, VC = 2048, KS = 4096, VS = 4224, W = 4352, BYTES = 4864; };
+struct Fp8Layout  { static constexpr int KC = 0, VC = 2048, W = 4096, BYTES = 4608; };
+struct KiviLayout { static constexpr int KC = 0, KP = 512, VC = 1024, VP = 1536, W = 1792, BYTES = 2304; };
+
+__host__ __device__ constexpr int block_bytes(int scheme) {
+  return scheme == kInt8 ? Int8Layout::BYTES : scheme == kFp8 ? Fp8Layout::BYTES : KiviLayout::BYTES;
+}
+__host__ __device__ constexpr int witness_off(int scheme) {
+  return scheme == kInt8 ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : KiviLayout::W;
+}
+
+// ------------------------------------------------------------------ fragment-order index maps
+// Lane L = 4g + t (g = L>>2, t = L&3).  mma.m16n8k16 A fragment of lane L:
+//   R0 = row g,   k {2t, 2t+1}     R1 = row g+8, k {2t, 2t+1}
+//   R2 = row g,   k {2t+8, 2t+9}   R3 = row g+8, k {2t+8, 2t+9}
+// and B fragment: R0 = k {2t, 2t+1}, col g;  R1 = k {2t+8, 2t+9}, col g.
+// The k index of a 16-wide step is mapped to four consecutive physical
+// elements per lane: k 2t,2t+1 -> 4t,4t+1 and k 2t+8,2t+9 -> 4t+2,4t+3.
+
+// 1-byte K code of token r (0..15), channel c: QK^T with tokens as rows.
+__host__ __device__ inline int kcode_off(int r, int c) {
+  int g = r & 7, h = r >> 3, kk = c >> 4, t = (c >> 2) & 3, e = c & 3;
+  int L = 4 * g + t, j = kk >> 1, slot = ((kk & 1) << 1) | h;
+  return j * 512 + L * 16 + slot * 4 + e;
+}
+// 1-byte V code: PV^T with channels as rows and tokens as k.
+__host__ __device__ inline int vcode_off(int r, int c) {
+  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = r >> 2, e = r & 3;
+  int L = 4 * g + t, j = mt >> 1, slot = ((mt & 1) << 1) | h;
+  return j * 512 + L * 16 + slot * 4 + e;
+}
+// fp16 witness of token r, band b: A operand of the Tier A product (bands as k, identity map).
+__host__ __device__ inline int wit_off(int r, int b) {
+  int g = r & 7, h = r >> 3, t = (b & 7) >> 1, hi = b >> 3, e = b & 1;
+  int L = 4 * g + t, reg = h + 2 * hi;
+  return L * 16 + reg * 4 + e * 2;
+}
+// 2-bit KIVI codes: word (byte offset) and bit position.  Each 32-bit word holds
+// eight fp16x2 register pairs; pair p keeps its two codes at bits 2p and 16+2p.
+__host__ __device__ inline void kivi_k_pos(int r, int c, int& word_off, int& bit) {
+  int g = r & 7, h = r >> 3, kk = c >> 4, t = (c >> 2) & 3, e = c & 3;
+  int L = 4 * g + t, j = kk >> 1, reg = h + 2 * (e >> 1), p = (kk & 1) * 4 + reg;
+  word_off = L * 16 + j * 4;
+  bit = 2 * p + 16 * (e & 1);
+}
+__host__ __device__ inline void kivi_v_pos(int r, int c, int& word_off, int& bit) {
+  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = r >> 2, e = r & 3;
+  int L = 4 * g + t, j = mt >> 1, reg = h + 2 * (e >> 1), p = (mt & 1) * 4 + reg;
+  word_off = L * 16 + j * 4;
+  bit = 2 * p + 16 * (e & 1);
+}
+// KIVI K per-channel scale (fp16) index; the zero point sits 256 bytes later.
+__host__ __device__ inline int kivi_kparam_idx(int c) { return ((c >> 2) & 3) * 32 + (c >> 4) * 4 + (c & 3); }
+
+// ------------------------------------------------------------------ Philox4x32-10 dither
+// Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+// xi = (u >> 8) * 2^-24 - 1/2, exact in fp32.
+__device__ __forceinline__ float xi_from_word(uint32_t u) {
+  return __fadd_rn(__fmul_rn(__uint2float_rn(u >> 8), 5.9604644775390625e-8f), -0.5f);
+}
+// Dither of channels 4*quad .. 4*quad+3 of token position t.
+__device__ __forceinline__ float4 dither4(uint64_t seed, int layer, int kvh, int t, int quad, int tensor) {
+  uint4 u = philox4x32_10(make_uint4((uint32_t)t, (uint32_t)quad | ((uint32_t)tensor << 16),
+                                     (uint32_t)kvh | ((uint32_t)layer << 16), 0u),
+                          (uint32_t)(seed & 0xFFFFFFFFull), (uint32_t)(seed >> 32));
+  return make_float4(xi_from_word(u.x), xi_from_word(u.y), xi_from_word(u.z), xi_from_word(u.w));
+}
+
+// ------------------------------------------------------------------ tensor-core product
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// ------------------------------------------------------------------ small conversions
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+__device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) { return h2_bits(__halves2half2(lo, hi)); }
+
+// Two biased INT8 codes (code + 128 in bytes b, b+1 of w) -> exact fp16x2 codes.
+// 0x64XX is the fp16 1024 + XX; subtracting 1152 = 1024 + 128 leaves the code.
+__device__ __forceinline__ uint32_t i8x2_lo(uint32_t w) {
+  return h2_bits(__hsub2(bits_h2(__byte_perm(w, 0x64646464u, 0x4140u)), __half2half2(__ushort_as_half(0x6480))));
+}
+__device__ __forceinline__ uint32_t i8x2_hi(uint32_t w) {
+  return h2_bits(__hsub2(bits_h2(__byte_perm(w, 0x64646464u, 0x4342u)), __half2half2(__ushort_as_half(0x6480))));
+}
+// Two E4M3 codes -> fp16x2 (every E4M3 value is exact in fp16).
+__device__ __forceinline__ uint32_t e4m3x2_lo(uint32_t w) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi(uint32_t w) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+// Two 2-bit codes at bits 2p and 16+2p of w -> exact fp16x2.
+__device__ __forceinline__ uint32_t u2x2(uint32_t w, int p) {
+  uint32_t x = ((w >> (2 * p)) & 0x00030003u) | 0x64006400u;
+  return h2_bits(__hsub2(bits_h2(x), __half2half2(__ushort_as_half(0x6400))));
+}
+
+// Split an fp32 value into fp16 hi + lo with hi + lo == v to ~22 bits.
+__device__ __forceinline__ void split_h(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// expm1 for c >= 0 with small relative error: Taylor-Horner below 1/2, exp - 1 above.
+__device__ __forceinline__ float expm1_pos(float c) {
+  if (c < 0.5f) {
+    float s = 1.0f + c * (1.0f / 8.0f);
+    s = 1.0f + c * (1.0f / 7.0f) * s;
+    s = 1.0f + c * (1.0f / 6.0f) * s;
+    s = 1.0f + c * (1.0f / 5.0f) * s;
+    s = 1.0f + c * (1.0f / 4.0f) * s;
+    s = 1.0f + c * (1.0f / 3.0f) * s;
+    s = 1.0f + c * 0.5f * s;
+    return c * s;
+  }
+  return exp2f(c * 1.4426950408889634f) - 1.0f;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded mbarrier wait: returns false once `limit_ns` of wall time has passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One-dimensional bulk copy global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+}  // namespace witcert

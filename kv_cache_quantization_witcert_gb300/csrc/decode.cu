@@ -1,0 +1,688 @@
+// Fused metered split-KV decode and its log-sum-exp merge.
+//
+// One CTA = (KV split, KV head, group of up to NW sequences); warp w owns one
+// sequence.  Each warp streams its sequence's 16-token blocks through a
+// private ring of shared-memory stages filled by one-dimensional bulk copies
+// (cp.async.bulk, completion on an mbarrier).  For the dithered INT8 scheme
+// the dither of a block is regenerated once per CTA by all its threads and
+// shared by every sequence of the group (the dither is keyed on layer, KV head,
+// position and channel, not on the sequence).
+//
+// Per block and sequence a warp computes, with mma.m16n8k16 (fp16 in, fp32 acc):
+//   logits   S[tok, head] = sum_G s_G(tok) * (codes_G . q - xi_hi,G . q - xi_lo,G . q)
+//            codes are exact in fp16 and the dither is split into two fp16 pieces,
+//            so the logits carry the compressed keys to ~2^-22;
+//   Tier A   eps[tok, head] = W[tok, :] . (||q_b|| / sqrt d)  (the norms as fp16 hi+lo,
+//            rounded up) [WitCert summary, Theorem 2];
+//   output   O^T[ch, head] += (codes - xi)[ch, tok] . (p * s_V)[tok, head].
+// Tier B u = kappa * sqrt(sum_G s_G^2 * sum_{c in G} q_c^2 / (12 d)) [WitCert
+// summary, Tier B paragraph] and the online softmax with the two meter
+// accumulators S_X = sum e^(l - m) expm1(c_X) run on the CUDA cores.  The TV
+// aggregation min(1, (A^2-1)/2) with A = 1 + S_X/Z [WitCert summary,
+// improvements list] is applied after the merge.
+#include <cfloat>
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace witcert {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kXiKHi = 0, kXiKLo = 4096, kXiV = 8192, kXiBytes = 12288;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
+// Upward bias applied to every meter sum: covers the fp32 / tensor-core
+// rounding of the logits and exponentials relative to exact arithmetic.
+constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
+
+template <int SCHEME> struct Lay;
+template <> struct Lay<kInt8> : Int8Layout {};
+template <> struct Lay<kFp8> : Fp8Layout {};
+template <> struct Lay<kKivi> : KiviLayout {};
+
+template <int NW, int NST, int SCHEME> struct Smem {
+  static constexpr int kRing = NW * NST * Lay<SCHEME>::BYTES;
+  static constexpr int kXi = SCHEME == kInt8 ? 2 * kXiBytes : 0;
+  static constexpr int kRingOff = 0;
+  static constexpr int kXiOff = (kRing + 127) / 128 * 128;
+  static constexpr int kPsmOff = kXiOff + kXi;                 // NW x float[8][16]
+  static constexpr int kQgOff = kPsmOff + NW * 512;            // NW x float[8][4]
+  static constexpr int kBarOff = kQgOff + NW * 128;            // NW x NST x u64
+  static constexpr int kBytes = kBarOff + NW * NST * 8;
+};
+
+// term p * expm1(c) without overflow for large c (there e^c - 1 ~ e^c; the
+// product is then formed in the exponent).  l2 is the logit in log2 units.
+__device__ __forceinline__ float meter_term(float pe, float l2, float m2, float c) {
+  if (pe == 0.0f || c <= 0.0f) return 0.0f;
+  if (c > 20.0f) return exp2f(l2 - m2 + c * kLog2e);
+  return pe * expm1_pos(c);
+}
+
+// Regenerate the dither of block `blk` of KV head h into shared memory, in the
+// fragment order of the QK (negated, fp16 hi + lo) and PV (fp16) operands.
+__device__ void gen_xi(uint8_t* xb, uint64_t seed, int layer, int h, int blk, int nthreads) {
+  for (int idx = threadIdx.x; idx < 1024; idx += nthreads) {
+    const int tensor = idx >> 9, r = (idx >> 5) & 15, quad = idx & 31;
+    const float4 x = dither4(seed, layer, h, blk * kBlk + r, quad, tensor);
+    if (tensor == 0) {
+      const int kk = quad >> 2, tq = quad & 3, gg = r & 7, hh = r >> 3;
+      const int L = 4 * gg + tq;
+      __half h0, l0, h1, l1, h2, l2, h3, l3;
+      split_h(-x.x, h0, l0); split_h(-x.y, h1, l1); split_h(-x.z, h2, l2); split_h(-x.w, h3, l3);
+      uint32_t* hi = reinterpret_cast<uint32_t*>(xb + kXiKHi + (kk * 32 + L) * 16);
+      uint32_t* lo = reinterpret_cast<uint32_t*>(xb + kXiKLo + (kk * 32 + L) * 16);
+      hi[hh] = pack_h2(h0, h1); hi[2 + hh] = pack_h2(h2, h3);
+      lo[hh] = pack_h2(l0, l1); lo[2 + hh] = pack_h2(l2, l3);
+    } else {
+      __half* v = reinterpret_cast<__half*>(xb + kXiV);
+      const float xs[4] = {x.x, x.y, x.z, x.w};
+      const int tq = r >> 2, er = r & 3;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = 4 * quad + e;
+        const int mt = c >> 4, gg = c & 7, hh = (c >> 3) & 1;
+        const int L = 4 * gg + tq, reg = hh + 2 * (er >> 1);
+        v[((mt * 32 + L) * 4 + reg) * 2 + (er & 1)] = __float2half_rn(xs[e]);
+      }
+    }
+  }
+}
+
+// Load four consecutive elements of an exact key row as fp32.
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <> __device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// Exact-key logits of one block (repaired block from the pool, or KIVI's unfinished block).
+template <typename KT, bool QLO>
+__device__ __forceinline__ void exact_block_logits(const KT* ex, const uint32_t (&qb)[8][2],
+                                                   const uint32_t (&qbl)[8][2], int g, int t,
+                                                   float (&acc)[4]) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const float4 x0 = load4<KT>(ex + g * kD + 16 * kk + 4 * t);
+    const float4 x1 = load4<KT>(ex + (g + 8) * kD + 16 * kk + 4 * t);
+    __half a0h, a0l, a1h, a1l, b0h, b0l, b1h, b1l, c0h, c0l, c1h, c1l, d0h, d0l, d1h, d1l;
+    split_h(x0.x, a0h, a0l); split_h(x0.y, a1h, a1l); split_h(x0.z, b0h, b0l); split_h(x0.w, b1h, b1l);
+    split_h(x1.x, c0h, c0l); split_h(x1.y, c1h, c1l); split_h(x1.z, d0h, d0l); split_h(x1.w, d1h, d1l);
+    const uint32_t ah[4] = {pack_h2(a0h, a1h), pack_h2(c0h, c1h), pack_h2(b0h, b1h), pack_h2(d0h, d1h)};
+    const uint32_t al[4] = {pack_h2(a0l, a1l), pack_h2(c0l, c1l), pack_h2(b0l, b1l), pack_h2(d0l, d1l)};
+    mma16816(acc, ah, qb[kk]);
+    mma16816(acc, al, qb[kk]);
+    if (QLO) mma16816(acc, ah, qbl[kk]);
+  }
+}
+
+template <int SCHEME, typename QT, bool METER, bool RISK, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs p) {
+  using L = Lay<SCHEME>;
+  using SM = Smem<NW, NST, SCHEME>;
+  constexpr bool QLO = sizeof(QT) == 4;          // fp32 queries carry an fp16 low piece
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int split = blockIdx.x, h = blockIdx.y;
+  const int i = blockIdx.z * p.seqs_per_cta + warp;
+  bool active = warp < p.seqs_per_cta && i < p.B;
+  const int grp = p.grp, j0 = h * grp;
+  const int nblk = (p.S + kBlk - 1) / kBlk;
+  const int b_begin = (int)(((long long)split * nblk) / p.n_splits);
+  const int b_end = (int)(((long long)(split + 1) * nblk) / p.n_splits);
+  const int nb = b_end - b_begin;
+
+  uint8_t* ring = smem + SM::kRingOff + warp * NST * L::BYTES;
+  uint8_t* xib = smem + SM::kXiOff;
+  float* psm = reinterpret_cast<float*>(smem + SM::kPsmOff) + warp * 128;
+  float* qgs = reinterpret_cast<float*>(smem + SM::kQgOff) + warp * 32;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOff) + warp * NST;
+
+  const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
+  const uint8_t* src = p.blocks + (seq_base + b_begin) * L::BYTES;
+
+  // ---------------------------------------------------------------- pipeline prologue
+  if (active && lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    fence_proxy_async();
+    for (int s = 0; s < NST && s < nb; ++s) {
+      mbar_expect_tx(smem_addr(&bars[s]), L::BYTES);
+      bulk_g2s(smem_addr(ring + s * L::BYTES), src + (size_t)s * L::BYTES, L::BYTES, smem_addr(&bars[s]));
+    }
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- query fragments
+  uint32_t qb[8][2], qbl[8][2], qnb[2], qnl[2];
+  float qg2[2][4];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) { qb[kk][0] = qb[kk][1] = qbl[kk][0] = qbl[kk][1] = 0u; }
+  qnb[0] = qnb[1] = qnl[0] = qnl[1] = 0u;
+  const QT* qbase = reinterpret_cast<const QT*>(p.q);
+  if (active) {
+    if (g < grp) {
+      const QT* qr = qbase + ((size_t)i * p.Hq + j0 + g) * kD;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = to_f32<QT>(qr[16 * kk + 4 * t + e]);
+        __half hv[4], lv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split_h(v[e], hv[e], lv[e]);
+        qb[kk][0] = pack_h2(hv[0], hv[1]); qb[kk][1] = pack_h2(hv[2], hv[3]);
+        qbl[kk][0] = pack_h2(lv[0], lv[1]); qbl[kk][1] = pack_h2(lv[2], lv[3]);
+      }
+      if (METER) {
+        // ||q_b|| / sqrt(d) for bands 2t, 2t+1, 2t+8, 2t+9, rounded up, as fp16 hi + lo (lo rounded up)
+        const float inv_sqrt_d_up = __fdiv_ru(1.0f, __fsqrt_rd(128.0f));
+        const int bands[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+        __half bh[4], bl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float ss = 0.0f;
+#pragma unroll
+          for (int d = 0; d < 4; ++d) {
+            const float a = to_f32<QT>(qr[4 * bands[e] + d]);
+            const float b = to_f32<QT>(qr[64 + 4 * bands[e] + d]);
+            ss = __fmaf_ru(a, a, ss);
+            ss = __fmaf_ru(b, b, ss);
+          }
+          const float nb_up = __fmul_ru(__fsqrt_ru(ss), inv_sqrt_d_up);
+          bh[e] = __float2half_rn(nb_up);
+          bl[e] = __float2half_ru(nb_up - __half2float(bh[e]));
+        }
+        qnb[0] = pack_h2(bh[0], bh[1]); qnb[1] = pack_h2(bh[2], bh[3]);
+        qnl[0] = pack_h2(bl[0], bl[1]); qnl[1] = pack_h2(bl[2], bl[3]);
+      }
+    }
+    if (METER && SCHEME == kInt8) {
+      // sum_{c in G} q_c^2 / (12 d), rounded up: lane -> (head lane/4, group lane%4)
+      const int hq = lane >> 2, G = lane & 3;
+      float ss = 0.0f;
+      if (hq < grp) {
+        const QT* qr = qbase + ((size_t)i * p.Hq + j0 + hq) * kD + G * kGroupCh;
+        for (int c = 0; c < kGroupCh; ++c) { const float a = to_f32<QT>(qr[c]); ss = __fmaf_ru(a, a, ss); }
+      }
+      qgs[lane] = __fmul_ru(ss, __fdiv_ru(1.0f, 1536.0f));
+      __syncwarp();
+#pragma unroll
+      for (int G2 = 0; G2 < 4; ++G2) { qg2[0][G2] = qgs[(2 * t) * 4 + G2]; qg2[1][G2] = qgs[(2 * t + 1) * 4 + G2]; }
+    }
+  }
+
+  // ---------------------------------------------------------------- state
+  float m2[2] = {-INFINITY, -INFINITY}, Zp[2] = {0.f, 0.f}, SAp[2] = {0.f, 0.f}, SBp[2] = {0.f, 0.f};
+  float acco[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) acco[mt][0] = acco[mt][1] = acco[mt][2] = acco[mt][3] = 0.f;
+  float zc[4] = {0.f, 0.f, 0.f, 0.f};           // KIVI: sum_t p_t zero_{t,G} for head g
+  const float lscale = __fdiv_rn(kLog2e, sqrtf(128.0f));
+
+  if (SCHEME == kInt8) {
+    if (nb > 0) gen_xi(xib, p.seed, p.layer, h, b_begin, NW * 32);
+    __syncthreads();
+  }
+
+  bool fault = false;
+  for (int n = 0; n < nb; ++n) {
+    const int blk = b_begin + n, stage = n % NST;
+    const uint32_t par = (uint32_t)((n / NST) & 1);
+    uint8_t* xb = xib + (n & 1) * kXiBytes;
+    if (SCHEME == kInt8 && n + 1 < nb) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p.seed, p.layer, h, blk + 1, NW * 32);
+
+    if (active && !fault) {
+      if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs)) {
+        fault = true;
+        if (lane == 0) atomicAdd(p.err, 1);
+      }
+    }
+    if (active && !fault) {
+      const uint8_t* sb = ring + stage * L::BYTES;
+      const int slot = p.slots ? p.slots[seq_base + blk] : -1;
+      const bool kivi_tail = SCHEME == kKivi && (blk + 1) * kBlk > p.S;
+      float lg[4], eps[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
+      float kvs_g[4], kvs_g8[4];      // INT8 K scales of tokens g and g+8
+
+      if (slot >= 0 || kivi_tail) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (slot >= 0)
+          exact_block_logits<QT, QLO>(reinterpret_cast<const QT*>(p.pool) + (size_t)slot * kBlk * kD, qb, qbl, g, t, acc);
+        else
+          exact_block_logits<float, QLO>(p.kivi_tail + seq_base / p.nblk_max * (size_t)(kBlk * kD), qb, qbl, g, t, acc);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lg[e] = acc[e] * lscale;
+      } else if constexpr (SCHEME == kInt8) {
+        float acc[4][4];
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+          const uint4 cw = *reinterpret_cast<const uint4*>(sb + L::KC + G * 512 + lane * 16);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int kk = 2 * G + hf;
+            const uint32_t w0 = hf ? cw.z : cw.x, w1 = hf ? cw.w : cw.y;
+            const uint32_t a[4] = {i8x2_lo(w0), i8x2_lo(w1), i8x2_hi(w0), i8x2_hi(w1)};
+            mma16816(acc[G], a, qb[kk]);
+            if (QLO) mma16816(acc[G], a, qbl[kk]);
+            const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
+            const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
+            const uint32_t ah[4] = {xh.x, xh.y, xh.z, xh.w};
+            const uint32_t al[4] = {xl.x, xl.y, xl.z, xl.w};
+            mma16816(acc[G], ah, qb[kk]);
+            mma16816(acc[G], al, qb[kk]);
+            if (QLO) mma16816(acc[G], ah, qbl[kk]);
+          }
+        }
+        const __half* ks = reinterpret_cast<const __half*>(sb + L::KS);
+        const uint2 s0 = *reinterpret_cast<const uint2*>(ks + g * 4);
+        const uint2 s1 = *reinterpret_cast<const uint2*>(ks + (g + 8) * 4);
+        const __half2 a01 = bits_h2(s0.x), a23 = bits_h2(s0.y), b01 = bits_h2(s1.x), b23 = bits_h2(s1.y);
+        kvs_g[0] = __low2float(a01); kvs_g[1] = __high2float(a01); kvs_g[2] = __low2float(a23); kvs_g[3] = __high2float(a23);
+        kvs_g8[0] = __low2float(b01); kvs_g8[1] = __high2float(b01); kvs_g8[2] = __low2float(b23); kvs_g8[3] = __high2float(b23);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float* sc = e < 2 ? kvs_g : kvs_g8;
+          float v = 0.f;
+#pragma unroll
+          for (int G = 0; G < 4; ++G) v = fmaf(sc[G], acc[G][e], v);
+          lg[e] = v * lscale;
+        }
+        if (METER) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float* sc = e < 2 ? kvs_g : kvs_g8;
+            const float* qg = qg2[e & 1];
+            float var = 0.f;
+#pragma unroll
+            for (int G = 0; G < 4; ++G) var = __fmaf_ru(__fmul_ru(sc[G], sc[G]), qg[G], var);
+            ub[e] = __fmul_ru(p.kappa, __fsqrt_ru(var));
+          }
+        }
+      } else if constexpr (SCHEME == kFp8) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(sb + L::KC + G * 512 + lane * 16);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int kk = 2 * G + hf;
+            const uint32_t w0 = hf ? cw.z : cw.x, w1 = hf ? cw.w : cw.y;
+            const uint32_t a[4] = {e4m3x2_lo(w0), e4m3x2_lo(w1), e4m3x2_hi(w0), e4m3x2_hi(w1)};
+            mma16816(acc, a, qb[kk]);
+            if (QLO) mma16816(acc, a, qbl[kk]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lg[e] = acc[e] * lscale;
+      } else {  // KIVI: logits = q . zero + (q * scale) . codes
+        const __half* ksc = reinterpret_cast<const __half*>(sb + L::KP);
+        const __half* kzr = reinterpret_cast<const __half*>(sb + L::KP + 256);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float zq = 0.f;
+        const uint4 cw = *reinterpret_cast<const uint4*>(sb + L::KC + lane * 16);
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int pidx = t * 32 + kk * 4;
+          float qv[4];
+          qv[0] = __low2float(bits_h2(qb[kk][0])) + __low2float(bits_h2(qbl[kk][0]));
+          qv[1] = __high2float(bits_h2(qb[kk][0])) + __high2float(bits_h2(qbl[kk][0]));
+          qv[2] = __low2float(bits_h2(qb[kk][1])) + __low2float(bits_h2(qbl[kk][1]));
+          qv[3] = __high2float(bits_h2(qb[kk][1])) + __high2float(bits_h2(qbl[kk][1]));
+          __half hh[4], hl[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            zq = fmaf(qv[e], __half2float(kzr[pidx + e]), zq);
+            split_h(qv[e] * __half2float(ksc[pidx + e]), hh[e], hl[e]);
+          }
+          const uint32_t bh[2] = {pack_h2(hh[0], hh[1]), pack_h2(hh[2], hh[3])};
+          const uint32_t bl[2] = {pack_h2(hl[0], hl[1]), pack_h2(hl[2], hl[3])};
+          const uint32_t w = words[kk >> 1];
+          const int pb = (kk & 1) * 4;
+          const uint32_t a[4] = {u2x2(w, pb + 0), u2x2(w, pb + 1), u2x2(w, pb + 2), u2x2(w, pb + 3)};
+          mma16816(acc, a, bh);
+          mma16816(acc, a, bl);
+        }
+        zq += __shfl_xor_sync(0xffffffffu, zq, 1);
+        zq += __shfl_xor_sync(0xffffffffu, zq, 2);      // lanes 4g..4g+3 hold q_g . zero
+        const float zq0 = __shfl_sync(0xffffffffu, zq, 4 * ((2 * t) & 7));
+        const float zq1 = __shfl_sync(0xffffffffu, zq, 4 * ((2 * t + 1) & 7));
+        lg[0] = (acc[0] + zq0) * lscale; lg[1] = (acc[1] + zq1) * lscale;
+        lg[2] = (acc[2] + zq0) * lscale; lg[3] = (acc[3] + zq1) * lscale;
+      }
+
+      // Tier A from the stored witness (zero for repaired blocks and KIVI's unfinished block)
+      if (METER && slot < 0) {
+        const uint4 wf = *reinterpret_cast<const uint4*>(sb + L::W + lane * 16);
+        const uint32_t a[4] = {wf.x, wf.y, wf.z, wf.w};
+        mma16816(eps, a, qnb);
+        mma16816(eps, a, qnl);
+      }
+      if (slot >= 0) { ub[0] = ub[1] = ub[2] = ub[3] = 0.f; }
+
+      // mask tokens past the context
+      const int tok0 = blk * kBlk + g, tok1 = tok0 + 8;
+      if (tok0 >= p.S) { lg[0] = lg[1] = -INFINITY; }
+      if (tok1 >= p.S) { lg[2] = lg[3] = -INFINITY; }
+
+      // ------------------------------------------------------------ online softmax + meters
+      float bm0 = fmaxf(lg[0], lg[2]), bm1 = fmaxf(lg[1], lg[3]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+      }
+      const float mn0 = fmaxf(m2[0], bm0), mn1 = fmaxf(m2[1], bm1);
+      const float sc0 = mn0 == -INFINITY ? 1.f : exp2f(m2[0] - mn0);
+      const float sc1 = mn1 == -INFINITY ? 1.f : exp2f(m2[1] - mn1);
+      float pe[4];
+      pe[0] = lg[0] == -INFINITY ? 0.f : exp2f(lg[0] - mn0);
+      pe[1] = lg[1] == -INFINITY ? 0.f : exp2f(lg[1] - mn1);
+      pe[2] = lg[2] == -INFINITY ? 0.f : exp2f(lg[2] - mn0);
+      pe[3] = lg[3] == -INFINITY ? 0.f : exp2f(lg[3] - mn1);
+      Zp[0] = fmaf(Zp[0], sc0, pe[0] + pe[2]);
+      Zp[1] = fmaf(Zp[1], sc1, pe[1] + pe[3]);
+      if (METER) {
+        const float mn[4] = {mn0, mn1, mn0, mn1};
+        float ta[4], tb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ta[e] = meter_term(pe[e], lg[e], mn[e], eps[e]);
+          tb[e] = SCHEME == kInt8 ? meter_term(pe[e], lg[e], mn[e], ub[e]) : 0.f;
+        }
+        SAp[0] = fmaf(SAp[0], sc0, ta[0] + ta[2]);
+        SAp[1] = fmaf(SAp[1], sc1, ta[1] + ta[3]);
+        SBp[0] = fmaf(SBp[0], sc0, tb[0] + tb[2]);
+        SBp[1] = fmaf(SBp[1], sc1, tb[1] + tb[3]);
+        if (RISK) {
+          float r0 = SCHEME == kInt8 ? tb[0] + tb[2] : ta[0] + ta[2];
+          float r1 = SCHEME == kInt8 ? tb[1] + tb[3] : ta[1] + ta[3];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            r0 += __shfl_xor_sync(0xffffffffu, r0, o);
+            r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+          }
+          if (g == 0) {
+            if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(mn0, r0);
+            if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(mn1, r1);
+          }
+        }
+      }
+      m2[0] = mn0; m2[1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) { acco[mt][0] *= sc0; acco[mt][1] *= sc1; acco[mt][2] *= sc0; acco[mt][3] *= sc1; }
+
+      // ------------------------------------------------------------ P V
+      psm[(2 * t) * 16 + g] = pe[0];
+      psm[(2 * t + 1) * 16 + g] = pe[1];
+      psm[(2 * t) * 16 + g + 8] = pe[2];
+      psm[(2 * t + 1) * 16 + g + 8] = pe[3];
+      __syncwarp();
+      const float4 pv = *reinterpret_cast<const float4*>(psm + g * 16 + 4 * t);
+      if constexpr (SCHEME == kFp8) {
+        const uint32_t bfr[2] = {h2_bits(__floats2half2_rn(pv.x, pv.y)), h2_bits(__floats2half2_rn(pv.z, pv.w))};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 vw = *reinterpret_cast<const uint4*>(sb + L::VC + j * 512 + lane * 16);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t w0 = hf ? vw.z : vw.x, w1 = hf ? vw.w : vw.y;
+            const uint32_t a[4] = {e4m3x2_lo(w0), e4m3x2_lo(w1), e4m3x2_hi(w0), e4m3x2_hi(w1)};
+            mma16816(acco[2 * j + hf], a, bfr);
+          }
+        }
+      } else if constexpr (SCHEME == kInt8) {
+        const __half* vs = reinterpret_cast<const __half*>(sb + L::VS) + 4 * t * 4;   // tokens 4t..4t+3
+        const uint4 va = *reinterpret_cast<const uint4*>(vs);
+        const uint4 vb = *reinterpret_cast<const uint4*>(vs + 8);
+        const __half* v0 = reinterpret_cast<const __half*>(&va);   // tok 4t (0..3), 4t+1 (4..7)
+        const __half* v1 = reinterpret_cast<const __half*>(&vb);   // tok 4t+2, 4t+3
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t bfr[2] = {
+              h2_bits(__floats2half2_rn(pv.x * __half2float(v0[j]), pv.y * __half2float(v0[4 + j]))),
+              h2_bits(__floats2half2_rn(pv.z * __half2float(v1[j]), pv.w * __half2float(v1[4 + j])))};
+          const uint4 vw = *reinterpret_cast<const uint4*>(sb + L::VC + j * 512 + lane * 16);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int mt = 2 * j + hf;
+            const uint32_t w0 = hf ? vw.z : vw.x, w1 = hf ? vw.w : vw.y;
+            const uint4 xv = *reinterpret_cast<const uint4*>(xb + kXiV + (mt * 32 + lane) * 16);
+            const uint32_t a[4] = {h2_bits(__hsub2(bits_h2(i8x2_lo(w0)), bits_h2(xv.x))),
+                                   h2_bits(__hsub2(bits_h2(i8x2_lo(w1)), bits_h2(xv.y))),
+                                   h2_bits(__hsub2(bits_h2(i8x2_hi(w0)), bits_h2(xv.z))),
+                                   h2_bits(__hsub2(bits_h2(i8x2_hi(w1)), bits_h2(xv.w)))};
+            mma16816(acco[mt], a, bfr);
+          }
+        }
+      } else {  // KIVI values: p*scale times codes, plus p*zero per group
+        const __half* vp = reinterpret_cast<const __half*>(sb + L::VP) + 4 * t * 8;   // [tok][G][scale, zero]
+        float sv[4][4], zv[4][4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int G = 0; G < 4; ++G) { sv[e][G] = __half2float(vp[(e * 4 + G) * 2]); zv[e][G] = __half2float(vp[(e * 4 + G) * 2 + 1]); }
+        const float pvv[4] = {pv.x, pv.y, pv.z, pv.w};
+        // rescale of head g's zero accumulator: fetch sc of head g from lane g/2
+        const float sa = __shfl_sync(0xffffffffu, sc0, g >> 1), sbb = __shfl_sync(0xffffffffu, sc1, g >> 1);
+        const float scg = (g & 1) ? sbb : sa;
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          float z = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) z = fmaf(pvv[e], zv[e][G], z);
+          z += __shfl_xor_sync(0xffffffffu, z, 1);
+          z += __shfl_xor_sync(0xffffffffu, z, 2);
+          zc[G] = fmaf(zc[G], scg, z);
+        }
+        const uint4 vw4 = *reinterpret_cast<const uint4*>(sb + L::VC + lane * 16);
+        const uint32_t vwords[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t bfr[2] = {h2_bits(__floats2half2_rn(pvv[0] * sv[0][j], pvv[1] * sv[1][j])),
+                                   h2_bits(__floats2half2_rn(pvv[2] * sv[2][j], pvv[3] * sv[3][j]))};
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int pb = hf * 4;
+            const uint32_t a[4] = {u2x2(vwords[j], pb + 0), u2x2(vwords[j], pb + 1), u2x2(vwords[j], pb + 2),
+                                   u2x2(vwords[j], pb + 3)};
+            mma16816(acco[2 * j + hf], a, bfr);
+          }
+        }
+      }
+      __syncwarp();
+      // refill this stage with the block NST ahead
+      if (lane == 0 && n + NST < nb) {
+        fence_proxy_async();
+        mbar_expect_tx(smem_addr(&bars[stage]), L::BYTES);
+        bulk_g2s(smem_addr(ring + stage * L::BYTES), src + (size_t)(n + NST) * L::BYTES, L::BYTES,
+                 smem_addr(&bars[stage]));
+      }
+    }
+    if (SCHEME == kInt8) __syncthreads();
+  }
+
+  if (fault) {
+    // drain copies still in flight before the CTA's shared memory is released
+    if (lane == 0)
+      for (int s = 0; s < NST; ++s) mbar_wait(smem_addr(&bars[s]), 0, 100000000ull), mbar_wait(smem_addr(&bars[s]), 1, 100000000ull);
+    return;
+  }
+  if (!active) return;
+
+  // ---------------------------------------------------------------- partial state of this split
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    Zp[0] += __shfl_xor_sync(0xffffffffu, Zp[0], o);
+    Zp[1] += __shfl_xor_sync(0xffffffffu, Zp[1], o);
+    SAp[0] += __shfl_xor_sync(0xffffffffu, SAp[0], o);
+    SAp[1] += __shfl_xor_sync(0xffffffffu, SAp[1], o);
+    SBp[0] += __shfl_xor_sync(0xffffffffu, SBp[0], o);
+    SBp[1] += __shfl_xor_sync(0xffffffffu, SBp[1], o);
+  }
+  if (SCHEME == kKivi) {
+    // add sum_t p_t zero_{t,G} of heads 2t, 2t+1 (held by lanes 4*head)
+    float z0[4], z1[4];
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      z0[G] = __shfl_sync(0xffffffffu, zc[G], 4 * ((2 * t) & 7));
+      z1[G] = __shfl_sync(0xffffffffu, zc[G], 4 * ((2 * t + 1) & 7));
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      acco[mt][0] += z0[mt >> 1]; acco[mt][2] += z0[mt >> 1];
+      acco[mt][1] += z1[mt >> 1]; acco[mt][3] += z1[mt >> 1];
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int head = 2 * t + hh;
+    if (head >= grp) continue;
+    float* rec = p.part + (((size_t)i * p.Hq + j0 + head) * p.n_splits + split) * kPartStride;
+    if (g == 0) { rec[0] = m2[hh]; rec[1] = Zp[hh]; rec[2] = SAp[hh]; rec[3] = SBp[hh]; }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      rec[4 + 16 * mt + g] = acco[mt][hh];
+      rec[4 + 16 * mt + g + 8] = acco[mt][2 + hh];
+    }
+  }
+}
+
+// One warp per (sequence, query head): merge the splits, normalize, finish the meters.
+template <bool INT8, bool RISK>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= p.B * p.Hq) return;
+  const float* recs = p.part + (size_t)wid * p.n_splits * kPartStride;
+  float M = -INFINITY;
+  for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, recs[(size_t)s * kPartStride]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float Z = 0.f, SA = 0.f, SB = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float* r = recs + (size_t)s * kPartStride;
+      const float ms = r[0];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      Z = fmaf(f, r[1], Z); SA = fmaf(f, r[2], SA); SB = fmaf(f, r[3], SB);
+      const float4 a = *reinterpret_cast<const float4*>(r + 4 + 4 * lane);
+      acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
+    }
+  }
+  const float inv = Z > 0.f ? 1.0f / Z : 0.f;
+  *reinterpret_cast<float4*>(p.out + (size_t)wid * kD + 4 * lane) =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (!p.meter) return;
+  if (lane == 0) {
+    const float DA = Z > 0.f ? __fmul_ru(__fdiv_ru(SA, Z), kMeterMargin) : 0.f;
+    const float rawA = __fmaf_ru(__fmul_ru(0.5f, DA), DA, DA);
+    if (p.raw_a) p.raw_a[wid] = rawA;
+    if (p.meter_a) p.meter_a[wid] = fminf(1.0f, rawA);
+    float rawB = NAN;
+    if (INT8) {
+      const float DB = Z > 0.f ? __fmul_ru(__fdiv_ru(SB, Z), kMeterMargin) : 0.f;
+      rawB = __fmaf_ru(__fmul_ru(0.5f, DB), DB, DB);
+    }
+    if (p.raw_b) p.raw_b[wid] = rawB;
+    if (p.meter_b) p.meter_b[wid] = INT8 ? fminf(1.0f, rawB) : NAN;
+  }
+  if (RISK) {
+    const int nblk = (p.S + kBlk - 1) / kBlk;
+    const float2* rr = p.risk_raw + (size_t)wid * p.nblk_max;
+    float* ro = p.risk + (size_t)wid * p.nblk_max;
+    for (int b = lane; b < nblk; b += 32) {
+      const float2 v = rr[b];
+      ro[b] = (v.y == 0.f || Z == 0.f) ? 0.f : v.y * exp2f(v.x - M) * inv;
+    }
+  }
+}
+
+template <int SCHEME, typename QT, bool METER, bool RISK, int NW, int NST>
+cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  using SM = Smem<NW, NST, SCHEME>;
+  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, NW, NST>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  if (e != cudaSuccess) return e;
+  k<<<grid, NW * 32, SM::kBytes, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int SCHEME, typename QT, bool METER, bool RISK>
+cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  switch (a.seqs_per_cta) {
+    case 1: return run_split<SCHEME, QT, METER, RISK, 1, 4>(a, grid, st);
+    case 2: return run_split<SCHEME, QT, METER, RISK, 2, 4>(a, grid, st);
+    case 4: return run_split<SCHEME, QT, METER, RISK, 4, 3>(a, grid, st);
+    default: return run_split<SCHEME, QT, METER, RISK, 8, 3>(a, grid, st);
+  }
+}
+
+template <int SCHEME>
+cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+  const bool risk = a.risk_raw != nullptr;
+  if (a.is_bf16) {
+    if (!a.meter) return dispatch_nw<SCHEME, __nv_bfloat16, false, false>(a, grid, st);
+    return risk ? dispatch_nw<SCHEME, __nv_bfloat16, true, true>(a, grid, st)
+                : dispatch_nw<SCHEME, __nv_bfloat16, true, false>(a, grid, st);
+  }
+  if (!a.meter) return dispatch_nw<SCHEME, float, false, false>(a, grid, st);
+  return risk ? dispatch_nw<SCHEME, float, true, true>(a, grid, st)
+              : dispatch_nw<SCHEME, float, true, false>(a, grid, st);
+}
+
+int seqs_per_cta_for(int B) { return B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
+
+}  // namespace
+
+int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count) {
+  const int spc = seqs_per_cta_for(B);
+  const int groups = (B + spc - 1) / spc;
+  const int per_sm = spc >= 8 ? 1 : spc >= 4 ? 2 : 4;
+  const int target = sm_count * per_sm;
+  int s = (target + Hkv * groups - 1) / (Hkv * groups);
+  if (s > nblk) s = nblk;
+  if (s < 1) s = 1;
+  (void)scheme;
+  return s;
+}
+
+cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaStream_t st,
+                          cudaEvent_t split_start, cudaEvent_t split_stop) {
+  (void)sm_count;
+  DecodeArgs a = a0;
+  a.seqs_per_cta = seqs_per_cta_for(a.B);
+  const int groups = (a.B + a.seqs_per_cta - 1) / a.seqs_per_cta;
+  dim3 grid(a.n_splits, a.Hkv, groups);
+  if (split_start) cudaEventRecord(split_start, st);
+  cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, st)
+                  : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, st)
+                                   : dispatch_flags<kKivi>(a, grid, st);
+  if (split_stop) cudaEventRecord(split_stop, st);
+  if (e != cudaSuccess) return e;
+  const int warps = a.B * a.Hq;
+  const int blocks = (warps * 32 + 127) / 128;
+  const bool risk = a.risk_raw != nullptr && a.meter;
+  if (scheme == kInt8) {
+    if (risk) decode_merge_kernel<true, true><<<blocks, 128, 0, st>>>(a);
+    else decode_merge_kernel<true, false><<<blocks, 128, 0, st>>>(a);
+  } else {
+    if (risk) decode_merge_kernel<false, true><<<blocks, 128, 0, st>>>(a);
+    else decode_merge_kernel<false, false><<<blocks, 128, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace witcert

@@ -1,0 +1,82 @@
+// Internal kernel launchers (host side).  Not part of the public ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace witcert {
+
+constexpr int kPartStride = 132;   // m (log2 units), Z, S_A, S_B, acc[128]
+
+struct WriteArgs {
+  uint8_t* blocks;           // layer base: [B][Hkv][nblk_max][block_bytes]
+  int nblk_max;
+  const void* K;             // [B][n_tok][Hkv][128]
+  const void* V;
+  int B, Hkv, n_tok, t0, layer, backing_rows;   // backing_rows: rows per (seq, KV head) in the backing store
+  int is_bf16;
+  uint64_t seed;
+  void* backing;             // device-mapped pinned host, layer base [B][Hkv][backing_rows][128], or null
+  const int32_t* slots;      // layer base [B][Hkv][nblk_max], or null
+  void* pool;                // exact-key pool [slots][16][128]
+  float* kivi_tail;          // layer base [B][Hkv][16][128] (KIVI)
+  unsigned long long* clamps;
+};
+
+struct DecodeArgs {
+  const uint8_t* blocks;     // layer base
+  int nblk_max;
+  const int32_t* slots;      // layer base or null
+  const void* pool;
+  const float* kivi_tail;    // layer base (KIVI)
+  const void* q;             // [B][Hq][128]
+  int is_bf16;
+  int B, Hq, Hkv, grp, S, n_splits, seqs_per_cta;
+  uint64_t seed;
+  int layer;
+  float kappa;               // sqrt(2 ln(2S/delta_loc)), rounded up (Tier B)
+  float* part;               // [B][Hq][n_splits][kPartStride]
+  float2* risk_raw;          // [B][Hq][nblk_max] (block max in log2 units, risk sum), or null
+  float* risk;               // [B][Hq][nblk_max] normalized block risk, or null
+  float* out;                // [B][Hq][128]
+  float *meter_a, *meter_b, *raw_a, *raw_b;
+  int* err;                  // device error word (spin limits)
+  bool meter;
+};
+
+cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st);
+// Split-KV decode + merge.  Returns the split kernel's launch error; `split_start`
+// and `split_stop` (optional) bracket the split kernel alone.
+cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStream_t st,
+                          cudaEvent_t split_start, cudaEvent_t split_stop);
+int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count);
+
+struct GateArgs {
+  const float* risk;         // [B][Hq][nblk_max] (this layer)
+  int32_t* slots;            // [B][Hkv][nblk_max] (this layer)
+  uint32_t* selmask;         // [B][Hkv][nblk_max/32 + 1] scratch bitmap
+  int4* todo;                // [capacity] (seq, kv head, block, slot)
+  unsigned int* todo_count;  // device counter (reset per call)
+  unsigned int* pool_next;   // device counter (persistent)
+  unsigned long long* stats; // [6] device counters (witcert_gate_stats order)
+  uint8_t* blocks;           // layer base
+  const void* backing;       // device-mapped pinned host, layer base
+  void* pool;
+  int nblk_max, B, Hq, Hkv, grp, S, backing_rows, pool_capacity, scheme, elem_bytes;
+  double d_star;
+};
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t st);
+
+struct ExportArgs {
+  const uint8_t* blocks;
+  int nblk_max, B, Hkv, Hq, S, scheme;
+  const int32_t* slots;
+  const float* risk;
+  void* dst;
+  int what;
+};
+cudaError_t launch_export(const ExportArgs& a, cudaStream_t st);
+cudaError_t launch_dither(uint64_t seed, int layer, int kvh, int t0, int n, int tensor, float* out,
+                          cudaStream_t st);
+
+}  // namespace witcert

@@ -1,0 +1,441 @@
+// Host runtime behind the C ABI in include/witcert.h: owns the cache's device
+// pools, the pinned backing store, the side stream of the gate and the events
+// that order it against writes and decodes; validates every argument and maps
+// failures to status codes with a thread-local message.
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/witcert.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace witcert;
+
+namespace {
+
+thread_local std::string g_err;
+
+witcert_status fail(witcert_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+witcert_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(e == cudaErrorMemoryAllocation ? WITCERT_ENOMEM : WITCERT_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+void ok() { g_err.clear(); }
+
+struct ProfPair { cudaEvent_t a, b; };
+
+}  // namespace
+
+struct witcert_cache {
+  witcert_config cfg{};
+  int device = 0, sm_count = 0, scheme = 0, bblk = 0, nblk_max = 0, elem = 0, max_splits = 1;
+  size_t layer_blocks = 0;          // bytes of one layer's block store
+  uint8_t* blocks = nullptr;
+  float* kivi_tail = nullptr;       // [L][B][Hkv][16][128]
+  int32_t* slots = nullptr;         // [L][B][Hkv][nblk_max]
+  void* pool = nullptr;             // [cap][16][128] kv dtype
+  void* backing_host = nullptr;     // [L][B][Hkv][max_tokens][128] kv dtype, pinned + mapped
+  void* backing_dev = nullptr;
+  float2* risk_raw = nullptr;       // [B][Hq][nblk_max]
+  float* risk = nullptr;            // [L][B][Hq][nblk_max]
+  float* part = nullptr;            // [B][Hq][max_splits][kPartStride]
+  uint32_t* selmask = nullptr;
+  int4* todo = nullptr;
+  unsigned int* todo_count = nullptr;
+  unsigned int* pool_next = nullptr;
+  unsigned long long* gstats = nullptr;   // [6]
+  unsigned long long* clamps = nullptr;
+  int* err = nullptr;
+  std::vector<int> len, risk_len;
+  std::vector<cudaEvent_t> gate_done;
+  std::vector<char> gate_pending;
+  cudaStream_t side = nullptr;
+  bool profiling = false;
+  std::vector<ProfPair> prof_pending, prof_free;
+  double prof_ms = 0.0;
+  uint64_t prof_n = 0, tokens_written = 0, decode_calls = 0, gate_calls = 0;
+  int last_n_splits = 0;
+};
+
+namespace {
+
+size_t layer_rows(const witcert_cache* c) { return (size_t)c->cfg.batch * c->cfg.n_kv_heads; }
+// Backing-store rows per (sequence, KV head): capacity rounded up to whole 16-token blocks,
+// so page-in can always copy a full block.
+size_t backing_rows(const witcert_cache* c) { return (size_t)c->nblk_max * kBlk; }
+
+witcert_status check_layer(const witcert_cache* c, int layer) {
+  if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(WITCERT_EINVAL, "layer %d out of range [0, %d)", layer, c->cfg.n_layers);
+  return WITCERT_OK;
+}
+
+void free_all(witcert_cache* c) {
+  cudaFree(c->blocks); cudaFree(c->kivi_tail); cudaFree(c->slots); cudaFree(c->pool);
+  if (c->backing_host) cudaFreeHost(c->backing_host);
+  cudaFree(c->risk_raw); cudaFree(c->risk); cudaFree(c->part); cudaFree(c->selmask); cudaFree(c->todo);
+  cudaFree(c->todo_count); cudaFree(c->pool_next); cudaFree(c->gstats); cudaFree(c->clamps); cudaFree(c->err);
+  for (auto e : c->gate_done) if (e) cudaEventDestroy(e);
+  for (auto& p : c->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  for (auto& p : c->prof_free) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+  if (c->side) cudaStreamDestroy(c->side);
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t bytes) {
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes ? bytes : 16);
+  if (e == cudaSuccess) e = cudaMemset(*p, 0, bytes ? bytes : 16);
+  return e;
+}
+
+// Wait for the gate of `layer` (device-side) before touching that layer again.
+void order_after_gate(witcert_cache* c, int layer, cudaStream_t st) {
+  if (c->gate_pending[layer]) cudaStreamWaitEvent(st, c->gate_done[layer], 0);
+}
+
+void collect_profile(witcert_cache* c) {
+  for (auto& p : c->prof_pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) { c->prof_ms += ms; ++c->prof_n; }
+    c->prof_free.push_back(p);
+  }
+  c->prof_pending.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* witcert_last_error(void) { return g_err.c_str(); }
+
+witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
+  if (!cfg || !out) return fail(WITCERT_EINVAL, "NULL argument");
+  *out = nullptr;
+  const witcert_config& f = *cfg;
+  if (f.head_dim != 128) return fail(WITCERT_EINVAL, "head_dim must be 128 (got %d)", f.head_dim);
+  if (f.n_layers <= 0 || f.n_layers > 65535) return fail(WITCERT_EINVAL, "n_layers must be in [1, 65535]");
+  if (f.n_kv_heads <= 0 || f.n_kv_heads > 65535 || f.n_q_heads <= 0 || f.n_q_heads % f.n_kv_heads)
+    return fail(WITCERT_EINVAL, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (f.n_q_heads / f.n_kv_heads > kMaxGroupHeads) return fail(WITCERT_EINVAL, "at most %d query heads per KV head", kMaxGroupHeads);
+  if (f.batch <= 0 || f.max_tokens <= 0) return fail(WITCERT_EINVAL, "batch and max_tokens must be positive");
+  if (f.scheme < WITCERT_INT8_DITHER || f.scheme > WITCERT_KIVI2) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)f.scheme);
+  if (f.kv_dtype != WITCERT_F32 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "unknown dtype %d", (int)f.kv_dtype);
+  if (f.total_steps <= 0) return fail(WITCERT_EINVAL, "total_steps must be positive");
+  if (f.n_splits < 0 || f.max_repair_blocks < 0) return fail(WITCERT_EINVAL, "n_splits and max_repair_blocks must be >= 0");
+
+  auto* c = new (std::nothrow) witcert_cache();
+  if (!c) return fail(WITCERT_ENOMEM, "host allocation failed");
+  c->cfg = f;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) { delete c; return cuda_fail(e, "device query"); }
+  c->scheme = (int)f.scheme;
+  c->bblk = block_bytes(c->scheme);
+  c->nblk_max = (f.max_tokens + kBlk - 1) / kBlk;
+  c->elem = f.kv_dtype == WITCERT_BF16 ? 2 : 4;
+  c->layer_blocks = layer_rows(c) * c->nblk_max * c->bblk;
+  const int auto_max = decode_auto_splits(c->scheme, f.batch, f.n_kv_heads, c->nblk_max, c->sm_count);
+  c->max_splits = f.n_splits > auto_max ? f.n_splits : auto_max;
+  c->len.assign(f.n_layers, 0);
+  c->risk_len.assign(f.n_layers, -1);
+  c->gate_done.assign(f.n_layers, nullptr);
+  c->gate_pending.assign(f.n_layers, 0);
+  const size_t L = f.n_layers, cells = (size_t)f.batch * f.n_q_heads;
+  const bool gate = f.max_repair_blocks > 0;
+
+#define TRY(x, what) do { e = (x); if (e != cudaSuccess) { free_all(c); delete c; return cuda_fail(e, what); } } while (0)
+  TRY(dalloc(&c->blocks, L * c->layer_blocks), "allocating the block store");
+  if (c->scheme == kKivi) TRY(dalloc(&c->kivi_tail, L * layer_rows(c) * kBlk * kD * sizeof(float)), "allocating the KIVI tail");
+  TRY(dalloc(&c->part, cells * c->max_splits * kPartStride * sizeof(float)), "allocating split scratch");
+  TRY(dalloc(&c->clamps, sizeof(unsigned long long)), "allocating counters");
+  TRY(dalloc(&c->err, sizeof(int)), "allocating the error word");
+  if (gate) {
+    TRY(dalloc(&c->slots, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "allocating repair slots");
+    TRY(cudaMemset(c->slots, 0xFF, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "clearing repair slots");
+    TRY(dalloc(&c->pool, (size_t)f.max_repair_blocks * kBlk * kD * c->elem), "allocating the exact-key pool");
+    const size_t bbytes = L * layer_rows(c) * (size_t)c->nblk_max * kBlk * kD * c->elem;
+    TRY(cudaHostAlloc(&c->backing_host, bbytes, cudaHostAllocMapped), "allocating the pinned backing store");
+    memset(c->backing_host, 0, bbytes);
+    TRY(cudaHostGetDevicePointer(&c->backing_dev, c->backing_host, 0), "mapping the backing store");
+    TRY(dalloc(&c->risk_raw, cells * c->nblk_max * sizeof(float2)), "allocating block-risk scratch");
+    TRY(dalloc(&c->risk, L * cells * c->nblk_max * sizeof(float)), "allocating block risks");
+    TRY(dalloc(&c->selmask, layer_rows(c) * (c->nblk_max / 32 + 1) * sizeof(uint32_t)), "allocating gate masks");
+    TRY(dalloc(&c->todo, layer_rows(c) * c->nblk_max * sizeof(int4)), "allocating the gate todo list");
+    TRY(dalloc(&c->todo_count, sizeof(unsigned int)), "allocating gate counters");
+    TRY(dalloc(&c->pool_next, sizeof(unsigned int)), "allocating gate counters");
+    TRY(dalloc(&c->gstats, 6 * sizeof(unsigned long long)), "allocating gate counters");
+    TRY(cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking), "creating the gate stream");
+    for (auto& ev : c->gate_done) TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "creating gate events");
+  }
+#undef TRY
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) { free_all(c); delete c; return cuda_fail(e, "create"); }
+  *out = c;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_destroy(witcert_cache* c) {
+  if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const void* V, int n_tok, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (n_tok < 0) return fail(WITCERT_EINVAL, "n_tok must be >= 0");
+  if (n_tok > 0 && (!K || !V)) return fail(WITCERT_EINVAL, "K and V must not be NULL");
+  if ((long long)c->len[layer] + n_tok > c->cfg.max_tokens)
+    return fail(WITCERT_EINVAL, "layer %d would hold %lld tokens, capacity %d", layer,
+                (long long)c->len[layer] + n_tok, c->cfg.max_tokens);
+  if (n_tok == 0) { ok(); return WITCERT_OK; }
+  auto st = static_cast<cudaStream_t>(stream);
+  order_after_gate(c, layer, st);
+  WriteArgs a{};
+  a.blocks = c->blocks + layer * c->layer_blocks;
+  a.nblk_max = c->nblk_max;
+  a.K = K; a.V = V;
+  a.B = c->cfg.batch; a.Hkv = c->cfg.n_kv_heads; a.n_tok = n_tok; a.t0 = c->len[layer]; a.layer = layer;
+  a.backing_rows = (int)backing_rows(c);
+  a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
+  a.seed = c->cfg.seed;
+  if (c->backing_dev)
+    a.backing = static_cast<uint8_t*>(c->backing_dev) + layer * layer_rows(c) * backing_rows(c) * kD * c->elem;
+  if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
+  a.pool = c->pool;
+  if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
+  a.clamps = c->clamps;
+  cudaError_t e = launch_write(c->scheme, a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "write launch");
+  c->len[layer] += n_tok;
+  c->risk_len[layer] = -1;
+  c->tokens_written += (uint64_t)n_tok * layer_rows(c);
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
+                              float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
+  const bool meter = meter_a || meter_b || raw_a || raw_b;
+  if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
+  auto st = static_cast<cudaStream_t>(stream);
+  order_after_gate(c, layer, st);
+  const int S = c->len[layer];
+  const int nblk = (S + kBlk - 1) / kBlk;
+  DecodeArgs a{};
+  a.blocks = c->blocks + layer * c->layer_blocks;
+  a.nblk_max = c->nblk_max;
+  if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
+  a.pool = c->pool;
+  if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
+  a.q = q;
+  a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
+  a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
+  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits
+                                   : decode_auto_splits(c->scheme, a.B, a.Hkv, nblk > 0 ? nblk : 1, c->sm_count);
+  a.seed = c->cfg.seed;
+  a.layer = layer;
+  float kappa = 0.f;
+  if (meter && S > 0) {
+    const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
+    const double k = std::sqrt(2.0 * std::log(2.0 * S / dloc));
+    kappa = (float)k;
+    if ((double)kappa < k) kappa = std::nextafter(kappa, INFINITY);
+  }
+  a.kappa = kappa;
+  a.part = c->part;
+  const bool gate = c->cfg.max_repair_blocks > 0;
+  if (gate && meter) {
+    a.risk_raw = c->risk_raw;
+    a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
+  }
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
+  a.err = c->err;
+  a.meter = meter;
+  ProfPair pp{nullptr, nullptr};
+  if (c->profiling) {
+    if (c->prof_free.empty()) {
+      ProfPair n{};
+      if (cudaEventCreate(&n.a) != cudaSuccess || cudaEventCreate(&n.b) != cudaSuccess)
+        return fail(WITCERT_ECUDA, "creating profiling events");
+      c->prof_free.push_back(n);
+    }
+    pp = c->prof_free.back();
+    c->prof_free.pop_back();
+  }
+  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b);
+  if (pp.a) c->prof_pending.push_back(pp);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (gate && meter) c->risk_len[layer] = S;
+  c->last_n_splits = a.n_splits;
+  ++c->decode_calls;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (c->cfg.max_repair_blocks <= 0) return fail(WITCERT_ESTATE, "the gate is disabled (max_repair_blocks = 0)");
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return fail(WITCERT_EINVAL, "tau must be finite and >= 0");
+  if (c->risk_len[layer] != c->len[layer] || c->len[layer] == 0)
+    return fail(WITCERT_ESTATE, "layer %d has no metered decode since its last write", layer);
+  auto st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t ready = c->gate_done[layer];
+  cudaError_t e = cudaEventRecord(ready, st);   // reuse: marks the point the gate must follow
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(c->side, ready, 0);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->todo_count, 0, sizeof(unsigned int), c->side);
+  if (e != cudaSuccess) return cuda_fail(e, "gate ordering");
+  GateArgs a{};
+  const size_t cells = (size_t)c->cfg.batch * c->cfg.n_q_heads;
+  a.risk = c->risk + (size_t)layer * cells * c->nblk_max;
+  a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
+  a.selmask = c->selmask; a.todo = c->todo; a.todo_count = c->todo_count; a.pool_next = c->pool_next;
+  a.stats = c->gstats;
+  a.blocks = c->blocks + layer * c->layer_blocks;
+  a.backing = static_cast<uint8_t*>(c->backing_dev) + layer * layer_rows(c) * backing_rows(c) * kD * c->elem;
+  a.pool = c->pool;
+  a.nblk_max = c->nblk_max; a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads;
+  a.grp = a.Hq / a.Hkv; a.S = c->len[layer]; a.backing_rows = (int)backing_rows(c);
+  a.pool_capacity = c->cfg.max_repair_blocks; a.scheme = c->scheme; a.elem_bytes = c->elem;
+  a.d_star = std::sqrt(1.0 + 2.0 * (double)tau) - 1.0;
+  e = launch_gate(a, c->side);
+  if (e == cudaSuccess) e = cudaEventRecord(c->gate_done[layer], c->side);
+  if (e != cudaSuccess) return cuda_fail(e, "gate launch");
+  c->gate_pending[layer] = 1;
+  ++c->gate_calls;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_gate_stats(witcert_cache* c, witcert_gate_counters* out, int timeout_ms) {
+  if (!c || !out) return fail(WITCERT_EINVAL, "NULL argument");
+  memset(out, 0, sizeof *out);
+  out->gate_calls = c->gate_calls;
+  if (c->cfg.max_repair_blocks <= 0) { ok(); return WITCERT_OK; }
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms < 0 ? 0 : timeout_ms);
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    if (!c->gate_pending[l]) continue;
+    for (;;) {
+      cudaError_t q = cudaEventQuery(c->gate_done[l]);
+      if (q == cudaSuccess) break;
+      if (q != cudaErrorNotReady) return cuda_fail(q, "gate event");
+      if (std::chrono::steady_clock::now() > deadline) return fail(WITCERT_ETIMEDOUT, "gate of layer %d still running", l);
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+  }
+  unsigned long long s[6] = {0, 0, 0, 0, 0, 0};
+  cudaError_t e = cudaMemcpy(s, c->gstats, sizeof s, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading gate counters");
+  out->cells_triggered = s[0]; out->blocks_selected = s[1]; out->blocks_paged_in = s[2];
+  out->bytes_paged_in = s[3]; out->blocks_dropped = s[4];
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_stats(witcert_cache* c, witcert_stats_t* out) {
+  if (!c || !out) return fail(WITCERT_EINVAL, "NULL argument");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "stats");
+  memset(out, 0, sizeof *out);
+  unsigned long long cl = 0;
+  int er = 0;
+  if ((e = cudaMemcpy(&cl, c->clamps, sizeof cl, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "stats");
+  if ((e = cudaMemcpy(&er, c->err, sizeof er, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "stats");
+  collect_profile(c);
+  out->tokens_written = c->tokens_written;
+  out->decode_calls = c->decode_calls;
+  out->int8_clamps = cl;
+  out->device_errors = (uint64_t)er;
+  out->decode_kernel_ms = c->prof_ms;
+  out->decode_kernel_launches = c->prof_n;
+  out->last_n_splits = c->last_n_splits;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_set_profiling(witcert_cache* c, int on) {
+  if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
+  if (!on && c->profiling) {
+    cudaDeviceSynchronize();
+    collect_profile(c);
+  }
+  if (on && !c->profiling) { cudaDeviceSynchronize(); collect_profile(c); c->prof_ms = 0.0; c->prof_n = 0; }
+  c->profiling = on != 0;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_length(const witcert_cache* c, int layer, int* len) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!len) return fail(WITCERT_EINVAL, "len is NULL");
+  *len = c->len[layer];
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind what, void* dst, size_t bytes,
+                              void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  const int S = c->len[layer], nblk = (S + kBlk - 1) / kBlk;
+  const size_t B = c->cfg.batch, Hkv = c->cfg.n_kv_heads, Hq = c->cfg.n_q_heads;
+  size_t need = 0;
+  switch (what) {
+    case WITCERT_X_K_CODES: case WITCERT_X_V_CODES: need = B * S * Hkv * kD; break;
+    case WITCERT_X_K_SCALES: case WITCERT_X_V_SCALES: case WITCERT_X_V_ZEROS: need = B * S * Hkv * 4 * 2; break;
+    case WITCERT_X_KIVI_K_SCALE: case WITCERT_X_KIVI_K_ZERO: need = B * nblk * Hkv * kD * 2; break;
+    case WITCERT_X_WITNESS: need = B * S * Hkv * kBands * 2; break;
+    case WITCERT_X_SLOTS: need = B * Hkv * nblk * 4; break;
+    case WITCERT_X_BLOCK_RISK: need = B * Hq * nblk * 4; break;
+    default: return fail(WITCERT_EINVAL, "unknown export kind %d", (int)what);
+  }
+  const bool int8 = c->scheme == kInt8, kivi = c->scheme == kKivi;
+  if ((what == WITCERT_X_K_SCALES && !int8) || ((what == WITCERT_X_V_SCALES) && !(int8 || kivi)) ||
+      ((what == WITCERT_X_V_ZEROS || what == WITCERT_X_KIVI_K_SCALE || what == WITCERT_X_KIVI_K_ZERO) && !kivi))
+    return fail(WITCERT_EINVAL, "export kind %d does not exist for this scheme", (int)what);
+  if (what == WITCERT_X_BLOCK_RISK && !c->risk) return fail(WITCERT_ESTATE, "block risks need the gate enabled");
+  if (!dst || bytes < need) return fail(WITCERT_EINVAL, "export needs %zu bytes, got %zu", need, bytes);
+  auto st = static_cast<cudaStream_t>(stream);
+  order_after_gate(c, layer, st);
+  ExportArgs a{};
+  a.blocks = c->blocks + layer * c->layer_blocks;
+  a.nblk_max = c->nblk_max; a.B = (int)B; a.Hkv = (int)Hkv; a.Hq = (int)Hq; a.S = S; a.scheme = c->scheme;
+  a.slots = c->slots ? c->slots + layer * layer_rows(c) * c->nblk_max : nullptr;
+  a.risk = c->risk ? c->risk + (size_t)layer * B * Hq * c->nblk_max : nullptr;
+  a.dst = dst;
+  a.what = (int)what;
+  cudaError_t e = launch_export(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "export launch");
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_dither(uint64_t seed, int layer, int kv_head, int t0, int n, int tensor, float* out,
+                              void* stream) {
+  if (layer < 0 || layer > 65535 || kv_head < 0 || kv_head > 65535 || t0 < 0 || n < 0 || (tensor != 0 && tensor != 1))
+    return fail(WITCERT_EINVAL, "bad dither arguments");
+  if (n > 0 && !out) return fail(WITCERT_EINVAL, "out is NULL");
+  cudaError_t e = launch_dither(seed, layer, kv_head, t0, n, tensor, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dither launch");
+  ok();
+  return WITCERT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,286 @@
+// Write path: quantize appended keys/values into the block store and compute
+// the key witness w_{t,b} = ||r_{t,b}|| of 16 bands [WitCert summary, witness
+// paragraph and implementation paragraph].
+//
+// One warp per (sequence, token, KV head); lane l owns channels 4l..4l+3, so a
+// 32-channel scale group is 8 lanes and band b (dims 4b..4b+3 and
+// 64+4b..64+4b+3) is lanes b and b+16.  The residual is formed in fp64, where
+// x - s*(code - xi) is exact, and the band norm is rounded up to fp16 after a
+// 2^-48 relative margin, so the stored witness never falls below the true norm.
+// KIVI keys are quantized per channel over a 16-token block when the block's
+// last token arrives (one warp per (sequence, KV head) walks the blocks in
+// order); until then they wait, exact, in a per-(sequence, head) tail buffer.
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace witcert {
+
+namespace {
+
+constexpr double kWitMargin = 1.0 + 3.552713678800501e-15;   // 1 + 2^-48
+
+template <typename T> __device__ __forceinline__ void load4f(const T* p, float (&x)[4]);
+template <> __device__ __forceinline__ void load4f<float>(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <> __device__ __forceinline__ void load4f<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+template <typename T> __device__ __forceinline__ void store4(T* p, const T* src) {
+  if (sizeof(T) == 4) *reinterpret_cast<float4*>(p) = *reinterpret_cast<const float4*>(src);
+  else *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(src);
+}
+
+__device__ __forceinline__ float grp_max8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  return v;
+}
+__device__ __forceinline__ float grp_min8(float v) {
+  v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  return v;
+}
+
+// Witness of token r from the lane's four fp64 residuals; lanes 0..15 store band `lane`.
+__device__ __forceinline__ void store_witness(uint8_t* wreg, int r, const double (&res)[4], int lane, bool zero) {
+  double ss = res[0] * res[0] + res[1] * res[1] + res[2] * res[2] + res[3] * res[3];
+  ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+  if (lane < 16) {
+    __half w = __float2half_ru(__double2float_ru(sqrt(ss) * kWitMargin));
+    if (zero) w = __float2half_rn(0.f);
+    *reinterpret_cast<__half*>(wreg + wit_off(r, lane)) = w;
+  }
+}
+
+// Exact-key side effects shared by all schemes: backing store and repaired blocks.
+template <typename T>
+__device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int t, int lane, const T* krow) {
+  const size_t sh = (size_t)i * a.Hkv + h;
+  if (a.backing) store4<T>(reinterpret_cast<T*>(a.backing) + (sh * a.backing_rows + t) * kD + 4 * lane, krow + 4 * lane);
+  if (a.slots) {
+    const int slot = a.slots[sh * a.nblk_max + (t >> 4)];
+    if (slot >= 0) {
+      store4<T>(reinterpret_cast<T*>(a.pool) + ((size_t)slot * kBlk + (t & 15)) * kD + 4 * lane, krow + 4 * lane);
+      return true;
+    }
+  }
+  return false;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= a.B * a.n_tok * a.Hkv) return;
+  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
+  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * Int8Layout::BYTES;
+  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+  const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
+  const int G = lane >> 3;
+#pragma unroll
+  for (int tensor = 0; tensor < 2; ++tensor) {
+    float x[4];
+    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    amax = grp_max8(amax);
+    // s = fp16 round-up of fp32(amax / 127), at most 65504
+    __half s16 = __float2half_ru(__fdiv_rn(amax, 127.0f));
+    if (__half2float(s16) > 65504.0f) s16 = __float2half_rn(65504.0f);
+    const float s = __half2float(s16);
+    const float4 xi = dither4(a.seed, a.layer, h, t, lane, tensor);
+    const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
+    uint32_t packed = 0;
+    double res[4];
+    int clamps = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int code = 0;
+      if (s > 0.0f) {
+        const float z = __fadd_rn(__fdiv_rn(x[e], s), xs[e]);
+        float rz = rintf(z);
+        if (rz < -128.f) { rz = -128.f; ++clamps; }
+        if (rz > 127.f) { rz = 127.f; ++clamps; }
+        code = (int)rz;
+      }
+      res[e] = (double)x[e] - (double)s * ((double)code - (double)xs[e]);
+      const uint32_t biased = (uint32_t)(code + 128) & 0xFFu;
+      if (tensor == 0) packed |= biased << (8 * e);
+      else bp[Int8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)biased;
+    }
+    if (clamps) atomicAdd(a.clamps, (unsigned long long)clamps);
+    if ((lane & 7) == 0)
+      *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS : Int8Layout::KS) + (r * 4 + G) * 2) = s16;
+    if (tensor == 0) {
+      *reinterpret_cast<uint32_t*>(bp + Int8Layout::KC + kcode_off(r, 4 * lane)) = packed;
+      store_witness(bp + Int8Layout::W, r, res, lane, repaired);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) write_fp8_kernel(const WriteArgs a) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= a.B * a.n_tok * a.Hkv) return;
+  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
+  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * Fp8Layout::BYTES;
+  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+  const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
+#pragma unroll
+  for (int tensor = 0; tensor < 2; ++tensor) {
+    float x[4];
+    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
+    uint32_t packed = 0;
+    double res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x[e], __NV_SATFINITE, __NV_E4M3);
+      const float xh = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+      res[e] = (double)x[e] - (double)xh;
+      if (tensor == 0) packed |= (uint32_t)c << (8 * e);
+      else bp[Fp8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)c;
+    }
+    if (tensor == 0) {
+      *reinterpret_cast<uint32_t*>(bp + Fp8Layout::KC + kcode_off(r, 4 * lane)) = packed;
+      store_witness(bp + Fp8Layout::W, r, res, lane, repaired);
+    }
+  }
+}
+
+// KIVI asymmetric 2-bit of one value against fp16 scale/zero (fp32 steps as the oracle states them).
+__device__ __forceinline__ int kivi_code(float x, float zr, float sc) {
+  if (!(sc > 0.0f)) return 0;
+  float v = rintf(__fdiv_rn(__fsub_rn(x, zr), sc));
+  v = fminf(fmaxf(v, 0.0f), 3.0f);
+  return (int)v;
+}
+__device__ __forceinline__ __half f16_sat_rn(float v) { return __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f)); }
+
+// KIVI values (per token, per 32-channel group) + backing store of keys.
+template <typename T>
+__global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= a.B * a.n_tok * a.Hkv) return;
+  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
+  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * KiviLayout::BYTES;
+  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+  exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
+  float x[4];
+  load4f<T>(reinterpret_cast<const T*>(a.V) + row + 4 * lane, x);
+  const float mn = grp_min8(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
+  const float mx = grp_max8(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+  const __half sc16 = f16_sat_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+  const __half zr16 = f16_sat_rn(mn);
+  const float sc = __half2float(sc16), zr = __half2float(zr16);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int code = kivi_code(x[e], zr, sc);
+    int off, bit;
+    kivi_v_pos(r, 4 * lane + e, off, bit);
+    if (code) atomicOr(reinterpret_cast<unsigned int*>(bp + KiviLayout::VC + off), (unsigned int)code << bit);
+  }
+  if ((lane & 7) == 0) {
+    __half* vp = reinterpret_cast<__half*>(bp + KiviLayout::VP) + (r * 4 + (lane >> 3)) * 2;
+    vp[0] = sc16;
+    vp[1] = zr16;
+  }
+}
+
+// KIVI keys: one warp per (sequence, KV head) walks the blocks this write touches.
+template <typename T>
+__global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
+  const int sh = blockIdx.x, lane = threadIdx.x;       // sh = i * Hkv + h
+  const int i = sh / a.Hkv, h = sh % a.Hkv;
+  __shared__ unsigned int img[128];                    // K code words of one block
+  float* tail = a.kivi_tail + (size_t)sh * kBlk * kD;
+  const int t_end = a.t0 + a.n_tok;
+  for (int blk = a.t0 / kBlk; blk * kBlk < t_end; ++blk) {
+    const int lo = blk * kBlk;
+    if (lo + kBlk > t_end) {   // unfinished block: keep the new keys exact in the tail
+      for (int t = (a.t0 > lo ? a.t0 : lo); t < t_end; ++t) {
+        float x[4];
+        load4f<T>(reinterpret_cast<const T*>(a.K) + (((size_t)i * a.n_tok + (t - a.t0)) * a.Hkv + h) * kD + 4 * lane, x);
+        *reinterpret_cast<float4*>(tail + (t - lo) * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+      }
+      __syncwarp();
+      break;
+    }
+    float x[16][4];
+#pragma unroll
+    for (int r = 0; r < kBlk; ++r) {
+      const int t = lo + r;
+      if (t < a.t0) {
+        const float4 v = *reinterpret_cast<const float4*>(tail + r * kD + 4 * lane);
+        x[r][0] = v.x; x[r][1] = v.y; x[r][2] = v.z; x[r][3] = v.w;
+      } else {
+        load4f<T>(reinterpret_cast<const T*>(a.K) + (((size_t)i * a.n_tok + (t - a.t0)) * a.Hkv + h) * kD + 4 * lane, x[r]);
+      }
+    }
+    for (int k = lane; k < 128; k += 32) img[k] = 0u;
+    __syncwarp();
+    uint8_t* bp = a.blocks + ((size_t)sh * a.nblk_max + blk) * KiviLayout::BYTES;
+    __half* ksc = reinterpret_cast<__half*>(bp + KiviLayout::KP);
+    __half* kzr = reinterpret_cast<__half*>(bp + KiviLayout::KP + 256);
+    float sc[4], zr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float mn = x[0][e], mx = x[0][e];
+#pragma unroll
+      for (int r = 1; r < kBlk; ++r) { mn = fminf(mn, x[r][e]); mx = fmaxf(mx, x[r][e]); }
+      const __half s16 = f16_sat_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half z16 = f16_sat_rn(mn);
+      const int c = 4 * lane + e;
+      ksc[kivi_kparam_idx(c)] = s16;
+      kzr[kivi_kparam_idx(c)] = z16;
+      sc[e] = __half2float(s16);
+      zr[e] = __half2float(z16);
+    }
+#pragma unroll
+    for (int r = 0; r < kBlk; ++r) {
+      double res[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int code = kivi_code(x[r][e], zr[e], sc[e]);
+        res[e] = (double)x[r][e] - ((double)zr[e] + (double)sc[e] * (double)code);
+        int off, bit;
+        kivi_k_pos(r, 4 * lane + e, off, bit);
+        if (code) atomicOr(&img[off / 4], (unsigned int)code << bit);
+      }
+      store_witness(bp + KiviLayout::W, r, res, lane, false);
+    }
+    __syncwarp();
+    for (int k = lane; k < 128; k += 32) reinterpret_cast<unsigned int*>(bp + KiviLayout::KC)[k] = img[k];
+    __syncwarp();
+  }
+}
+
+template <typename T>
+cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st) {
+  const int warps = a.B * a.n_tok * a.Hkv;
+  const int blocks = (warps * 32 + 127) / 128;
+  if (scheme == kInt8) write_int8_kernel<T><<<blocks, 128, 0, st>>>(a);
+  else if (scheme == kFp8) write_fp8_kernel<T><<<blocks, 128, 0, st>>>(a);
+  else {
+    write_kivi_v_kernel<T><<<blocks, 128, 0, st>>>(a);
+    write_kivi_k_kernel<T><<<a.B * a.Hkv, 32, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st) {
+  if (a.B * a.n_tok * a.Hkv == 0) return cudaSuccess;
+  return a.is_bf16 ? launch_t<__nv_bfloat16>(scheme, a, st) : launch_t<float>(scheme, a, st);
+}
+
+}  // namespace witcert

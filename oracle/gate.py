@@ -1,9 +1,9 @@
 """Meter-driven gate of the oracle: which exact key blocks to page in.
 
-The pages state that when the meter exceeds a threshold the gate pages exact
-keys in from the CPU backing store at block granularity and zeroes the repaired
-witnesses, risk-ranked where the witness is saturated (tau >= 1) and certified
-where it is informative (tau < 1), with incremental persistent repair
+Per the pages, once the meter passes a threshold the gate brings exact keys
+back from host memory a block at a time and clears the witnesses of what it
+repaired; it ranks by risk when the threshold is 1 or more and certifies below
+1, and repairs accumulate and persist
 [WitCert summary, implementation paragraph; WitCert Lean page, Approach and
 Figures 2 and 5].  The ranking and stopping rule below are this build's
 reading of those sentences:

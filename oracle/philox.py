@@ -7,9 +7,10 @@ which multiplies counter words 0 and 2 by two fixed odd constants, splits the
 two counter words and the round key; the key is advanced by two Weyl
 increments between rounds.
 
-The dither stream is this module's reading of "dither regenerated
-deterministically at read time" [WitCert summary, Tier B paragraph], keyed on
-(layer, head, token, channel):
+The dither stream is this module's reading of the Tier B paragraph's
+requirement that the decoder recompute the writer's dither exactly rather than
+store it [WitCert summary, Tier B paragraph]; it is keyed on (layer, head,
+token, channel):
 
     key     = (seed mod 2^32, seed div 2^32)
     counter = (token position t, (channel // 4) | (tensor << 16),

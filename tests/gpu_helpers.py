@@ -1,0 +1,127 @@
+"""Shared helpers of the GPU parity tests: run a workload through the library and the oracle."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import kv_cache_quantization_witcert_gb300 as wc
+from kv_cache_quantization_witcert_gb300 import _lib
+from oracle import OracleCache, meter, quant
+from oracle.philox import dither
+
+# Meters: GPU >= oracle (one fp32 ulp of slack for rounding the oracle's value to fp32)
+# and GPU <= oracle * (1 + 1e-4).
+METER_REL = 1e-4
+FP32_ULP = 2.0 ** -23
+
+
+def torch_dtype(w):
+    return torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+
+def to_dev(x, w):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(torch_dtype(w))
+
+
+def make_pair(w, scheme=None, n_splits=None, extra_tokens=None, gate_blocks=0):
+    scheme = scheme or w.scheme
+    cap = w.context + (w.steps if extra_tokens is None else extra_tokens)
+    gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, cap, scheme, dtype=torch_dtype(w),
+                   seed=w.seed, total_steps=w.steps, n_splits=w.n_splits if n_splits is None else n_splits,
+                   max_repair_blocks=gate_blocks)
+    ref = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, scheme, w.seed, w.steps)
+    return gpu, ref
+
+
+def check_meter(gpu, ref, rel=METER_REL, what=""):
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    low = g < r * (1 - FP32_ULP)
+    high = g > r * (1 + rel) + 1e-30
+    if low.any() or high.any():
+        idx = np.argwhere(low | high)[:5]
+        detail = [(tuple(ix), g[tuple(ix)], r[tuple(ix)]) for ix in idx]
+        raise AssertionError(f"{what}: {low.sum()} below, {high.sum()} above tolerance: {detail}")
+
+
+def check_write(gpu, ref, layer, scheme):
+    """Codes and scales bit-exact; stored witness bit-exact and bracketing the float64 norm."""
+    S = ref.length(layer)
+    kc = gpu.export(layer, _lib.X_K_CODES).cpu().numpy()
+    vc = gpu.export(layer, _lib.X_V_CODES).cpu().numpy()
+    if scheme == "int8_dither":
+        np.testing.assert_array_equal(kc.view(np.int8).astype(np.int16), ref.kcode[layer])
+        np.testing.assert_array_equal(vc.view(np.int8).astype(np.int16), ref.vcode[layer])
+        ks = gpu.export(layer, _lib.X_K_SCALES).cpu().numpy()
+        vs = gpu.export(layer, _lib.X_V_SCALES).cpu().numpy()
+        np.testing.assert_array_equal(ks.view(np.uint16), ref.kscale[layer].view(np.uint16))
+        np.testing.assert_array_equal(vs.view(np.uint16), ref.vscale[layer].view(np.uint16))
+    elif scheme == "fp8_e4m3":
+        np.testing.assert_array_equal(kc.astype(np.int16), ref.kcode[layer])
+        np.testing.assert_array_equal(vc.astype(np.int16), ref.vcode[layer])
+    else:
+        full = (S // 16) * 16
+        np.testing.assert_array_equal(kc[:, :full].astype(np.int16), ref.kcode[layer][:, :full])
+        np.testing.assert_array_equal(vc.astype(np.int16), ref.vcode[layer])
+        vs = gpu.export(layer, _lib.X_V_SCALES).cpu().numpy()
+        vz = gpu.export(layer, _lib.X_V_ZEROS).cpu().numpy()
+        np.testing.assert_array_equal(vs.view(np.uint16), ref.vscale[layer].view(np.uint16))
+        np.testing.assert_array_equal(vz.view(np.uint16), ref.vzero[layer].view(np.uint16))
+        ksc = gpu.export(layer, _lib.X_KIVI_K_SCALE).cpu().numpy()
+        kzr = gpu.export(layer, _lib.X_KIVI_K_ZERO).cpu().numpy()
+        for (i, h, b), (s, z) in ref.kivi_kp[layer].items():
+            np.testing.assert_array_equal(ksc[i, b, h].view(np.uint16), s.view(np.uint16))
+            np.testing.assert_array_equal(kzr[i, b, h].view(np.uint16), z.view(np.uint16))
+    w = gpu.export(layer, _lib.X_WITNESS).cpu().numpy()
+    np.testing.assert_array_equal(w.view(np.uint16), ref.w16[layer].view(np.uint16))
+    w64 = ref.w64[layer]
+    wg = w.astype(np.float64)
+    assert np.all(wg >= w64)
+    assert np.all(wg <= np.maximum(w64 * (1 + 1e-3), w64 + 2.0 ** -24))
+    return w
+
+
+def check_decode(gpu, ref, layer, q_host, w, delta_req, rel=METER_REL):
+    """Decode both sides on the same query; the oracle uses the GPU's stored witness."""
+    out, m = gpu.decode(layer, to_dev(q_host, w), delta_req)
+    ref.w16[layer] = gpu.export(layer, _lib.X_WITNESS).cpu().numpy()
+    r = ref.decode(layer, q_host, delta_req)
+    o = out.cpu().numpy().astype(np.float64)
+    g = ref.g
+    for i in range(ref.B):
+        for h in range(ref.Hkv):
+            vmax = np.abs(ref.v[layer][i, :, h]).max() if ref.length(layer) else 1.0
+            d = np.abs(o[i, h * g:(h + 1) * g] - r["out"][i, h * g:(h + 1) * g]).max()
+            assert d <= 2e-3 * vmax, f"out seq {i} head {h}: {d} > {2e-3 * vmax}"
+    check_meter(m["raw_a"].cpu().numpy(), r["raw_a"], rel, "raw_a")
+    check_meter(m["meter_a"].cpu().numpy(), r["meter_a"], rel, "meter_a")
+    if ref.scheme == "int8_dither":
+        check_meter(m["raw_b"].cpu().numpy(), r["raw_b"], rel, "raw_b")
+        check_meter(m["meter_b"].cpu().numpy(), r["meter_b"], rel, "meter_b")
+    else:
+        assert np.all(np.isnan(m["meter_b"].cpu().numpy()))
+    return out, m, r
+
+
+def oracle_group(w, layer, K, V, q, i, h, scheme, dloc, k_pos0=0):
+    """Oracle decode of one (sequence, KV head) group straight from K/V [S, d] (for sampled cells)."""
+    S = K.shape[0]
+    pos = np.arange(k_pos0, k_pos0 + S)
+    if scheme == "int8_dither":
+        _, ks, kh, _ = quant.write_int8_dither(K, dither(w.seed, layer, h, pos, 0))
+        _, _, vh, _ = quant.write_int8_dither(V, dither(w.seed, layer, h, pos, 1))
+        kscales = ks.astype(np.float64)
+    elif scheme == "fp8_e4m3":
+        _, kh = quant.write_fp8(K)
+        _, vh = quant.write_fp8(V)
+        kscales = None
+    else:
+        kh = K.astype(np.float64).copy()
+        for b in range(S // 16):
+            kh[16 * b:16 * b + 16] = quant.write_kivi2_k(K[16 * b:16 * b + 16])[3]
+        vh = quant.write_kivi2_v(V)[3]
+        kscales = None
+    wst = quant.witness_stored(quant.witness(K - kh)).astype(np.float64)
+    return meter.decode_ref(q, kh, vh, wst, kscales, None, dloc)

@@ -1,0 +1,187 @@
+"""GPU parity through the C ABI against the float64 oracle (needs a GB300)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_quantization_witcert_gb300 as wc
+from kv_cache_quantization_witcert_gb300 import _lib
+from oracle import meter
+from oracle.philox import dither
+from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload
+
+from gpu_helpers import check_decode, check_meter, check_write, make_pair, oracle_group, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    wc.load()
+
+
+def test_dither_stream_bit_exact():
+    for seed, layer, h, t0, tensor in [(0, 0, 0, 0, 0), (12345678901234, 27, 3, 4090, 1), (2 ** 64 - 1, 5, 7, 131000, 0)]:
+        g = wc.witcert_dither(seed, layer, h, t0, 40, tensor).cpu().numpy()
+        np.testing.assert_array_equal(g, dither(seed, layer, h, np.arange(t0, t0 + 40), tensor))
+
+
+@pytest.mark.parametrize("n_splits", [0, 1, 2, 8, 37])
+def test_tiny_write_and_metered_decode_with_appends(n_splits):
+    w = WORKLOADS["tiny"]
+    gpu, ref = make_pair(w, n_splits=n_splits)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    wst = check_write(gpu, ref, 0, w.scheme)
+    for step in range(w.steps):
+        check_decode(gpu, ref, 0, gen_q(w, 0, step), w, w.delta_req)
+        k1, v1 = gen_append_kv(w, 0, step)
+        gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
+        ref.write(0, k1, v1)
+    check_write(gpu, ref, 0, w.scheme)
+    check_decode(gpu, ref, 0, gen_q(w, 0, w.steps), w, w.delta_req)
+    st = gpu.witcert_stats()
+    assert st["int8_clamps"] == 0 and st["device_errors"] == 0
+
+
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+def test_qwen_shaped_bf16_ragged(scheme):
+    """28q/4kv, bf16, planted keys and x50 outliers; 3 sequences (a partial sequence group),
+    1000 tokens (several splits and a ragged 8-token tail), two steps with an append."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=1000, steps=2, scheme=scheme)
+    gpu, ref = make_pair(w)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    check_write(gpu, ref, 0, scheme)
+    check_decode(gpu, ref, 0, gen_q(w, 0, 0), w, w.delta_req)
+    k1, v1 = gen_append_kv(w, 0, 0)
+    gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
+    ref.write(0, k1, v1)
+    check_write(gpu, ref, 0, scheme)
+    check_decode(gpu, ref, 0, gen_q(w, 0, 1), w, 1e-3)
+
+
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+def test_kivi_and_all_schemes_across_block_boundaries(scheme):
+    """Appends one token at a time across two 16-token boundaries (KIVI closes blocks)."""
+    w = WORKLOADS["tiny"].with_(context=29, steps=20, scheme=scheme, batch=2)
+    gpu, ref = make_pair(w)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    for step in range(w.steps):
+        k1, v1 = gen_append_kv(w, 0, step)
+        gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
+        ref.write(0, k1, v1)
+        if step % 5 == 4:
+            check_write(gpu, ref, 0, scheme)
+            check_decode(gpu, ref, 0, gen_q(w, 0, step), w, w.delta_req)
+
+
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+def test_meter_off_output_is_bit_identical(scheme):
+    w = WORKLOADS["qwen_1l"].with_(batch=5, context=700, scheme=scheme)
+    gpu, _ = make_pair(w)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    q = to_dev(gen_q(w, 0, 0), w)
+    on, _ = gpu.decode(0, q, w.delta_req, meters=True)
+    off, _ = gpu.decode(0, q, w.delta_req, meters=False)
+    assert torch.equal(on, off)
+
+
+def test_split_invariance_on_gpu():
+    w = WORKLOADS["qwen_1l"].with_(batch=2, context=2000)
+    K, V = gen_kv(w, 0)
+    q = gen_q(w, 0, 0)
+    outs = []
+    for ns in (1, 2, 8, 37):
+        gpu, _ = make_pair(w, n_splits=ns)
+        gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+        outs.append(gpu.decode(0, to_dev(q, w), w.delta_req))
+    for o, m in outs[1:]:
+        np.testing.assert_allclose(o.cpu().numpy(), outs[0][0].cpu().numpy(), atol=2e-5, rtol=0)
+        for k in ("raw_a", "raw_b"):
+            np.testing.assert_allclose(m[k].cpu().numpy(), outs[0][1][k].cpu().numpy(), rtol=2e-5)
+
+
+def test_empty_layer_decodes_to_zero():
+    w = WORKLOADS["tiny"]
+    gpu, _ = make_pair(w)
+    out, m = gpu.decode(0, to_dev(gen_q(w, 0, 0), w), w.delta_req)
+    assert torch.count_nonzero(out) == 0
+    assert torch.count_nonzero(m["meter_a"]) == 0 and torch.count_nonzero(m["meter_b"]) == 0
+
+
+def test_gate_decisions_bit_exact_and_repaired_decode():
+    """Raw-cast FP8: the oracle's gate, fed the GPU's block risks, picks exactly the blocks the
+    GPU pages in; the next decode matches the oracle on the repaired cache."""
+    w = WORKLOADS["qwen_1l"].with_(batch=2, context=400, steps=3, scheme="fp8_e4m3")
+    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    for step, tau in enumerate((0.5, 0.2, 0.05)):
+        q = gen_q(w, 0, step)
+        check_decode(gpu, ref, 0, q, w, w.delta_req)
+        risk = gpu.export(0, _lib.X_BLOCK_RISK).cpu().numpy()
+        gpu.witcert_gate(0, tau)
+        picked = ref.gate(0, tau, risk)
+        slots = gpu.export(0, _lib.X_SLOTS).cpu().numpy()
+        np.testing.assert_array_equal(slots >= 0, ref.repaired[0])
+        assert len(picked) == len(set(picked))
+    check_decode(gpu, ref, 0, gen_q(w, 0, 9), w, w.delta_req)
+    st = gpu.witcert_gate_stats()
+    assert st["blocks_paged_in"] == int(ref.repaired[0].sum()) > 0
+    assert st["bytes_paged_in"] == st["blocks_paged_in"] * 16 * 128 * 2
+    # appends into a repaired partial block keep the exact pool row in step
+    k1, v1 = gen_append_kv(w, 0, 0)
+    gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
+    ref.write(0, k1, v1)
+    check_decode(gpu, ref, 0, gen_q(w, 0, 10), w, w.delta_req)
+
+
+@pytest.mark.parametrize("delta_req", [1e-2, 1e-3])
+def test_full_28_layer_config_sampled_cells(delta_req):
+    """Full-size Qwen decode shape (B=16 x 4096, 28q/4kv, 8 KV splits), two of its layers
+    written and decoded in the bench's launch configuration; sampled (seq, KV head) groups
+    are checked against the oracle computed for those groups alone."""
+    w = WORKLOADS["qwen_28l"].with_(n_layers=28, steps=64)
+    gpu, _ = make_pair(w, extra_tokens=1)
+    dl = meter.delta_loc(delta_req, w.n_layers, w.n_q_heads, w.steps)
+    for layer in (0, 27):
+        K, V = gen_kv(w, layer)
+        gpu.witcert_write(layer, to_dev(K, w), to_dev(V, w))
+        q = gen_q(w, layer, 0)
+        out, m = gpu.decode(layer, to_dev(q, w), delta_req)
+        o = out.cpu().numpy()
+        for i, h in [(0, 0), (7, 3), (15, 1)]:
+            js = slice(h * w.group, (h + 1) * w.group)
+            r = oracle_group(w, layer, K[i, :, h], V[i, :, h], q[i, js], i, h, w.scheme, dl)
+            assert np.abs(o[i, js] - r["out"]).max() <= 2e-3 * np.abs(V[i, :, h]).max()
+            check_meter(m["raw_a"].cpu().numpy()[i, js], r["raw_a"], what="raw_a")
+            check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what="raw_b")
+
+
+def test_errors_are_reported_not_raised_on_device():
+    w = WORKLOADS["tiny"]
+    gpu, _ = make_pair(w)
+    K, V = gen_kv(w, 0)
+    with pytest.raises(wc.WitcertError) as e:
+        big = np.concatenate([K] * 2, 1)
+        gpu.witcert_write(0, to_dev(big, w), to_dev(big, w))
+    assert e.value.status == _lib.EINVAL and "capacity" in str(e.value)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    with pytest.raises(wc.WitcertError) as e:
+        gpu.decode(0, to_dev(gen_q(w, 0, 0), w), 0.0)
+    assert e.value.status == _lib.EINVAL
+    with pytest.raises(wc.WitcertError) as e:
+        gpu.witcert_gate(0, 1.0)
+    assert e.value.status == _lib.ESTATE
+    assert gpu.witcert_stats()["device_errors"] == 0
