@@ -105,8 +105,12 @@ def test_split_invariance_on_gpu():
         gpu, _ = make_pair(w, n_splits=ns)
         gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
         outs.append(gpu.decode(0, to_dev(q, w), w.delta_req))
+    # P enters the P.V product as fp16 relative to each split's running max, so outputs of
+    # different split counts agree to the output bar (2e-3 max|V|), not bitwise; meters are
+    # summed in fp32 and agree far inside their 1e-4 bar
+    vmax = np.abs(V).max()
     for o, m in outs[1:]:
-        np.testing.assert_allclose(o.cpu().numpy(), outs[0][0].cpu().numpy(), atol=2e-5, rtol=0)
+        np.testing.assert_allclose(o.cpu().numpy(), outs[0][0].cpu().numpy(), atol=2e-3 * vmax, rtol=0)
         for k in ("raw_a", "raw_b"):
             np.testing.assert_allclose(m[k].cpu().numpy(), outs[0][1][k].cpu().numpy(), rtol=2e-5)
 
