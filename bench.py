@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--scheme", default=None)
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     return ap.parse_args()
 
 
@@ -369,6 +370,8 @@ def run_ours(args, w):
 def main():
     args = parse()
     w = workload_of(args.workload, args.scheme)
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, w)
     else:

@@ -151,13 +151,14 @@ def test_gate_decisions_bit_exact_and_repaired_decode():
     check_decode(gpu, ref, 0, gen_q(w, 0, 10), w, w.delta_req)
 
 
-@pytest.mark.parametrize("delta_req", [1e-2, 1e-3])
-def test_full_28_layer_config_sampled_cells(delta_req):
-    """Full-size Qwen decode shape (B=16 x 4096, 28q/4kv, 8 KV splits), two of its layers
-    written and decoded in the bench's launch configuration; sampled (seq, KV head) groups
-    are checked against the oracle computed for those groups alone."""
+@pytest.mark.parametrize("delta_req,n_splits", [(1e-2, 8), (1e-3, 0)])
+def test_full_28_layer_config_sampled_cells(delta_req, n_splits):
+    """Full-size Qwen decode shape (B=16 x 4096, 28q/4kv), two of its 28 layers written and
+    decoded with the configured 8 KV splits and with the automatic split count the bench
+    uses; sampled (seq, KV head) groups are checked against the oracle computed for those
+    groups alone."""
     w = WORKLOADS["qwen_28l"].with_(n_layers=28, steps=64)
-    gpu, _ = make_pair(w, extra_tokens=1)
+    gpu, _ = make_pair(w, n_splits=n_splits, extra_tokens=1)
     dl = meter.delta_loc(delta_req, w.n_layers, w.n_q_heads, w.steps)
     for layer in (0, 27):
         K, V = gen_kv(w, layer)
