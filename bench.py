@@ -227,7 +227,7 @@ def run_ours(args, w):
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     total = args.warmup + args.steps
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, args.steps // 2)
-    n_app = total + e2e_steps + 1
+    n_app = total + args.steps + e2e_steps + 1
     cache = wc.Cache(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.batch, wl.context + n_app, wl.scheme,
                      dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0)
     stream = torch.cuda.current_stream()
@@ -280,7 +280,6 @@ def run_ours(args, w):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    cache.witcert_set_profiling(True)
     s_len0 = cache.witcert_length(0)
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -290,6 +289,13 @@ def run_ours(args, w):
     ev1.record(stream)
     barrier()
     ms = ev0.elapsed_time(ev1)
+    # second pass of the same K steps with CUDA events around every decode split kernel
+    # (the events sit on the launching stream; they also break the launch overlap, so the
+    # step time above comes from the pass without them)
+    cache.witcert_set_profiling(True)
+    prof_len0 = cache.witcert_length(0)
+    for s in range(args.steps):
+        one_step(dev_inputs[(args.warmup + args.steps + s) % 8])
     st = cache.witcert_stats()
     cache.witcert_set_profiling(False)
     clk = clocks.stop()
@@ -307,7 +313,7 @@ def run_ours(args, w):
     # roofline of the dominant kernel (decode split kernel), timed by the library's events
     n_launch = st["decode_kernel_launches"]
     avg_ms = st["decode_kernel_ms"] / max(1, n_launch)
-    avg_S = s_len0 + 1 + (args.steps - 1) / 2.0
+    avg_S = prof_len0 + 1 + (args.steps - 1) / 2.0
     alg_bytes = wl.batch * wl.n_kv_heads * avg_S * BYTES_PER_TOK_HEAD[wl.scheme]
     achieved = alg_bytes / (avg_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
@@ -353,7 +359,8 @@ def run_ours(args, w):
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                              "kernel": "decode_split_kernel", "avg_launch_ms": avg_ms, "launches": n_launch,
-                             "alg_bytes_per_launch": alg_bytes},
+                             "alg_bytes_per_launch": alg_bytes,
+                             "timing": "CUDA events around each decode split launch over a second pass of the K steps"},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},

@@ -107,6 +107,41 @@ __device__ __forceinline__ float4 dither4(uint64_t seed, int layer, int kvh, int
   return make_float4(xi_from_word(u.x), xi_from_word(u.y), xi_from_word(u.z), xi_from_word(u.w));
 }
 
+// Philox with the ten round keys precomputed (k0 + r*0x9E3779B9, k1 + r*0xBB67AE85):
+// the keys sit in kernel parameters and enter the XORs as constant operands.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ rk0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ rk1[r], (uint32_t)p0);
+  }
+  return c;
+}
+__device__ __forceinline__ float4 dither4_rk(const uint32_t (&rk0)[10], const uint32_t (&rk1)[10], int layer, int kvh,
+                                             int t, int quad, int tensor) {
+  const uint4 u = philox4x32_10_rk(make_uint4((uint32_t)t, (uint32_t)quad | ((uint32_t)tensor << 16),
+                                              (uint32_t)kvh | ((uint32_t)layer << 16), 0u), rk0, rk1);
+  return make_float4(xi_from_word(u.x), xi_from_word(u.y), xi_from_word(u.z), xi_from_word(u.w));
+}
+
+// 2^x on the special-function unit (relative error about 2^-22; -inf -> +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rsqrt_approx(float x) {
+  float y;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Programmatic dependent launch: wait for the preceding kernel on the stream (its
+// memory is then visible), then let the next kernel start its own prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------------ tensor-core product
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
   asm volatile(

@@ -20,6 +20,11 @@
 // accumulators S_X = sum e^(l - m) expm1(c_X) run on the CUDA cores.  The TV
 // aggregation min(1, (A^2-1)/2) with A = 1 + S_X/Z [WitCert summary,
 // improvements list] is applied after the merge.
+//
+// Launches chain through programmatic dependent launch: a kernel waits for its
+// predecessor on the stream before touching memory that predecessor may write,
+// then lets its own successor begin (the dither of the first block, which
+// depends on no memory, is generated before that wait).
 #include <cfloat>
 #include <cmath>
 
@@ -33,8 +38,8 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kXiKHi = 0, kXiKLo = 4096, kXiV = 8192, kXiBytes = 12288;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
-// Upward bias applied to every meter sum: covers the fp32 / tensor-core
-// rounding of the logits and exponentials relative to exact arithmetic.
+// Upward bias applied to every meter sum: covers the fp32 / tensor-core / SFU
+// rounding of the logits, exponentials and square roots relative to exact arithmetic.
 constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
 
 template <int SCHEME> struct Lay;
@@ -42,7 +47,11 @@ template <> struct Lay<kInt8> : Int8Layout {};
 template <> struct Lay<kFp8> : Fp8Layout {};
 template <> struct Lay<kKivi> : KiviLayout {};
 
-template <int NW, int NST, int SCHEME> struct Smem {
+template <int NW> struct Stages { static constexpr int value = NW >= 8 ? 2 : NW == 4 ? 3 : 4; };
+template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : 2; };
+
+template <int NW, int SCHEME> struct Smem {
+  static constexpr int NST = Stages<NW>::value;
   static constexpr int kRing = NW * NST * Lay<SCHEME>::BYTES;
   static constexpr int kXi = SCHEME == kInt8 ? 2 * kXiBytes : 0;
   static constexpr int kRingOff = 0;
@@ -53,39 +62,58 @@ template <int NW, int NST, int SCHEME> struct Smem {
   static constexpr int kBytes = kBarOff + NW * NST * 8;
 };
 
-// term p * expm1(c) without overflow for large c (there e^c - 1 ~ e^c; the
-// product is then formed in the exponent).  l2 is the logit in log2 units.
+// expm1(c) for c >= 0: Taylor-Horner below 1/2 (truncation < 1e-8 relative), e^c - 1 above.
+__device__ __forceinline__ float expm1_fast(float c) {
+  float s = fmaf(c, 1.0f / 8.0f, 1.0f);
+  s = fmaf(c * (1.0f / 7.0f), s, 1.0f);
+  s = fmaf(c * (1.0f / 6.0f), s, 1.0f);
+  s = fmaf(c * (1.0f / 5.0f), s, 1.0f);
+  s = fmaf(c * 0.25f, s, 1.0f);
+  s = fmaf(c * (1.0f / 3.0f), s, 1.0f);
+  s = fmaf(c * 0.5f, s, 1.0f);
+  const float big = ex2(c * kLog2e) - 1.0f;
+  return c < 0.5f ? c * s : big;
+}
+// p * expm1(c) without overflow for large c (there e^c - 1 ~ e^c and the product is
+// formed in the exponent).  l2, m2 are the logit and running max in log2 units.
 __device__ __forceinline__ float meter_term(float pe, float l2, float m2, float c) {
-  if (pe == 0.0f || c <= 0.0f) return 0.0f;
-  if (c > 20.0f) return exp2f(l2 - m2 + c * kLog2e);
-  return pe * expm1_pos(c);
+  const float t = c > 20.0f ? ex2(l2 - m2 + c * kLog2e) : pe * expm1_fast(c);
+  return pe > 0.0f && c > 0.0f ? t : 0.0f;
 }
 
 // Regenerate the dither of block `blk` of KV head h into shared memory, in the
-// fragment order of the QK (negated, fp16 hi + lo) and PV (fp16) operands.
-__device__ void gen_xi(uint8_t* xb, uint64_t seed, int layer, int h, int blk, int nthreads) {
-  for (int idx = threadIdx.x; idx < 1024; idx += nthreads) {
-    const int tensor = idx >> 9, r = (idx >> 5) & 15, quad = idx & 31;
-    const float4 x = dither4(seed, layer, h, blk * kBlk + r, quad, tensor);
+// fragment order of the QK operands (negated, fp16 hi + lo; per lane the four
+// registers are stored as R0, R2, R1, R3) and of the PV operand (fp16).
+// Work item = (tensor, column of 4 channels, pair of tokens); a warp's 32 items
+// cover 8 token pairs x 4 quads, which keeps the stores free of bank conflicts.
+__device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
+  for (int idx = threadIdx.x; idx < 512; idx += nthreads) {
+    const int tq = idx & 3, rp = (idx >> 2) & 7, kq = (idx >> 5) & 7, tensor = idx >> 8;
+    const int quad = kq * 4 + tq;
+    const int r0 = 2 * rp;
+    const float4 x0 = dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0, quad, tensor);
+    const float4 x1 = dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0 + 1, quad, tensor);
     if (tensor == 0) {
-      const int kk = quad >> 2, tq = quad & 3, gg = r & 7, hh = r >> 3;
-      const int L = 4 * gg + tq;
-      __half h0, l0, h1, l1, h2, l2, h3, l3;
-      split_h(-x.x, h0, l0); split_h(-x.y, h1, l1); split_h(-x.z, h2, l2); split_h(-x.w, h3, l3);
-      uint32_t* hi = reinterpret_cast<uint32_t*>(xb + kXiKHi + (kk * 32 + L) * 16);
-      uint32_t* lo = reinterpret_cast<uint32_t*>(xb + kXiKLo + (kk * 32 + L) * 16);
-      hi[hh] = pack_h2(h0, h1); hi[2 + hh] = pack_h2(h2, h3);
-      lo[hh] = pack_h2(l0, l1); lo[2 + hh] = pack_h2(l2, l3);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float4 x = u ? x1 : x0;
+        const int r = r0 + u, L = 4 * (r & 7) + tq, hh = r >> 3;
+        __half h0, l0, h1, l1, h2, l2, h3, l3;
+        split_h(-x.x, h0, l0); split_h(-x.y, h1, l1); split_h(-x.z, h2, l2); split_h(-x.w, h3, l3);
+        const int off = (kq * 32 + L) * 16 + hh * 8;
+        *reinterpret_cast<uint2*>(xb + kXiKHi + off) = make_uint2(pack_h2(h0, h1), pack_h2(h2, h3));
+        *reinterpret_cast<uint2*>(xb + kXiKLo + off) = make_uint2(pack_h2(l0, l1), pack_h2(l2, l3));
+      }
     } else {
-      __half* v = reinterpret_cast<__half*>(xb + kXiV);
-      const float xs[4] = {x.x, x.y, x.z, x.w};
-      const int tq = r >> 2, er = r & 3;
+      const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
+      const int tv = r0 >> 2, reg_hi = 2 * ((r0 & 3) >> 1);
+      uint32_t* v = reinterpret_cast<uint32_t*>(xb + kXiV);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = 4 * quad + e;
-        const int mt = c >> 4, gg = c & 7, hh = (c >> 3) & 1;
-        const int L = 4 * gg + tq, reg = hh + 2 * (er >> 1);
-        v[((mt * 32 + L) * 4 + reg) * 2 + (er & 1)] = __float2half_rn(xs[e]);
+        const int gg = c & 7, hh = (c >> 3) & 1;
+        const int L = 4 * gg + tv, reg = hh + reg_hi;
+        v[(kq * 32 + L) * 4 + reg] = pack_h2(__float2half_rn(a0[e]), __float2half_rn(a1[e]));
       }
     }
   }
@@ -123,10 +151,11 @@ __device__ __forceinline__ void exact_block_logits(const KT* ex, const uint32_t 
   }
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs p) {
+template <int SCHEME, typename QT, bool METER, bool RISK, int NW>
+__global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_kernel(const DecodeArgs p) {
   using L = Lay<SCHEME>;
-  using SM = Smem<NW, NST, SCHEME>;
+  using SM = Smem<NW, SCHEME>;
+  constexpr int NST = SM::NST;
   constexpr bool QLO = sizeof(QT) == 4;          // fp32 queries carry an fp16 low piece
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -134,7 +163,7 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
   const int g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, h = blockIdx.y;
   const int i = blockIdx.z * p.seqs_per_cta + warp;
-  bool active = warp < p.seqs_per_cta && i < p.B;
+  const bool active = warp < p.seqs_per_cta && i < p.B;
   const int grp = p.grp, j0 = h * grp;
   const int nblk = (p.S + kBlk - 1) / kBlk;
   const int b_begin = (int)(((long long)split * nblk) / p.n_splits);
@@ -150,10 +179,17 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
   const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
   const uint8_t* src = p.blocks + (seq_base + b_begin) * L::BYTES;
 
-  // ---------------------------------------------------------------- pipeline prologue
+  // ---------------------------------------------------------------- prologue independent of memory
   if (active && lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
+
+  pdl_wait();
+  pdl_trigger();
+
+  if (active && lane == 0) {
     fence_proxy_async();
     for (int s = 0; s < NST && s < nb; ++s) {
       mbar_expect_tx(smem_addr(&bars[s]), L::BYTES);
@@ -228,18 +264,17 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
   for (int mt = 0; mt < 8; ++mt) acco[mt][0] = acco[mt][1] = acco[mt][2] = acco[mt][3] = 0.f;
   float zc[4] = {0.f, 0.f, 0.f, 0.f};           // KIVI: sum_t p_t zero_{t,G} for head g
   const float lscale = __fdiv_rn(kLog2e, sqrtf(128.0f));
+  // Tier B: u = kappa * sqrt(var); the SFU square root is within 2^-21 relative, covered by this factor
+  const float kappa_up = p.kappa * (1.0f + 9.5367431640625e-7f);
 
-  if (SCHEME == kInt8) {
-    if (nb > 0) gen_xi(xib, p.seed, p.layer, h, b_begin, NW * 32);
-    __syncthreads();
-  }
+  if (SCHEME == kInt8) __syncthreads();
 
   bool fault = false;
   for (int n = 0; n < nb; ++n) {
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
-    uint8_t* xb = xib + (n & 1) * kXiBytes;
-    if (SCHEME == kInt8 && n + 1 < nb) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p.seed, p.layer, h, blk + 1, NW * 32);
+    const uint8_t* xb = xib + (n & 1) * kXiBytes;
+    if (SCHEME == kInt8 && n + 1 < nb) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
 
     if (active && !fault) {
       if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs)) {
@@ -252,7 +287,6 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
       const int slot = p.slots ? p.slots[seq_base + blk] : -1;
       const bool kivi_tail = SCHEME == kKivi && (blk + 1) * kBlk > p.S;
       float lg[4], eps[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
-      float kvs_g[4], kvs_g8[4];      // INT8 K scales of tokens g and g+8
 
       if (slot >= 0 || kivi_tail) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -277,8 +311,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
             if (QLO) mma16816(acc[G], a, qbl[kk]);
             const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
             const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
-            const uint32_t ah[4] = {xh.x, xh.y, xh.z, xh.w};
-            const uint32_t al[4] = {xl.x, xl.y, xl.z, xl.w};
+            const uint32_t ah[4] = {xh.x, xh.z, xh.y, xh.w};     // stored as R0, R2, R1, R3
+            const uint32_t al[4] = {xl.x, xl.z, xl.y, xl.w};
             mma16816(acc[G], ah, qb[kk]);
             mma16816(acc[G], al, qb[kk]);
             if (QLO) mma16816(acc[G], ah, qbl[kk]);
@@ -288,8 +322,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
         const uint2 s0 = *reinterpret_cast<const uint2*>(ks + g * 4);
         const uint2 s1 = *reinterpret_cast<const uint2*>(ks + (g + 8) * 4);
         const __half2 a01 = bits_h2(s0.x), a23 = bits_h2(s0.y), b01 = bits_h2(s1.x), b23 = bits_h2(s1.y);
-        kvs_g[0] = __low2float(a01); kvs_g[1] = __high2float(a01); kvs_g[2] = __low2float(a23); kvs_g[3] = __high2float(a23);
-        kvs_g8[0] = __low2float(b01); kvs_g8[1] = __high2float(b01); kvs_g8[2] = __low2float(b23); kvs_g8[3] = __high2float(b23);
+        const float kvs_g[4] = {__low2float(a01), __high2float(a01), __low2float(a23), __high2float(a23)};
+        const float kvs_g8[4] = {__low2float(b01), __high2float(b01), __low2float(b23), __high2float(b23)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float* sc = e < 2 ? kvs_g : kvs_g8;
@@ -305,8 +339,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
             const float* qg = qg2[e & 1];
             float var = 0.f;
 #pragma unroll
-            for (int G = 0; G < 4; ++G) var = __fmaf_ru(__fmul_ru(sc[G], sc[G]), qg[G], var);
-            ub[e] = __fmul_ru(p.kappa, __fsqrt_ru(var));
+            for (int G = 0; G < 4; ++G) var = __fmaf_ru(sc[G] * sc[G], qg[G], var);
+            ub[e] = var > 0.f ? kappa_up * (var * rsqrt_approx(var)) : 0.f;
           }
         }
       } else if constexpr (SCHEME == kFp8) {
@@ -356,8 +390,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
         }
         zq += __shfl_xor_sync(0xffffffffu, zq, 1);
         zq += __shfl_xor_sync(0xffffffffu, zq, 2);      // lanes 4g..4g+3 hold q_g . zero
-        const float zq0 = __shfl_sync(0xffffffffu, zq, 4 * ((2 * t) & 7));
-        const float zq1 = __shfl_sync(0xffffffffu, zq, 4 * ((2 * t + 1) & 7));
+        const float zq0 = __shfl_sync(0xffffffffu, zq, 8 * t);
+        const float zq1 = __shfl_sync(0xffffffffu, zq, 8 * t + 4);
         lg[0] = (acc[0] + zq0) * lscale; lg[1] = (acc[1] + zq1) * lscale;
         lg[2] = (acc[2] + zq0) * lscale; lg[3] = (acc[3] + zq1) * lscale;
       }
@@ -384,13 +418,13 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
         bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
       }
       const float mn0 = fmaxf(m2[0], bm0), mn1 = fmaxf(m2[1], bm1);
-      const float sc0 = mn0 == -INFINITY ? 1.f : exp2f(m2[0] - mn0);
-      const float sc1 = mn1 == -INFINITY ? 1.f : exp2f(m2[1] - mn1);
+      const float sc0 = mn0 == -INFINITY ? 1.f : ex2(m2[0] - mn0);
+      const float sc1 = mn1 == -INFINITY ? 1.f : ex2(m2[1] - mn1);
       float pe[4];
-      pe[0] = lg[0] == -INFINITY ? 0.f : exp2f(lg[0] - mn0);
-      pe[1] = lg[1] == -INFINITY ? 0.f : exp2f(lg[1] - mn1);
-      pe[2] = lg[2] == -INFINITY ? 0.f : exp2f(lg[2] - mn0);
-      pe[3] = lg[3] == -INFINITY ? 0.f : exp2f(lg[3] - mn1);
+      pe[0] = ex2(lg[0] - mn0);
+      pe[1] = ex2(lg[1] - mn1);
+      pe[2] = ex2(lg[2] - mn0);
+      pe[3] = ex2(lg[3] - mn1);
       Zp[0] = fmaf(Zp[0], sc0, pe[0] + pe[2]);
       Zp[1] = fmaf(Zp[1], sc1, pe[1] + pe[3]);
       if (METER) {
@@ -420,8 +454,10 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
         }
       }
       m2[0] = mn0; m2[1] = mn1;
+      if (__any_sync(0xffffffffu, sc0 != 1.f || sc1 != 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) { acco[mt][0] *= sc0; acco[mt][1] *= sc1; acco[mt][2] *= sc0; acco[mt][3] *= sc1; }
+        for (int mt = 0; mt < 8; ++mt) { acco[mt][0] *= sc0; acco[mt][1] *= sc1; acco[mt][2] *= sc0; acco[mt][3] *= sc1; }
+      }
 
       // ------------------------------------------------------------ P V
       psm[(2 * t) * 16 + g] = pe[0];
@@ -536,8 +572,8 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
     float z0[4], z1[4];
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
-      z0[G] = __shfl_sync(0xffffffffu, zc[G], 4 * ((2 * t) & 7));
-      z1[G] = __shfl_sync(0xffffffffu, zc[G], 4 * ((2 * t + 1) & 7));
+      z0[G] = __shfl_sync(0xffffffffu, zc[G], 8 * t);
+      z1[G] = __shfl_sync(0xffffffffu, zc[G], 8 * t + 4);
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -562,22 +598,39 @@ __global__ void __launch_bounds__(NW * 32) decode_split_kernel(const DecodeArgs 
 // One warp per (sequence, query head): merge the splits, normalize, finish the meters.
 template <bool INT8, bool RISK>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
+  pdl_wait();
+  pdl_trigger();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.B * p.Hq) return;
   const float* recs = p.part + (size_t)wid * p.n_splits * kPartStride;
+  const int ns = p.n_splits;
+  // scalars: lanes across splits
   float M = -INFINITY;
-  for (int s = lane; s < p.n_splits; s += 32) M = fmaxf(M, recs[(size_t)s * kPartStride]);
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, recs[(size_t)s * kPartStride]);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float Z = 0.f, SA = 0.f, SB = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    for (int s = 0; s < p.n_splits; ++s) {
+    for (int s = lane; s < ns; s += 32) {
       const float* r = recs + (size_t)s * kPartStride;
       const float ms = r[0];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
+      const float f = ms == -INFINITY ? 0.f : ex2(ms - M);
       Z = fmaf(f, r[1], Z); SA = fmaf(f, r[2], SA); SB = fmaf(f, r[3], SB);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    Z += __shfl_xor_sync(0xffffffffu, Z, o);
+    SA += __shfl_xor_sync(0xffffffffu, SA, o);
+    SB += __shfl_xor_sync(0xffffffffu, SB, o);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) {
+      const float* r = recs + (size_t)s * kPartStride;
+      const float ms = r[0];
+      const float f = ms == -INFINITY ? 0.f : ex2(ms - M);
       const float4 a = *reinterpret_cast<const float4*>(r + 4 + 4 * lane);
       acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
     }
@@ -605,52 +658,67 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
     float* ro = p.risk + (size_t)wid * p.nblk_max;
     for (int b = lane; b < nblk; b += 32) {
       const float2 v = rr[b];
-      ro[b] = (v.y == 0.f || Z == 0.f) ? 0.f : v.y * exp2f(v.x - M) * inv;
+      ro[b] = (v.y == 0.f || Z == 0.f) ? 0.f : v.y * ex2(v.x - M) * inv;
     }
   }
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, int NW, int NST>
-cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
-  using SM = Smem<NW, NST, SCHEME>;
-  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, NW, NST>;
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int SCHEME, typename QT, bool METER, bool RISK, int NW>
+cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
+  using SM = Smem<NW, SCHEME>;
+  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, NW>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (e != cudaSuccess) return e;
-  k<<<grid, NW * 32, SM::kBytes, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(NW * 32), SM::kBytes, st, pdl, a);
 }
 
 template <int SCHEME, typename QT, bool METER, bool RISK>
-cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   switch (a.seqs_per_cta) {
-    case 1: return run_split<SCHEME, QT, METER, RISK, 1, 4>(a, grid, st);
-    case 2: return run_split<SCHEME, QT, METER, RISK, 2, 4>(a, grid, st);
-    case 4: return run_split<SCHEME, QT, METER, RISK, 4, 3>(a, grid, st);
-    default: return run_split<SCHEME, QT, METER, RISK, 8, 3>(a, grid, st);
+    case 1: return run_split<SCHEME, QT, METER, RISK, 1>(a, grid, st, pdl);
+    case 2: return run_split<SCHEME, QT, METER, RISK, 2>(a, grid, st, pdl);
+    case 4: return run_split<SCHEME, QT, METER, RISK, 4>(a, grid, st, pdl);
+    case 8: return run_split<SCHEME, QT, METER, RISK, 8>(a, grid, st, pdl);
+    default: return run_split<SCHEME, QT, METER, RISK, 16>(a, grid, st, pdl);
   }
 }
 
 template <int SCHEME>
-cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st) {
+cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   const bool risk = a.risk_raw != nullptr;
   if (a.is_bf16) {
-    if (!a.meter) return dispatch_nw<SCHEME, __nv_bfloat16, false, false>(a, grid, st);
-    return risk ? dispatch_nw<SCHEME, __nv_bfloat16, true, true>(a, grid, st)
-                : dispatch_nw<SCHEME, __nv_bfloat16, true, false>(a, grid, st);
+    if (!a.meter) return dispatch_nw<SCHEME, __nv_bfloat16, false, false>(a, grid, st, pdl);
+    return risk ? dispatch_nw<SCHEME, __nv_bfloat16, true, true>(a, grid, st, pdl)
+                : dispatch_nw<SCHEME, __nv_bfloat16, true, false>(a, grid, st, pdl);
   }
-  if (!a.meter) return dispatch_nw<SCHEME, float, false, false>(a, grid, st);
-  return risk ? dispatch_nw<SCHEME, float, true, true>(a, grid, st)
-              : dispatch_nw<SCHEME, float, true, false>(a, grid, st);
+  if (!a.meter) return dispatch_nw<SCHEME, float, false, false>(a, grid, st, pdl);
+  return risk ? dispatch_nw<SCHEME, float, true, true>(a, grid, st, pdl)
+              : dispatch_nw<SCHEME, float, true, false>(a, grid, st, pdl);
 }
 
-int seqs_per_cta_for(int B) { return B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
+int seqs_per_cta_for(int B) { return B >= 16 ? 16 : B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
 
 }  // namespace
 
 int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count) {
   const int spc = seqs_per_cta_for(B);
   const int groups = (B + spc - 1) / spc;
-  const int per_sm = spc >= 8 ? 1 : spc >= 4 ? 2 : 4;
+  const int per_sm = spc >= 16 ? 1 : spc >= 8 ? 2 : spc >= 4 ? 3 : 4;
   const int target = sm_count * per_sm;
   int s = (target + Hkv * groups - 1) / (Hkv * groups);
   if (s > nblk) s = nblk;
@@ -666,23 +734,23 @@ cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaSt
   a.seqs_per_cta = seqs_per_cta_for(a.B);
   const int groups = (a.B + a.seqs_per_cta - 1) / a.seqs_per_cta;
   dim3 grid(a.n_splits, a.Hkv, groups);
+  const bool pdl = split_start == nullptr;      // event boundaries around a timed split break the overlap anyway
   if (split_start) cudaEventRecord(split_start, st);
-  cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, st)
-                  : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, st)
-                                   : dispatch_flags<kKivi>(a, grid, st);
+  cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, st, pdl)
+                  : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, st, pdl)
+                                   : dispatch_flags<kKivi>(a, grid, st, pdl);
   if (split_stop) cudaEventRecord(split_stop, st);
   if (e != cudaSuccess) return e;
   const int warps = a.B * a.Hq;
-  const int blocks = (warps * 32 + 127) / 128;
+  const dim3 mg((warps * 32 + 127) / 128);
   const bool risk = a.risk_raw != nullptr && a.meter;
-  if (scheme == kInt8) {
-    if (risk) decode_merge_kernel<true, true><<<blocks, 128, 0, st>>>(a);
-    else decode_merge_kernel<true, false><<<blocks, 128, 0, st>>>(a);
-  } else {
-    if (risk) decode_merge_kernel<false, true><<<blocks, 128, 0, st>>>(a);
-    else decode_merge_kernel<false, false><<<blocks, 128, 0, st>>>(a);
-  }
-  return cudaGetLastError();
+  if (scheme == kInt8)
+    e = risk ? launch_pdl(decode_merge_kernel<true, true>, mg, dim3(128), 0, st, true, a)
+             : launch_pdl(decode_merge_kernel<true, false>, mg, dim3(128), 0, st, true, a);
+  else
+    e = risk ? launch_pdl(decode_merge_kernel<false, true>, mg, dim3(128), 0, st, true, a)
+             : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(128), 0, st, true, a);
+  return e;
 }
 
 }  // namespace witcert

@@ -33,6 +33,7 @@ struct DecodeArgs {
   int is_bf16;
   int B, Hq, Hkv, grp, S, n_splits, seqs_per_cta;
   uint64_t seed;
+  uint32_t rk0[10], rk1[10]; // Philox round keys of `seed` (key words advanced by the Weyl increments)
   int layer;
   float kappa;               // sqrt(2 ln(2S/delta_loc)), rounded up (Tier B)
   float* part;               // [B][Hq][n_splits][kPartStride]
@@ -45,6 +46,9 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st);
+// Philox4x32-10 round keys of a 64-bit seed: key (seed mod 2^32, seed div 2^32) advanced
+// by 0x9E3779B9 / 0xBB67AE85 before every round but the first.
+void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]);
 // Split-KV decode + merge.  Returns the split kernel's launch error; `split_start`
 // and `split_stop` (optional) bracket the split kernel alone.
 cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStream_t st,

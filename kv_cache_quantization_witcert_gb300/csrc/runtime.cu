@@ -252,6 +252,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits
                                    : decode_auto_splits(c->scheme, a.B, a.Hkv, nblk > 0 ? nblk : 1, c->sm_count);
   a.seed = c->cfg.seed;
+  philox_round_keys(a.seed, a.rk0, a.rk1);
   a.layer = layer;
   float kappa = 0.f;
   if (meter && S > 0) {

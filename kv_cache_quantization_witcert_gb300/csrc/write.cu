@@ -77,6 +77,8 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
 
 template <typename T>
 __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.B * a.n_tok * a.Hkv) return;
   const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
 
 template <typename T>
 __global__ void __launch_bounds__(128) write_fp8_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.B * a.n_tok * a.Hkv) return;
   const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
@@ -167,6 +171,8 @@ __device__ __forceinline__ __half f16_sat_rn(float v) { return __float2half_rn(f
 // KIVI values (per token, per 32-channel group) + backing store of keys.
 template <typename T>
 __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.B * a.n_tok * a.Hkv) return;
   const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
@@ -198,6 +204,8 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
 // KIVI keys: one warp per (sequence, KV head) walks the blocks this write touches.
 template <typename T>
 __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int sh = blockIdx.x, lane = threadIdx.x;       // sh = i * Hkv + h
   const int i = sh / a.Hkv, h = sh % a.Hkv;
   __shared__ unsigned int img[128];                    // K code words of one block
@@ -263,20 +271,41 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
   }
 }
 
+template <typename K>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, const WriteArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <typename T>
 cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st) {
   const int warps = a.B * a.n_tok * a.Hkv;
-  const int blocks = (warps * 32 + 127) / 128;
-  if (scheme == kInt8) write_int8_kernel<T><<<blocks, 128, 0, st>>>(a);
-  else if (scheme == kFp8) write_fp8_kernel<T><<<blocks, 128, 0, st>>>(a);
-  else {
-    write_kivi_v_kernel<T><<<blocks, 128, 0, st>>>(a);
-    write_kivi_k_kernel<T><<<a.B * a.Hkv, 32, 0, st>>>(a);
-  }
-  return cudaGetLastError();
+  const dim3 blocks((warps * 32 + 127) / 128);
+  if (scheme == kInt8) return launch_pdl(write_int8_kernel<T>, blocks, dim3(128), st, a);
+  if (scheme == kFp8) return launch_pdl(write_fp8_kernel<T>, blocks, dim3(128), st, a);
+  cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv), dim3(32), st, a);
 }
 
 }  // namespace
+
+void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]) {
+  uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFull), k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    rk0[r] = k0;
+    rk1[r] = k1;
+  }
+}
 
 cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st) {
   if (a.B * a.n_tok * a.Hkv == 0) return cudaSuccess;
