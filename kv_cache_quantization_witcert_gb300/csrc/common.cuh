@@ -60,12 +60,17 @@ __host__ __device__ inline int vcode_off(int r, int c) {
   int L = 4 * g + t, j = mt >> 1, slot = ((mt & 1) << 1) | h;
   return j * 512 + L * 16 + slot * 4 + e;
 }
-// fp16 witness of token r, band b: A operand of the Tier A product (bands as k, identity map).
+// fp16 witness of token r, band b: A operand of the Tier A product (bands as k).
+// Lane t's k indices 2t, 2t+1, 2t+8, 2t+9 carry bands t, t+4, t+8, t+12: the bands
+// whose dims (4b..4b+3 and 64+4b..64+4b+3) sit in that lane's query fragment.
 __host__ __device__ inline int wit_off(int r, int b) {
-  int g = r & 7, h = r >> 3, t = (b & 7) >> 1, hi = b >> 3, e = b & 1;
+  int g = r & 7, h = r >> 3, t = b & 3, m = b >> 2, hi = m >> 1, e = m & 1;
   int L = 4 * g + t, reg = h + 2 * hi;
   return L * 16 + reg * 4 + e * 2;
 }
+// fp16 INT8 value scale of token r, group G: stored group-major so the four
+// tokens a lane needs for the P.V operand are adjacent.
+__host__ __device__ inline int vscale_off(int r, int G) { return (G * 16 + r) * 2; }
 // 2-bit KIVI codes: word (byte offset) and bit position.  Each 32-bit word holds
 // eight fp16x2 register pairs; pair p keeps its two codes at bits 2p and 16+2p.
 __host__ __device__ inline void kivi_k_pos(int r, int c, int& word_off, int& bit) {

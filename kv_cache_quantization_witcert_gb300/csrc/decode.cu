@@ -62,28 +62,19 @@ template <int NW, int SCHEME> struct Smem {
   static constexpr int kBytes = kBarOff + NW * NST * 8;
 };
 
-// expm1(c) for c >= 0: Taylor-Horner below 1/2 (truncation < 1e-8 relative), e^c - 1 above.
-__device__ __forceinline__ float expm1_fast(float c) {
-  float s = fmaf(c, 1.0f / 8.0f, 1.0f);
-  s = fmaf(c * (1.0f / 7.0f), s, 1.0f);
-  s = fmaf(c * (1.0f / 6.0f), s, 1.0f);
-  s = fmaf(c * (1.0f / 5.0f), s, 1.0f);
-  s = fmaf(c * 0.25f, s, 1.0f);
-  s = fmaf(c * (1.0f / 3.0f), s, 1.0f);
-  s = fmaf(c * 0.5f, s, 1.0f);
-  const float big = ex2(c * kLog2e) - 1.0f;
-  return c < 0.5f ? c * s : big;
-}
-// p * expm1(c) without overflow for large c (there e^c - 1 ~ e^c and the product is
-// formed in the exponent).  l2, m2 are the logit and running max in log2 units.
+// p * expm1(c) for c >= 0, with p = e^(l - m) (l2, m2 in log2 units).  Below c = 1/8 the
+// series c + c^2/2 + c^3/6 + c^4/24 (truncation < 2e-6 relative); above it the term is
+// formed in the exponent, e^(l - m + c) - e^(l - m), which neither overflows for large c
+// nor loses a flushed p, and cancels at most a factor e^c/(e^c - 1) < 8.6 of precision.
 __device__ __forceinline__ float meter_term(float pe, float l2, float m2, float c) {
-  const float t = c > 20.0f ? ex2(l2 - m2 + c * kLog2e) : pe * expm1_fast(c);
-  return pe > 0.0f && c > 0.0f ? t : 0.0f;
+  const float poly = c * fmaf(c, fmaf(c, fmaf(c, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+  const float big = ex2(fmaf(c, kLog2e, l2 - m2)) - pe;
+  return c < 0.125f ? pe * poly : big;
 }
 
 // Regenerate the dither of block `blk` of KV head h into shared memory, in the
 // fragment order of the QK operands (negated, fp16 hi + lo; per lane the four
-// registers are stored as R0, R2, R1, R3) and of the PV operand (fp16).
+// registers are stored as R0, R2, R1, R3) and of the PV operand (negated, fp16).
 // Work item = (tensor, column of 4 channels, pair of tokens); a warp's 32 items
 // cover 8 token pairs x 4 quads, which keeps the stores free of bank conflicts.
 __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
@@ -113,7 +104,7 @@ __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, 
         const int c = 4 * quad + e;
         const int gg = c & 7, hh = (c >> 3) & 1;
         const int L = 4 * gg + tv, reg = hh + reg_hi;
-        v[(kq * 32 + L) * 4 + reg] = pack_h2(__float2half_rn(a0[e]), __float2half_rn(a1[e]));
+        v[(kq * 32 + L) * 4 + reg] = pack_h2(__float2half_rn(-a0[e]), __float2half_rn(-a1[e]));
       }
     }
   }
@@ -206,54 +197,55 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   qnb[0] = qnb[1] = qnl[0] = qnl[1] = 0u;
   const QT* qbase = reinterpret_cast<const QT*>(p.q);
   if (active) {
+    // lane (g, t) holds channels 16kk + 4t .. 16kk + 4t + 3 (kk = 0..7) of query head g:
+    // the B fragments of every k-step, the dims of bands t, t+4, t+8, t+12 and 8 channels of
+    // each 32-channel group
+    float bss[4] = {0.f, 0.f, 0.f, 0.f}, gss[4] = {0.f, 0.f, 0.f, 0.f};
     if (g < grp) {
-      const QT* qr = qbase + ((size_t)i * p.Hq + j0 + g) * kD;
+      const QT* qr = qbase + ((size_t)i * p.Hq + j0 + g) * kD + 4 * t;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = to_f32<QT>(qr[16 * kk + 4 * t + e]);
+        const float4 v4 = load4<QT>(qr + 16 * kk);
+        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
         __half hv[4], lv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_h(v[e], hv[e], lv[e]);
+        for (int e = 0; e < 4; ++e) {
+          split_h(v[e], hv[e], lv[e]);
+          bss[kk & 3] = __fmaf_ru(v[e], v[e], bss[kk & 3]);
+          gss[kk >> 1] = __fmaf_ru(v[e], v[e], gss[kk >> 1]);
+        }
         qb[kk][0] = pack_h2(hv[0], hv[1]); qb[kk][1] = pack_h2(hv[2], hv[3]);
         qbl[kk][0] = pack_h2(lv[0], lv[1]); qbl[kk][1] = pack_h2(lv[2], lv[3]);
       }
-      if (METER) {
-        // ||q_b|| / sqrt(d) for bands 2t, 2t+1, 2t+8, 2t+9, rounded up, as fp16 hi + lo (lo rounded up)
-        const float inv_sqrt_d_up = __fdiv_ru(1.0f, __fsqrt_rd(128.0f));
-        const int bands[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
-        __half bh[4], bl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float ss = 0.0f;
-#pragma unroll
-          for (int d = 0; d < 4; ++d) {
-            const float a = to_f32<QT>(qr[4 * bands[e] + d]);
-            const float b = to_f32<QT>(qr[64 + 4 * bands[e] + d]);
-            ss = __fmaf_ru(a, a, ss);
-            ss = __fmaf_ru(b, b, ss);
-          }
-          const float nb_up = __fmul_ru(__fsqrt_ru(ss), inv_sqrt_d_up);
-          bh[e] = __float2half_rn(nb_up);
-          bl[e] = __float2half_ru(nb_up - __half2float(bh[e]));
-        }
-        qnb[0] = pack_h2(bh[0], bh[1]); qnb[1] = pack_h2(bh[2], bh[3]);
-        qnl[0] = pack_h2(bl[0], bl[1]); qnl[1] = pack_h2(bl[2], bl[3]);
-      }
     }
-    if (METER && SCHEME == kInt8) {
-      // sum_{c in G} q_c^2 / (12 d), rounded up: lane -> (head lane/4, group lane%4)
-      const int hq = lane >> 2, G = lane & 3;
-      float ss = 0.0f;
-      if (hq < grp) {
-        const QT* qr = qbase + ((size_t)i * p.Hq + j0 + hq) * kD + G * kGroupCh;
-        for (int c = 0; c < kGroupCh; ++c) { const float a = to_f32<QT>(qr[c]); ss = __fmaf_ru(a, a, ss); }
-      }
-      qgs[lane] = __fmul_ru(ss, __fdiv_ru(1.0f, 1536.0f));
-      __syncwarp();
+    if (METER) {
+      // ||q_b|| / sqrt(d) for bands t, t+4 (k 2t, 2t+1) and t+8, t+12 (k 2t+8, 2t+9), rounded up,
+      // as fp16 hi + lo (lo rounded up)
+      const float inv_sqrt_d_up = __fdiv_ru(1.0f, __fsqrt_rd(128.0f));
+      __half bh[4], bl[4];
 #pragma unroll
-      for (int G2 = 0; G2 < 4; ++G2) { qg2[0][G2] = qgs[(2 * t) * 4 + G2]; qg2[1][G2] = qgs[(2 * t + 1) * 4 + G2]; }
+      for (int m = 0; m < 4; ++m) {
+        const float nb_up = __fmul_ru(__fsqrt_ru(bss[m]), inv_sqrt_d_up);
+        bh[m] = __float2half_rn(nb_up);
+        bl[m] = __float2half_ru(nb_up - __half2float(bh[m]));
+      }
+      qnb[0] = pack_h2(bh[0], bh[1]); qnb[1] = pack_h2(bh[2], bh[3]);
+      qnl[0] = pack_h2(bl[0], bl[1]); qnl[1] = pack_h2(bl[2], bl[3]);
+      if (SCHEME == kInt8) {
+        // sum_{c in G} q_c^2 / (12 d), rounded up, for heads 2t and 2t+1 (the logit layout)
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          float v = gss[G];
+          v = __fadd_ru(v, __shfl_xor_sync(0xffffffffu, v, 1));
+          v = __fadd_ru(v, __shfl_xor_sync(0xffffffffu, v, 2));
+          gss[G] = __fmul_ru(v, __fdiv_ru(1.0f, 1536.0f));
+        }
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          qg2[0][G] = __shfl_sync(0xffffffffu, gss[G], 8 * t);
+          qg2[1][G] = __shfl_sync(0xffffffffu, gss[G], 8 * t + 4);
+        }
+      }
     }
   }
 
@@ -333,13 +325,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           lg[e] = v * lscale;
         }
         if (METER) {
+          float s2g[4], s2g8[4];     // squares of fp16 scales are exact in fp32
+#pragma unroll
+          for (int G = 0; G < 4; ++G) { s2g[G] = kvs_g[G] * kvs_g[G]; s2g8[G] = kvs_g8[G] * kvs_g8[G]; }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float* sc = e < 2 ? kvs_g : kvs_g8;
+            const float* s2 = e < 2 ? s2g : s2g8;
             const float* qg = qg2[e & 1];
             float var = 0.f;
 #pragma unroll
-            for (int G = 0; G < 4; ++G) var = __fmaf_ru(sc[G] * sc[G], qg[G], var);
+            for (int G = 0; G < 4; ++G) var = __fmaf_ru(s2[G], qg[G], var);
             ub[e] = var > 0.f ? kappa_up * (var * rsqrt_approx(var)) : 0.f;
           }
         }
@@ -479,27 +474,22 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           }
         }
       } else if constexpr (SCHEME == kInt8) {
-        const __half* vs = reinterpret_cast<const __half*>(sb + L::VS) + 4 * t * 4;   // tokens 4t..4t+3
-        const uint4 va = *reinterpret_cast<const uint4*>(vs);
-        const uint4 vb = *reinterpret_cast<const uint4*>(vs + 8);
-        const __half* v0 = reinterpret_cast<const __half*>(&va);   // tok 4t (0..3), 4t+1 (4..7)
-        const __half* v1 = reinterpret_cast<const __half*>(&vb);   // tok 4t+2, 4t+3
+        // B_j = (p * s_j) in fp16 for tokens 4t..4t+3 of head g; A = exact codes, then -xi
+        const __half2 p01 = __floats2half2_rn(pv.x, pv.y), p23 = __floats2half2_rn(pv.z, pv.w);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t bfr[2] = {
-              h2_bits(__floats2half2_rn(pv.x * __half2float(v0[j]), pv.y * __half2float(v0[4 + j]))),
-              h2_bits(__floats2half2_rn(pv.z * __half2float(v1[j]), pv.w * __half2float(v1[4 + j])))};
+          const uint2 sv = *reinterpret_cast<const uint2*>(sb + L::VS + vscale_off(4 * t, j));
+          const uint32_t bfr[2] = {h2_bits(__hmul2(p01, bits_h2(sv.x))), h2_bits(__hmul2(p23, bits_h2(sv.y)))};
           const uint4 vw = *reinterpret_cast<const uint4*>(sb + L::VC + j * 512 + lane * 16);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int mt = 2 * j + hf;
             const uint32_t w0 = hf ? vw.z : vw.x, w1 = hf ? vw.w : vw.y;
+            const uint32_t a[4] = {i8x2_lo(w0), i8x2_lo(w1), i8x2_hi(w0), i8x2_hi(w1)};
             const uint4 xv = *reinterpret_cast<const uint4*>(xb + kXiV + (mt * 32 + lane) * 16);
-            const uint32_t a[4] = {h2_bits(__hsub2(bits_h2(i8x2_lo(w0)), bits_h2(xv.x))),
-                                   h2_bits(__hsub2(bits_h2(i8x2_lo(w1)), bits_h2(xv.y))),
-                                   h2_bits(__hsub2(bits_h2(i8x2_hi(w0)), bits_h2(xv.z))),
-                                   h2_bits(__hsub2(bits_h2(i8x2_hi(w1)), bits_h2(xv.w)))};
+            const uint32_t ax[4] = {xv.x, xv.y, xv.z, xv.w};
             mma16816(acco[mt], a, bfr);
+            mma16816(acco[mt], ax, bfr);
           }
         }
       } else {  // KIVI values: p*scale times codes, plus p*zero per group

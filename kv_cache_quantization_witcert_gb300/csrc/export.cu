@@ -46,7 +46,8 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
       if (a.scheme == kKivi) {
         v = reinterpret_cast<const __half*>(bp + KiviLayout::VP)[(r * 4 + G) * 2 + (a.what == X_VZ ? 1 : 0)];
       } else {
-        v = reinterpret_cast<const __half*>(bp + (a.what == X_KS ? Int8Layout::KS : Int8Layout::VS))[r * 4 + G];
+        v = a.what == X_KS ? reinterpret_cast<const __half*>(bp + Int8Layout::KS)[r * 4 + G]
+                           : *reinterpret_cast<const __half*>(bp + Int8Layout::VS + vscale_off(r, G));
       }
       reinterpret_cast<__half*>(a.dst)[idx] = v;
       break;

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
     }
     if (clamps) atomicAdd(a.clamps, (unsigned long long)clamps);
     if ((lane & 7) == 0)
-      *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS : Int8Layout::KS) + (r * 4 + G) * 2) = s16;
+      *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS + vscale_off(r, G) : Int8Layout::KS + (r * 4 + G) * 2)) = s16;
     if (tensor == 0) {
       *reinterpret_cast<uint32_t*>(bp + Int8Layout::KC + kcode_off(r, 4 * lane)) = packed;
       store_witness(bp + Int8Layout::W, r, res, lane, repaired);
