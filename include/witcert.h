@@ -138,6 +138,25 @@ witcert_status witcert_decode(witcert_cache* cache, int layer, const void* q, do
                               float* out, float* meter_a, float* meter_b, float* raw_a,
                               float* raw_b, void* stream);
 
+/* Metered decode that allocates nothing.  The paper has no counterpart; this
+ * entry point exists for callers that cannot call cudaMalloc while they serve:
+ * engines that hand all free device memory to their own pool or caching
+ * allocator at start-up (a raw cudaMalloc would then fail, or would bypass that
+ * allocator's accounting), and hosts that forbid device allocation outside
+ * start-up.  Arguments, results and ordering are those of witcert_decode.  The
+ * split-KV partial results live in one static device array of 16 MiB that
+ * every GPU loading the library keeps until the process exits; the call rejects
+ * with EINVAL a shape whose batch x n_q_heads x KV splits x 528 bytes exceeds
+ * it.  The array's device address is looked up (cudaGetSymbolAddress) on the
+ * first call made on each device, with that device current; make that first
+ * call before any stream capture.  All calls share the array and each call
+ * overwrites what it uses (nothing needs to start at zero): calls whose work
+ * overlaps on the GPU, on any stream or cache, race and must be serialized by
+ * the caller.  No cudaMalloc, cudaFree or allocating library routine is used. */
+witcert_status witcert_decode_noalloc(witcert_cache* cache, int layer, const void* q, double delta_req,
+                                      float* out, float* meter_a, float* meter_b, float* raw_a,
+                                      float* raw_b, void* stream);
+
 /* Meter-driven gate [summary, implementation paragraph (exact blocks come
  * back from host memory once the meter passes a threshold); Lean page,
  * Figure 2 (repair works on whole blocks and clears their witnesses) and

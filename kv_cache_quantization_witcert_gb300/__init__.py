@@ -58,6 +58,13 @@ class Cache:
                                     _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
               "witcert_decode")
 
+    def witcert_decode_noalloc(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
+                               stream=None):
+        assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
+        check(load().witcert_decode_noalloc(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
+                                            _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
+              "witcert_decode_noalloc")
+
     def witcert_gate(self, layer, tau, stream=None):
         check(load().witcert_gate(self._h, layer, float(tau), _stream_ptr(stream)), "witcert_gate")
 

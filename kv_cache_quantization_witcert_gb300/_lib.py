@@ -45,6 +45,7 @@ SIGNATURES = {
     "witcert_destroy": [_vp],
     "witcert_write": [_vp, _int, _vp, _vp, _int, _vp],
     "witcert_decode": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
+    "witcert_decode_noalloc": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_gate": [_vp, _int, ctypes.c_float, _vp],
     "witcert_gate_stats": [_vp, ctypes.POINTER(witcert_gate_counters), _int],
     "witcert_stats": [_vp, ctypes.POINTER(witcert_stats_t)],

@@ -27,6 +27,7 @@
 // depends on no memory, is generated before that wait).
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -704,6 +705,33 @@ cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool
 int seqs_per_cta_for(int B) { return B >= 16 ? 16 : B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
 
 }  // namespace
+
+// ------------------------------------------------------------------ scratch without allocation
+// Split partials of witcert_decode_noalloc live in this array, which every GPU that
+// loads the library holds until the process exits.  Host code must not pass the
+// symbol itself to a kernel (on the host it names a stand-in, not device memory):
+// its device address is looked up once per device below.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) float g_split_scratch[kStaticScratchBytes / sizeof(float)];
+
+cudaError_t decode_static_scratch(float** ptr, size_t* bytes) {
+  static std::mutex mu;
+  static float* addr[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_split_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float*>(p);
+  }
+  *ptr = addr[dev];
+  *bytes = kStaticScratchBytes;
+  return cudaSuccess;
+}
 
 int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count) {
   const int spc = seqs_per_cta_for(B);

@@ -292,6 +292,62 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   return WITCERT_OK;
 }
 
+witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
+                                      float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
+  const bool meter = meter_a || meter_b || raw_a || raw_b;
+  if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
+  const int S = c->len[layer];
+  const int nblk = (S + kBlk - 1) / kBlk;
+  DecodeArgs a{};
+  a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
+  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits
+                                   : decode_auto_splits(c->scheme, a.B, a.Hkv, nblk > 0 ? nblk : 1, c->sm_count);
+  float* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  cudaError_t e = decode_static_scratch(&scratch, &scratch_bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "locating the static split scratch");
+  const size_t need = (size_t)a.B * a.Hq * a.n_splits * kPartStride * sizeof(float);
+  if (need > scratch_bytes)
+    return fail(WITCERT_EINVAL, "batch %d x %d query heads x %d splits needs %zu bytes of split scratch; "
+                "the static array holds %zu", a.B, a.Hq, a.n_splits, need, scratch_bytes);
+  auto st = static_cast<cudaStream_t>(stream);
+  order_after_gate(c, layer, st);
+  a.blocks = c->blocks + layer * c->layer_blocks;
+  a.nblk_max = c->nblk_max;
+  if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
+  a.pool = c->pool;
+  if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
+  a.q = q;
+  a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
+  a.seed = c->cfg.seed;
+  philox_round_keys(a.seed, a.rk0, a.rk1);
+  a.layer = layer;
+  float kappa = 0.f;
+  if (meter && S > 0) {
+    const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
+    const double k = std::sqrt(2.0 * std::log(2.0 * S / dloc));
+    kappa = (float)k;
+    if ((double)kappa < k) kappa = std::nextafter(kappa, INFINITY);
+  }
+  a.kappa = kappa;
+  a.part = scratch;
+  const bool gate = c->cfg.max_repair_blocks > 0;
+  if (gate && meter) {
+    a.risk_raw = c->risk_raw;
+    a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
+  }
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
+  a.err = c->err;
+  a.meter = meter;
+  e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (gate && meter) c->risk_len[layer] = S;
+  ok();
+  return WITCERT_OK;
+}
+
 witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (c->cfg.max_repair_blocks <= 0) return fail(WITCERT_ESTATE, "the gate is disabled (max_repair_blocks = 0)");
