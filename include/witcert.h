@@ -183,6 +183,13 @@ witcert_status witcert_stats(witcert_cache* cache, witcert_stats_t* out);
 /* Turn per-launch CUDA-event timing of the decode split kernel on (1) or off (0). */
 witcert_status witcert_set_profiling(witcert_cache* cache, int on);
 
+/* Launch overlap (1, the default) or strict serialization (0) of the cache's
+ * kernels on a stream.  With overlap, write, decode and merge kernels are
+ * launched as programmatic dependents: each may start before its predecessor
+ * finishes and waits for it only where it reads or overwrites that
+ * predecessor's results.  Results are identical either way. */
+witcert_status witcert_set_launch_overlap(witcert_cache* cache, int on);
+
 /* Current length of `layer` (host, synchronous, no device work). */
 witcert_status witcert_length(const witcert_cache* cache, int layer, int* len);
 
@@ -216,6 +223,13 @@ witcert_status witcert_export(witcert_cache* cache, int layer, witcert_export_ki
  * [n][128] for positions t0..t0+n-1 to device `out`.  tensor 0 = K, 1 = V. */
 witcert_status witcert_dither(uint64_t seed, int layer, int kv_head, int t0, int n, int tensor,
                               float* out, void* stream);
+
+/* Failure-detection self test (no counterpart in the paper): runs, on `stream`,
+ * the bounded shared-memory barrier wait that the decode pipeline uses, against a
+ * barrier that nothing completes, with a limit of `limit_ns` nanoseconds (at most
+ * 1e10).  Returns WITCERT_ETIMEDOUT when the wait gives up as designed (the CUDA
+ * context stays usable), WITCERT_OK if it was satisfied.  Synchronizes `stream`. */
+witcert_status witcert_wait_selftest(int64_t limit_ns, void* stream);
 
 /* Thread-local message of the last failing call on this thread ("" if none). */
 const char* witcert_last_error(void);

@@ -81,6 +81,9 @@ class Cache:
     def witcert_set_profiling(self, on):
         check(load().witcert_set_profiling(self._h, int(bool(on))), "witcert_set_profiling")
 
+    def witcert_set_launch_overlap(self, on):
+        check(load().witcert_set_launch_overlap(self._h, int(bool(on))), "witcert_set_launch_overlap")
+
     def witcert_length(self, layer):
         n = ctypes.c_int()
         check(load().witcert_length(self._h, layer, ctypes.byref(n)), "witcert_length")
@@ -131,6 +134,11 @@ class Cache:
         if dst.numel():
             self.witcert_export(layer, what, dst, stream=stream)
         return dst
+
+
+def witcert_wait_selftest(limit_ns, stream=None):
+    """Run the bounded device wait against a barrier nothing completes; returns the status code."""
+    return load().witcert_wait_selftest(int(limit_ns), _stream_ptr(stream))
 
 
 def witcert_dither(seed, layer, kv_head, t0, n, tensor, out=None, stream=None):

@@ -50,9 +50,11 @@ SIGNATURES = {
     "witcert_gate_stats": [_vp, ctypes.POINTER(witcert_gate_counters), _int],
     "witcert_stats": [_vp, ctypes.POINTER(witcert_stats_t)],
     "witcert_set_profiling": [_vp, _int],
+    "witcert_set_launch_overlap": [_vp, _int],
     "witcert_length": [_vp, _int, ctypes.POINTER(_int)],
     "witcert_export": [_vp, _int, _int, _vp, _sz, _vp],
     "witcert_dither": [ctypes.c_uint64, _int, _int, _int, _int, _int, _vp, _vp],
+    "witcert_wait_selftest": [ctypes.c_int64, _vp],
     "witcert_last_error": [],
 }
 

@@ -130,6 +130,17 @@ __device__ __forceinline__ float4 dither4_rk(const uint32_t (&rk0)[10], const ui
   return make_float4(xi_from_word(u.x), xi_from_word(u.y), xi_from_word(u.z), xi_from_word(u.w));
 }
 
+// Negated dither -xi = 1/2 - (u >> 8) * 2^-24 in one FFMA (exact: 24-bit integer, power-of-two scale).
+__device__ __forceinline__ float neg_xi_from_word(uint32_t u) {
+  return __fmaf_rn(__uint2float_rn(u >> 8), -5.9604644775390625e-8f, 0.5f);
+}
+__device__ __forceinline__ float4 neg_dither4_rk(const uint32_t (&rk0)[10], const uint32_t (&rk1)[10], int layer,
+                                                 int kvh, int t, int quad, int tensor) {
+  const uint4 u = philox4x32_10_rk(make_uint4((uint32_t)t, (uint32_t)quad | ((uint32_t)tensor << 16),
+                                              (uint32_t)kvh | ((uint32_t)layer << 16), 0u), rk0, rk1);
+  return make_float4(neg_xi_from_word(u.x), neg_xi_from_word(u.y), neg_xi_from_word(u.z), neg_xi_from_word(u.w));
+}
+
 // 2^x on the special-function unit (relative error about 2^-22; -inf -> +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;

@@ -21,10 +21,15 @@
 // aggregation min(1, (A^2-1)/2) with A = 1 + S_X/Z [WitCert summary,
 // improvements list] is applied after the merge.
 //
-// Launches chain through programmatic dependent launch: a kernel waits for its
-// predecessor on the stream before touching memory that predecessor may write,
-// then lets its own successor begin (the dither of the first block, which
-// depends on no memory, is generated before that wait).
+// Launches chain through programmatic dependent launch.  Every kernel of the chain
+// except the split kernel waits for its predecessor before it lets its successor
+// start, so when a split kernel starts, everything but its immediate predecessor is
+// complete.  The split kernel lets its successor start at once and waits for that
+// predecessor only where it depends on it: before staging a block the preceding
+// write may touch (p.dirty_blk on; for a one-token append that is the final block),
+// before writing its partial results, and, with block risks on, before its first
+// risk store.  Older blocks, the dither and the queries are used without waiting,
+// so the write's latency overlaps the decode.
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -83,18 +88,20 @@ __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, 
     const int tq = idx & 3, rp = (idx >> 2) & 7, kq = (idx >> 5) & 7, tensor = idx >> 8;
     const int quad = kq * 4 + tq;
     const int r0 = 2 * rp;
-    const float4 x0 = dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0, quad, tensor);
-    const float4 x1 = dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0 + 1, quad, tensor);
+    const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0, quad, tensor);
+    const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0 + 1, quad, tensor);
     if (tensor == 0) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float4 x = u ? x1 : x0;
         const int r = r0 + u, L = 4 * (r & 7) + tq, hh = r >> 3;
-        __half h0, l0, h1, l1, h2, l2, h3, l3;
-        split_h(-x.x, h0, l0); split_h(-x.y, h1, l1); split_h(-x.z, h2, l2); split_h(-x.w, h3, l3);
+        // hi = fp16(-xi), lo = fp16(-xi - hi): packed conversions, two values per instruction
+        const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(x.x - f01.x, x.y - f01.y), l23 = __floats2half2_rn(x.z - f23.x, x.w - f23.y);
         const int off = (kq * 32 + L) * 16 + hh * 8;
-        *reinterpret_cast<uint2*>(xb + kXiKHi + off) = make_uint2(pack_h2(h0, h1), pack_h2(h2, h3));
-        *reinterpret_cast<uint2*>(xb + kXiKLo + off) = make_uint2(pack_h2(l0, l1), pack_h2(l2, l3));
+        *reinterpret_cast<uint2*>(xb + kXiKHi + off) = make_uint2(h2_bits(h01), h2_bits(h23));
+        *reinterpret_cast<uint2*>(xb + kXiKLo + off) = make_uint2(h2_bits(l01), h2_bits(l23));
       }
     } else {
       const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
@@ -105,7 +112,7 @@ __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, 
         const int c = 4 * quad + e;
         const int gg = c & 7, hh = (c >> 3) & 1;
         const int L = 4 * gg + tv, reg = hh + reg_hi;
-        v[(kq * 32 + L) * 4 + reg] = pack_h2(__float2half_rn(-a0[e]), __float2half_rn(-a1[e]));
+        v[(kq * 32 + L) * 4 + reg] = h2_bits(__floats2half2_rn(a0[e], a1[e]));
       }
     }
   }
@@ -176,14 +183,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
-
-  pdl_wait();
   pdl_trigger();
+  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
+  // blocks from p.dirty_blk on may still be written by the immediately preceding kernel
+  if (RISK) pdl_wait();
 
   if (active && lane == 0) {
     fence_proxy_async();
     for (int s = 0; s < NST && s < nb; ++s) {
+      if (b_begin + s >= p.dirty_blk) pdl_wait();
       mbar_expect_tx(smem_addr(&bars[s]), L::BYTES);
       bulk_g2s(smem_addr(ring + s * L::BYTES), src + (size_t)s * L::BYTES, L::BYTES, smem_addr(&bars[s]));
     }
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         if (lane == 0) atomicAdd(p.err, 1);
       }
     }
+    if (blk >= p.dirty_blk) pdl_wait();             // also covers the exact pool and KIVI tail rows
     if (active && !fault) {
       const uint8_t* sb = ring + stage * L::BYTES;
       const int slot = p.slots ? p.slots[seq_base + blk] : -1;
@@ -531,6 +540,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       __syncwarp();
       // refill this stage with the block NST ahead
       if (lane == 0 && n + NST < nb) {
+        if (blk + NST >= p.dirty_blk) pdl_wait();
         fence_proxy_async();
         mbar_expect_tx(smem_addr(&bars[stage]), L::BYTES);
         bulk_g2s(smem_addr(ring + stage * L::BYTES), src + (size_t)(n + NST) * L::BYTES, L::BYTES,
@@ -540,6 +550,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     if (SCHEME == kInt8) __syncthreads();
   }
 
+  pdl_wait();     // partial results overwrite scratch the preceding merge may still read
   if (fault) {
     // drain copies still in flight before the CTA's shared memory is released
     if (lane == 0)
@@ -586,68 +597,66 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   }
 }
 
-// One warp per (sequence, query head): merge the splits, normalize, finish the meters.
+// One 4-warp CTA per (sequence, query head): warp w merges splits w, w+4, ...; the four
+// partial states meet in shared memory; then the output, the meters and the block risks.
 template <bool INT8, bool RISK>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
   pdl_wait();
   pdl_trigger();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wid >= p.B * p.Hq) return;
-  const float* recs = p.part + (size_t)wid * p.n_splits * kPartStride;
+  __shared__ float s_acc[4][kD];
+  __shared__ float s_sc[4][4];
+  __shared__ float s_m[4];
+  const int cell = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* recs = p.part + (size_t)cell * p.n_splits * kPartStride;
   const int ns = p.n_splits;
-  // scalars: lanes across splits
   float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, recs[(size_t)s * kPartStride]);
+  for (int s = threadIdx.x; s < ns; s += 128) M = fmaxf(M, recs[(size_t)s * kPartStride]);
 #pragma unroll
   for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) s_m[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
   float Z = 0.f, SA = 0.f, SB = 0.f;
-  if (M != -INFINITY) {
-    for (int s = lane; s < ns; s += 32) {
-      const float* r = recs + (size_t)s * kPartStride;
-      const float ms = r[0];
-      const float f = ms == -INFINITY ? 0.f : ex2(ms - M);
-      Z = fmaf(f, r[1], Z); SA = fmaf(f, r[2], SA); SB = fmaf(f, r[3], SB);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    SA += __shfl_xor_sync(0xffffffffu, SA, o);
-    SB += __shfl_xor_sync(0xffffffffu, SB, o);
-  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
 #pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
+    for (int s = warp; s < ns; s += 4) {
       const float* r = recs + (size_t)s * kPartStride;
-      const float ms = r[0];
-      const float f = ms == -INFINITY ? 0.f : ex2(ms - M);
+      const float4 h = *reinterpret_cast<const float4*>(r);           // m, Z, S_A, S_B
+      const float f = h.x == -INFINITY ? 0.f : ex2(h.x - M);
+      Z = fmaf(f, h.y, Z); SA = fmaf(f, h.z, SA); SB = fmaf(f, h.w, SB);
       const float4 a = *reinterpret_cast<const float4*>(r + 4 + 4 * lane);
       acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
     }
   }
+  *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
+  if (lane == 0) { s_sc[warp][0] = Z; s_sc[warp][1] = SA; s_sc[warp][2] = SB; }
+  __syncthreads();
+  Z = s_sc[0][0] + s_sc[1][0] + s_sc[2][0] + s_sc[3][0];
+  SA = s_sc[0][1] + s_sc[1][1] + s_sc[2][1] + s_sc[3][1];
+  SB = s_sc[0][2] + s_sc[1][2] + s_sc[2][2] + s_sc[3][2];
   const float inv = Z > 0.f ? 1.0f / Z : 0.f;
-  *reinterpret_cast<float4*>(p.out + (size_t)wid * kD + 4 * lane) =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  p.out[(size_t)cell * kD + threadIdx.x] =
+      (s_acc[0][threadIdx.x] + s_acc[1][threadIdx.x] + s_acc[2][threadIdx.x] + s_acc[3][threadIdx.x]) * inv;
   if (!p.meter) return;
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     const float DA = Z > 0.f ? __fmul_ru(__fdiv_ru(SA, Z), kMeterMargin) : 0.f;
     const float rawA = __fmaf_ru(__fmul_ru(0.5f, DA), DA, DA);
-    if (p.raw_a) p.raw_a[wid] = rawA;
-    if (p.meter_a) p.meter_a[wid] = fminf(1.0f, rawA);
+    if (p.raw_a) p.raw_a[cell] = rawA;
+    if (p.meter_a) p.meter_a[cell] = fminf(1.0f, rawA);
     float rawB = NAN;
     if (INT8) {
       const float DB = Z > 0.f ? __fmul_ru(__fdiv_ru(SB, Z), kMeterMargin) : 0.f;
       rawB = __fmaf_ru(__fmul_ru(0.5f, DB), DB, DB);
     }
-    if (p.raw_b) p.raw_b[wid] = rawB;
-    if (p.meter_b) p.meter_b[wid] = INT8 ? fminf(1.0f, rawB) : NAN;
+    if (p.raw_b) p.raw_b[cell] = rawB;
+    if (p.meter_b) p.meter_b[cell] = INT8 ? fminf(1.0f, rawB) : NAN;
   }
   if (RISK) {
     const int nblk = (p.S + kBlk - 1) / kBlk;
-    const float2* rr = p.risk_raw + (size_t)wid * p.nblk_max;
-    float* ro = p.risk + (size_t)wid * p.nblk_max;
-    for (int b = lane; b < nblk; b += 32) {
+    const float2* rr = p.risk_raw + (size_t)cell * p.nblk_max;
+    float* ro = p.risk + (size_t)cell * p.nblk_max;
+    for (int b = threadIdx.x; b < nblk; b += 128) {
       const float2 v = rr[b];
       ro[b] = (v.y == 0.f || Z == 0.f) ? 0.f : v.y * ex2(v.x - M) * inv;
     }
@@ -746,28 +755,28 @@ int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count) {
 }
 
 cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaStream_t st,
-                          cudaEvent_t split_start, cudaEvent_t split_stop) {
+                          cudaEvent_t split_start, cudaEvent_t split_stop, bool pdl_allowed) {
   (void)sm_count;
   DecodeArgs a = a0;
   a.seqs_per_cta = seqs_per_cta_for(a.B);
   const int groups = (a.B + a.seqs_per_cta - 1) / a.seqs_per_cta;
   dim3 grid(a.n_splits, a.Hkv, groups);
-  const bool pdl = split_start == nullptr;      // event boundaries around a timed split break the overlap anyway
+  // event boundaries around a timed split (and an event wait before it) get a plain launch
+  const bool pdl = pdl_allowed && split_start == nullptr;
   if (split_start) cudaEventRecord(split_start, st);
   cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, st, pdl)
                   : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, st, pdl)
                                    : dispatch_flags<kKivi>(a, grid, st, pdl);
   if (split_stop) cudaEventRecord(split_stop, st);
   if (e != cudaSuccess) return e;
-  const int warps = a.B * a.Hq;
-  const dim3 mg((warps * 32 + 127) / 128);
+  const dim3 mg(a.B * a.Hq);
   const bool risk = a.risk_raw != nullptr && a.meter;
   if (scheme == kInt8)
-    e = risk ? launch_pdl(decode_merge_kernel<true, true>, mg, dim3(128), 0, st, true, a)
-             : launch_pdl(decode_merge_kernel<true, false>, mg, dim3(128), 0, st, true, a);
+    e = risk ? launch_pdl(decode_merge_kernel<true, true>, mg, dim3(128), 0, st, pdl_allowed, a)
+             : launch_pdl(decode_merge_kernel<true, false>, mg, dim3(128), 0, st, pdl_allowed, a);
   else
-    e = risk ? launch_pdl(decode_merge_kernel<false, true>, mg, dim3(128), 0, st, true, a)
-             : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(128), 0, st, true, a);
+    e = risk ? launch_pdl(decode_merge_kernel<false, true>, mg, dim3(128), 0, st, pdl_allowed, a)
+             : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(128), 0, st, pdl_allowed, a);
   return e;
 }
 

@@ -92,7 +92,29 @@ __global__ void dither_kernel(uint64_t seed, int layer, int kvh, int t0, int n, 
   *reinterpret_cast<float4*>(out + (size_t)r * kD + 4 * quad) = x;
 }
 
+// Status of the last bounded-wait self test: 0 = satisfied, 1 = timed out.
+static __device__ int g_wait_status;
+
+// An mbarrier that expects one arrival nobody makes: the bounded wait used by the
+// decode pipeline must give up after `limit_ns` and report it.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    g_wait_status = mbar_wait(smem_addr(&bar), 0, limit_ns) ? 0 : 1;
+  }
+}
+
 }  // namespace
+
+cudaError_t run_wait_selftest(uint64_t limit_ns, cudaStream_t st, int* timed_out) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(timed_out, g_wait_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e;
+}
 
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t st) {
   const int nblk = (a.S + kBlk - 1) / kBlk;

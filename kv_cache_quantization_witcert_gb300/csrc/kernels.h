@@ -32,6 +32,7 @@ struct DecodeArgs {
   const void* q;             // [B][Hq][128]
   int is_bf16;
   int B, Hq, Hkv, grp, S, n_splits, seqs_per_cta;
+  int dirty_blk;             // first block the immediately preceding kernel may write (INT_MAX: none)
   uint64_t seed;
   uint32_t rk0[10], rk1[10]; // Philox round keys of `seed` (key words advanced by the Weyl increments)
   int layer;
@@ -45,14 +46,15 @@ struct DecodeArgs {
   bool meter;
 };
 
-cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st);
+// pdl: launch with programmatic stream serialization (off right after an event wait).
+cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl);
 // Philox4x32-10 round keys of a 64-bit seed: key (seed mod 2^32, seed div 2^32) advanced
 // by 0x9E3779B9 / 0xBB67AE85 before every round but the first.
 void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]);
 // Split-KV decode + merge.  Returns the split kernel's launch error; `split_start`
 // and `split_stop` (optional) bracket the split kernel alone.
 cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStream_t st,
-                          cudaEvent_t split_start, cudaEvent_t split_stop);
+                          cudaEvent_t split_start, cudaEvent_t split_stop, bool pdl);
 int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count);
 // Device address (current device) and size of the library's static split scratch,
 // used by witcert_decode_noalloc; the first call on a device looks the address up.
@@ -83,6 +85,8 @@ struct ExportArgs {
   int what;
 };
 cudaError_t launch_export(const ExportArgs& a, cudaStream_t st);
+// Runs the bounded mbarrier wait against a barrier nothing completes; sets *timed_out.
+cudaError_t run_wait_selftest(uint64_t limit_ns, cudaStream_t st, int* timed_out);
 cudaError_t launch_dither(uint64_t seed, int layer, int kvh, int t0, int n, int tensor, float* out,
                           cudaStream_t st);
 

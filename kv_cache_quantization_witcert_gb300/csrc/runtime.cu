@@ -3,6 +3,7 @@
 // that order it against writes and decodes; validates every argument and maps
 // failures to status codes with a thread-local message.
 #include <chrono>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -68,6 +69,9 @@ struct witcert_cache {
   double prof_ms = 0.0;
   uint64_t prof_n = 0, tokens_written = 0, decode_calls = 0, gate_calls = 0;
   int last_n_splits = 0;
+  bool overlap = true;       // programmatic dependent launch between the cache's kernels
+  // most recent launch on the cache's stream when it was a write: its layer and first block
+  int last_write_layer = -1, last_write_blk = 0;
 };
 
 namespace {
@@ -102,8 +106,11 @@ cudaError_t dalloc(T** p, size_t bytes) {
 }
 
 // Wait for the gate of `layer` (device-side) before touching that layer again.
-void order_after_gate(witcert_cache* c, int layer, cudaStream_t st) {
-  if (c->gate_pending[layer]) cudaStreamWaitEvent(st, c->gate_done[layer], 0);
+// Returns true when it inserted an event wait (the next launch then goes without PDL).
+bool order_after_gate(witcert_cache* c, int layer, cudaStream_t st) {
+  if (!c->gate_pending[layer]) return false;
+  cudaStreamWaitEvent(st, c->gate_done[layer], 0);
+  return true;
 }
 
 void collect_profile(witcert_cache* c) {
@@ -206,7 +213,7 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
                 (long long)c->len[layer] + n_tok, c->cfg.max_tokens);
   if (n_tok == 0) { ok(); return WITCERT_OK; }
   auto st = static_cast<cudaStream_t>(stream);
-  order_after_gate(c, layer, st);
+  const bool waited = order_after_gate(c, layer, st);
   WriteArgs a{};
   a.blocks = c->blocks + layer * c->layer_blocks;
   a.nblk_max = c->nblk_max;
@@ -221,8 +228,10 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   a.pool = c->pool;
   if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
   a.clamps = c->clamps;
-  cudaError_t e = launch_write(c->scheme, a, st);
+  cudaError_t e = launch_write(c->scheme, a, st, c->overlap && !waited);
   if (e != cudaSuccess) return cuda_fail(e, "write launch");
+  c->last_write_layer = layer;
+  c->last_write_blk = a.t0 / kBlk;
   c->len[layer] += n_tok;
   c->risk_len[layer] = -1;
   c->tokens_written += (uint64_t)n_tok * layer_rows(c);
@@ -237,7 +246,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   const bool meter = meter_a || meter_b || raw_a || raw_b;
   if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
   auto st = static_cast<cudaStream_t>(stream);
-  order_after_gate(c, layer, st);
+  const bool waited = order_after_gate(c, layer, st);
   const int S = c->len[layer];
   const int nblk = (S + kBlk - 1) / kBlk;
   DecodeArgs a{};
@@ -254,6 +263,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
   a.layer = layer;
+  a.dirty_blk = c->last_write_layer == layer ? c->last_write_blk : INT_MAX;
   float kappa = 0.f;
   if (meter && S > 0) {
     const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
@@ -282,10 +292,11 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
     pp = c->prof_free.back();
     c->prof_free.pop_back();
   }
-  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b);
+  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b, c->overlap && !waited);
   if (pp.a) c->prof_pending.push_back(pp);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (gate && meter) c->risk_len[layer] = S;
+  c->last_write_layer = -1;
   c->last_n_splits = a.n_splits;
   ++c->decode_calls;
   ok();
@@ -313,7 +324,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
     return fail(WITCERT_EINVAL, "batch %d x %d query heads x %d splits needs %zu bytes of split scratch; "
                 "the static array holds %zu", a.B, a.Hq, a.n_splits, need, scratch_bytes);
   auto st = static_cast<cudaStream_t>(stream);
-  order_after_gate(c, layer, st);
+  const bool waited = order_after_gate(c, layer, st);
   a.blocks = c->blocks + layer * c->layer_blocks;
   a.nblk_max = c->nblk_max;
   if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
@@ -324,6 +335,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
   a.layer = layer;
+  a.dirty_blk = c->last_write_layer == layer ? c->last_write_blk : INT_MAX;
   float kappa = 0.f;
   if (meter && S > 0) {
     const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
@@ -341,9 +353,10 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
   a.err = c->err;
   a.meter = meter;
-  e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr);
+  e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (gate && meter) c->risk_len[layer] = S;
+  c->last_write_layer = -1;
   ok();
   return WITCERT_OK;
 }
@@ -440,6 +453,13 @@ witcert_status witcert_set_profiling(witcert_cache* c, int on) {
   return WITCERT_OK;
 }
 
+witcert_status witcert_set_launch_overlap(witcert_cache* c, int on) {
+  if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
+  c->overlap = on != 0;
+  ok();
+  return WITCERT_OK;
+}
+
 witcert_status witcert_length(const witcert_cache* c, int layer, int* len) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (!len) return fail(WITCERT_EINVAL, "len is NULL");
@@ -480,6 +500,17 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
   a.what = (int)what;
   cudaError_t e = launch_export(a, st);
   if (e != cudaSuccess) return cuda_fail(e, "export launch");
+  c->last_write_layer = -1;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_wait_selftest(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 10000000000ll) return fail(WITCERT_EINVAL, "limit_ns must be in (0, 1e10]");
+  int timed_out = -1;
+  cudaError_t e = run_wait_selftest((uint64_t)limit_ns, static_cast<cudaStream_t>(stream), &timed_out);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self test");
+  if (timed_out) return fail(WITCERT_ETIMEDOUT, "device wait gave up after %lld ns", (long long)limit_ns);
   ok();
   return WITCERT_OK;
 }

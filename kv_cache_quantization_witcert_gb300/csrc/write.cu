@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
 }
 
 template <typename K>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, const WriteArgs& a) {
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, bool pdl, const WriteArgs& a) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -281,19 +281,19 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, const W
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <typename T>
-cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st) {
+cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   const int warps = a.B * a.n_tok * a.Hkv;
   const dim3 blocks((warps * 32 + 127) / 128);
-  if (scheme == kInt8) return launch_pdl(write_int8_kernel<T>, blocks, dim3(128), st, a);
-  if (scheme == kFp8) return launch_pdl(write_fp8_kernel<T>, blocks, dim3(128), st, a);
-  cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, a);
+  if (scheme == kInt8) return launch_pdl(write_int8_kernel<T>, blocks, dim3(128), st, pdl, a);
+  if (scheme == kFp8) return launch_pdl(write_fp8_kernel<T>, blocks, dim3(128), st, pdl, a);
+  cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, pdl, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv), dim3(32), st, a);
+  return launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv), dim3(32), st, pdl, a);
 }
 
 }  // namespace
@@ -307,9 +307,9 @@ void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]) 
   }
 }
 
-cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st) {
+cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   if (a.B * a.n_tok * a.Hkv == 0) return cudaSuccess;
-  return a.is_bf16 ? launch_t<__nv_bfloat16>(scheme, a, st) : launch_t<float>(scheme, a, st);
+  return a.is_bf16 ? launch_t<__nv_bfloat16>(scheme, a, st, pdl) : launch_t<float>(scheme, a, st, pdl);
 }
 
 }  // namespace witcert
