@@ -68,21 +68,29 @@ template <int NW, int SCHEME> struct Smem {
   static constexpr int kBytes = kBarOff + NW * NST * 8;
 };
 
-// p * expm1(c) for c >= 0, with p = e^(l - m) (l2, m2 in log2 units).  Below c = 1/8 the
-// series c + c^2/2 + c^3/6 + c^4/24 (truncation < 2e-6 relative); above it the term is
+// Packed pairs (two query heads of a lane): fp32x2 arithmetic of sm_100+.
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+
+// p * expm1(c) for c >= 0, with p = e^(l - m) and d = l - m in log2 units.  Below c = 1/8
+// the series c + c^2/2 + c^3/6 + c^4/24 (truncation < 2e-6 relative); above it the term is
 // formed in the exponent, e^(l - m + c) - e^(l - m), which neither overflows for large c
 // nor loses a flushed p, and cancels at most a factor e^c/(e^c - 1) < 8.6 of precision.
-__device__ __forceinline__ float meter_term(float pe, float l2, float m2, float c) {
-  const float poly = c * fmaf(c, fmaf(c, fmaf(c, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-  const float big = ex2(fmaf(c, kLog2e, l2 - m2)) - pe;
-  return c < 0.125f ? pe * poly : big;
+__device__ __forceinline__ float2 meter_term2(float2 pe, float2 d, float2 c) {
+  float2 poly = __ffma2_rn(c, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
+  poly = __ffma2_rn(c, poly, f2(0.5f));
+  poly = __ffma2_rn(c, poly, f2(1.0f));
+  poly = __fmul2_rn(__fmul2_rn(c, poly), pe);
+  const float2 big = f2sub(ex2x2(__ffma2_rn(c, f2(kLog2e), d)), pe);
+  return make_float2(pe.x > 0.0f && c.x > 0.0f ? (c.x < 0.125f ? poly.x : big.x) : 0.0f,
+                     pe.y > 0.0f && c.y > 0.0f ? (c.y < 0.125f ? poly.y : big.y) : 0.0f);
 }
 
 // Regenerate the dither of block `blk` of KV head h into shared memory, in the
-// fragment order of the QK operands (negated, fp16 hi + lo; per lane the four
-// registers are stored as R0, R2, R1, R3) and of the PV operand (negated, fp16).
-// Work item = (tensor, column of 4 channels, pair of tokens); a warp's 32 items
-// cover 8 token pairs x 4 quads, which keeps the stores free of bank conflicts.
+// fragment order of the QK operands (negated, fp16 hi + lo) and of the PV operand
+// (negated, fp16): each lane's four A registers are contiguous, so one 16-byte load
+// fills an MMA operand.  Work item = (tensor, column of 4 channels, pair of tokens).
 __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
   for (int idx = threadIdx.x; idx < 512; idx += nthreads) {
     const int tq = idx & 3, rp = (idx >> 2) & 7, kq = (idx >> 5) & 7, tensor = idx >> 8;
@@ -95,13 +103,15 @@ __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, 
       for (int u = 0; u < 2; ++u) {
         const float4 x = u ? x1 : x0;
         const int r = r0 + u, L = 4 * (r & 7) + tq, hh = r >> 3;
-        // hi = fp16(-xi), lo = fp16(-xi - hi): packed conversions, two values per instruction
+        // hi = fp16(-xi), lo = fp16(-xi - hi): packed conversions, two values per instruction;
+        // channels +0,+1 go to register R(hh), channels +2,+3 to R(2+hh) of lane L
         const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
         const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
         const __half2 l01 = __floats2half2_rn(x.x - f01.x, x.y - f01.y), l23 = __floats2half2_rn(x.z - f23.x, x.w - f23.y);
-        const int off = (kq * 32 + L) * 16 + hh * 8;
-        *reinterpret_cast<uint2*>(xb + kXiKHi + off) = make_uint2(h2_bits(h01), h2_bits(h23));
-        *reinterpret_cast<uint2*>(xb + kXiKLo + off) = make_uint2(h2_bits(l01), h2_bits(l23));
+        uint32_t* hi = reinterpret_cast<uint32_t*>(xb + kXiKHi + (kq * 32 + L) * 16);
+        uint32_t* lo = reinterpret_cast<uint32_t*>(xb + kXiKLo + (kq * 32 + L) * 16);
+        hi[hh] = h2_bits(h01); hi[2 + hh] = h2_bits(h23);
+        lo[hh] = h2_bits(l01); lo[2 + hh] = h2_bits(l23);
       }
     } else {
       const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
@@ -150,7 +160,7 @@ __device__ __forceinline__ void exact_block_logits(const KT* ex, const uint32_t 
   }
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, int NW>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, int NW>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_kernel(const DecodeArgs p) {
   using L = Lay<SCHEME>;
   using SM = Smem<NW, SCHEME>;
@@ -259,14 +269,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   }
 
   // ---------------------------------------------------------------- state
-  float m2[2] = {-INFINITY, -INFINITY}, Zp[2] = {0.f, 0.f}, SAp[2] = {0.f, 0.f}, SBp[2] = {0.f, 0.f};
+  // per lane: heads 2t (.x) and 2t+1 (.y); A = token g, B = token g+8 of the block
+  float2 m2 = f2(-INFINITY), Zp = f2(0.f), SAp = f2(0.f), SBp = f2(0.f);
   float acco[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) acco[mt][0] = acco[mt][1] = acco[mt][2] = acco[mt][3] = 0.f;
   float zc[4] = {0.f, 0.f, 0.f, 0.f};           // KIVI: sum_t p_t zero_{t,G} for head g
   const float lscale = __fdiv_rn(kLog2e, sqrtf(128.0f));
-  // Tier B: u = kappa * sqrt(var); the SFU square root is within 2^-21 relative, covered by this factor
-  const float kappa_up = p.kappa * (1.0f + 9.5367431640625e-7f);
+  // Tier B: u = kappa * sqrt(var).  var is summed with nearest rounding (4 terms) and the
+  // SFU square root is within 2^-21 relative; this factor covers both.
+  const float kappa_up = p.kappa * (1.0f + 1.9073486328125e-6f);
+  float2 qgp[4];
+#pragma unroll
+  for (int G = 0; G < 4; ++G) qgp[G] = make_float2(qg2[0][G], qg2[1][G]);
 
   if (SCHEME == kInt8) __syncthreads();
 
@@ -286,18 +301,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     if (blk >= p.dirty_blk) pdl_wait();             // also covers the exact pool and KIVI tail rows
     if (active && !fault) {
       const uint8_t* sb = ring + stage * L::BYTES;
-      const int slot = p.slots ? p.slots[seq_base + blk] : -1;
+      const int slot = GATE ? p.slots[seq_base + blk] : -1;
       const bool kivi_tail = SCHEME == kKivi && (blk + 1) * kBlk > p.S;
-      float lg[4], eps[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 lgA, lgB, epsA = f2(0.f), epsB = f2(0.f), ubA = f2(0.f), ubB = f2(0.f);
 
-      if (slot >= 0 || kivi_tail) {
+      if ((GATE && slot >= 0) || kivi_tail) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (slot >= 0)
+        if (GATE && slot >= 0)
           exact_block_logits<QT, QLO>(reinterpret_cast<const QT*>(p.pool) + (size_t)slot * kBlk * kD, qb, qbl, g, t, acc);
         else
           exact_block_logits<float, QLO>(p.kivi_tail + seq_base / p.nblk_max * (size_t)(kBlk * kD), qb, qbl, g, t, acc);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) lg[e] = acc[e] * lscale;
+        lgA = __fmul2_rn(make_float2(acc[0], acc[1]), f2(lscale));
+        lgB = __fmul2_rn(make_float2(acc[2], acc[3]), f2(lscale));
       } else if constexpr (SCHEME == kInt8) {
         float acc[4][4];
 #pragma unroll
@@ -313,8 +328,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             if (QLO) mma16816(acc[G], a, qbl[kk]);
             const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
             const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
-            const uint32_t ah[4] = {xh.x, xh.z, xh.y, xh.w};     // stored as R0, R2, R1, R3
-            const uint32_t al[4] = {xl.x, xl.z, xl.y, xl.w};
+            const uint32_t ah[4] = {xh.x, xh.y, xh.z, xh.w};
+            const uint32_t al[4] = {xl.x, xl.y, xl.z, xl.w};
             mma16816(acc[G], ah, qb[kk]);
             mma16816(acc[G], al, qb[kk]);
             if (QLO) mma16816(acc[G], ah, qbl[kk]);
@@ -323,33 +338,35 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         const __half* ks = reinterpret_cast<const __half*>(sb + L::KS);
         const uint2 s0 = *reinterpret_cast<const uint2*>(ks + g * 4);
         const uint2 s1 = *reinterpret_cast<const uint2*>(ks + (g + 8) * 4);
-        const __half2 a01 = bits_h2(s0.x), a23 = bits_h2(s0.y), b01 = bits_h2(s1.x), b23 = bits_h2(s1.y);
-        const float kvs_g[4] = {__low2float(a01), __high2float(a01), __low2float(a23), __high2float(a23)};
-        const float kvs_g8[4] = {__low2float(b01), __high2float(b01), __low2float(b23), __high2float(b23)};
+        const float2 sg01 = __half22float2(bits_h2(s0.x)), sg23 = __half22float2(bits_h2(s0.y));
+        const float2 sh01 = __half22float2(bits_h2(s1.x)), sh23 = __half22float2(bits_h2(s1.y));
+        const float sgA[4] = {sg01.x, sg01.y, sg23.x, sg23.y}, sgB[4] = {sh01.x, sh01.y, sh23.x, sh23.y};
+        lgA = f2(0.f);
+        lgB = f2(0.f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float* sc = e < 2 ? kvs_g : kvs_g8;
-          float v = 0.f;
-#pragma unroll
-          for (int G = 0; G < 4; ++G) v = fmaf(sc[G], acc[G][e], v);
-          lg[e] = v * lscale;
+        for (int G = 0; G < 4; ++G) {
+          lgA = __ffma2_rn(f2(sgA[G]), make_float2(acc[G][0], acc[G][1]), lgA);
+          lgB = __ffma2_rn(f2(sgB[G]), make_float2(acc[G][2], acc[G][3]), lgB);
         }
+        lgA = __fmul2_rn(lgA, f2(lscale));
+        lgB = __fmul2_rn(lgB, f2(lscale));
         if (METER) {
-          float s2g[4], s2g8[4];     // squares of fp16 scales are exact in fp32
+          // squares of fp16 scales are exact in fp32
+          float2 varA = f2(0.f), varB = f2(0.f);
 #pragma unroll
-          for (int G = 0; G < 4; ++G) { s2g[G] = kvs_g[G] * kvs_g[G]; s2g8[G] = kvs_g8[G] * kvs_g8[G]; }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float* s2 = e < 2 ? s2g : s2g8;
-            const float* qg = qg2[e & 1];
-            float var = 0.f;
-#pragma unroll
-            for (int G = 0; G < 4; ++G) var = __fmaf_ru(s2[G], qg[G], var);
-            ub[e] = var > 0.f ? kappa_up * (var * rsqrt_approx(var)) : 0.f;
+          for (int G = 0; G < 4; ++G) {
+            varA = __ffma2_rn(f2(sgA[G] * sgA[G]), qgp[G], varA);
+            varB = __ffma2_rn(f2(sgB[G] * sgB[G]), qgp[G], varB);
           }
+          const float2 rA = make_float2(rsqrt_approx(varA.x), rsqrt_approx(varA.y));
+          const float2 rB = make_float2(rsqrt_approx(varB.x), rsqrt_approx(varB.y));
+          const float2 uA = __fmul2_rn(__fmul2_rn(varA, rA), f2(kappa_up));
+          const float2 uB = __fmul2_rn(__fmul2_rn(varB, rB), f2(kappa_up));
+          ubA = make_float2(varA.x > 0.f ? uA.x : 0.f, varA.y > 0.f ? uA.y : 0.f);
+          ubB = make_float2(varB.x > 0.f ? uB.x : 0.f, varB.y > 0.f ? uB.y : 0.f);
         }
       } else if constexpr (SCHEME == kFp8) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
           const uint4 cw = *reinterpret_cast<const uint4*>(sb + L::KC + G * 512 + lane * 16);
@@ -358,12 +375,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             const int kk = 2 * G + hf;
             const uint32_t w0 = hf ? cw.z : cw.x, w1 = hf ? cw.w : cw.y;
             const uint32_t a[4] = {e4m3x2_lo(w0), e4m3x2_lo(w1), e4m3x2_hi(w0), e4m3x2_hi(w1)};
-            mma16816(acc, a, qb[kk]);
-            if (QLO) mma16816(acc, a, qbl[kk]);
+            mma16816(hf ? acc2 : acc, a, qb[kk]);
+            if (QLO) mma16816(hf ? acc2 : acc, a, qbl[kk]);
           }
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) lg[e] = acc[e] * lscale;
+        lgA = __fmul2_rn(make_float2(acc[0] + acc2[0], acc[1] + acc2[1]), f2(lscale));
+        lgB = __fmul2_rn(make_float2(acc[2] + acc2[2], acc[3] + acc2[3]), f2(lscale));
       } else {  // KIVI: logits = q . zero + (q * scale) . codes
         const __half* ksc = reinterpret_cast<const __half*>(sb + L::KP);
         const __half* kzr = reinterpret_cast<const __half*>(sb + L::KP + 256);
@@ -397,72 +414,72 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         zq += __shfl_xor_sync(0xffffffffu, zq, 2);      // lanes 4g..4g+3 hold q_g . zero
         const float zq0 = __shfl_sync(0xffffffffu, zq, 8 * t);
         const float zq1 = __shfl_sync(0xffffffffu, zq, 8 * t + 4);
-        lg[0] = (acc[0] + zq0) * lscale; lg[1] = (acc[1] + zq1) * lscale;
-        lg[2] = (acc[2] + zq0) * lscale; lg[3] = (acc[3] + zq1) * lscale;
+        lgA = __fmul2_rn(make_float2(acc[0] + zq0, acc[1] + zq1), f2(lscale));
+        lgB = __fmul2_rn(make_float2(acc[2] + zq0, acc[3] + zq1), f2(lscale));
       }
 
       // Tier A from the stored witness (zero for repaired blocks and KIVI's unfinished block)
-      if (METER && slot < 0) {
+      if (METER && !(GATE && slot >= 0)) {
+        float eps[4] = {0.f, 0.f, 0.f, 0.f};
         const uint4 wf = *reinterpret_cast<const uint4*>(sb + L::W + lane * 16);
         const uint32_t a[4] = {wf.x, wf.y, wf.z, wf.w};
         mma16816(eps, a, qnb);
         mma16816(eps, a, qnl);
+        epsA = make_float2(eps[0], eps[1]);
+        epsB = make_float2(eps[2], eps[3]);
       }
-      if (slot >= 0) { ub[0] = ub[1] = ub[2] = ub[3] = 0.f; }
+      if (GATE && slot >= 0) { ubA = f2(0.f); ubB = f2(0.f); }
 
       // mask tokens past the context
       const int tok0 = blk * kBlk + g, tok1 = tok0 + 8;
-      if (tok0 >= p.S) { lg[0] = lg[1] = -INFINITY; }
-      if (tok1 >= p.S) { lg[2] = lg[3] = -INFINITY; }
+      if (tok0 >= p.S) lgA = f2(-INFINITY);
+      if (tok1 >= p.S) lgB = f2(-INFINITY);
 
       // ------------------------------------------------------------ online softmax + meters
-      float bm0 = fmaxf(lg[0], lg[2]), bm1 = fmaxf(lg[1], lg[3]);
+      float2 bm = make_float2(fmaxf(lgA.x, lgB.x), fmaxf(lgA.y, lgB.y));
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+        bm.x = fmaxf(bm.x, __shfl_xor_sync(0xffffffffu, bm.x, o));
+        bm.y = fmaxf(bm.y, __shfl_xor_sync(0xffffffffu, bm.y, o));
       }
-      const float mn0 = fmaxf(m2[0], bm0), mn1 = fmaxf(m2[1], bm1);
-      const float sc0 = mn0 == -INFINITY ? 1.f : ex2(m2[0] - mn0);
-      const float sc1 = mn1 == -INFINITY ? 1.f : ex2(m2[1] - mn1);
-      float pe[4];
-      pe[0] = ex2(lg[0] - mn0);
-      pe[1] = ex2(lg[1] - mn1);
-      pe[2] = ex2(lg[2] - mn0);
-      pe[3] = ex2(lg[3] - mn1);
-      Zp[0] = fmaf(Zp[0], sc0, pe[0] + pe[2]);
-      Zp[1] = fmaf(Zp[1], sc1, pe[1] + pe[3]);
+      const float2 mn = make_float2(fmaxf(m2.x, bm.x), fmaxf(m2.y, bm.y));
+      const float2 scr = ex2x2(f2sub(m2, mn));
+      const float2 sc = make_float2(mn.x == -INFINITY ? 1.f : scr.x, mn.y == -INFINITY ? 1.f : scr.y);
+      const float2 dA = f2sub(lgA, mn), dB = f2sub(lgB, mn);
+      const float2 peA = ex2x2(dA), peB = ex2x2(dB);
+      Zp = __ffma2_rn(Zp, sc, __fadd2_rn(peA, peB));
       if (METER) {
-        const float mn[4] = {mn0, mn1, mn0, mn1};
-        float ta[4], tb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          ta[e] = meter_term(pe[e], lg[e], mn[e], eps[e]);
-          tb[e] = SCHEME == kInt8 ? meter_term(pe[e], lg[e], mn[e], ub[e]) : 0.f;
+        const float2 taA = meter_term2(peA, dA, epsA), taB = meter_term2(peB, dB, epsB);
+        SAp = __ffma2_rn(SAp, sc, __fadd2_rn(taA, taB));
+        float2 tbA = f2(0.f), tbB = f2(0.f);
+        if (SCHEME == kInt8) {
+          tbA = meter_term2(peA, dA, ubA);
+          tbB = meter_term2(peB, dB, ubB);
+          SBp = __ffma2_rn(SBp, sc, __fadd2_rn(tbA, tbB));
         }
-        SAp[0] = fmaf(SAp[0], sc0, ta[0] + ta[2]);
-        SAp[1] = fmaf(SAp[1], sc1, ta[1] + ta[3]);
-        SBp[0] = fmaf(SBp[0], sc0, tb[0] + tb[2]);
-        SBp[1] = fmaf(SBp[1], sc1, tb[1] + tb[3]);
         if (RISK) {
-          float r0 = SCHEME == kInt8 ? tb[0] + tb[2] : ta[0] + ta[2];
-          float r1 = SCHEME == kInt8 ? tb[1] + tb[3] : ta[1] + ta[3];
+          float2 r = SCHEME == kInt8 ? __fadd2_rn(tbA, tbB) : __fadd2_rn(taA, taB);
 #pragma unroll
           for (int o = 4; o < 32; o <<= 1) {
-            r0 += __shfl_xor_sync(0xffffffffu, r0, o);
-            r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+            r.x += __shfl_xor_sync(0xffffffffu, r.x, o);
+            r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
           }
           if (g == 0) {
-            if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(mn0, r0);
-            if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(mn1, r1);
+            if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(mn.x, r.x);
+            if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(mn.y, r.y);
           }
         }
       }
-      m2[0] = mn0; m2[1] = mn1;
-      if (__any_sync(0xffffffffu, sc0 != 1.f || sc1 != 1.f)) {
+      m2 = mn;
+      if (__any_sync(0xffffffffu, sc.x != 1.f || sc.y != 1.f)) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) { acco[mt][0] *= sc0; acco[mt][1] *= sc1; acco[mt][2] *= sc0; acco[mt][3] *= sc1; }
+        for (int mt = 0; mt < 8; ++mt) {
+          const float2 lo = __fmul2_rn(make_float2(acco[mt][0], acco[mt][1]), sc);
+          const float2 hi = __fmul2_rn(make_float2(acco[mt][2], acco[mt][3]), sc);
+          acco[mt][0] = lo.x; acco[mt][1] = lo.y; acco[mt][2] = hi.x; acco[mt][3] = hi.y;
+        }
       }
+      const float pe[4] = {peA.x, peA.y, peB.x, peB.y};
 
       // ------------------------------------------------------------ P V
       psm[(2 * t) * 16 + g] = pe[0];
@@ -511,7 +528,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           for (int G = 0; G < 4; ++G) { sv[e][G] = __half2float(vp[(e * 4 + G) * 2]); zv[e][G] = __half2float(vp[(e * 4 + G) * 2 + 1]); }
         const float pvv[4] = {pv.x, pv.y, pv.z, pv.w};
         // rescale of head g's zero accumulator: fetch sc of head g from lane g/2
-        const float sa = __shfl_sync(0xffffffffu, sc0, g >> 1), sbb = __shfl_sync(0xffffffffu, sc1, g >> 1);
+        const float sa = __shfl_sync(0xffffffffu, sc.x, g >> 1), sbb = __shfl_sync(0xffffffffu, sc.y, g >> 1);
         const float scg = (g & 1) ? sbb : sa;
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
@@ -562,12 +579,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // ---------------------------------------------------------------- partial state of this split
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
-    Zp[0] += __shfl_xor_sync(0xffffffffu, Zp[0], o);
-    Zp[1] += __shfl_xor_sync(0xffffffffu, Zp[1], o);
-    SAp[0] += __shfl_xor_sync(0xffffffffu, SAp[0], o);
-    SAp[1] += __shfl_xor_sync(0xffffffffu, SAp[1], o);
-    SBp[0] += __shfl_xor_sync(0xffffffffu, SBp[0], o);
-    SBp[1] += __shfl_xor_sync(0xffffffffu, SBp[1], o);
+    Zp.x += __shfl_xor_sync(0xffffffffu, Zp.x, o);
+    Zp.y += __shfl_xor_sync(0xffffffffu, Zp.y, o);
+    SAp.x += __shfl_xor_sync(0xffffffffu, SAp.x, o);
+    SAp.y += __shfl_xor_sync(0xffffffffu, SAp.y, o);
+    SBp.x += __shfl_xor_sync(0xffffffffu, SBp.x, o);
+    SBp.y += __shfl_xor_sync(0xffffffffu, SBp.y, o);
   }
   if (SCHEME == kKivi) {
     // add sum_t p_t zero_{t,G} of heads 2t, 2t+1 (held by lanes 4*head)
@@ -588,7 +605,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     const int head = 2 * t + hh;
     if (head >= grp) continue;
     float* rec = p.part + (((size_t)i * p.Hq + j0 + head) * p.n_splits + split) * kPartStride;
-    if (g == 0) { rec[0] = m2[hh]; rec[1] = Zp[hh]; rec[2] = SAp[hh]; rec[3] = SBp[hh]; }
+    if (g == 0)
+      *reinterpret_cast<float4*>(rec) = hh ? make_float4(m2.y, Zp.y, SAp.y, SBp.y) : make_float4(m2.x, Zp.x, SAp.x, SBp.x);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       rec[4 + 16 * mt + g] = acco[mt][hh];
@@ -678,37 +696,40 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, int NW>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, int NW>
 cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   using SM = Smem<NW, SCHEME>;
-  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, NW>;
+  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, GATE, NW>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, grid, dim3(NW * 32), SM::kBytes, st, pdl, a);
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE>
 cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   switch (a.seqs_per_cta) {
-    case 1: return run_split<SCHEME, QT, METER, RISK, 1>(a, grid, st, pdl);
-    case 2: return run_split<SCHEME, QT, METER, RISK, 2>(a, grid, st, pdl);
-    case 4: return run_split<SCHEME, QT, METER, RISK, 4>(a, grid, st, pdl);
-    case 8: return run_split<SCHEME, QT, METER, RISK, 8>(a, grid, st, pdl);
-    default: return run_split<SCHEME, QT, METER, RISK, 16>(a, grid, st, pdl);
+    case 1: return run_split<SCHEME, QT, METER, RISK, GATE, 1>(a, grid, st, pdl);
+    case 2: return run_split<SCHEME, QT, METER, RISK, GATE, 2>(a, grid, st, pdl);
+    case 4: return run_split<SCHEME, QT, METER, RISK, GATE, 4>(a, grid, st, pdl);
+    case 8: return run_split<SCHEME, QT, METER, RISK, GATE, 8>(a, grid, st, pdl);
+    default: return run_split<SCHEME, QT, METER, RISK, GATE, 16>(a, grid, st, pdl);
   }
+}
+
+// Instantiated combinations: meters off with and without a gate; meters on without a gate;
+// meters on with a gate, which always keeps block risks.
+template <int SCHEME, typename QT>
+cudaError_t dispatch_qt(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
+  const bool gate = a.slots != nullptr;
+  if (!a.meter) return gate ? dispatch_nw<SCHEME, QT, false, false, true>(a, grid, st, pdl)
+                            : dispatch_nw<SCHEME, QT, false, false, false>(a, grid, st, pdl);
+  if (gate) return dispatch_nw<SCHEME, QT, true, true, true>(a, grid, st, pdl);
+  return dispatch_nw<SCHEME, QT, true, false, false>(a, grid, st, pdl);
 }
 
 template <int SCHEME>
 cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
-  const bool risk = a.risk_raw != nullptr;
-  if (a.is_bf16) {
-    if (!a.meter) return dispatch_nw<SCHEME, __nv_bfloat16, false, false>(a, grid, st, pdl);
-    return risk ? dispatch_nw<SCHEME, __nv_bfloat16, true, true>(a, grid, st, pdl)
-                : dispatch_nw<SCHEME, __nv_bfloat16, true, false>(a, grid, st, pdl);
-  }
-  if (!a.meter) return dispatch_nw<SCHEME, float, false, false>(a, grid, st, pdl);
-  return risk ? dispatch_nw<SCHEME, float, true, true>(a, grid, st, pdl)
-              : dispatch_nw<SCHEME, float, true, false>(a, grid, st, pdl);
+  return a.is_bf16 ? dispatch_qt<SCHEME, __nv_bfloat16>(a, grid, st, pdl) : dispatch_qt<SCHEME, float>(a, grid, st, pdl);
 }
 
 int seqs_per_cta_for(int B) { return B >= 16 ? 16 : B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
