@@ -54,9 +54,15 @@ __host__ __device__ inline int kcode_off(int r, int c) {
   int L = 4 * g + t, j = kk >> 1, slot = ((kk & 1) << 1) | h;
   return j * 512 + L * 16 + slot * 4 + e;
 }
+// Token r of a block as a k index of the P.V product (tokens as k, natural order):
+// lane t holds k 2t, 2t+1 in its first register and 2t+8, 2t+9 in its second, the
+// layout a transposed (movmatrix) softmax fragment arrives in.  Slot e = 0..3 of
+// lane t is token 2t, 2t+1, 2t+8, 2t+9.
+__host__ __device__ inline int pv_lane(int r) { return (r & 7) >> 1; }
+__host__ __device__ inline int pv_slot(int r) { return (r & 1) | ((r >> 3) << 1); }
 // 1-byte V code: PV^T with channels as rows and tokens as k.
 __host__ __device__ inline int vcode_off(int r, int c) {
-  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = r >> 2, e = r & 3;
+  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = pv_lane(r), e = pv_slot(r);
   int L = 4 * g + t, j = mt >> 1, slot = ((mt & 1) << 1) | h;
   return j * 512 + L * 16 + slot * 4 + e;
 }
@@ -68,9 +74,9 @@ __host__ __device__ inline int wit_off(int r, int b) {
   int L = 4 * g + t, reg = h + 2 * hi;
   return L * 16 + reg * 4 + e * 2;
 }
-// fp16 INT8 value scale of token r, group G: stored group-major so the four
-// tokens a lane needs for the P.V operand are adjacent.
-__host__ __device__ inline int vscale_off(int r, int G) { return (G * 16 + r) * 2; }
+// fp16 INT8 value scale of token r, group G: stored group-major, tokens in P.V slot
+// order, so the four scales a lane needs for the P.V operand are adjacent.
+__host__ __device__ inline int vscale_off(int r, int G) { return (G * 16 + 4 * pv_lane(r) + pv_slot(r)) * 2; }
 // 2-bit KIVI codes: word (byte offset) and bit position.  Each 32-bit word holds
 // eight fp16x2 register pairs; pair p keeps its two codes at bits 2p and 16+2p.
 __host__ __device__ inline void kivi_k_pos(int r, int c, int& word_off, int& bit) {
@@ -80,7 +86,7 @@ __host__ __device__ inline void kivi_k_pos(int r, int c, int& word_off, int& bit
   bit = 2 * p + 16 * (e & 1);
 }
 __host__ __device__ inline void kivi_v_pos(int r, int c, int& word_off, int& bit) {
-  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = r >> 2, e = r & 3;
+  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = pv_lane(r), e = pv_slot(r);
   int L = 4 * g + t, j = mt >> 1, reg = h + 2 * (e >> 1), p = (mt & 1) * 4 + reg;
   word_off = L * 16 + j * 4;
   bit = 2 * p + 16 * (e & 1);
@@ -147,9 +153,9 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float rsqrt_approx(float x) {
+__device__ __forceinline__ float sqrt_approx(float x) {
   float y;
-  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -165,6 +171,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Transpose of an 8x8 fp16 matrix held as mma fragments (lane 4g + t holds row g,
+// columns 2t, 2t+1; afterwards it holds row g of the transpose).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // ------------------------------------------------------------------ small conversions
@@ -225,16 +239,21 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded mbarrier wait: returns false once `limit_ns` of wall time has passed.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded mbarrier wait: returns false once `limit_ns` of wall time has passed.  The
+// clock is read only when the first attempt does not find the phase complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    if (ok) return true;
+    if (mbar_try(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
 }

@@ -62,9 +62,7 @@ template <int NW, int SCHEME> struct Smem {
   static constexpr int kXi = SCHEME == kInt8 ? 2 * kXiBytes : 0;
   static constexpr int kRingOff = 0;
   static constexpr int kXiOff = (kRing + 127) / 128 * 128;
-  static constexpr int kPsmOff = kXiOff + kXi;                 // NW x float[8][16]
-  static constexpr int kQgOff = kPsmOff + NW * 512;            // NW x float[8][4]
-  static constexpr int kBarOff = kQgOff + NW * 128;            // NW x NST x u64
+  static constexpr int kBarOff = kXiOff + kXi;                 // NW x NST x u64
   static constexpr int kBytes = kBarOff + NW * NST * 8;
 };
 
@@ -76,53 +74,59 @@ __device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __fadd2_rn(
 // p * expm1(c) for c >= 0, with p = e^(l - m) and d = l - m in log2 units.  Below c = 1/8
 // the series c + c^2/2 + c^3/6 + c^4/24 (truncation < 2e-6 relative); above it the term is
 // formed in the exponent, e^(l - m + c) - e^(l - m), which neither overflows for large c
-// nor loses a flushed p, and cancels at most a factor e^c/(e^c - 1) < 8.6 of precision.
+// nor loses a p that flushed to zero, and cancels at most a factor e^c/(e^c - 1) < 8.6 of
+// precision.  Tokens past the context arrive with d = -inf and c = 0 and give 0.
 __device__ __forceinline__ float2 meter_term2(float2 pe, float2 d, float2 c) {
   float2 poly = __ffma2_rn(c, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
   poly = __ffma2_rn(c, poly, f2(0.5f));
   poly = __ffma2_rn(c, poly, f2(1.0f));
   poly = __fmul2_rn(__fmul2_rn(c, poly), pe);
   const float2 big = f2sub(ex2x2(__ffma2_rn(c, f2(kLog2e), d)), pe);
-  return make_float2(pe.x > 0.0f && c.x > 0.0f ? (c.x < 0.125f ? poly.x : big.x) : 0.0f,
-                     pe.y > 0.0f && c.y > 0.0f ? (c.y < 0.125f ? poly.y : big.y) : 0.0f);
+  return make_float2(c.x < 0.125f ? poly.x : big.x, c.y < 0.125f ? poly.y : big.y);
 }
 
 // Regenerate the dither of block `blk` of KV head h into shared memory, in the
 // fragment order of the QK operands (negated, fp16 hi + lo) and of the PV operand
 // (negated, fp16): each lane's four A registers are contiguous, so one 16-byte load
-// fills an MMA operand.  Work item = (tensor, column of 4 channels, pair of tokens).
+// fills an MMA operand.  Items 0..255 fill the QK operands, one (k-step, lane) each, with
+// 16-byte stores; items 256..511 fill the PV operand, one (token pair, channel quad) each.
 __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
+  const int tb = blk * kBlk;
   for (int idx = threadIdx.x; idx < 512; idx += nthreads) {
-    const int tq = idx & 3, rp = (idx >> 2) & 7, kq = (idx >> 5) & 7, tensor = idx >> 8;
-    const int quad = kq * 4 + tq;
-    const int r0 = 2 * rp;
-    const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0, quad, tensor);
-    const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, blk * kBlk + r0 + 1, quad, tensor);
-    if (tensor == 0) {
+    if (idx < 256) {
+      // k-step kk, lane L = 4g + tq: tokens g and g + 8, channels 16kk + 4tq .. 16kk + 4tq + 3.
+      // Registers R0 = (g, ch +0,+1), R1 = (g + 8, ch +0,+1), R2 = (g, ch +2,+3), R3 = (g + 8, ch +2,+3).
+      const int kk = idx >> 5, L = idx & 31, g = L >> 2, quad = 4 * kk + (L & 3);
+      const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g, quad, 0);
+      const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g + 8, quad, 0);
+      const float2 v[4] = {make_float2(x0.x, x0.y), make_float2(x1.x, x1.y), make_float2(x0.z, x0.w),
+                           make_float2(x1.z, x1.w)};
+      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float4 x = u ? x1 : x0;
-        const int r = r0 + u, L = 4 * (r & 7) + tq, hh = r >> 3;
-        // hi = fp16(-xi), lo = fp16(-xi - hi): packed conversions, two values per instruction;
-        // channels +0,+1 go to register R(hh), channels +2,+3 to R(2+hh) of lane L
-        const __half2 h01 = __floats2half2_rn(x.x, x.y), h23 = __floats2half2_rn(x.z, x.w);
-        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-        const __half2 l01 = __floats2half2_rn(x.x - f01.x, x.y - f01.y), l23 = __floats2half2_rn(x.z - f23.x, x.w - f23.y);
-        uint32_t* hi = reinterpret_cast<uint32_t*>(xb + kXiKHi + (kq * 32 + L) * 16);
-        uint32_t* lo = reinterpret_cast<uint32_t*>(xb + kXiKLo + (kq * 32 + L) * 16);
-        hi[hh] = h2_bits(h01); hi[2 + hh] = h2_bits(h23);
-        lo[hh] = h2_bits(l01); lo[2 + hh] = h2_bits(l23);
+      for (int r = 0; r < 4; ++r) {
+        // hi = fp16(-xi), lo = fp16(-xi - hi), two values per conversion
+        const __half2 hh = __floats2half2_rn(v[r].x, v[r].y);
+        const float2 f = __half22float2(hh);
+        hw[r] = h2_bits(hh);
+        lw[r] = h2_bits(__floats2half2_rn(v[r].x - f.x, v[r].y - f.y));
       }
+      *reinterpret_cast<uint4*>(xb + kXiKHi + idx * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(xb + kXiKLo + idx * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     } else {
+      // Tokens 2pr, 2pr + 1 (pr = t + 4 hi) of channels 4q .. 4q + 3.  Channel c goes to m-tile
+      // c >> 4, lane 4 (c & 7) + t, register ((c >> 3) & 1) + 2 hi.  The item's bits are laid
+      // out so that a warp's stores fall on 16 banks.
+      const int v = idx - 256;
+      const int t = v & 3, hi = (v >> 2) & 1, q = ((v >> 4) & 1) | (((v >> 3) & 1) << 1) | ((v >> 5) << 2);
+      const int r0 = 2 * (t + 4 * hi);
+      const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + r0, q, 1);
+      const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + r0 + 1, q, 1);
       const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
-      const int tv = r0 >> 2, reg_hi = 2 * ((r0 & 3) >> 1);
-      uint32_t* v = reinterpret_cast<uint32_t*>(xb + kXiV);
+      uint32_t* vb = reinterpret_cast<uint32_t*>(xb + kXiV);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c = 4 * quad + e;
-        const int gg = c & 7, hh = (c >> 3) & 1;
-        const int L = 4 * gg + tv, reg = hh + reg_hi;
-        v[(kq * 32 + L) * 4 + reg] = h2_bits(__floats2half2_rn(a0[e], a1[e]));
+        const int c = 4 * q + e;
+        vb[((c >> 4) * 32 + 4 * (c & 7) + t) * 4 + ((c >> 3) & 1) + 2 * hi] = h2_bits(__floats2half2_rn(a0[e], a1[e]));
       }
     }
   }
@@ -181,8 +185,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
   uint8_t* ring = smem + SM::kRingOff + warp * NST * L::BYTES;
   uint8_t* xib = smem + SM::kXiOff;
-  float* psm = reinterpret_cast<float*>(smem + SM::kPsmOff) + warp * 128;
-  float* qgs = reinterpret_cast<float*>(smem + SM::kQgOff) + warp * 32;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOff) + warp * NST;
 
   const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   float zc[4] = {0.f, 0.f, 0.f, 0.f};           // KIVI: sum_t p_t zero_{t,G} for head g
   const float lscale = __fdiv_rn(kLog2e, sqrtf(128.0f));
   // Tier B: u = kappa * sqrt(var).  var is summed with nearest rounding (4 terms) and the
-  // SFU square root is within 2^-21 relative; this factor covers both.
+  // SFU square root is within 2^-22 relative; this factor covers both.
   const float kappa_up = p.kappa * (1.0f + 1.9073486328125e-6f);
   float2 qgp[4];
 #pragma unroll
@@ -302,7 +304,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     if (active && !fault) {
       const uint8_t* sb = ring + stage * L::BYTES;
       const int slot = GATE ? p.slots[seq_base + blk] : -1;
-      const bool kivi_tail = SCHEME == kKivi && (blk + 1) * kBlk > p.S;
+      const bool ragged = (blk + 1) * kBlk > p.S;      // the context ends inside this block
+      const bool kivi_tail = SCHEME == kKivi && ragged;
       float2 lgA, lgB, epsA = f2(0.f), epsB = f2(0.f), ubA = f2(0.f), ubB = f2(0.f);
 
       if ((GATE && slot >= 0) || kivi_tail) {
@@ -358,12 +361,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             varA = __ffma2_rn(f2(sgA[G] * sgA[G]), qgp[G], varA);
             varB = __ffma2_rn(f2(sgB[G] * sgB[G]), qgp[G], varB);
           }
-          const float2 rA = make_float2(rsqrt_approx(varA.x), rsqrt_approx(varA.y));
-          const float2 rB = make_float2(rsqrt_approx(varB.x), rsqrt_approx(varB.y));
-          const float2 uA = __fmul2_rn(__fmul2_rn(varA, rA), f2(kappa_up));
-          const float2 uB = __fmul2_rn(__fmul2_rn(varB, rB), f2(kappa_up));
-          ubA = make_float2(varA.x > 0.f ? uA.x : 0.f, varA.y > 0.f ? uA.y : 0.f);
-          ubB = make_float2(varB.x > 0.f ? uB.x : 0.f, varB.y > 0.f ? uB.y : 0.f);
+          ubA = __fmul2_rn(make_float2(sqrt_approx(varA.x), sqrt_approx(varA.y)), f2(kappa_up));
+          ubB = __fmul2_rn(make_float2(sqrt_approx(varB.x), sqrt_approx(varB.y)), f2(kappa_up));
         }
       } else if constexpr (SCHEME == kFp8) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};   // two chains
@@ -430,32 +429,57 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
       if (GATE && slot >= 0) { ubA = f2(0.f); ubB = f2(0.f); }
 
-      // mask tokens past the context
-      const int tok0 = blk * kBlk + g, tok1 = tok0 + 8;
-      if (tok0 >= p.S) lgA = f2(-INFINITY);
-      if (tok1 >= p.S) lgB = f2(-INFINITY);
+      if (ragged) {   // tokens past the context: no weight, no meter term
+        const int tok0 = blk * kBlk + g, tok1 = tok0 + 8;
+        if (tok0 >= p.S) { lgA = f2(-INFINITY); epsA = f2(0.f); ubA = f2(0.f); }
+        if (tok1 >= p.S) { lgB = f2(-INFINITY); epsB = f2(0.f); ubB = f2(0.f); }
+      }
 
       // ------------------------------------------------------------ online softmax + meters
-      float2 bm = make_float2(fmaxf(lgA.x, lgB.x), fmaxf(lgA.y, lgB.y));
+      // The running max m2 moves only when a logit of the block exceeds it; otherwise the
+      // block's weights are taken against m2 as it stands (p <= 1 either way).
+      float2 dA = f2sub(lgA, m2), dB = f2sub(lgB, m2);
+      const bool grows = lgA.x > m2.x || lgA.y > m2.y || lgB.x > m2.x || lgB.y > m2.y;
+      if (__any_sync(0xffffffffu, grows)) {
+        float2 bm = make_float2(fmaxf(lgA.x, lgB.x), fmaxf(lgA.y, lgB.y));
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        bm.x = fmaxf(bm.x, __shfl_xor_sync(0xffffffffu, bm.x, o));
-        bm.y = fmaxf(bm.y, __shfl_xor_sync(0xffffffffu, bm.y, o));
+        for (int o = 4; o < 32; o <<= 1) {
+          bm.x = fmaxf(bm.x, __shfl_xor_sync(0xffffffffu, bm.x, o));
+          bm.y = fmaxf(bm.y, __shfl_xor_sync(0xffffffffu, bm.y, o));
+        }
+        const float2 mn = make_float2(fmaxf(m2.x, bm.x), fmaxf(m2.y, bm.y));
+        const float2 scr = ex2x2(f2sub(m2, mn));
+        const float2 sc = make_float2(mn.x == -INFINITY ? 1.f : scr.x, mn.y == -INFINITY ? 1.f : scr.y);
+        dA = f2sub(lgA, mn);
+        dB = f2sub(lgB, mn);
+        m2 = mn;
+        Zp = __fmul2_rn(Zp, sc);
+        SAp = __fmul2_rn(SAp, sc);
+        SBp = __fmul2_rn(SBp, sc);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const float2 lo = __fmul2_rn(make_float2(acco[mt][0], acco[mt][1]), sc);
+          const float2 hi = __fmul2_rn(make_float2(acco[mt][2], acco[mt][3]), sc);
+          acco[mt][0] = lo.x; acco[mt][1] = lo.y; acco[mt][2] = hi.x; acco[mt][3] = hi.y;
+        }
+        if constexpr (SCHEME == kKivi) {
+          // head g's zero accumulator: its factor sits in lane g/2
+          const float sa = __shfl_sync(0xffffffffu, sc.x, g >> 1), sbb = __shfl_sync(0xffffffffu, sc.y, g >> 1);
+          const float scg = (g & 1) ? sbb : sa;
+#pragma unroll
+          for (int G = 0; G < 4; ++G) zc[G] *= scg;
+        }
       }
-      const float2 mn = make_float2(fmaxf(m2.x, bm.x), fmaxf(m2.y, bm.y));
-      const float2 scr = ex2x2(f2sub(m2, mn));
-      const float2 sc = make_float2(mn.x == -INFINITY ? 1.f : scr.x, mn.y == -INFINITY ? 1.f : scr.y);
-      const float2 dA = f2sub(lgA, mn), dB = f2sub(lgB, mn);
       const float2 peA = ex2x2(dA), peB = ex2x2(dB);
-      Zp = __ffma2_rn(Zp, sc, __fadd2_rn(peA, peB));
+      Zp = __fadd2_rn(Zp, __fadd2_rn(peA, peB));
       if (METER) {
         const float2 taA = meter_term2(peA, dA, epsA), taB = meter_term2(peB, dB, epsB);
-        SAp = __ffma2_rn(SAp, sc, __fadd2_rn(taA, taB));
+        SAp = __fadd2_rn(SAp, __fadd2_rn(taA, taB));
         float2 tbA = f2(0.f), tbB = f2(0.f);
         if (SCHEME == kInt8) {
           tbA = meter_term2(peA, dA, ubA);
           tbB = meter_term2(peB, dB, ubB);
-          SBp = __ffma2_rn(SBp, sc, __fadd2_rn(tbA, tbB));
+          SBp = __fadd2_rn(SBp, __fadd2_rn(tbA, tbB));
         }
         if (RISK) {
           float2 r = SCHEME == kInt8 ? __fadd2_rn(tbA, tbB) : __fadd2_rn(taA, taB);
@@ -465,31 +489,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             r.y += __shfl_xor_sync(0xffffffffu, r.y, o);
           }
           if (g == 0) {
-            if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(mn.x, r.x);
-            if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(mn.y, r.y);
+            if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(m2.x, r.x);
+            if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(m2.y, r.y);
           }
         }
       }
-      m2 = mn;
-      if (__any_sync(0xffffffffu, sc.x != 1.f || sc.y != 1.f)) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const float2 lo = __fmul2_rn(make_float2(acco[mt][0], acco[mt][1]), sc);
-          const float2 hi = __fmul2_rn(make_float2(acco[mt][2], acco[mt][3]), sc);
-          acco[mt][0] = lo.x; acco[mt][1] = lo.y; acco[mt][2] = hi.x; acco[mt][3] = hi.y;
-        }
-      }
-      const float pe[4] = {peA.x, peA.y, peB.x, peB.y};
 
       // ------------------------------------------------------------ P V
-      psm[(2 * t) * 16 + g] = pe[0];
-      psm[(2 * t + 1) * 16 + g] = pe[1];
-      psm[(2 * t) * 16 + g + 8] = pe[2];
-      psm[(2 * t + 1) * 16 + g + 8] = pe[3];
-      __syncwarp();
-      const float4 pv = *reinterpret_cast<const float4*>(psm + g * 16 + 4 * t);
+      // Weights as fp16 (token g / g + 8 by heads 2t, 2t+1), transposed in registers into the
+      // B operand: P0 = head g, tokens 2t, 2t+1; P1 = head g, tokens 2t+8, 2t+9.
+      const uint32_t P0 = movmatrix_trans(h2_bits(__floats2half2_rn(peA.x, peA.y)));
+      const uint32_t P1 = movmatrix_trans(h2_bits(__floats2half2_rn(peB.x, peB.y)));
       if constexpr (SCHEME == kFp8) {
-        const uint32_t bfr[2] = {h2_bits(__floats2half2_rn(pv.x, pv.y)), h2_bits(__floats2half2_rn(pv.z, pv.w))};
+        const uint32_t bfr[2] = {P0, P1};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint4 vw = *reinterpret_cast<const uint4*>(sb + L::VC + j * 512 + lane * 16);
@@ -501,12 +513,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           }
         }
       } else if constexpr (SCHEME == kInt8) {
-        // B_j = (p * s_j) in fp16 for tokens 4t..4t+3 of head g; A = exact codes, then -xi
-        const __half2 p01 = __floats2half2_rn(pv.x, pv.y), p23 = __floats2half2_rn(pv.z, pv.w);
+        // B_j = (p * s_j) in fp16; A = exact codes, then -xi
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint2 sv = *reinterpret_cast<const uint2*>(sb + L::VS + vscale_off(4 * t, j));
-          const uint32_t bfr[2] = {h2_bits(__hmul2(p01, bits_h2(sv.x))), h2_bits(__hmul2(p23, bits_h2(sv.y)))};
+          const uint2 sv = *reinterpret_cast<const uint2*>(sb + L::VS + (j * 16 + 4 * t) * 2);
+          const uint32_t bfr[2] = {h2_bits(__hmul2(bits_h2(P0), bits_h2(sv.x))), h2_bits(__hmul2(bits_h2(P1), bits_h2(sv.y)))};
           const uint4 vw = *reinterpret_cast<const uint4*>(sb + L::VC + j * 512 + lane * 16);
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
@@ -520,16 +531,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           }
         }
       } else {  // KIVI values: p*scale times codes, plus p*zero per group
-        const __half* vp = reinterpret_cast<const __half*>(sb + L::VP) + 4 * t * 8;   // [tok][G][scale, zero]
+        // [tok][G][scale, zero]; this lane's tokens 2t, 2t+1 and 2t+8, 2t+9 are two 32-byte runs
+        const __half* vp = reinterpret_cast<const __half*>(sb + L::VP);
+        const float2 p01 = __half22float2(bits_h2(P0)), p23 = __half22float2(bits_h2(P1));
+        const float pvv[4] = {p01.x, p01.y, p23.x, p23.y};
         float sv[4][4], zv[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
+        for (int e = 0; e < 4; ++e) {
+          const __half* row = vp + (2 * t + (e & 1) + 8 * (e >> 1)) * 8;
 #pragma unroll
-          for (int G = 0; G < 4; ++G) { sv[e][G] = __half2float(vp[(e * 4 + G) * 2]); zv[e][G] = __half2float(vp[(e * 4 + G) * 2 + 1]); }
-        const float pvv[4] = {pv.x, pv.y, pv.z, pv.w};
-        // rescale of head g's zero accumulator: fetch sc of head g from lane g/2
-        const float sa = __shfl_sync(0xffffffffu, sc.x, g >> 1), sbb = __shfl_sync(0xffffffffu, sc.y, g >> 1);
-        const float scg = (g & 1) ? sbb : sa;
+          for (int G = 0; G < 4; ++G) { sv[e][G] = __half2float(row[2 * G]); zv[e][G] = __half2float(row[2 * G + 1]); }
+        }
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
           float z = 0.f;
@@ -537,7 +549,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           for (int e = 0; e < 4; ++e) z = fmaf(pvv[e], zv[e][G], z);
           z += __shfl_xor_sync(0xffffffffu, z, 1);
           z += __shfl_xor_sync(0xffffffffu, z, 2);
-          zc[G] = fmaf(zc[G], scg, z);
+          zc[G] += z;
         }
         const uint4 vw4 = *reinterpret_cast<const uint4*>(sb + L::VC + lane * 16);
         const uint32_t vwords[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
