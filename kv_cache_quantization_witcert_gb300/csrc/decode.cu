@@ -30,6 +30,7 @@
 // before writing its partial results, and, with block risks on, before its first
 // risk store.  Older blocks, the dither and the queries are used without waiting,
 // so the write's latency overlaps the decode.
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -65,6 +66,16 @@ template <int NW, int SCHEME> struct Smem {
   static constexpr int kBarOff = kXiOff + kXi;                 // NW x NST x u64
   static constexpr int kBytes = kBarOff + NW * NST * 8;
 };
+
+// An upper bound of sqrt(x) at most one unit above the correctly rounded value: the SFU
+// root, raised one unit while its square (exact sign from one FMA) is below x; the exactly
+// rounded-up root if that is still short.
+__device__ __forceinline__ float sqrt_up(float x) {
+  float y = sqrt_approx(x);
+  if (fmaf(y, y, -x) < 0.0f) y = __uint_as_float(__float_as_uint(y) + 1u);
+  if (fmaf(y, y, -x) < 0.0f) y = __fsqrt_ru(x);
+  return y;
+}
 
 // Packed pairs (two query heads of a lane): fp32x2 arithmetic of sm_100+.
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
@@ -144,6 +155,24 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bf
                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
 }
 
+// Four consecutive elements kept as loaded (bf16: two registers) until they are needed.
+template <typename T> struct Raw4;
+template <> struct Raw4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ void zero() { v = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float4 get() const { return v; }
+};
+template <> struct Raw4<__nv_bfloat16> {
+  uint2 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ void zero() { u = make_uint2(0u, 0u); }
+  __device__ __forceinline__ float4 get() const {
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+  }
+};
+
 // Exact-key logits of one block (repaired block from the pool, or KIVI's unfinished block).
 template <typename KT, bool QLO>
 __device__ __forceinline__ void exact_block_logits(const KT* ex, const uint32_t (&qb)[8][2],
@@ -190,18 +219,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
   const uint8_t* src = p.blocks + (seq_base + b_begin) * L::BYTES;
 
-  // ---------------------------------------------------------------- prologue independent of memory
+  // ---------------------------------------------------------------- prologue
   if (active && lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&bars[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   pdl_trigger();
-  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
-  // blocks from p.dirty_blk on may still be written by the immediately preceding kernel
-  if (RISK) pdl_wait();
-
+  // the first blocks' copies go out before anything else; blocks from p.dirty_blk on may
+  // still be written by the immediately preceding kernel
   if (active && lane == 0) {
-    fence_proxy_async();
     for (int s = 0; s < NST && s < nb; ++s) {
       if (b_begin + s >= p.dirty_blk) pdl_wait();
       mbar_expect_tx(smem_addr(&bars[s]), L::BYTES);
@@ -211,55 +237,61 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   __syncwarp();
 
   // ---------------------------------------------------------------- query fragments
-  uint32_t qb[8][2], qbl[8][2], qnb[2], qnl[2];
-  float qg2[2][4];
+  // lane (g, t) holds channels 16kk + 4t .. 16kk + 4t + 3 (kk = 0..7) of query head g: the B
+  // fragments of every k-step, the dims of bands t, t+4, t+8, t+12 and 8 channels of each
+  // 32-channel group.  The loads are issued here and consumed after the first block's dither.
+  const bool has_q = active && g < grp;
+  Raw4<QT> qraw[8];
+  {
+    const QT* qr = reinterpret_cast<const QT*>(p.q) + ((size_t)(has_q ? i : 0) * p.Hq + j0 + (has_q ? g : 0)) * kD + 4 * t;
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) { qb[kk][0] = qb[kk][1] = qbl[kk][0] = qbl[kk][1] = 0u; }
-  qnb[0] = qnb[1] = qnl[0] = qnl[1] = 0u;
-  const QT* qbase = reinterpret_cast<const QT*>(p.q);
-  if (active) {
-    // lane (g, t) holds channels 16kk + 4t .. 16kk + 4t + 3 (kk = 0..7) of query head g:
-    // the B fragments of every k-step, the dims of bands t, t+4, t+8, t+12 and 8 channels of
-    // each 32-channel group
-    float bss[4] = {0.f, 0.f, 0.f, 0.f}, gss[4] = {0.f, 0.f, 0.f, 0.f};
-    if (g < grp) {
-      const QT* qr = qbase + ((size_t)i * p.Hq + j0 + g) * kD + 4 * t;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const float4 v4 = load4<QT>(qr + 16 * kk);
-        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-        __half hv[4], lv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          split_h(v[e], hv[e], lv[e]);
-          bss[kk & 3] = __fmaf_ru(v[e], v[e], bss[kk & 3]);
-          gss[kk >> 1] = __fmaf_ru(v[e], v[e], gss[kk >> 1]);
-        }
-        qb[kk][0] = pack_h2(hv[0], hv[1]); qb[kk][1] = pack_h2(hv[2], hv[3]);
-        qbl[kk][0] = pack_h2(lv[0], lv[1]); qbl[kk][1] = pack_h2(lv[2], lv[3]);
-      }
+    for (int kk = 0; kk < 8; ++kk) {
+      if (has_q) qraw[kk].load(qr + 16 * kk); else qraw[kk].zero();
     }
+  }
+  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
+
+  uint32_t qb[8][2], qbl[8][2], qnb[2], qnl[2];
+  float qg2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  {
+    float bss[4] = {0.f, 0.f, 0.f, 0.f}, gss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const float4 v4 = qraw[kk].get();
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      __half hv[4], lv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        split_h(v[e], hv[e], lv[e]);
+        bss[kk & 3] = __fmaf_ru(v[e], v[e], bss[kk & 3]);
+        gss[kk >> 1] = __fmaf_ru(v[e], v[e], gss[kk >> 1]);
+      }
+      qb[kk][0] = pack_h2(hv[0], hv[1]); qb[kk][1] = pack_h2(hv[2], hv[3]);
+      qbl[kk][0] = pack_h2(lv[0], lv[1]); qbl[kk][1] = pack_h2(lv[2], lv[3]);
+    }
+    qnb[0] = qnb[1] = qnl[0] = qnl[1] = 0u;
     if (METER) {
       // ||q_b|| / sqrt(d) for bands t, t+4 (k 2t, 2t+1) and t+8, t+12 (k 2t+8, 2t+9), rounded up,
-      // as fp16 hi + lo (lo rounded up)
-      const float inv_sqrt_d_up = __fdiv_ru(1.0f, __fsqrt_rd(128.0f));
+      // as fp16 hi + lo (lo rounded up).  0x1.6a09e8p-4 is 1/sqrt(128) rounded up.  The Tier A
+      // meter grows like e^eps, so the norm is kept within one unit of its true value.
       __half bh[4], bl[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const float nb_up = __fmul_ru(__fsqrt_ru(bss[m]), inv_sqrt_d_up);
+        const float nb_up = __fmul_ru(sqrt_up(bss[m]), 0x1.6a09e8p-4f);
         bh[m] = __float2half_rn(nb_up);
         bl[m] = __float2half_ru(nb_up - __half2float(bh[m]));
       }
       qnb[0] = pack_h2(bh[0], bh[1]); qnb[1] = pack_h2(bh[2], bh[3]);
       qnl[0] = pack_h2(bl[0], bl[1]); qnl[1] = pack_h2(bl[2], bl[3]);
       if (SCHEME == kInt8) {
-        // sum_{c in G} q_c^2 / (12 d), rounded up, for heads 2t and 2t+1 (the logit layout)
+        // sum_{c in G} q_c^2 / (12 d), rounded up (0x1.555556p-11 is 1/1536 rounded up), for
+        // heads 2t and 2t+1 (the logit layout)
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
           float v = gss[G];
           v = __fadd_ru(v, __shfl_xor_sync(0xffffffffu, v, 1));
           v = __fadd_ru(v, __shfl_xor_sync(0xffffffffu, v, 2));
-          gss[G] = __fmul_ru(v, __fdiv_ru(1.0f, 1536.0f));
+          gss[G] = __fmul_ru(v, 0x1.555556p-11f);
         }
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
@@ -269,6 +301,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
     }
   }
+  if (RISK) pdl_wait();    // block risks overwrite rows the preceding merge may still read
 
   // ---------------------------------------------------------------- state
   // per lane: heads 2t (.x) and 2t+1 (.y); A = token g, B = token g+8 of the block
@@ -277,7 +310,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) acco[mt][0] = acco[mt][1] = acco[mt][2] = acco[mt][3] = 0.f;
   float zc[4] = {0.f, 0.f, 0.f, 0.f};           // KIVI: sum_t p_t zero_{t,G} for head g
-  const float lscale = __fdiv_rn(kLog2e, sqrtf(128.0f));
+  const float lscale = kLog2e * 0x1.6a09e6p-4f;   // log2(e) / sqrt(128), 1/sqrt(128) to nearest
   // Tier B: u = kappa * sqrt(var).  var is summed with nearest rounding (4 terms) and the
   // SFU square root is within 2^-22 relative; this factor covers both.
   const float kappa_up = p.kappa * (1.0f + 1.9073486328125e-6f);
@@ -708,11 +741,26 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Dynamic shared memory above 48 KB is opted into once per kernel and device; `done` is
+// the calling kernel's own record (one per instantiation of the caller).
+template <typename K>
+cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, int NW>
 cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   using SM = Smem<NW, SCHEME>;
+  static std::atomic<uint64_t> smem_done{0};
   auto k = decode_split_kernel<SCHEME, QT, METER, RISK, GATE, NW>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+  cudaError_t e = allow_smem(k, SM::kBytes, smem_done);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, grid, dim3(NW * 32), SM::kBytes, st, pdl, a);
 }
