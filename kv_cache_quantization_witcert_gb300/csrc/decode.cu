@@ -321,11 +321,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   if (SCHEME == kInt8) __syncthreads();
 
   bool fault = false;
+  const bool gen_early = ((warp >> 2) & 1) == 0;
   for (int n = 0; n < nb; ++n) {
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
     const uint8_t* xb = xib + (n & 1) * kXiBytes;
-    if (SCHEME == kInt8 && n + 1 < nb) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
+    // The next block's dither: half of the warps (two per scheduler) make their share before
+    // this block's logits, the other half between its softmax and its P.V product, so that the
+    // integer work of the one overlaps the tensor and FP32 work of the other.
+    const bool gen_next = SCHEME == kInt8 && n + 1 < nb;
+    if (gen_next && gen_early) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
 
     if (active && !fault) {
       if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs)) {
@@ -334,8 +339,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
     }
     if (blk >= p.dirty_blk) pdl_wait();             // also covers the exact pool and KIVI tail rows
-    if (active && !fault) {
-      const uint8_t* sb = ring + stage * L::BYTES;
+    const bool live = active && !fault;
+    const uint8_t* sb = ring + stage * L::BYTES;
+    uint32_t P0 = 0u, P1 = 0u;
+    if (live) {
       const int slot = GATE ? p.slots[seq_base + blk] : -1;
       const bool ragged = (blk + 1) * kBlk > p.S;      // the context ends inside this block
       const bool kivi_tail = SCHEME == kKivi && ragged;
@@ -531,8 +538,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       // ------------------------------------------------------------ P V
       // Weights as fp16 (token g / g + 8 by heads 2t, 2t+1), transposed in registers into the
       // B operand: P0 = head g, tokens 2t, 2t+1; P1 = head g, tokens 2t+8, 2t+9.
-      const uint32_t P0 = movmatrix_trans(h2_bits(__floats2half2_rn(peA.x, peA.y)));
-      const uint32_t P1 = movmatrix_trans(h2_bits(__floats2half2_rn(peB.x, peB.y)));
+      P0 = movmatrix_trans(h2_bits(__floats2half2_rn(peA.x, peA.y)));
+      P1 = movmatrix_trans(h2_bits(__floats2half2_rn(peB.x, peB.y)));
+    }
+    if (gen_next && !gen_early) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
+    if (live) {
       if constexpr (SCHEME == kFp8) {
         const uint32_t bfr[2] = {P0, P1};
 #pragma unroll
