@@ -57,14 +57,23 @@ template <> struct Lay<kKivi> : KiviLayout {};
 template <int NW> struct Stages { static constexpr int value = NW >= 8 ? 2 : NW == 4 ? 3 : 4; };
 template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : 2; };
 
+// Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
+// warps consume, so warps may drift up to two blocks apart (one with three slots, which is
+// what two 8-warp CTAs per SM leave room for).
+template <int NW> struct XiSlots { static constexpr int value = NW == 8 ? 3 : 4; };
+
 template <int NW, int SCHEME> struct Smem {
   static constexpr int NST = Stages<NW>::value;
+  static constexpr int NXI = SCHEME == kInt8 ? XiSlots<NW>::value : 0;
+  static constexpr int XD = NXI > 2 ? NXI - 2 : 1;
   static constexpr int kRing = NW * NST * Lay<SCHEME>::BYTES;
-  static constexpr int kXi = SCHEME == kInt8 ? 2 * kXiBytes : 0;
+  static constexpr int kXi = NXI * kXiBytes;
   static constexpr int kRingOff = 0;
   static constexpr int kXiOff = (kRing + 127) / 128 * 128;
-  static constexpr int kBarOff = kXiOff + kXi;                 // NW x NST x u64
-  static constexpr int kBytes = kBarOff + NW * NST * 8;
+  // NW x NST stage barriers (one warp each), then NXI "dither slot filled" and NXI
+  // "dither slot free" barriers (NW arrivals each)
+  static constexpr int kBarOff = kXiOff + kXi;
+  static constexpr int kBytes = kBarOff + (NW * NST + 2 * NXI) * 8;
 };
 
 // An upper bound of sqrt(x) at most one unit above the correctly rounded value: the SFU
@@ -208,22 +217,32 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   const bool active = warp < p.seqs_per_cta && i < p.B;
   const int grp = p.grp, j0 = h * grp;
   const int nblk = (p.S + kBlk - 1) / kBlk;
-  const int b_begin = (int)(((long long)split * nblk) / p.n_splits);
-  const int b_end = (int)(((long long)(split + 1) * nblk) / p.n_splits);
+  int b_begin, b_end;
+  if (nblk < 65536 && p.n_splits < 65536) {
+    b_begin = (int)((unsigned)(split * nblk) / (unsigned)p.n_splits);
+    b_end = (int)((unsigned)((split + 1) * nblk) / (unsigned)p.n_splits);
+  } else {
+    b_begin = (int)(((long long)split * nblk) / p.n_splits);
+    b_end = (int)(((long long)(split + 1) * nblk) / p.n_splits);
+  }
   const int nb = b_end - b_begin;
 
   uint8_t* ring = smem + SM::kRingOff + warp * NST * L::BYTES;
   uint8_t* xib = smem + SM::kXiOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOff) + warp * NST;
+  uint64_t* xfull = reinterpret_cast<uint64_t*>(smem + SM::kBarOff) + NW * NST;
+  uint64_t* xfree = xfull + SM::NXI;
 
   const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
   const uint8_t* src = p.blocks + (seq_base + b_begin) * L::BYTES;
 
   // ---------------------------------------------------------------- prologue
-  if (active && lane == 0) {
+  if (SCHEME == kInt8 && threadIdx.x == 0)
+    for (int s = 0; s < SM::NXI; ++s) { mbar_init(smem_addr(&xfull[s]), NW); mbar_init(smem_addr(&xfree[s]), NW); }
+  if (active && lane == 0)
     for (int s = 0; s < NST; ++s) mbar_init(smem_addr(&bars[s]), 1);
+  if ((active && lane == 0) || (SCHEME == kInt8 && threadIdx.x == 0))
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
   pdl_trigger();
   // the first blocks' copies go out before anything else; blocks from p.dirty_blk on may
   // still be written by the immediately preceding kernel
@@ -249,7 +268,23 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       if (has_q) qraw[kk].load(qr + 16 * kk); else qraw[kk].zero();
     }
   }
-  if (SCHEME == kInt8 && nb > 0) gen_xi(xib, p, h, b_begin, NW * 32);
+  bool fault = false;
+  // Dither of block b_begin + m into its slot: wait until every warp is done with the block
+  // that used the slot before, write this thread's share, then count the warp in.
+  auto produce = [&](int m) {
+    const int ps = m % SM::NXI;
+    if (m >= SM::NXI && !mbar_wait(smem_addr(&xfree[ps]), (uint32_t)((m / SM::NXI - 1) & 1), kWaitLimitNs)) {
+      if (!fault && lane == 0) atomicAdd(p.err, 1);
+      fault = true;
+    }
+    gen_xi(xib + ps * kXiBytes, p, h, b_begin + m, NW * 32);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&xfull[ps]));
+  };
+  if (SCHEME == kInt8) {
+    __syncthreads();                  // the dither barriers exist before any warp arrives
+    for (int m = 0; m < SM::XD && m < nb; ++m) produce(m);
+  }
 
   uint32_t qb[8][2], qbl[8][2], qnb[2], qnl[2];
   float qg2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -318,22 +353,21 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 #pragma unroll
   for (int G = 0; G < 4; ++G) qgp[G] = make_float2(qg2[0][G], qg2[1][G]);
 
-  if (SCHEME == kInt8) __syncthreads();
-
-  bool fault = false;
   const bool gen_early = ((warp >> 2) & 1) == 0;
   for (int n = 0; n < nb; ++n) {
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
-    const uint8_t* xb = xib + (n & 1) * kXiBytes;
-    // The next block's dither: half of the warps (two per scheduler) make their share before
+    const int xs = SCHEME == kInt8 ? n % SM::NXI : 0;
+    const uint8_t* xb = xib + xs * kXiBytes;
+    // The dither XD blocks ahead: half of the warps (two per scheduler) make their share before
     // this block's logits, the other half between its softmax and its P.V product, so that the
     // integer work of the one overlaps the tensor and FP32 work of the other.
-    const bool gen_next = SCHEME == kInt8 && n + 1 < nb;
-    if (gen_next && gen_early) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
+    const bool gen_next = SCHEME == kInt8 && n + SM::XD < nb;
+    if (gen_next && gen_early) produce(n + SM::XD);
 
     if (active && !fault) {
-      if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs)) {
+      if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs) ||
+          (SCHEME == kInt8 && !mbar_wait(smem_addr(&xfull[xs]), (uint32_t)((n / SM::NXI) & 1), kWaitLimitNs))) {
         fault = true;
         if (lane == 0) atomicAdd(p.err, 1);
       }
@@ -541,7 +575,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       P0 = movmatrix_trans(h2_bits(__floats2half2_rn(peA.x, peA.y)));
       P1 = movmatrix_trans(h2_bits(__floats2half2_rn(peB.x, peB.y)));
     }
-    if (gen_next && !gen_early) gen_xi(xib + ((n + 1) & 1) * kXiBytes, p, h, blk + 1, NW * 32);
+    if (gen_next && !gen_early) produce(n + SM::XD);
     if (live) {
       if constexpr (SCHEME == kFp8) {
         const uint32_t bfr[2] = {P0, P1};
@@ -619,7 +653,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
                  smem_addr(&bars[stage]));
       }
     }
-    if (SCHEME == kInt8) __syncthreads();
+    if (SCHEME == kInt8) {            // this warp is done with the block's dither slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&xfree[xs]));
+    }
   }
 
   pdl_wait();     // partial results overwrite scratch the preceding merge may still read
