@@ -802,41 +802,54 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done) {
   return e;
 }
 
+// Launches the split kernel, or (occ != nullptr) reports how many of its CTAs fit on an SM.
 template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, int NW>
-cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
+cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
   using SM = Smem<NW, SCHEME>;
   static std::atomic<uint64_t> smem_done{0};
+  static std::atomic<int> resident{0};
   auto k = decode_split_kernel<SCHEME, QT, METER, RISK, GATE, NW>;
   cudaError_t e = allow_smem(k, SM::kBytes, smem_done);
   if (e != cudaSuccess) return e;
+  if (occ) {
+    int n = resident.load(std::memory_order_relaxed);
+    if (n <= 0) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, NW * 32, SM::kBytes);
+      if (e != cudaSuccess) return e;
+      resident.store(n, std::memory_order_relaxed);
+    }
+    *occ = n;
+    return cudaSuccess;
+  }
   return launch_pdl(k, grid, dim3(NW * 32), SM::kBytes, st, pdl, a);
 }
 
 template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE>
-cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
+cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
   switch (a.seqs_per_cta) {
-    case 1: return run_split<SCHEME, QT, METER, RISK, GATE, 1>(a, grid, st, pdl);
-    case 2: return run_split<SCHEME, QT, METER, RISK, GATE, 2>(a, grid, st, pdl);
-    case 4: return run_split<SCHEME, QT, METER, RISK, GATE, 4>(a, grid, st, pdl);
-    case 8: return run_split<SCHEME, QT, METER, RISK, GATE, 8>(a, grid, st, pdl);
-    default: return run_split<SCHEME, QT, METER, RISK, GATE, 16>(a, grid, st, pdl);
+    case 1: return run_split<SCHEME, QT, METER, RISK, GATE, 1>(a, grid, st, pdl, occ);
+    case 2: return run_split<SCHEME, QT, METER, RISK, GATE, 2>(a, grid, st, pdl, occ);
+    case 4: return run_split<SCHEME, QT, METER, RISK, GATE, 4>(a, grid, st, pdl, occ);
+    case 8: return run_split<SCHEME, QT, METER, RISK, GATE, 8>(a, grid, st, pdl, occ);
+    default: return run_split<SCHEME, QT, METER, RISK, GATE, 16>(a, grid, st, pdl, occ);
   }
 }
 
 // Instantiated combinations: meters off with and without a gate; meters on without a gate;
 // meters on with a gate, which always keeps block risks.
 template <int SCHEME, typename QT>
-cudaError_t dispatch_qt(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
+cudaError_t dispatch_qt(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
   const bool gate = a.slots != nullptr;
-  if (!a.meter) return gate ? dispatch_nw<SCHEME, QT, false, false, true>(a, grid, st, pdl)
-                            : dispatch_nw<SCHEME, QT, false, false, false>(a, grid, st, pdl);
-  if (gate) return dispatch_nw<SCHEME, QT, true, true, true>(a, grid, st, pdl);
-  return dispatch_nw<SCHEME, QT, true, false, false>(a, grid, st, pdl);
+  if (!a.meter) return gate ? dispatch_nw<SCHEME, QT, false, false, true>(a, grid, st, pdl, occ)
+                            : dispatch_nw<SCHEME, QT, false, false, false>(a, grid, st, pdl, occ);
+  if (gate) return dispatch_nw<SCHEME, QT, true, true, true>(a, grid, st, pdl, occ);
+  return dispatch_nw<SCHEME, QT, true, false, false>(a, grid, st, pdl, occ);
 }
 
 template <int SCHEME>
-cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
-  return a.is_bf16 ? dispatch_qt<SCHEME, __nv_bfloat16>(a, grid, st, pdl) : dispatch_qt<SCHEME, float>(a, grid, st, pdl);
+cudaError_t dispatch_flags(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ = nullptr) {
+  return a.is_bf16 ? dispatch_qt<SCHEME, __nv_bfloat16>(a, grid, st, pdl, occ)
+                   : dispatch_qt<SCHEME, float>(a, grid, st, pdl, occ);
 }
 
 int seqs_per_cta_for(int B) { return B >= 16 ? 16 : B >= 8 ? 8 : B >= 4 ? 4 : B >= 2 ? 2 : 1; }
@@ -870,16 +883,36 @@ cudaError_t decode_static_scratch(float** ptr, size_t* bytes) {
   return cudaSuccess;
 }
 
-int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count) {
+int decode_ctas_per_sm(int scheme, const DecodeArgs& a0) {
+  DecodeArgs a = a0;
+  a.seqs_per_cta = seqs_per_cta_for(a.B);
+  int n = 0;
+  const dim3 grid(1);
+  const cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, nullptr, false, &n)
+                        : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, nullptr, false, &n)
+                                         : dispatch_flags<kKivi>(a, grid, nullptr, false, &n);
+  return e == cudaSuccess && n > 0 ? n : 1;
+}
+
+// Splits per (KV head, sequence group): the fewest that fill the GPU's CTA slots
+// (per_sm resident CTAs on each of sm_count SMs) to at least 90% in whole waves, so that
+// no wave runs with most SMs idle.
+int decode_auto_splits(int B, int Hkv, int nblk, int sm_count, int per_sm) {
   const int spc = seqs_per_cta_for(B);
-  const int groups = (B + spc - 1) / spc;
-  const int per_sm = spc >= 16 ? 1 : spc >= 8 ? 2 : spc >= 4 ? 3 : 4;
-  const int target = sm_count * per_sm;
-  int s = (target + Hkv * groups - 1) / (Hkv * groups);
-  if (s > nblk) s = nblk;
-  if (s < 1) s = 1;
-  (void)scheme;
-  return s;
+  const long long units = (long long)Hkv * ((B + spc - 1) / spc);
+  const long long slots = (long long)sm_count * (per_sm > 0 ? per_sm : 1);
+  long long best = 1;
+  double best_eff = -1.0;
+  for (int w = 1; w <= 4; ++w) {
+    long long s = w * slots / units;
+    if (s < 1) s = 1;
+    if (s > nblk) s = nblk;
+    const long long ctas = units * s, waves = (ctas + slots - 1) / slots;
+    const double eff = (double)ctas / (double)(waves * slots);
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+    if (eff >= 0.9 || s == nblk) break;
+  }
+  return (int)best;
 }
 
 cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaStream_t st,

@@ -55,7 +55,8 @@ void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]);
 // and `split_stop` (optional) bracket the split kernel alone.
 cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStream_t st,
                           cudaEvent_t split_start, cudaEvent_t split_stop, bool pdl);
-int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count);
+int decode_ctas_per_sm(int scheme, const DecodeArgs& a);
+int decode_auto_splits(int B, int Hkv, int nblk, int sm_count, int per_sm);
 // Device address (current device) and size of the library's static split scratch,
 // used by witcert_decode_noalloc; the first call on a device looks the address up.
 cudaError_t decode_static_scratch(float** ptr, size_t* bytes);

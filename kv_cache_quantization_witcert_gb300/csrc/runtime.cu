@@ -128,6 +128,8 @@ extern "C" {
 
 const char* witcert_last_error(void) { return g_err.c_str(); }
 
+static int auto_splits(const witcert_cache* c, int nblk, bool meter, int cap);
+
 witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   if (!cfg || !out) return fail(WITCERT_EINVAL, "NULL argument");
   *out = nullptr;
@@ -154,7 +156,8 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   c->nblk_max = (f.max_tokens + kBlk - 1) / kBlk;
   c->elem = f.kv_dtype == WITCERT_BF16 ? 2 : 4;
   c->layer_blocks = layer_rows(c) * c->nblk_max * c->bblk;
-  const int auto_max = decode_auto_splits(c->scheme, f.batch, f.n_kv_heads, c->nblk_max, c->sm_count);
+  const int auto_on = auto_splits(c, c->nblk_max, true, 0), auto_off = auto_splits(c, c->nblk_max, false, 0);
+  const int auto_max = auto_on > auto_off ? auto_on : auto_off;
   c->max_splits = f.n_splits > auto_max ? f.n_splits : auto_max;
   c->len.assign(f.n_layers, 0);
   c->risk_len.assign(f.n_layers, -1);
@@ -239,6 +242,20 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   return WITCERT_OK;
 }
 
+// Automatic split count for a decode of nblk blocks: sized by how many split-kernel CTAs of
+// this configuration fit on an SM, and never above the scratch sized at create time.
+static int auto_splits(const witcert_cache* c, int nblk, bool meter, int cap) {
+  DecodeArgs a{};
+  a.B = c->cfg.batch;
+  a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
+  a.meter = meter;
+  a.slots = c->slots;
+  const int per_sm = decode_ctas_per_sm(c->scheme, a);
+  int s = decode_auto_splits(c->cfg.batch, c->cfg.n_kv_heads, nblk > 0 ? nblk : 1, c->sm_count, per_sm);
+  if (cap > 0 && s > cap) s = cap;
+  return s;
+}
+
 witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
                               float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
   if (witcert_status s = check_layer(c, layer)) return s;
@@ -258,8 +275,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   a.q = q;
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
-  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits
-                                   : decode_auto_splits(c->scheme, a.B, a.Hkv, nblk > 0 ? nblk : 1, c->sm_count);
+  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits : auto_splits(c, nblk, meter, c->max_splits);
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
   a.layer = layer;
@@ -313,8 +329,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   const int nblk = (S + kBlk - 1) / kBlk;
   DecodeArgs a{};
   a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
-  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits
-                                   : decode_auto_splits(c->scheme, a.B, a.Hkv, nblk > 0 ? nblk : 1, c->sm_count);
+  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits : auto_splits(c, nblk, meter, c->max_splits);
   float* scratch = nullptr;
   size_t scratch_bytes = 0;
   cudaError_t e = decode_static_scratch(&scratch, &scratch_bytes);
