@@ -707,56 +707,65 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   }
 }
 
-// One 4-warp CTA per (sequence, query head): warp w merges splits w, w+4, ...; the four
-// partial states meet in shared memory; then the output, the meters and the block risks.
+// One CTA of kMergeWarps warps per (sequence, query head).  Warp w folds splits w,
+// w + kMergeWarps, ... into a running (max, Z, S_A, S_B, values) with online rescaling, so
+// that all its record loads are independent of one another; the warps' states meet in shared
+// memory, where thread j finishes channel j.  Then the meters and the block risks.
+constexpr int kMergeWarps = 8;
+
 template <bool INT8, bool RISK>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeArgs p) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float s_acc[4][kD];
-  __shared__ float s_sc[4][4];
-  __shared__ float s_m[4];
+  __shared__ float4 s_hdr[kMergeWarps];
+  __shared__ __align__(16) float s_acc[kMergeWarps][kD];
   const int cell = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* recs = p.part + (size_t)cell * p.n_splits * kPartStride;
   const int ns = p.n_splits;
-  float M = -INFINITY;
-  for (int s = threadIdx.x; s < ns; s += 128) M = fmaxf(M, recs[(size_t)s * kPartStride]);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) s_m[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
-  float Z = 0.f, SA = 0.f, SB = 0.f;
+  float M = -INFINITY, Z = 0.f, SA = 0.f, SB = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int s = warp; s < ns; s += 4) {
-      const float* r = recs + (size_t)s * kPartStride;
-      const float4 h = *reinterpret_cast<const float4*>(r);           // m, Z, S_A, S_B
-      const float f = h.x == -INFINITY ? 0.f : ex2(h.x - M);
-      Z = fmaf(f, h.y, Z); SA = fmaf(f, h.z, SA); SB = fmaf(f, h.w, SB);
-      const float4 a = *reinterpret_cast<const float4*>(r + 4 + 4 * lane);
-      acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
+#pragma unroll 8
+  for (int s = warp; s < ns; s += kMergeWarps) {
+    const float* r = recs + (size_t)s * kPartStride;
+    const float4 h = *reinterpret_cast<const float4*>(r);           // m, Z, S_A, S_B of the split
+    const float4 a = *reinterpret_cast<const float4*>(r + 4 + 4 * lane);
+    if (h.x > M) {                                                  // same for every lane
+      const float sc = M == -INFINITY ? 0.f : ex2(M - h.x);
+      Z *= sc; SA *= sc; SB *= sc;
+      acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+      M = h.x;
+    }
+    const float f = h.x == -INFINITY ? 0.f : ex2(h.x - M);
+    Z = fmaf(f, h.y, Z); SA = fmaf(f, h.z, SA); SB = fmaf(f, h.w, SB);
+    acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
+  }
+  if (lane == 0) s_hdr[warp] = make_float4(M, Z, SA, SB);
+  *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
+  __syncthreads();
+  float Mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Mx = fmaxf(Mx, s_hdr[w].x);
+  float Zt = 0.f, SAt = 0.f, SBt = 0.f, o = 0.f;
+  if (Mx != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      const float4 hw = s_hdr[w];
+      const float wt = hw.x == -INFINITY ? 0.f : ex2(hw.x - Mx);
+      Zt = fmaf(wt, hw.y, Zt); SAt = fmaf(wt, hw.z, SAt); SBt = fmaf(wt, hw.w, SBt);
+      if (threadIdx.x < kD) o = fmaf(wt, s_acc[w][threadIdx.x], o);
     }
   }
-  *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
-  if (lane == 0) { s_sc[warp][0] = Z; s_sc[warp][1] = SA; s_sc[warp][2] = SB; }
-  __syncthreads();
-  Z = s_sc[0][0] + s_sc[1][0] + s_sc[2][0] + s_sc[3][0];
-  SA = s_sc[0][1] + s_sc[1][1] + s_sc[2][1] + s_sc[3][1];
-  SB = s_sc[0][2] + s_sc[1][2] + s_sc[2][2] + s_sc[3][2];
-  const float inv = Z > 0.f ? 1.0f / Z : 0.f;
-  p.out[(size_t)cell * kD + threadIdx.x] =
-      (s_acc[0][threadIdx.x] + s_acc[1][threadIdx.x] + s_acc[2][threadIdx.x] + s_acc[3][threadIdx.x]) * inv;
+  const float inv = Zt > 0.f ? 1.0f / Zt : 0.f;
+  if (threadIdx.x < kD) p.out[(size_t)cell * kD + threadIdx.x] = o * inv;
   if (!p.meter) return;
   if (threadIdx.x == 0) {
-    const float DA = Z > 0.f ? __fmul_ru(__fdiv_ru(SA, Z), kMeterMargin) : 0.f;
+    const float DA = Zt > 0.f ? __fmul_ru(__fdiv_ru(SAt, Zt), kMeterMargin) : 0.f;
     const float rawA = __fmaf_ru(__fmul_ru(0.5f, DA), DA, DA);
     if (p.raw_a) p.raw_a[cell] = rawA;
     if (p.meter_a) p.meter_a[cell] = fminf(1.0f, rawA);
     float rawB = NAN;
     if (INT8) {
-      const float DB = Z > 0.f ? __fmul_ru(__fdiv_ru(SB, Z), kMeterMargin) : 0.f;
+      const float DB = Zt > 0.f ? __fmul_ru(__fdiv_ru(SBt, Zt), kMeterMargin) : 0.f;
       rawB = __fmaf_ru(__fmul_ru(0.5f, DB), DB, DB);
     }
     if (p.raw_b) p.raw_b[cell] = rawB;
@@ -766,9 +775,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs p) {
     const int nblk = (p.S + kBlk - 1) / kBlk;
     const float2* rr = p.risk_raw + (size_t)cell * p.nblk_max;
     float* ro = p.risk + (size_t)cell * p.nblk_max;
-    for (int b = threadIdx.x; b < nblk; b += 128) {
+    for (int b = threadIdx.x; b < nblk; b += kMergeWarps * 32) {
       const float2 v = rr[b];
-      ro[b] = (v.y == 0.f || Z == 0.f) ? 0.f : v.y * ex2(v.x - M) * inv;
+      ro[b] = (v.y == 0.f || Zt == 0.f) ? 0.f : v.y * ex2(v.x - Mx) * inv;
     }
   }
 }
@@ -933,11 +942,11 @@ cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaSt
   const dim3 mg(a.B * a.Hq);
   const bool risk = a.risk_raw != nullptr && a.meter;
   if (scheme == kInt8)
-    e = risk ? launch_pdl(decode_merge_kernel<true, true>, mg, dim3(128), 0, st, pdl_allowed, a)
-             : launch_pdl(decode_merge_kernel<true, false>, mg, dim3(128), 0, st, pdl_allowed, a);
+    e = risk ? launch_pdl(decode_merge_kernel<true, true>, mg, dim3(kMergeWarps * 32), 0, st, pdl_allowed, a)
+             : launch_pdl(decode_merge_kernel<true, false>, mg, dim3(kMergeWarps * 32), 0, st, pdl_allowed, a);
   else
-    e = risk ? launch_pdl(decode_merge_kernel<false, true>, mg, dim3(128), 0, st, pdl_allowed, a)
-             : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(128), 0, st, pdl_allowed, a);
+    e = risk ? launch_pdl(decode_merge_kernel<false, true>, mg, dim3(kMergeWarps * 32), 0, st, pdl_allowed, a)
+             : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(kMergeWarps * 32), 0, st, pdl_allowed, a);
   return e;
 }
 

@@ -67,6 +67,19 @@ def test_qwen_shaped_bf16_ragged(scheme):
     check_decode(gpu, ref, 0, gen_q(w, 0, 1), w, 1e-3)
 
 
+@pytest.mark.parametrize("scheme", ["int8_dither", "kivi2"])
+def test_more_split_ctas_than_the_gpu_holds(scheme):
+    """300 splits x 4 KV heads: several waves of split CTAs and 300 partial records per cell
+    to merge; results still match the oracle."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=1000, steps=1, scheme=scheme)
+    gpu, ref = make_pair(w, n_splits=300)
+    K, V = gen_kv(w, 0)
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    check_decode(gpu, ref, 0, gen_q(w, 0, 0), w, w.delta_req)
+    assert gpu.witcert_stats()["device_errors"] == 0
+
+
 @pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
 def test_kivi_and_all_schemes_across_block_boundaries(scheme):
     """Appends one token at a time across two 16-token boundaries (KIVI closes blocks)."""
