@@ -8,7 +8,7 @@ metered split-KV decode + merge.  Metric: attended-KV-tokens/s, one attended
 token being one (sequence, layer, position) read across all KV heads.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload qwen_28l|qwen_1l|sweep:<mistral|yi>:<B>:<S>] [--scheme ...]
+                  [--workload qwen_28l|qwen_1l|gated|sweep:<mistral|yi>:<B>:<S>] [--scheme ...]
 
 --impl reference times the CPU oracle (the slow float64 statement of the same
 computation) on this host's cores, on a bounded sample of the same workload.
@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
+    ap.add_argument("--taus", default="0.5,1,2", help="gate thresholds of the gated workload")
+    ap.add_argument("--gated-steps", type=int, default=256, help="decode steps per threshold (gated workload)")
     return ap.parse_args()
 
 
@@ -382,6 +384,96 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- gated repair run
+
+def run_gated(args, w):
+    """Gated repair (raw-cast FP8 cache, pinned bf16 key backing store): every step appends a
+    token, decodes with meters and gates every layer at tau, for each tau of --taus.  Reports
+    page-in bytes and the gate rate (repaired blocks / all blocks) per step and cumulative,
+    and the attended-KV-tokens/s of the gated steps (write + decode + merge + gate)."""
+    import torch
+    import kv_cache_quantization_witcert_gb300 as wc
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dt = torch.bfloat16
+    steps = args.gated_steps
+    taus = [float(x) for x in args.taus.split(",")]
+    nblk = (w.context + steps + 15) // 16
+    total_blocks = w.n_layers * w.batch * w.n_kv_heads * nblk
+    pool = total_blocks                      # room for every block: nothing is dropped
+    sets = {}
+    for sid in range(min(DISTINCT_LAYERS, w.n_layers)):
+        K, V = gen_kv(w, sid)
+        sets[sid] = (torch.from_numpy(K).to(dt), torch.from_numpy(V).to(dt))
+    # every step's appended token and queries, generated once and resident in HBM
+    step_in = []
+    for step in range(steps):
+        row = []
+        for layer in range(w.n_layers):
+            k1, v1 = gen_append_kv(w, layer % DISTINCT_LAYERS, step)
+            q = gen_q(w, layer % DISTINCT_LAYERS, step)
+            row.append(tuple(torch.from_numpy(a).to(dev, dt) for a in (k1, v1, q)))
+        step_in.append(row)
+    results = {}
+    rate = None
+    for tau in taus:
+        cache = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, w.context + steps + 1, w.scheme,
+                         dtype=dt, seed=w.seed, total_steps=steps, max_repair_blocks=pool)
+        for layer in range(w.n_layers):
+            K, V = sets[layer % DISTINCT_LAYERS]
+            cache.witcert_write(layer, K.to(dev), V.to(dev))
+        torch.cuda.synchronize()
+        out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float32, device=dev)
+        mtr = torch.empty((4, w.batch, w.n_q_heads), dtype=torch.float32, device=dev)
+        per_step = []
+        prev = cache.witcert_gate_stats()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_len0 = cache.witcert_length(0)
+        ev0.record()
+        for step in range(steps):
+            for layer in range(w.n_layers):
+                k1, v1, q = step_in[step][layer]
+                cache.witcert_write(layer, k1, v1)
+                cache.witcert_decode(layer, q, w.delta_req, out, mtr[0], mtr[1], mtr[2], mtr[3])
+                cache.witcert_gate(layer, tau)
+            cur = cache.witcert_gate_stats()
+            per_step.append({k: cur[k] - prev[k] for k in ("blocks_paged_in", "bytes_paged_in", "cells_triggered",
+                                                          "blocks_dropped")})
+            prev = cur
+        ev1.record()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        st = cache.witcert_gate_stats()
+        attended = sum(w.batch * (s_len0 + 1 + s) for s in range(steps)) * w.n_layers
+        rate = attended / (ms / 1e3)
+        results[str(tau)] = {
+            "bytes_paged_in": st["bytes_paged_in"], "blocks_paged_in": st["blocks_paged_in"],
+            "blocks_dropped": st["blocks_dropped"], "cells_triggered": st["cells_triggered"],
+            "gate_rate_cumulative": st["blocks_paged_in"] / total_blocks,
+            "gate_rate_first_step": per_step[0]["blocks_paged_in"] / total_blocks,
+            "gate_rate_last_step": per_step[-1]["blocks_paged_in"] / total_blocks,
+            "bytes_paged_in_first_step": per_step[0]["bytes_paged_in"],
+            "bytes_paged_in_last_step": per_step[-1]["bytes_paged_in"],
+            "tokens_per_s": rate, "ms_per_step": ms / steps,
+            "device_errors": cache.witcert_stats()["device_errors"],
+        }
+        cache.close()
+        del cache
+        torch.cuda.empty_cache()
+    print(json.dumps({
+        "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": 1, "steps": steps, "warmup": 0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32 (fp8 codes)",
+        "data": "synthetic (seeded numpy; bf16 N(0,1) K/V, x50 outlier RoPE pair, planted keys; fresh queries "
+                "every step, non-adaptive)",
+        "config": {"workload": f"gated: {w.n_layers} layers, {w.n_q_heads}q/{w.n_kv_heads}kv heads, batch "
+                               f"{w.batch} x {w.context} context, {w.scheme} cache, bf16 key backing store in "
+                               f"pinned host memory, exact-key pool of {pool} blocks",
+                   "taus": taus, "total_blocks": total_blocks},
+        "gate": results,
+    }))
+
+
 def main():
     args = parse()
     w = workload_of(args.workload, args.scheme)
@@ -389,6 +481,8 @@ def main():
         w = w.with_(n_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.workload == "gated":
+        run_gated(args, w)
     else:
         run_ours(args, w)
 

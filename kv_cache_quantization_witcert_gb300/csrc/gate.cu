@@ -6,10 +6,12 @@
 // Selection of one (sequence, query head) cell, a deterministic function of the
 // fp32 block risks the decode reported:
 //   candidates = unrepaired blocks, ordered by risk (largest first, ties to the
-//   lower block index); suffix sums of that order accumulated in fp64 from the
-//   last candidate upward; the cell triggers if the full sum exceeds
-//   D* = sqrt(1 + 2 tau) - 1 and then takes the shortest prefix whose
-//   remaining suffix is <= D*.
+//   lower block index); remaining-risk sums in fp64 in a fixed order: runs of 32
+//   ranked blocks each summed from the run's last block upward (one thread per
+//   run), run totals summed from the last run upward, and the remaining risk
+//   after block j = j's run-local sum + the runs after it; the cell triggers if
+//   the full sum exceeds D* = sqrt(1 + 2 tau) - 1 and then takes the shortest
+//   prefix whose remaining sum is <= D*.
 #include <cmath>
 
 #include "common.cuh"
@@ -20,64 +22,90 @@ namespace witcert {
 namespace {
 
 constexpr int kSelThreads = 256;
+constexpr int kRun = 32;
 
+__device__ __forceinline__ double key_risk(unsigned long long key) {
+  return (double)__uint_as_float(~(unsigned int)(key >> 32));
+}
+
+// Dynamic shared memory: keys [npow2] u64, run-local sums [npow2] f64, runs after [npow2/32] f64.
 __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateArgs a, int npow2) {
   extern __shared__ unsigned long long keys[];
+  double* local = reinterpret_cast<double*>(keys + npow2);
+  double* after = local + npow2;
   __shared__ double red[kSelThreads];
-  __shared__ int kstar;
+  __shared__ int s_n, s_jmax;
   const int cell = blockIdx.x;                 // i * Hq + j
   const int i = cell / a.Hq, j = cell % a.Hq, h = j / a.grp;
   const int nblk = (a.S + kBlk - 1) / kBlk;
   const float* risk = a.risk + (size_t)cell * a.nblk_max;
   const int32_t* slots = a.slots + ((size_t)i * a.Hkv + h) * a.nblk_max;
+  if (threadIdx.x == 0) { s_n = 0; s_jmax = -1; }
   double part = 0.0;
+  int cnt = 0;
   for (int b = threadIdx.x; b < npow2; b += blockDim.x) {
     unsigned long long key = ~0ull;
     if (b < nblk && slots[b] < 0) {
       const float r = risk[b];
       part += (double)r;
+      ++cnt;
       key = ((unsigned long long)(~__float_as_uint(r)) << 32) | (unsigned int)b;
     }
     keys[b] = key;
   }
   red[threadIdx.x] = part;
   __syncthreads();
+  if (cnt) atomicAdd(&s_n, cnt);
   for (int s = blockDim.x / 2; s; s >>= 1) {
     if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
   }
-  // a parallel sum differs from the ordered one by far less than 1e-9 relative:
-  // cells clearly below D* skip the exact walk
+  // a parallel sum differs from the run-ordered one by far less than 1e-9 relative:
+  // cells clearly below D* skip the ordered sums
   if (red[0] <= a.d_star * (1.0 - 1e-9)) return;
-  // bitonic sort, ascending keys = descending risk then ascending block
+  const int n = s_n;
+  // bitonic sort, ascending keys = descending risk then ascending block; each thread
+  // takes compare-exchange pairs (x, x + jj) directly, x having bit jj clear
   for (int k = 2; k <= npow2; k <<= 1) {
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int x = threadIdx.x; x < npow2; x += blockDim.x) {
-        const int y = x ^ jj;
-        if (y > x) {
-          const unsigned long long kx = keys[x], ky = keys[y];
-          const bool up = (x & k) == 0;
-          if ((kx > ky) == up) { keys[x] = ky; keys[y] = kx; }
-        }
+      for (int pr = threadIdx.x; pr < (npow2 >> 1); pr += blockDim.x) {
+        const int x = ((pr & ~(jj - 1)) << 1) | (pr & (jj - 1)), y = x + jj;
+        const unsigned long long kx = keys[x], ky = keys[y];
+        const bool up = (x & k) == 0;
+        if ((kx > ky) == up) { keys[x] = ky; keys[y] = kx; }
       }
       __syncthreads();
     }
   }
-  if (threadIdx.x == 0) {
-    int n = 0;
-    while (n < npow2 && keys[n] != ~0ull) ++n;
-    double suffix = 0.0;
-    int k = n;
-    while (k > 0) {
-      const double s_new = suffix + (double)__uint_as_float(~(unsigned int)(keys[k - 1] >> 32));
-      if (s_new > a.d_star) break;
-      suffix = s_new;
-      --k;
+  // run-local remaining sums, one thread per run of kRun ranked blocks
+  const int nruns = (n + kRun - 1) / kRun;
+  for (int rr = threadIdx.x; rr < nruns; rr += blockDim.x) {
+    const int lo = rr * kRun, hi = min(n, lo + kRun);
+    double s = 0.0;
+    for (int m = hi - 1; m >= lo; --m) {
+      s = s + key_risk(keys[m]);
+      local[m] = s;
     }
-    kstar = k;
-    if (k > 0) atomicAdd(&a.stats[0], 1ull);
+    after[rr] = s;                 // run total for now
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    double u = 0.0;
+    for (int rr = nruns - 1; rr >= 0; --rr) {
+      const double tot = after[rr];
+      after[rr] = u;
+      u = u + tot;
+    }
+  }
+  __syncthreads();
+  // the remaining sums never increase down the list: the cut is one past the last one above D*
+  int jmax = -1;
+  for (int m = threadIdx.x; m < n; m += blockDim.x)
+    if (local[m] + after[m / kRun] > a.d_star) jmax = m;
+  if (jmax >= 0) atomicMax(&s_jmax, jmax);
+  __syncthreads();
+  const int kstar = s_jmax + 1;
+  if (kstar > 0 && threadIdx.x == 0) atomicAdd(&a.stats[0], 1ull);
   uint32_t* mask = a.selmask + ((size_t)i * a.Hkv + h) * (a.nblk_max / 32 + 1);
   for (int m = threadIdx.x; m < kstar; m += blockDim.x) {
     const int b = (int)(keys[m] & 0xFFFFFFFFu);
@@ -85,25 +113,46 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateArgs
   }
 }
 
-// Per (sequence, KV head): turn the selection bitmap into pool slots and a todo list.
-__global__ void gate_compact_kernel(const GateArgs a) {
-  const int sh = blockIdx.x * blockDim.x + threadIdx.x;
+// Per (sequence, KV head), one warp: turn the selection bitmap into pool slots and todo
+// entries, 32 bitmap words at a time (one pool and one todo reservation per batch).
+// A selected block is unrepaired (the selection ranks unrepaired blocks only); slots past
+// the pool's capacity are counted as dropped.
+__global__ void __launch_bounds__(128) gate_compact_kernel(const GateArgs a) {
+  const int sh = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (sh >= a.B * a.Hkv) return;
   const int nwords = a.nblk_max / 32 + 1;
   uint32_t* mask = a.selmask + (size_t)sh * nwords;
-  const int32_t* slots = a.slots + (size_t)sh * a.nblk_max;
-  for (int w = 0; w < nwords; ++w) {
-    uint32_t bits = mask[w];
-    mask[w] = 0u;
+  const unsigned int cap = (unsigned int)a.pool_capacity;
+  for (int w0 = 0; w0 < nwords; w0 += 32) {
+    const int w = w0 + lane;
+    uint32_t bits = w < nwords ? mask[w] : 0u;
+    if (bits) mask[w] = 0u;
+    const int cnt = __popc(bits);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const unsigned int total = (unsigned int)__shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) continue;
+    unsigned int base = 0, tbase = 0, fit = 0;
+    if (lane == 0) {
+      base = atomicAdd(a.pool_next, total);
+      fit = base >= cap ? 0u : min(total, cap - base);
+      atomicAdd(&a.stats[1], (unsigned long long)total);
+      if (fit < total) atomicAdd(&a.stats[4], (unsigned long long)(total - fit));
+      if (fit) tbase = atomicAdd(a.todo_count, fit);
+    }
+    base = __shfl_sync(0xffffffffu, base, 0);
+    fit = __shfl_sync(0xffffffffu, fit, 0);
+    tbase = __shfl_sync(0xffffffffu, tbase, 0);
+    unsigned int r = (unsigned int)(incl - cnt);
     while (bits) {
       const int b = w * 32 + __ffs(bits) - 1;
       bits &= bits - 1;
-      if (slots[b] >= 0) continue;
-      atomicAdd(&a.stats[1], 1ull);
-      const unsigned int slot = atomicAdd(a.pool_next, 1u);
-      if ((int)slot >= a.pool_capacity) { atomicAdd(&a.stats[4], 1ull); continue; }
-      const unsigned int e = atomicAdd(a.todo_count, 1u);
-      a.todo[e] = make_int4(sh / a.Hkv, sh % a.Hkv, b, (int)slot);
+      if (r < fit) a.todo[tbase + r] = make_int4(sh / a.Hkv, sh % a.Hkv, b, (int)(base + r));
+      ++r;
     }
   }
 }
@@ -142,12 +191,13 @@ cudaError_t launch_gate(const GateArgs& a, cudaStream_t st) {
   const int nblk = (a.S + kBlk - 1) / kBlk;
   int npow2 = 1;
   while (npow2 < nblk) npow2 <<= 1;
-  const size_t smem = (size_t)npow2 * sizeof(unsigned long long);
+  const size_t smem = (size_t)npow2 * (sizeof(unsigned long long) + sizeof(double)) +
+                      (size_t)(npow2 / kRun + 1) * sizeof(double);
   cudaError_t e = cudaFuncSetAttribute(gate_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   gate_select_kernel<<<a.B * a.Hq, kSelThreads, smem, st>>>(a, npow2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  gate_compact_kernel<<<(a.B * a.Hkv + 127) / 128, 128, 0, st>>>(a);
+  gate_compact_kernel<<<(a.B * a.Hkv * 32 + 127) / 128, 128, 0, st>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gate_pagein_kernel<<<1024, 256, 0, st>>>(a);
   return cudaGetLastError();

@@ -16,9 +16,14 @@ reading of those sentences:
   which brings the cell's meter to <= tau from the next step on;
 * a block is repaired once any query head of its KV head's group selects it.
 
-D and the remaining risks are suffix sums of the ranked risks, accumulated in
-float64 from the lowest-ranked block upward; the risks themselves are the fp32
-values the decode reported.  Repaired blocks carry zero risk and are not ranked.
+D and the remaining risks are suffix sums of the ranked risks in float64; the
+risks themselves are the fp32 values the decode reported.  Repaired blocks
+carry zero risk and are not ranked.  The pages fix no summation order; this
+reading fixes one so that the choice is reproducible bit for bit: the ranked
+list is cut into runs of RUN consecutive blocks, each run is summed from its
+lowest-ranked block upward, the run totals are summed from the last run
+upward, and the remaining risk after block j is (j's run-local suffix) + (the
+total of the runs after j's run).
 """
 from __future__ import annotations
 
@@ -32,6 +37,29 @@ def d_star(tau: float) -> float:
     return math.sqrt(1.0 + 2.0 * tau) - 1.0
 
 
+RUN = 32
+
+
+def suffix_sums(values):
+    """Remaining-risk sums of a ranked list: entry k = sum of values[k:], in the run order above;
+    entry len(values) = 0."""
+    n = len(values)
+    local = [0.0] * n
+    totals = []
+    for lo in range(0, n, RUN):
+        s = 0.0
+        for k in range(min(n, lo + RUN) - 1, lo - 1, -1):
+            s = s + float(values[k])
+            local[k] = s
+        totals.append(s)
+    after = [0.0] * len(totals)          # total of the runs after run c
+    u = 0.0
+    for c in range(len(totals) - 1, -1, -1):
+        after[c] = u
+        u = u + totals[c]
+    return [local[k] + after[k // RUN] for k in range(n)] + [0.0]
+
+
 def select_cell(risk_row, repaired, tau: float):
     """Blocks one (sequence, query head) cell asks for.  risk_row: fp32 [nblk]."""
     r = np.asarray(risk_row, dtype=np.float32)
@@ -40,10 +68,7 @@ def select_cell(risk_row, repaired, tau: float):
         return []
     # rank: larger risk first, ties to the lower block index
     order = sorted(cand.tolist(), key=lambda b: (-float(r[b]), b))
-    n = len(order)
-    suffix = [0.0] * (n + 1)
-    for k in range(n - 1, -1, -1):
-        suffix[k] = suffix[k + 1] + float(r[order[k]])
+    suffix = suffix_sums([r[b] for b in order])
     ds = d_star(tau)
     if not suffix[0] > ds:
         return []

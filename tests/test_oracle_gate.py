@@ -100,3 +100,37 @@ def test_oracle_cache_append_and_kivi_tail():
         c.write(0, k1, v1)
     kh, _, wst, _, _ = c.group_view(0, 0, 0)   # 48 tokens: block 2 closed on the last append
     assert np.any(wst[32:48] > 0) and not np.array_equal(kh[32:48], K[0, 32:48, 0])
+
+
+def test_run_order_suffix_sums_match_exact_sums_and_are_monotone():
+    """The fixed summation order stays within float64 rounding of the exact remaining risk
+    (math.fsum) and never increases down the ranked list, over several runs of 32."""
+    rng = np.random.default_rng(5)
+    for n in (1, 31, 32, 33, 100, 257, 2048):
+        vals = np.sort((rng.exponential(1.0, n) ** 4 * 10.0 ** rng.uniform(-12, 0, n)).astype(np.float32))[::-1]
+        suf = gate.suffix_sums(vals)
+        assert len(suf) == n + 1 and suf[n] == 0.0
+        for k in range(0, n, max(1, n // 50)):
+            exact = math.fsum(float(v) for v in vals[k:])
+            assert abs(suf[k] - exact) <= 1e-13 * exact
+        assert all(suf[k] >= suf[k + 1] for k in range(n))
+
+
+def test_selection_over_many_runs_is_the_exact_minimum_repair():
+    """Hundreds of blocks (many runs): the ranked prefix is the smallest whose exact remaining
+    risk (math.fsum) is <= D*; ranking by size makes a prefix the optimum."""
+    rng = np.random.default_rng(6)
+    for trial in range(40):
+        n = int(rng.integers(40, 400))
+        risk = (rng.exponential(0.01, n) * (rng.random(n) < 0.9)).astype(np.float32)
+        rep = rng.random(n) < 0.1
+        risk[rep] = 0.0
+        total = math.fsum(float(x) for x in risk)
+        tau = float(rng.uniform(0.05, 0.9)) * (total + total * total / 2)
+        ds = gate.d_star(tau)
+        sel = gate.select_cell(risk, rep, tau)
+        order = sorted((b for b in range(n) if not rep[b]), key=lambda b: (-float(risk[b]), b))
+        k_exact = 0
+        while math.fsum(float(risk[b]) for b in order[k_exact:]) > ds:
+            k_exact += 1
+        assert sel == order[:k_exact]
