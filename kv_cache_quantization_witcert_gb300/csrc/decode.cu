@@ -304,6 +304,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       qb[kk][0] = pack_h2(hv[0], hv[1]); qb[kk][1] = pack_h2(hv[2], hv[3]);
       qbl[kk][0] = pack_h2(lv[0], lv[1]); qbl[kk][1] = pack_h2(lv[2], lv[3]);
     }
+    if constexpr (SCHEME == kKivi) {
+      // KIVI scales the query per block and channel from qraw; exact blocks rebuild the fragments
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) qb[kk][0] = qb[kk][1] = qbl[kk][0] = qbl[kk][1] = 0u;
+    }
     qnb[0] = qnb[1] = qnl[0] = qnl[1] = 0u;
     if (METER) {
       // ||q_b|| / sqrt(d) for bands t, t+4 (k 2t, 2t+1) and t+8, t+12 (k 2t+8, 2t+9), rounded up,
@@ -384,10 +389,23 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
       if ((GATE && slot >= 0) || kivi_tail) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t fb[8][2], fbl[8][2];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          if constexpr (SCHEME == kKivi) {
+            const float4 v4 = qraw[kk].get();
+            __half h0, h1, h2, h3, l0, l1, l2, l3;
+            split_h(v4.x, h0, l0); split_h(v4.y, h1, l1); split_h(v4.z, h2, l2); split_h(v4.w, h3, l3);
+            fb[kk][0] = pack_h2(h0, h1); fb[kk][1] = pack_h2(h2, h3);
+            fbl[kk][0] = pack_h2(l0, l1); fbl[kk][1] = pack_h2(l2, l3);
+          } else {
+            fb[kk][0] = qb[kk][0]; fb[kk][1] = qb[kk][1]; fbl[kk][0] = qbl[kk][0]; fbl[kk][1] = qbl[kk][1];
+          }
+        }
         if (GATE && slot >= 0)
-          exact_block_logits<QT, QLO>(reinterpret_cast<const QT*>(p.pool) + (size_t)slot * kBlk * kD, qb, qbl, g, t, acc);
+          exact_block_logits<QT, QLO>(reinterpret_cast<const QT*>(p.pool) + (size_t)slot * kBlk * kD, fb, fbl, g, t, acc);
         else
-          exact_block_logits<float, QLO>(p.kivi_tail + seq_base / p.nblk_max * (size_t)(kBlk * kD), qb, qbl, g, t, acc);
+          exact_block_logits<float, QLO>(p.kivi_tail + seq_base / p.nblk_max * (size_t)(kBlk * kD), fb, fbl, g, t, acc);
         lgA = __fmul2_rn(make_float2(acc[0], acc[1]), f2(lscale));
         lgB = __fmul2_rn(make_float2(acc[2], acc[3]), f2(lscale));
       } else if constexpr (SCHEME == kInt8) {
@@ -455,40 +473,45 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         lgA = __fmul2_rn(make_float2(acc[0] + acc2[0], acc[1] + acc2[1]), f2(lscale));
         lgB = __fmul2_rn(make_float2(acc[2] + acc2[2], acc[3] + acc2[3]), f2(lscale));
       } else {  // KIVI: logits = q . zero + (q * scale) . codes
-        const __half* ksc = reinterpret_cast<const __half*>(sb + L::KP);
-        const __half* kzr = reinterpret_cast<const __half*>(sb + L::KP + 256);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        float zq = 0.f;
+        // this lane's channels 16kk + 4t + e: their scales (and zeros) are 64 contiguous bytes
+        const uint4* sp = reinterpret_cast<const uint4*>(sb + L::KP) + 4 * t;
+        const uint4* zp = reinterpret_cast<const uint4*>(sb + L::KP + 256) + 4 * t;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};     // two chains
+        float2 zq2 = f2(0.f);
         const uint4 cw = *reinterpret_cast<const uint4*>(sb + L::KC + lane * 16);
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int pidx = t * 32 + kk * 4;
-          float qv[4];
-          qv[0] = __low2float(bits_h2(qb[kk][0])) + __low2float(bits_h2(qbl[kk][0]));
-          qv[1] = __high2float(bits_h2(qb[kk][0])) + __high2float(bits_h2(qbl[kk][0]));
-          qv[2] = __low2float(bits_h2(qb[kk][1])) + __low2float(bits_h2(qbl[kk][1]));
-          qv[3] = __high2float(bits_h2(qb[kk][1])) + __high2float(bits_h2(qbl[kk][1]));
-          __half hh[4], hl[4];
+        for (int kq = 0; kq < 4; ++kq) {
+          const uint4 s4 = sp[kq], z4 = zp[kq];                   // k-steps 2kq and 2kq + 1
+          const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w}, zw[4] = {z4.x, z4.y, z4.z, z4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            zq = fmaf(qv[e], __half2float(kzr[pidx + e]), zq);
-            split_h(qv[e] * __half2float(ksc[pidx + e]), hh[e], hl[e]);
+          for (int hf = 0; hf < 2; ++hf) {
+            const int kk = 2 * kq + hf;
+            const float4 q4 = qraw[kk].get();
+            const float2 q01 = make_float2(q4.x, q4.y), q23 = make_float2(q4.z, q4.w);
+            zq2 = __ffma2_rn(q01, __half22float2(bits_h2(zw[2 * hf])), zq2);
+            zq2 = __ffma2_rn(q23, __half22float2(bits_h2(zw[2 * hf + 1])), zq2);
+            // (q * scale) as fp16 hi + lo, two channels per conversion
+            const float2 x01 = __fmul2_rn(q01, __half22float2(bits_h2(sw[2 * hf])));
+            const float2 x23 = __fmul2_rn(q23, __half22float2(bits_h2(sw[2 * hf + 1])));
+            const __half2 h01 = __floats2half2_rn(x01.x, x01.y), h23 = __floats2half2_rn(x23.x, x23.y);
+            const float2 r01 = f2sub(x01, __half22float2(h01)), r23 = f2sub(x23, __half22float2(h23));
+            const uint32_t bh[2] = {h2_bits(h01), h2_bits(h23)};
+            const uint32_t bl[2] = {h2_bits(__floats2half2_rn(r01.x, r01.y)), h2_bits(__floats2half2_rn(r23.x, r23.y))};
+            const uint32_t w = words[kk >> 1];
+            const int pb = (kk & 1) * 4;
+            const uint32_t a[4] = {u2x2(w, pb + 0), u2x2(w, pb + 1), u2x2(w, pb + 2), u2x2(w, pb + 3)};
+            mma16816(acc[hf], a, bh);
+            mma16816(acc[hf], a, bl);
           }
-          const uint32_t bh[2] = {pack_h2(hh[0], hh[1]), pack_h2(hh[2], hh[3])};
-          const uint32_t bl[2] = {pack_h2(hl[0], hl[1]), pack_h2(hl[2], hl[3])};
-          const uint32_t w = words[kk >> 1];
-          const int pb = (kk & 1) * 4;
-          const uint32_t a[4] = {u2x2(w, pb + 0), u2x2(w, pb + 1), u2x2(w, pb + 2), u2x2(w, pb + 3)};
-          mma16816(acc, a, bh);
-          mma16816(acc, a, bl);
         }
+        float zq = zq2.x + zq2.y;
         zq += __shfl_xor_sync(0xffffffffu, zq, 1);
         zq += __shfl_xor_sync(0xffffffffu, zq, 2);      // lanes 4g..4g+3 hold q_g . zero
         const float zq0 = __shfl_sync(0xffffffffu, zq, 8 * t);
         const float zq1 = __shfl_sync(0xffffffffu, zq, 8 * t + 4);
-        lgA = __fmul2_rn(make_float2(acc[0] + zq0, acc[1] + zq1), f2(lscale));
-        lgB = __fmul2_rn(make_float2(acc[2] + zq0, acc[3] + zq1), f2(lscale));
+        lgA = __fmul2_rn(make_float2(acc[0][0] + acc[1][0] + zq0, acc[0][1] + acc[1][1] + zq1), f2(lscale));
+        lgB = __fmul2_rn(make_float2(acc[0][2] + acc[1][2] + zq0, acc[0][3] + acc[1][3] + zq1), f2(lscale));
       }
 
       // Tier A from the stored witness (zero for repaired blocks and KIVI's unfinished block)
@@ -608,32 +631,26 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           }
         }
       } else {  // KIVI values: p*scale times codes, plus p*zero per group
-        // [tok][G][scale, zero]; this lane's tokens 2t, 2t+1 and 2t+8, 2t+9 are two 32-byte runs
-        const __half* vp = reinterpret_cast<const __half*>(sb + L::VP);
+        // [tok][G][scale, zero]: 16 bytes per token; this lane's tokens are 2t, 2t+1, 2t+8, 2t+9,
+        // and group j's (scale, zero) of token e is word j of row e
+        const uint4* vp4 = reinterpret_cast<const uint4*>(sb + L::VP);
+        const uint4 r0 = vp4[2 * t], r1 = vp4[2 * t + 1], r2 = vp4[2 * t + 8], r3 = vp4[2 * t + 9];
+        const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+        const uint32_t w2[4] = {r2.x, r2.y, r2.z, r2.w}, w3[4] = {r3.x, r3.y, r3.z, r3.w};
         const float2 p01 = __half22float2(bits_h2(P0)), p23 = __half22float2(bits_h2(P1));
-        const float pvv[4] = {p01.x, p01.y, p23.x, p23.y};
-        float sv[4][4], zv[4][4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half* row = vp + (2 * t + (e & 1) + 8 * (e >> 1)) * 8;
-#pragma unroll
-          for (int G = 0; G < 4; ++G) { sv[e][G] = __half2float(row[2 * G]); zv[e][G] = __half2float(row[2 * G + 1]); }
-        }
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-          float z = 0.f;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) z = fmaf(pvv[e], zv[e][G], z);
-          z += __shfl_xor_sync(0xffffffffu, z, 1);
-          z += __shfl_xor_sync(0xffffffffu, z, 2);
-          zc[G] += z;
-        }
         const uint4 vw4 = *reinterpret_cast<const uint4*>(sb + L::VC + lane * 16);
         const uint32_t vwords[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t bfr[2] = {h2_bits(__floats2half2_rn(pvv[0] * sv[0][j], pvv[1] * sv[1][j])),
-                                   h2_bits(__floats2half2_rn(pvv[2] * sv[2][j], pvv[3] * sv[3][j]))};
+          const float2 sz0 = __half22float2(bits_h2(w0[j])), sz1 = __half22float2(bits_h2(w1[j]));
+          const float2 sz2 = __half22float2(bits_h2(w2[j])), sz3 = __half22float2(bits_h2(w3[j]));
+          // sum_t p_t zero_{t,j} of head g over the lane's four tokens, then over the four lanes
+          float z = fmaf(p01.x, sz0.y, fmaf(p01.y, sz1.y, fmaf(p23.x, sz2.y, p23.y * sz3.y)));
+          z += __shfl_xor_sync(0xffffffffu, z, 1);
+          z += __shfl_xor_sync(0xffffffffu, z, 2);
+          zc[j] += z;
+          const float2 ps01 = __fmul2_rn(p01, make_float2(sz0.x, sz1.x)), ps23 = __fmul2_rn(p23, make_float2(sz2.x, sz3.x));
+          const uint32_t bfr[2] = {h2_bits(__floats2half2_rn(ps01.x, ps01.y)), h2_bits(__floats2half2_rn(ps23.x, ps23.y))};
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int pb = hf * 4;
