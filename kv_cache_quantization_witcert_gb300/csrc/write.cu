@@ -60,6 +60,92 @@ __device__ __forceinline__ void store_witness(uint8_t* wreg, int r, const double
   }
 }
 
+// ---------------------------------------------------------------- fp32 double-float witness
+// The stored witness is fp16_ru(w * (1 + 2^-48)) of the fp64 band norm.  GB300's FP64 unit is
+// too slow to form every norm in fp64, so the norm is formed from the exact residual in
+// double-float (pairs of fp32 with error-free sums and products) to about 2^-44, and the fp16
+// rounding is taken from that unless an fp16 value lies within the error band of the
+// result or the values leave the safe range; then the warp repeats the fp64 computation.
+struct Df {
+  float hi, lo;
+};
+__device__ __forceinline__ Df two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ Df fast_two_sum(float a, float b) {      // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ Df two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ Df df_add(Df a, Df b) {
+  const Df s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+// Residual t0 + t1 + t2 + t3 (exact fp32 terms) as a double-float; its absolute error is
+// below 2^-46 (|t0| + |t1| + |t2| + |t3|).
+__device__ __forceinline__ Df residual_df(float t0, float t1, float t2, float t3) {
+  const Df a = two_sum(t0, t1);
+  const Df b = two_sum(a.hi, t2);
+  const Df c = two_sum(b.hi, t3);
+  const float e = __fadd_rn(__fadd_rn(a.lo, b.lo), c.lo);
+  return fabsf(c.hi) >= fabsf(e) ? fast_two_sum(c.hi, e) : two_sum(c.hi, e);
+}
+// Smallest fp16 >= hi + lo (lo below one fp32 unit of hi).
+__device__ __forceinline__ __half f16_ru_df(float hi, float lo) {
+  __half h = __float2half_ru(hi);
+  if (__half2float(h) == hi && lo > 0.f) h = __ushort_as_half((unsigned short)(__half_as_ushort(h) + 1));
+  return h;
+}
+
+// Lanes 0..15 store band `lane` of token r from the lane's four residuals (double-float, with
+// absolute error bound `err` summed over them) and its partner lane's (lane ^ 16).  Returns
+// false, storing nothing, when the warp must fall back to the fp64 computation.
+__device__ __forceinline__ bool store_witness_df(uint8_t* wreg, int r, const Df (&res)[4], float err, int lane,
+                                                 bool zero) {
+  Df ss = {0.f, 0.f};
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = fabsf(res[e].hi);
+    bad |= a > 0x1p60f || (a != 0.f && a < 0x1p-45f);
+    Df sq = two_prod(res[e].hi, res[e].hi);
+    sq.lo = __fmaf_rn(2.0f * res[e].hi, res[e].lo, sq.lo);
+    ss = df_add(ss, sq);
+  }
+  ss = df_add(ss, {__shfl_xor_sync(0xffffffffu, ss.hi, 16), __shfl_xor_sync(0xffffffffu, ss.lo, 16)});
+  err = __fadd_ru(err, __shfl_xor_sync(0xffffffffu, err, 16));
+  __half w16 = __float2half_rn(0.f);
+  if (lane < 16 && !zero) {
+    if (ss.hi > 0.f) {
+      // w = sqrt(ss): correctly rounded root, one correction from the exact remainder
+      const float y = __fsqrt_rn(ss.hi);
+      const float rem = __fmaf_rn(-y, y, ss.hi);
+      const Df w = fast_two_sum(y, __fdividef(__fadd_rn(rem, ss.lo), 2.0f * y));
+      // z = w (1 + 2^-48)
+      const Df z = fast_two_sum(w.hi, __fmaf_rn(w.hi, 0x1p-48f, w.lo));
+      w16 = f16_ru_df(z.hi, z.lo);
+      // relative error band of z: double-float arithmetic plus the residuals' own error
+      const float band = __fadd_ru(0x1p-40f, __fdiv_ru(__fmul_ru(4.0f, err), w.hi));
+      const float up = __fsub_rn(__fsub_rn(__half2float(w16), z.hi), z.lo);         // >= 0
+      const unsigned short bits = __half_as_ushort(w16);
+      const float down = bits ? __fadd_rn(__fsub_rn(z.hi, __half2float(__ushort_as_half((unsigned short)(bits - 1)))), z.lo)
+                              : INFINITY;
+      const float lim = __fmul_ru(__fmul_ru(2.0f, band), z.hi);
+      bad |= !(up > lim) || !(down > lim) || ss.hi < 0x1p-90f;
+    } else {
+      bad |= err > 0.f;            // an exact zero only when the residuals are exact
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) return false;
+  if (lane < 16) *reinterpret_cast<__half*>(wreg + wit_off(r, lane)) = w16;
+  return true;
+}
+
 // Exact-key side effects shared by all schemes: backing store and repaired blocks.
 template <typename T>
 __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int t, int lane, const T* krow) {
@@ -100,7 +186,9 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
     const float4 xi = dither4(a.seed, a.layer, h, t, lane, tensor);
     const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
     uint32_t packed = 0;
-    double res[4];
+    int codes[4];
+    Df rdf[4];
+    float err = 0.f;
     int clamps = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -112,7 +200,16 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
         if (rz > 127.f) { rz = 127.f; ++clamps; }
         code = (int)rz;
       }
-      res[e] = (double)x[e] - (double)s * ((double)code - (double)xs[e]);
+      codes[e] = code;
+      if (tensor == 0) {
+        // residual x - s (code - xi) = x - s code + s xi, as exact fp32 terms (s code has at most
+        // 19 significant bits; s xi is an exact product pair)
+        const float sc = __fmul_rn(s, (float)code);
+        const Df sx = two_prod(s, xs[e]);
+        rdf[e] = residual_df(x[e], -sc, sx.hi, sx.lo);
+        err = __fadd_ru(err, __fmul_ru(0x1p-46f, __fadd_ru(__fadd_ru(fabsf(x[e]), fabsf(sc)),
+                                                           __fadd_ru(fabsf(sx.hi), fabsf(sx.lo)))));
+      }
       const uint32_t biased = (uint32_t)(code + 128) & 0xFFu;
       if (tensor == 0) packed |= biased << (8 * e);
       else bp[Int8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)biased;
@@ -122,7 +219,12 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
       *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS + vscale_off(r, G) : Int8Layout::KS + (r * 4 + G) * 2)) = s16;
     if (tensor == 0) {
       *reinterpret_cast<uint32_t*>(bp + Int8Layout::KC + kcode_off(r, 4 * lane)) = packed;
-      store_witness(bp + Int8Layout::W, r, res, lane, repaired);
+      if (!store_witness_df(bp + Int8Layout::W, r, rdf, err, lane, repaired)) {
+        double res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
+        store_witness(bp + Int8Layout::W, r, res, lane, repaired);
+      }
     }
   }
 }
@@ -143,18 +245,25 @@ __global__ void __launch_bounds__(128) write_fp8_kernel(const WriteArgs a) {
     float x[4];
     load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
     uint32_t packed = 0;
-    double res[4];
+    float xhs[4];
+    Df rdf[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x[e], __NV_SATFINITE, __NV_E4M3);
       const float xh = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
-      res[e] = (double)x[e] - (double)xh;
+      xhs[e] = xh;
+      rdf[e] = residual_df(x[e], -xh, 0.f, 0.f);            // exact: one error-free sum
       if (tensor == 0) packed |= (uint32_t)c << (8 * e);
       else bp[Fp8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)c;
     }
     if (tensor == 0) {
       *reinterpret_cast<uint32_t*>(bp + Fp8Layout::KC + kcode_off(r, 4 * lane)) = packed;
-      store_witness(bp + Fp8Layout::W, r, res, lane, repaired);
+      if (!store_witness_df(bp + Fp8Layout::W, r, rdf, 0.f, lane, repaired)) {
+        double res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xhs[e];
+        store_witness(bp + Fp8Layout::W, r, res, lane, repaired);
+      }
     }
   }
 }
@@ -254,16 +363,27 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
     }
 #pragma unroll
     for (int r = 0; r < kBlk; ++r) {
-      double res[4];
+      int codes[4];
+      Df rdf[4];
+      float err = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int code = kivi_code(x[r][e], zr[e], sc[e]);
-        res[e] = (double)x[r][e] - ((double)zr[e] + (double)sc[e] * (double)code);
+        codes[e] = code;
+        // residual x - (zero + scale code): scale code is exact (at most 13 significant bits)
+        const float scc = __fmul_rn(sc[e], (float)code);
+        rdf[e] = residual_df(x[r][e], -zr[e], -scc, 0.f);
+        err = __fadd_ru(err, __fmul_ru(0x1p-46f, __fadd_ru(__fadd_ru(fabsf(x[r][e]), fabsf(zr[e])), fabsf(scc))));
         int off, bit;
         kivi_k_pos(r, 4 * lane + e, off, bit);
         if (code) atomicOr(&img[off / 4], (unsigned int)code << bit);
       }
-      store_witness(bp + KiviLayout::W, r, res, lane, false);
+      if (!store_witness_df(bp + KiviLayout::W, r, rdf, err, lane, false)) {
+        double res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[r][e] - ((double)zr[e] + (double)sc[e] * (double)codes[e]);
+        store_witness(bp + KiviLayout::W, r, res, lane, false);
+      }
     }
     __syncwarp();
     for (int k = lane; k < 128; k += 32) reinterpret_cast<unsigned int*>(bp + KiviLayout::KC)[k] = img[k];
