@@ -310,9 +310,12 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
   }
 }
 
-// KIVI keys: one warp per (sequence, KV head) walks the blocks this write touches.
+// KIVI keys: one warp per (sequence, KV head, block) this write touches.  Blocks the write
+// completes are quantized (block blk0 + blockIdx.y); the block it leaves unfinished is
+// launched after them and keeps its new keys exact in the tail, which the first completed
+// block may still have to read.
 template <typename T>
-__global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
+__global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int blk0) {
   pdl_wait();
   pdl_trigger();
   const int sh = blockIdx.x, lane = threadIdx.x;       // sh = i * Hkv + h
@@ -320,7 +323,8 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
   __shared__ unsigned int img[128];                    // K code words of one block
   float* tail = a.kivi_tail + (size_t)sh * kBlk * kD;
   const int t_end = a.t0 + a.n_tok;
-  for (int blk = a.t0 / kBlk; blk * kBlk < t_end; ++blk) {
+  {
+    const int blk = blk0 + blockIdx.y;
     const int lo = blk * kBlk;
     if (lo + kBlk > t_end) {   // unfinished block: keep the new keys exact in the tail
       for (int t = (a.t0 > lo ? a.t0 : lo); t < t_end; ++t) {
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
         *reinterpret_cast<float4*>(tail + (t - lo) * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
       }
       __syncwarp();
-      break;
+      return;
     }
     float x[16][4];
 #pragma unroll
@@ -391,8 +395,8 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a) {
   }
 }
 
-template <typename K>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, bool pdl, const WriteArgs& a) {
+template <typename K, typename... Extra>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, bool pdl, const WriteArgs& a, Extra... extra) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -402,7 +406,7 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, bool pd
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a, extra...);
 }
 
 template <typename T>
@@ -413,7 +417,14 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
   if (scheme == kFp8) return launch_pdl(write_fp8_kernel<T>, blocks, dim3(128), st, pdl, a);
   cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, pdl, a);
   if (e != cudaSuccess) return e;
-  return launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv), dim3(32), st, pdl, a);
+  // blocks this write completes, then the unfinished one (if any)
+  const int t_end = a.t0 + a.n_tok, b0 = a.t0 / kBlk, nfull = t_end / kBlk - b0;
+  if (nfull > 0) {
+    e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, nfull), dim3(32), st, pdl, a, b0);
+    if (e != cudaSuccess) return e;
+  }
+  if (t_end % kBlk) e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, 1), dim3(32), st, pdl, a, t_end / kBlk);
+  return e;
 }
 
 }  // namespace
