@@ -203,3 +203,20 @@ def test_errors_are_reported_not_raised_on_device():
         gpu.witcert_gate(0, 1.0)
     assert e.value.status == _lib.ESTATE
     assert gpu.witcert_stats()["device_errors"] == 0
+
+
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+def test_witness_fallback_on_extreme_keys(scheme):
+    """Keys near 1e-20 and near 1e25 push the writers' fp32 double-float witness outside its
+    safe range, so those bands take the fp64 computation; keys near 1e-9 give witnesses in
+    fp16's subnormal range.  Every stored witness must still equal the oracle's bit for bit."""
+    w = WORKLOADS["tiny"].with_(scheme=scheme)
+    gpu, ref = make_pair(w)
+    K, V = gen_kv(w, 0)
+    K = K.copy()
+    K[:, 0:5] *= 1e-20         # residuals far below 2^-45
+    K[:, 5:9] *= 1e25          # residuals above 2^60
+    K[:, 9:13] *= 1e-9         # witnesses below fp16's smallest normal
+    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    ref.write(0, K, V)
+    check_write(gpu, ref, 0, scheme)
