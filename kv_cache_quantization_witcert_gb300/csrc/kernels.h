@@ -14,6 +14,7 @@ struct WriteArgs {
   const void* K;             // [B][n_tok][Hkv][128]
   const void* V;
   int B, Hkv, n_tok, t0, layer, backing_rows;   // backing_rows: rows per (seq, KV head) in the backing store
+  int tok_begin, tok_count;  // tokens of this write a per-token launch covers
   int is_bf16;
   uint64_t seed;
   void* backing;             // device-mapped pinned host, layer base [B][Hkv][backing_rows][128], or null

@@ -161,15 +161,11 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
   return false;
 }
 
+// Token n of the write (position t = t0 + n, row r = t mod 16 of its block) of sequence i,
+// KV head h, quantized into the block image at bp (device memory or shared memory).
 template <typename T>
-__global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wid >= a.B * a.n_tok * a.Hkv) return;
-  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
-  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * Int8Layout::BYTES;
+__device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
+  const int t = a.t0 + n, r = t & 15;
   const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
   const int G = lane >> 3;
@@ -229,15 +225,11 @@ __global__ void __launch_bounds__(128) write_int8_kernel(const WriteArgs a) {
   }
 }
 
+// Token n of the write (position t = t0 + n, row r = t mod 16 of its block) of sequence i,
+// KV head h, quantized into the block image at bp (device memory or shared memory).
 template <typename T>
-__global__ void __launch_bounds__(128) write_fp8_kernel(const WriteArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wid >= a.B * a.n_tok * a.Hkv) return;
-  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
-  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * Fp8Layout::BYTES;
+__device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
+  const int t = a.t0 + n, r = t & 15;
   const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
 #pragma unroll
@@ -266,6 +258,49 @@ __global__ void __launch_bounds__(128) write_fp8_kernel(const WriteArgs a) {
       }
     }
   }
+}
+
+
+// One warp per (sequence, token, KV head) of tokens tok_begin .. tok_begin + tok_count - 1:
+// appends and the parts of a write that do not fill whole blocks.
+template <typename T, bool INT8>
+__global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= a.B * a.tok_count * a.Hkv) return;
+  const int h = wid % a.Hkv, n = a.tok_begin + (wid / a.Hkv) % a.tok_count, i = wid / (a.Hkv * a.tok_count);
+  const int blk = (a.t0 + n) >> 4;
+  constexpr int kBytes = INT8 ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * kBytes;
+  if constexpr (INT8) int8_token<T>(a, bp, i, h, n, lane);
+  else fp8_token<T>(a, bp, i, h, n, lane);
+}
+
+// One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
+// completely: the warp builds the block's image in shared memory token by token and stores
+// it with 16-byte writes.
+template <typename T, bool INT8>
+__global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kBytes = INT8 ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  __shared__ __align__(16) uint8_t img[4][kBytes];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long unit = (long long)blockIdx.x * 4 + warp;       // (i * Hkv + h) * nblocks + b
+  if (unit >= (long long)a.B * a.Hkv * nblocks) return;
+  const int b = (int)(unit % nblocks), sh = (int)(unit / nblocks);
+  const int i = sh / a.Hkv, h = sh % a.Hkv, blk = blk0 + b;
+  uint8_t* im = img[warp];
+  for (int r = 0; r < kBlk; ++r) {
+    const int n = blk * kBlk + r - a.t0;
+    if constexpr (INT8) int8_token<T>(a, im, i, h, n, lane);
+    else fp8_token<T>(a, im, i, h, n, lane);
+  }
+  __syncwarp();
+  uint4* dst = reinterpret_cast<uint4*>(a.blocks + ((size_t)sh * a.nblk_max + blk) * kBytes);
+  const uint4* src = reinterpret_cast<const uint4*>(im);
+  for (int k = lane; k < kBytes / 16; k += 32) dst[k] = src[k];
 }
 
 // KIVI asymmetric 2-bit of one value against fp16 scale/zero (fp32 steps as the oracle states them).
@@ -413,8 +448,29 @@ template <typename T>
 cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   const int warps = a.B * a.n_tok * a.Hkv;
   const dim3 blocks((warps * 32 + 127) / 128);
-  if (scheme == kInt8) return launch_pdl(write_int8_kernel<T>, blocks, dim3(128), st, pdl, a);
-  if (scheme == kFp8) return launch_pdl(write_fp8_kernel<T>, blocks, dim3(128), st, pdl, a);
+  if (scheme == kInt8 || scheme == kFp8) {
+    // whole blocks through shared-memory images, the rest token by token
+    const int t_end = a.t0 + a.n_tok;
+    const int lo_full = (a.t0 + kBlk - 1) / kBlk * kBlk, hi_full = t_end / kBlk * kBlk;
+    auto tokens = [&](int begin, int count) -> cudaError_t {
+      if (count <= 0) return cudaSuccess;
+      WriteArgs b = a;
+      b.tok_begin = begin;
+      b.tok_count = count;
+      const dim3 g(((unsigned)(a.B * count * a.Hkv) * 32u + 127u) / 128u);
+      return scheme == kInt8 ? launch_pdl(write_token_kernel<T, true>, g, dim3(128), st, pdl, b)
+                             : launch_pdl(write_token_kernel<T, false>, g, dim3(128), st, pdl, b);
+    };
+    if (hi_full <= lo_full) return tokens(0, a.n_tok);
+    cudaError_t e = tokens(0, lo_full - a.t0);
+    if (e != cudaSuccess) return e;
+    const int nblocks = (hi_full - lo_full) / kBlk;
+    const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + 3) / 4));
+    e = scheme == kInt8 ? launch_pdl(write_block_kernel<T, true>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
+                        : launch_pdl(write_block_kernel<T, false>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
+    if (e != cudaSuccess) return e;
+    return tokens(hi_full - a.t0, t_end - hi_full);
+  }
   cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, pdl, a);
   if (e != cudaSuccess) return e;
   // blocks this write completes, then the unfinished one (if any)
