@@ -676,6 +676,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     }
   }
 
+  // Layers are decoded in order: the first blocks this warp will stream in the next layer go
+  // to L2 now, so the next decode's pipeline fill overlaps this one's merge and the next write.
+  if (p.next_blocks && active && !fault && lane == 0)
+    for (int s = 0; s < NST && s < nb; ++s)
+      prefetch_l2(p.next_blocks + (seq_base + b_begin + s) * L::BYTES, L::BYTES);
   pdl_wait();     // partial results overwrite scratch the preceding merge may still read
   if (fault) {
     // drain copies still in flight before the CTA's shared memory is released

@@ -44,6 +44,7 @@ struct DecodeArgs {
   float* out;                // [B][Hq][128]
   float *meter_a, *meter_b, *raw_a, *raw_b;
   int* err;                  // device error word (spin limits)
+  const uint8_t* next_blocks;  // the next layer's base: its first blocks are prefetched into L2, or null
   bool meter;
 };
 

@@ -296,6 +296,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   }
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
   a.err = c->err;
+  if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
   a.meter = meter;
   ProfPair pp{nullptr, nullptr};
   if (c->profiling) {
@@ -367,6 +368,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   }
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
   a.err = c->err;
+  if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
   a.meter = meter;
   e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
