@@ -76,6 +76,10 @@ struct witcert_cache {
 
 namespace {
 
+// Writes of at least this many tokens copy their exact keys to the backing store with the
+// copy engines rather than with the write kernels' stores.
+constexpr int kBulkBackingTokens = 64;
+
 size_t layer_rows(const witcert_cache* c) { return (size_t)c->cfg.batch * c->cfg.n_kv_heads; }
 // Backing-store rows per (sequence, KV head): capacity rounded up to whole 16-token blocks,
 // so page-in can always copy a full block.
@@ -231,7 +235,23 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   a.pool = c->pool;
   if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
   a.clamps = c->clamps;
-  cudaError_t e = launch_write(c->scheme, a, st, c->overlap && !waited);
+  cudaError_t e = cudaSuccess;
+  bool pdl = c->overlap && !waited;
+  if (c->backing_host && n_tok >= kBulkBackingTokens) {
+    // bulk writes copy their exact keys to the pinned backing store with the copy engines,
+    // one strided copy per (sequence, KV head), instead of the kernels' stores over C2C
+    const size_t row = (size_t)kD * c->elem;
+    uint8_t* host = static_cast<uint8_t*>(c->backing_host) + layer * layer_rows(c) * backing_rows(c) * row;
+    for (int i = 0; i < a.B && e == cudaSuccess; ++i)
+      for (int h = 0; h < a.Hkv && e == cudaSuccess; ++h)
+        e = cudaMemcpy2DAsync(host + (((size_t)i * a.Hkv + h) * backing_rows(c) + a.t0) * row, row,
+                              static_cast<const uint8_t*>(K) + ((size_t)i * n_tok * a.Hkv + h) * row, a.Hkv * row,
+                              row, n_tok, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
+    a.backing = nullptr;
+    pdl = false;                     // the copies sit between this write and its predecessor
+  }
+  e = launch_write(c->scheme, a, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "write launch");
   c->last_write_layer = layer;
   c->last_write_blk = a.t0 / kBlk;
