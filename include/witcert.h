@@ -67,6 +67,9 @@ typedef struct {
   int n_splits;            /* KV splits per (sequence, KV head) in decode; 0 = choose from the SM count */
   int max_repair_blocks;   /* capacity of the exact-key pool in 16-token blocks; 0 disables the gate
                               and the pinned backing store */
+  int pos_offset;          /* global position of the cache's first token: a cache holding one slice of
+                              a longer context (one shard of a context-parallel decode) keys its dither
+                              on global positions; 0 for a whole context */
 } witcert_config;
 
 typedef struct witcert_cache witcert_cache;
@@ -176,6 +179,30 @@ witcert_status witcert_gate(witcert_cache* cache, int layer, float tau, void* st
 /* Gate counters, summed over all gate calls.  Waits for outstanding gate work
  * with a host deadline of `timeout_ms` (ETIMEDOUT if it runs out). */
 witcert_status witcert_gate_stats(witcert_cache* cache, witcert_gate_counters* out, int timeout_ms);
+
+/* Context-parallel decode, one shard: this cache holds one slice of a longer context (its
+ * tokens at global positions pos_offset, pos_offset + 1, ...; see witcert_config).  The
+ * shard's decode of `layer` is merged over the shard's own splits but not normalized: for
+ * every (sequence, query head) cell it writes one record of kPartStride = 132 floats to
+ * `part` (device, [batch][n_q_heads][132]): the running maximum m of the logits in log2 units,
+ * Z = sum 2^(l - m), S_A and S_B = sum 2^(l - m) expm1(c) of the Tier A and Tier B bounds,
+ * and the 128 value sums relative to m.  Tier B's kappa uses s_total, the whole context's
+ * length (>= this slice's), so the shards of one decode share delta_loc.  The records of all
+ * shards, gathered in any order into [batch][n_q_heads][n_parts][132], are merged by
+ * witcert_merge_partials into the same output and meters a single cache holding the whole
+ * context would give (up to floating-point summation order).  Block risks are not kept
+ * (gating needs a whole-context decode).  Same-stream ordering as witcert_decode. */
+witcert_status witcert_decode_partial(witcert_cache* cache, int layer, const void* q, double delta_req,
+                                      long long s_total, float* part, void* stream);
+
+/* Merge of context-parallel shard records (see witcert_decode_partial; the log-sum-exp merge
+ * of the pages' split-KV decode, applied across shards): parts is device [batch][n_q_heads]
+ * [n_parts][132]; out [batch][n_q_heads][128] fp32 and the optional meters [batch][n_q_heads]
+ * as in witcert_decode (meter_b NaN unless scheme is WITCERT_INT8_DITHER).  Asynchronous on
+ * `stream`; no cache is involved. */
+witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch, int n_q_heads,
+                                      witcert_scheme scheme, float* out, float* meter_a, float* meter_b,
+                                      float* raw_a, float* raw_b, void* stream);
 
 /* Library counters.  Synchronizes the device. */
 witcert_status witcert_stats(witcert_cache* cache, witcert_stats_t* out);

@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import (BF16, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER, KIVI2,  # noqa: F401
                    SCHEMES, WitcertError, check, load)
 
-__all__ = ["Cache", "witcert_dither", "WitcertError", "load", "SCHEMES"]
+__all__ = ["Cache", "witcert_dither", "witcert_merge_partials", "WitcertError", "load", "SCHEMES", "PART_STRIDE"]
 
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -33,13 +33,13 @@ class Cache:
     """One WitCert cache: compressed K/V store, witnesses, optional gate state."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, batch, max_tokens, scheme="int8_dither",
-                 dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0):
+                 dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0, pos_offset=0):
         lib = load()
         self.dtype = dtype
         self.cfg = _lib.witcert_config(n_layers, n_q_heads, n_kv_heads, 128, batch, max_tokens,
                                        SCHEMES[scheme] if isinstance(scheme, str) else scheme,
                                        BF16 if dtype == torch.bfloat16 else F32, seed, total_steps, n_splits,
-                                       max_repair_blocks)
+                                       max_repair_blocks, pos_offset)
         self.scheme = scheme
         h = ctypes.c_void_p()
         check(lib.witcert_create(ctypes.byref(self.cfg), ctypes.byref(h)), "witcert_create")
@@ -64,6 +64,17 @@ class Cache:
         check(load().witcert_decode_noalloc(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
                                             _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
               "witcert_decode_noalloc")
+
+    def witcert_decode_partial(self, layer, q, delta_req, s_total, part, stream=None):
+        assert q.is_contiguous() and q.dtype == self.dtype and part.dtype == torch.float32 and part.is_contiguous()
+        check(load().witcert_decode_partial(self._h, layer, _ptr(q), float(delta_req), int(s_total), _ptr(part),
+                                            _stream_ptr(stream)), "witcert_decode_partial")
+
+    def decode_partial(self, layer, q, delta_req, s_total, stream=None):
+        """This shard's per-cell records [B, Hq, 132] (see witcert_decode_partial)."""
+        part = torch.empty((q.shape[0], q.shape[1], PART_STRIDE), dtype=torch.float32, device=q.device)
+        self.witcert_decode_partial(layer, q, delta_req, s_total, part, stream=stream)
+        return part
 
     def witcert_gate(self, layer, tau, stream=None):
         check(load().witcert_gate(self._h, layer, float(tau), _stream_ptr(stream)), "witcert_gate")
@@ -134,6 +145,23 @@ class Cache:
         if dst.numel():
             self.witcert_export(layer, what, dst, stream=stream)
         return dst
+
+
+PART_STRIDE = 132     # floats per (sequence, query head) record: m, Z, S_A, S_B, 128 value sums
+
+
+def witcert_merge_partials(parts, scheme, out=None, meters=True, stream=None):
+    """Merge shard records parts [B, Hq, n_parts, 132] (device fp32) into the output [B, Hq, 128]
+    and, with meters, {"meter_a", "meter_b", "raw_a", "raw_b"} (see witcert_merge_partials)."""
+    assert parts.dtype == torch.float32 and parts.is_contiguous() and parts.shape[-1] == PART_STRIDE
+    B, Hq, n = parts.shape[0], parts.shape[1], parts.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, 128), dtype=torch.float32, device=parts.device)
+    m = torch.empty((4, B, Hq), dtype=torch.float32, device=parts.device) if meters else None
+    ptrs = (_ptr(m[0]), _ptr(m[1]), _ptr(m[2]), _ptr(m[3])) if meters else (None,) * 4
+    check(load().witcert_merge_partials(_ptr(parts), n, B, Hq, SCHEMES[scheme] if isinstance(scheme, str) else scheme,
+                                        _ptr(out), *ptrs, _stream_ptr(stream)), "witcert_merge_partials")
+    return out, ({"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3]} if meters else None)
 
 
 def witcert_wait_selftest(limit_ns, stream=None):

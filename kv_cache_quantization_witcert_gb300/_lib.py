@@ -22,7 +22,8 @@ class witcert_config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("batch", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("scheme", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("seed", ctypes.c_uint64),
-                ("total_steps", ctypes.c_int), ("n_splits", ctypes.c_int), ("max_repair_blocks", ctypes.c_int)]
+                ("total_steps", ctypes.c_int), ("n_splits", ctypes.c_int), ("max_repair_blocks", ctypes.c_int),
+                ("pos_offset", ctypes.c_int)]
 
 
 class witcert_gate_counters(ctypes.Structure):
@@ -46,6 +47,8 @@ SIGNATURES = {
     "witcert_write": [_vp, _int, _vp, _vp, _int, _vp],
     "witcert_decode": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_decode_noalloc": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
+    "witcert_decode_partial": [_vp, _int, _vp, ctypes.c_double, ctypes.c_longlong, _vp, _vp],
+    "witcert_merge_partials": [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_gate": [_vp, _int, ctypes.c_float, _vp],
     "witcert_gate_stats": [_vp, ctypes.POINTER(witcert_gate_counters), _int],
     "witcert_stats": [_vp, ctypes.POINTER(witcert_stats_t)],

@@ -111,7 +111,7 @@ __device__ __forceinline__ float2 meter_term2(float2 pe, float2 d, float2 c) {
 // fills an MMA operand.  Items 0..255 fill the QK operands, one (k-step, lane) each, with
 // 16-byte stores; items 256..511 fill the PV operand, one (token pair, channel quad) each.
 __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
-  const int tb = blk * kBlk;
+  const int tb = p.pos0 + blk * kBlk;
   for (int idx = threadIdx.x; idx < 512; idx += nthreads) {
     if (idx < 256) {
       // k-step kk, lane L = 4g + tq: tokens g and g + 8, channels 16kk + 4tq .. 16kk + 4tq + 3.
@@ -777,6 +777,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
       if (threadIdx.x < kD) o = fmaf(wt, s_acc[w][threadIdx.x], o);
     }
   }
+  if (p.part_out) {           // context-parallel shard: the cell's combined record, unnormalized
+    float* rec = p.part_out + (size_t)cell * kPartStride;
+    if (threadIdx.x == 0) *reinterpret_cast<float4*>(rec) = make_float4(Mx, Zt, SAt, SBt);
+    if (threadIdx.x < kD) rec[4 + threadIdx.x] = o;
+    return;
+  }
   const float inv = Zt > 0.f ? 1.0f / Zt : 0.f;
   if (threadIdx.x < kD) p.out[(size_t)cell * kD + threadIdx.x] = o * inv;
   if (!p.meter) return;
@@ -912,6 +918,12 @@ cudaError_t decode_static_scratch(float** ptr, size_t* bytes) {
   *ptr = addr[dev];
   *bytes = kStaticScratchBytes;
   return cudaSuccess;
+}
+
+cudaError_t launch_merge_records(int scheme, const DecodeArgs& a, cudaStream_t st) {
+  const dim3 mg(a.B * a.Hq);
+  return scheme == kInt8 ? launch_pdl(decode_merge_kernel<true, false>, mg, dim3(kMergeWarps * 32), 0, st, false, a)
+                         : launch_pdl(decode_merge_kernel<false, false>, mg, dim3(kMergeWarps * 32), 0, st, false, a);
 }
 
 int decode_ctas_per_sm(int scheme, const DecodeArgs& a0) {

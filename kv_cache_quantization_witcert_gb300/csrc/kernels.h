@@ -15,6 +15,7 @@ struct WriteArgs {
   const void* V;
   int B, Hkv, n_tok, t0, layer, backing_rows;   // backing_rows: rows per (seq, KV head) in the backing store
   int tok_begin, tok_count;  // tokens of this write a per-token launch covers
+  int pos0;                  // global position of the cache's first token (dither key)
   int is_bf16;
   uint64_t seed;
   void* backing;             // device-mapped pinned host, layer base [B][Hkv][backing_rows][128], or null
@@ -45,6 +46,9 @@ struct DecodeArgs {
   float *meter_a, *meter_b, *raw_a, *raw_b;
   int* err;                  // device error word (spin limits)
   const uint8_t* next_blocks;  // the next layer's base: its first blocks are prefetched into L2, or null
+  int pos0;                  // global position of the cache's first token (dither key)
+  float* part_out;           // [B][Hq][kPartStride]: merge writes each cell's combined record here
+                             // (context-parallel shard) instead of the output and meters, or null
   bool meter;
 };
 
@@ -58,6 +62,8 @@ void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]);
 cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStream_t st,
                           cudaEvent_t split_start, cudaEvent_t split_stop, bool pdl);
 int decode_ctas_per_sm(int scheme, const DecodeArgs& a);
+// Merge kernel alone over caller-given records a.part [B][Hq][a.n_splits][kPartStride].
+cudaError_t launch_merge_records(int scheme, const DecodeArgs& a, cudaStream_t st);
 int decode_auto_splits(int B, int Hkv, int nblk, int sm_count, int per_sm);
 // Device address (current device) and size of the library's static split scratch,
 // used by witcert_decode_noalloc; the first call on a device looks the address up.

@@ -148,6 +148,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   if (f.kv_dtype != WITCERT_F32 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "unknown dtype %d", (int)f.kv_dtype);
   if (f.total_steps <= 0) return fail(WITCERT_EINVAL, "total_steps must be positive");
   if (f.n_splits < 0 || f.max_repair_blocks < 0) return fail(WITCERT_EINVAL, "n_splits and max_repair_blocks must be >= 0");
+  if (f.pos_offset < 0) return fail(WITCERT_EINVAL, "pos_offset must be >= 0");
 
   auto* c = new (std::nothrow) witcert_cache();
   if (!c) return fail(WITCERT_ENOMEM, "host allocation failed");
@@ -229,6 +230,7 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   a.backing_rows = (int)backing_rows(c);
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.seed = c->cfg.seed;
+  a.pos0 = c->cfg.pos_offset;
   if (c->backing_dev)
     a.backing = static_cast<uint8_t*>(c->backing_dev) + layer * layer_rows(c) * backing_rows(c) * kD * c->elem;
   if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
@@ -276,17 +278,13 @@ static int auto_splits(const witcert_cache* c, int nblk, bool meter, int cap) {
   return s;
 }
 
-witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
-                              float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
-  if (witcert_status s = check_layer(c, layer)) return s;
-  if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
-  const bool meter = meter_a || meter_b || raw_a || raw_b;
-  if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
-  auto st = static_cast<cudaStream_t>(stream);
-  const bool waited = order_after_gate(c, layer, st);
+// Decode arguments shared by every decode entry point: the layer's store, the query, the
+// split count and the Tier B factor kappa = sqrt(2 ln(2 S / delta_loc)) rounded up, with S
+// the attended context (s_kappa; the layer's own length when 0).
+static void fill_decode(witcert_cache* c, int layer, const void* q, double delta_req, bool meter, long long s_kappa,
+                        DecodeArgs& a) {
   const int S = c->len[layer];
   const int nblk = (S + kBlk - 1) / kBlk;
-  DecodeArgs a{};
   a.blocks = c->blocks + layer * c->layer_blocks;
   a.nblk_max = c->nblk_max;
   if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
@@ -299,15 +297,32 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
   a.layer = layer;
+  a.pos0 = c->cfg.pos_offset;
   a.dirty_blk = c->last_write_layer == layer ? c->last_write_blk : INT_MAX;
   float kappa = 0.f;
-  if (meter && S > 0) {
+  const long long Sk = s_kappa > 0 ? s_kappa : S;
+  if (meter && Sk > 0) {
     const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
-    const double k = std::sqrt(2.0 * std::log(2.0 * S / dloc));
+    const double k = std::sqrt(2.0 * std::log(2.0 * (double)Sk / dloc));
     kappa = (float)k;
     if ((double)kappa < k) kappa = std::nextafter(kappa, INFINITY);
   }
   a.kappa = kappa;
+  a.err = c->err;
+  if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
+  a.meter = meter;
+}
+
+witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
+                              float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
+  const bool meter = meter_a || meter_b || raw_a || raw_b;
+  if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
+  auto st = static_cast<cudaStream_t>(stream);
+  const bool waited = order_after_gate(c, layer, st);
+  DecodeArgs a{};
+  fill_decode(c, layer, q, delta_req, meter, 0, a);
   a.part = c->part;
   const bool gate = c->cfg.max_repair_blocks > 0;
   if (gate && meter) {
@@ -315,9 +330,6 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
     a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
   }
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
-  a.err = c->err;
-  if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
-  a.meter = meter;
   ProfPair pp{nullptr, nullptr};
   if (c->profiling) {
     if (c->prof_free.empty()) {
@@ -332,7 +344,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
   cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b, c->overlap && !waited);
   if (pp.a) c->prof_pending.push_back(pp);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (gate && meter) c->risk_len[layer] = S;
+  if (gate && meter) c->risk_len[layer] = a.S;
   c->last_write_layer = -1;
   c->last_n_splits = a.n_splits;
   ++c->decode_calls;
@@ -346,11 +358,8 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
   const bool meter = meter_a || meter_b || raw_a || raw_b;
   if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
-  const int S = c->len[layer];
-  const int nblk = (S + kBlk - 1) / kBlk;
   DecodeArgs a{};
-  a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
-  a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits : auto_splits(c, nblk, meter, c->max_splits);
+  fill_decode(c, layer, q, delta_req, meter, 0, a);
   float* scratch = nullptr;
   size_t scratch_bytes = 0;
   cudaError_t e = decode_static_scratch(&scratch, &scratch_bytes);
@@ -361,25 +370,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
                 "the static array holds %zu", a.B, a.Hq, a.n_splits, need, scratch_bytes);
   auto st = static_cast<cudaStream_t>(stream);
   const bool waited = order_after_gate(c, layer, st);
-  a.blocks = c->blocks + layer * c->layer_blocks;
-  a.nblk_max = c->nblk_max;
-  if (c->slots) a.slots = c->slots + layer * layer_rows(c) * c->nblk_max;
-  a.pool = c->pool;
-  if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
-  a.q = q;
-  a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
-  a.seed = c->cfg.seed;
-  philox_round_keys(a.seed, a.rk0, a.rk1);
-  a.layer = layer;
   a.dirty_blk = c->last_write_layer == layer ? c->last_write_blk : INT_MAX;
-  float kappa = 0.f;
-  if (meter && S > 0) {
-    const double dloc = delta_req / ((double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps);
-    const double k = std::sqrt(2.0 * std::log(2.0 * S / dloc));
-    kappa = (float)k;
-    if ((double)kappa < k) kappa = std::nextafter(kappa, INFINITY);
-  }
-  a.kappa = kappa;
   a.part = scratch;
   const bool gate = c->cfg.max_repair_blocks > 0;
   if (gate && meter) {
@@ -387,13 +378,50 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
     a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
   }
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
-  a.err = c->err;
-  if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
-  a.meter = meter;
   e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (gate && meter) c->risk_len[layer] = S;
+  if (gate && meter) c->risk_len[layer] = a.S;
   c->last_write_layer = -1;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_decode_partial(witcert_cache* c, int layer, const void* q, double delta_req,
+                                      long long s_total, float* part, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!q || !part) return fail(WITCERT_EINVAL, "q and part must not be NULL");
+  if (!(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
+  if (s_total < c->len[layer]) return fail(WITCERT_EINVAL, "s_total %lld is below the slice's own %d tokens",
+                                           s_total, c->len[layer]);
+  auto st = static_cast<cudaStream_t>(stream);
+  const bool waited = order_after_gate(c, layer, st);
+  DecodeArgs a{};
+  fill_decode(c, layer, q, delta_req, true, s_total, a);
+  a.part = c->part;
+  a.part_out = part;
+  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  c->last_write_layer = -1;
+  c->last_n_splits = a.n_splits;
+  ++c->decode_calls;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch, int n_q_heads,
+                                      witcert_scheme scheme, float* out, float* meter_a, float* meter_b,
+                                      float* raw_a, float* raw_b, void* stream) {
+  if (!parts || !out) return fail(WITCERT_EINVAL, "parts and out must not be NULL");
+  if (n_parts < 1 || batch < 1 || n_q_heads < 1) return fail(WITCERT_EINVAL, "n_parts, batch and n_q_heads must be >= 1");
+  if (scheme < WITCERT_INT8_DITHER || scheme > WITCERT_KIVI2) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)scheme);
+  DecodeArgs a{};
+  a.part = const_cast<float*>(parts);
+  a.n_splits = n_parts;
+  a.B = batch; a.Hq = n_q_heads;
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
+  a.meter = meter_a || meter_b || raw_a || raw_b;
+  cudaError_t e = launch_merge_records((int)scheme, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   ok();
   return WITCERT_OK;
 }

@@ -179,7 +179,7 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     __half s16 = __float2half_ru(__fdiv_rn(amax, 127.0f));
     if (__half2float(s16) > 65504.0f) s16 = __float2half_rn(65504.0f);
     const float s = __half2float(s16);
-    const float4 xi = dither4(a.seed, a.layer, h, t, lane, tensor);
+    const float4 xi = dither4(a.seed, a.layer, h, a.pos0 + t, lane, tensor);
     const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
     uint32_t packed = 0;
     int codes[4];

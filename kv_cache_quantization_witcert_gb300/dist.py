@@ -4,6 +4,12 @@ The decode shards by independent sequences (no exchange on the data path), so a
 run on N GPUs is N replicas: rank r draws its own sequences (seed + r), and the
 only communication is the timing reduction at the end (max of the per-rank
 times, sum of the per-rank attended tokens).
+
+A context too long for one GPU shards by position instead: rank r holds one slice
+of every sequence's context (a cache created with pos_offset at the slice's first
+position), decodes it with witcert_decode_partial, and the ranks' per-cell records
+are gathered (one all_gather, about 0.5 KB per sequence, query head and rank) and
+merged with witcert_merge_partials.
 """
 from __future__ import annotations
 
@@ -32,3 +38,14 @@ def reduce_timing(ms: float, tokens: float, device=None):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(n, op=dist.ReduceOp.SUM)
     return float(t.item()), float(n.item())
+
+
+def gather_partials(part):
+    """Context-parallel exchange: every rank's shard records [B, Hq, R] -> [B, Hq, world, R] in
+    rank order on every rank (one all_gather); a single process returns its own as one shard."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return part.unsqueeze(2).contiguous()
+    import torch.distributed as dist
+    bufs = [torch.empty_like(part) for _ in range(dist.get_world_size())]
+    dist.all_gather(bufs, part.contiguous())
+    return torch.stack(bufs, dim=2).contiguous()

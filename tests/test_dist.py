@@ -47,3 +47,67 @@ def test_two_rank_timing_reduction_over_gloo():
 
 def test_single_process_reduction_is_identity():
     assert wdist.reduce_timing(3.5, 42) == (3.5, 42.0)
+
+
+# ----------------------------------------------------------------------------- context-parallel exchange
+
+def _pack(st, g):
+    """Oracle partial state -> records [g, 132] (m, Z, S_A, S_B, acc)."""
+    rec = torch.zeros((g, 132), dtype=torch.float64)
+    rec[:, 0] = torch.from_numpy(st["m"])
+    rec[:, 1] = torch.from_numpy(st["Z"])
+    rec[:, 2] = torch.from_numpy(st["SA"])
+    rec[:, 3] = torch.from_numpy(st["SB"])
+    rec[:, 4:] = torch.from_numpy(st["acc"])
+    return rec
+
+
+def _cp_worker(rank, world, port, q):
+    import numpy as np
+    from oracle import meter
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rng = np.random.default_rng(11)                      # same data on every rank
+    S, g, d = 300, 4, 128
+    qv = rng.standard_normal((g, d))
+    kh = rng.standard_normal((S, d))
+    vh = rng.standard_normal((S, d))
+    ca = rng.uniform(0, 0.3, (g, S))
+    cb = rng.uniform(0, 0.1, (g, S))
+    bounds = [0, 137, S]                                 # rank r holds positions bounds[r] .. bounds[r+1]-1
+    local = _pack(meter.partial_state(qv, kh, vh, ca, cb, bounds[rank], bounds[rank + 1]), g)
+    allp = wdist.gather_partials(local.unsqueeze(0)).squeeze(0)     # [g, world, 132]
+    states = [dict(m=allp[:, r, 0].numpy(), Z=allp[:, r, 1].numpy(), SA=allp[:, r, 2].numpy(),
+                   SB=allp[:, r, 3].numpy(), acc=allp[:, r, 4:].numpy()) for r in range(world)]
+    merged = meter.merge_states(states)
+    whole = meter.merge_states([meter.partial_state(qv, kh, vh, ca, cb, 0, S)])
+    _, p, out = meter.attention(qv, kh, vh)
+    ok = (torch.equal(allp[:, rank], local)
+          and np.allclose(merged["out"], out, rtol=1e-12, atol=1e-12)
+          and np.allclose(merged["D_a"], whole["D_a"], rtol=1e-12)
+          and np.allclose(merged["D_b"], whole["D_b"], rtol=1e-12))
+    q.put((rank, bool(ok)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_context_parallel_exchange_and_merge_over_gloo():
+    """Two ranks hold positions [0, 137) and [137, 300) of one context; their partial records,
+    gathered over gloo, merge to the single-context attention output and meter sums."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_cp_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, True), (1, True)]
+
+
+def test_single_process_gather_is_one_shard():
+    x = torch.arange(12.0).reshape(1, 2, 6)
+    assert wdist.gather_partials(x).shape == (1, 2, 1, 6)
