@@ -33,7 +33,8 @@ import numpy as np  # noqa: E402
 
 from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload  # noqa: E402
 
-BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144}
+BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304}
+CODE_KIND = {"int8_dither": "int8", "fp8_e4m3": "e4m3", "kivi2": "2-bit", "int8_rtn": "int8"}
 DISTINCT_LAYERS = 4        # prefill K/V sets generated on the host; layer l uses set l % 4
 METRIC = "metered decode attended-KV-tokens/s"
 UNIT = "tokens/s"
@@ -369,7 +370,7 @@ def run_ours(args, w):
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32 (int8 codes)",
+                "scaling": "weak", "vs_baseline": None, "dtype": f"fp16-mma/fp32 ({CODE_KIND[wl.scheme]} codes)",
                 "data": "synthetic (seeded numpy; bf16 N(0,1) K/V/q, x50 outlier RoPE pair, planted keys)",
                 "config": config_of(wl, args, f"auto ({st['last_n_splits']})", world),
                 "hbm_gbs_decode": achieved, "bytes_per_attended_token": wl.n_kv_heads * BYTES_PER_TOK_HEAD[wl.scheme],

@@ -45,7 +45,9 @@ typedef enum {
 typedef enum {
   WITCERT_INT8_DITHER = 0, /* subtractively dithered INT8, per-(token, 32-channel) fp16 scales [summary, Tier B] */
   WITCERT_FP8_E4M3 = 1,    /* black-box raw cast to OCP E4M3, no scale [summary, gate results] */
-  WITCERT_KIVI2 = 2        /* KIVI-style asymmetric 2-bit: K per channel over 16 tokens, V per token per 32 channels */
+  WITCERT_KIVI2 = 2,       /* KIVI-style asymmetric 2-bit: K per channel over 16 tokens, V per token per 32 channels */
+  WITCERT_INT8_RTN = 3     /* INT8 with the same scales, rounded to nearest without dither (the dithered
+                              quantizer with xi = 0); Tier A only */
 } witcert_scheme;
 
 typedef enum {

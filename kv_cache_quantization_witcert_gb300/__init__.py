@@ -11,7 +11,7 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (BF16, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER, KIVI2,  # noqa: F401
+from ._lib import (BF16, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER, INT8_RTN, KIVI2,  # noqa: F401
                    SCHEMES, WitcertError, check, load)
 
 __all__ = ["Cache", "witcert_dither", "witcert_merge_partials", "WitcertError", "load", "SCHEMES", "PART_STRIDE"]

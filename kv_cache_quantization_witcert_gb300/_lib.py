@@ -8,12 +8,12 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libwitcert.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ETIMEDOUT, EPAGEIN, ESTATE = 0, -1, -2, -3, -4, -5, -6
-INT8_DITHER, FP8_E4M3, KIVI2 = 0, 1, 2
+INT8_DITHER, FP8_E4M3, KIVI2, INT8_RTN = 0, 1, 2, 3
 F32, BF16 = 0, 1
 (X_K_CODES, X_V_CODES, X_K_SCALES, X_V_SCALES, X_V_ZEROS, X_KIVI_K_SCALE, X_KIVI_K_ZERO, X_WITNESS,
  X_SLOTS, X_BLOCK_RISK) = range(10)
 
-SCHEMES = {"int8_dither": INT8_DITHER, "fp8_e4m3": FP8_E4M3, "kivi2": KIVI2}
+SCHEMES = {"int8_dither": INT8_DITHER, "fp8_e4m3": FP8_E4M3, "kivi2": KIVI2, "int8_rtn": INT8_RTN}
 STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ETIMEDOUT: "ETIMEDOUT",
                 EPAGEIN: "EPAGEIN", ESTATE: "ESTATE"}
 

@@ -27,17 +27,19 @@ constexpr int kGroupCh = 32;
 constexpr int kGroups = 4;
 constexpr int kMaxGroupHeads = 8;
 
-enum SchemeId : int { kInt8 = 0, kFp8 = 1, kKivi = 2 };
+enum SchemeId : int { kInt8 = 0, kFp8 = 1, kKivi = 2, kRtn = 3 };
+// INT8 round-to-nearest (kRtn) keeps the dithered scheme's block layout without the dither.
+__host__ __device__ constexpr bool int8_layout(int scheme) { return scheme == kInt8 || scheme == kRtn; }
 
 struct Int8Layout { static constexpr int KC = 0, VC = 2048, KS = 4096, VS = 4224, W = 4352, BYTES = 4864; };
 struct Fp8Layout  { static constexpr int KC = 0, VC = 2048, W = 4096, BYTES = 4608; };
 struct KiviLayout { static constexpr int KC = 0, KP = 512, VC = 1024, VP = 1536, W = 1792, BYTES = 2304; };
 
 __host__ __device__ constexpr int block_bytes(int scheme) {
-  return scheme == kInt8 ? Int8Layout::BYTES : scheme == kFp8 ? Fp8Layout::BYTES : KiviLayout::BYTES;
+  return int8_layout(scheme) ? Int8Layout::BYTES : scheme == kFp8 ? Fp8Layout::BYTES : KiviLayout::BYTES;
 }
 __host__ __device__ constexpr int witness_off(int scheme) {
-  return scheme == kInt8 ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : KiviLayout::W;
+  return int8_layout(scheme) ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : KiviLayout::W;
 }
 
 // ------------------------------------------------------------------ fragment-order index maps

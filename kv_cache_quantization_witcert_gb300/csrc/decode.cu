@@ -51,6 +51,7 @@ constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
 
 template <int SCHEME> struct Lay;
 template <> struct Lay<kInt8> : Int8Layout {};
+template <> struct Lay<kRtn> : Int8Layout {};
 template <> struct Lay<kFp8> : Fp8Layout {};
 template <> struct Lay<kKivi> : KiviLayout {};
 
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           exact_block_logits<float, QLO>(p.kivi_tail + seq_base / p.nblk_max * (size_t)(kBlk * kD), fb, fbl, g, t, acc);
         lgA = __fmul2_rn(make_float2(acc[0], acc[1]), f2(lscale));
         lgB = __fmul2_rn(make_float2(acc[2], acc[3]), f2(lscale));
-      } else if constexpr (SCHEME == kInt8) {
+      } else if constexpr (int8_layout(SCHEME)) {
         float acc[4][4];
 #pragma unroll
         for (int G = 0; G < 4; ++G) {
@@ -421,6 +422,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             const uint32_t a[4] = {i8x2_lo(w0), i8x2_lo(w1), i8x2_hi(w0), i8x2_hi(w1)};
             mma16816(acc[G], a, qb[kk]);
             if (QLO) mma16816(acc[G], a, qbl[kk]);
+            if constexpr (SCHEME != kInt8) continue;                 // no dither to subtract
             const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
             const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
             const uint32_t ah[4] = {xh.x, xh.y, xh.z, xh.w};
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         }
         lgA = __fmul2_rn(lgA, f2(lscale));
         lgB = __fmul2_rn(lgB, f2(lscale));
-        if (METER) {
+        if (METER && SCHEME == kInt8) {
           // squares of fp16 scales are exact in fp32
           float2 varA = f2(0.f), varB = f2(0.f);
 #pragma unroll
@@ -612,8 +614,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             mma16816(acco[2 * j + hf], a, bfr);
           }
         }
-      } else if constexpr (SCHEME == kInt8) {
-        // B_j = (p * s_j) in fp16; A = exact codes, then -xi
+      } else if constexpr (int8_layout(SCHEME)) {
+        // B_j = (p * s_j) in fp16; A = exact codes, then -xi (dithered scheme)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint2 sv = *reinterpret_cast<const uint2*>(sb + L::VS + (j * 16 + 4 * t) * 2);
@@ -624,10 +626,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             const int mt = 2 * j + hf;
             const uint32_t w0 = hf ? vw.z : vw.x, w1 = hf ? vw.w : vw.y;
             const uint32_t a[4] = {i8x2_lo(w0), i8x2_lo(w1), i8x2_hi(w0), i8x2_hi(w1)};
-            const uint4 xv = *reinterpret_cast<const uint4*>(xb + kXiV + (mt * 32 + lane) * 16);
-            const uint32_t ax[4] = {xv.x, xv.y, xv.z, xv.w};
             mma16816(acco[mt], a, bfr);
-            mma16816(acco[mt], ax, bfr);
+            if constexpr (SCHEME == kInt8) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xb + kXiV + (mt * 32 + lane) * 16);
+              const uint32_t ax[4] = {xv.x, xv.y, xv.z, xv.w};
+              mma16816(acco[mt], ax, bfr);
+            }
           }
         }
       } else {  // KIVI values: p*scale times codes, plus p*zero per group
@@ -932,6 +936,7 @@ int decode_ctas_per_sm(int scheme, const DecodeArgs& a0) {
   int n = 0;
   const dim3 grid(1);
   const cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, nullptr, false, &n)
+                        : scheme == kRtn ? dispatch_flags<kRtn>(a, grid, nullptr, false, &n)
                         : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, nullptr, false, &n)
                                          : dispatch_flags<kKivi>(a, grid, nullptr, false, &n);
   return e == cudaSuccess && n > 0 ? n : 1;
@@ -969,6 +974,7 @@ cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaSt
   const bool pdl = pdl_allowed && split_start == nullptr;
   if (split_start) cudaEventRecord(split_start, st);
   cudaError_t e = scheme == kInt8  ? dispatch_flags<kInt8>(a, grid, st, pdl)
+                  : scheme == kRtn ? dispatch_flags<kRtn>(a, grid, st, pdl)
                   : scheme == kFp8 ? dispatch_flags<kFp8>(a, grid, st, pdl)
                                    : dispatch_flags<kKivi>(a, grid, st, pdl);
   if (split_stop) cudaEventRecord(split_stop, st);

@@ -30,7 +30,7 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
       } else {
         const int base = a.what == X_KC ? 0 : 2048;
         v = bp[base + (a.what == X_KC ? kcode_off(r, c) : vcode_off(r, c))];
-        if (a.scheme == kInt8) v = (uint8_t)(v ^ 0x80u);    // stored biased by 128
+        if (int8_layout(a.scheme)) v = (uint8_t)(v ^ 0x80u);    // stored biased by 128
       }
       reinterpret_cast<uint8_t*>(a.dst)[idx] = v;
       break;

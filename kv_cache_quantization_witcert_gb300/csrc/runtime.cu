@@ -144,7 +144,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
     return fail(WITCERT_EINVAL, "n_q_heads must be a positive multiple of n_kv_heads");
   if (f.n_q_heads / f.n_kv_heads > kMaxGroupHeads) return fail(WITCERT_EINVAL, "at most %d query heads per KV head", kMaxGroupHeads);
   if (f.batch <= 0 || f.max_tokens <= 0) return fail(WITCERT_EINVAL, "batch and max_tokens must be positive");
-  if (f.scheme < WITCERT_INT8_DITHER || f.scheme > WITCERT_KIVI2) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)f.scheme);
+  if (f.scheme < WITCERT_INT8_DITHER || f.scheme > WITCERT_INT8_RTN) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)f.scheme);
   if (f.kv_dtype != WITCERT_F32 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "unknown dtype %d", (int)f.kv_dtype);
   if (f.total_steps <= 0) return fail(WITCERT_EINVAL, "total_steps must be positive");
   if (f.n_splits < 0 || f.max_repair_blocks < 0) return fail(WITCERT_EINVAL, "n_splits and max_repair_blocks must be >= 0");
@@ -413,7 +413,7 @@ witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch
                                       float* raw_a, float* raw_b, void* stream) {
   if (!parts || !out) return fail(WITCERT_EINVAL, "parts and out must not be NULL");
   if (n_parts < 1 || batch < 1 || n_q_heads < 1) return fail(WITCERT_EINVAL, "n_parts, batch and n_q_heads must be >= 1");
-  if (scheme < WITCERT_INT8_DITHER || scheme > WITCERT_KIVI2) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)scheme);
+  if (scheme < WITCERT_INT8_DITHER || scheme > WITCERT_INT8_RTN) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)scheme);
   DecodeArgs a{};
   a.part = const_cast<float*>(parts);
   a.n_splits = n_parts;
@@ -548,7 +548,7 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
     case WITCERT_X_BLOCK_RISK: need = B * Hq * nblk * 4; break;
     default: return fail(WITCERT_EINVAL, "unknown export kind %d", (int)what);
   }
-  const bool int8 = c->scheme == kInt8, kivi = c->scheme == kKivi;
+  const bool int8 = int8_layout(c->scheme), kivi = c->scheme == kKivi;
   if ((what == WITCERT_X_K_SCALES && !int8) || ((what == WITCERT_X_V_SCALES) && !(int8 || kivi)) ||
       ((what == WITCERT_X_V_ZEROS || what == WITCERT_X_KIVI_K_SCALE || what == WITCERT_X_KIVI_K_ZERO) && !kivi))
     return fail(WITCERT_EINVAL, "export kind %d does not exist for this scheme", (int)what);

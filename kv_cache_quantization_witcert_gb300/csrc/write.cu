@@ -163,7 +163,7 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
 
 // Token n of the write (position t = t0 + n, row r = t mod 16 of its block) of sequence i,
 // KV head h, quantized into the block image at bp (device memory or shared memory).
-template <typename T>
+template <typename T, bool DITHER>
 __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
   const int t = a.t0 + n, r = t & 15;
   const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
@@ -179,7 +179,8 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     __half s16 = __float2half_ru(__fdiv_rn(amax, 127.0f));
     if (__half2float(s16) > 65504.0f) s16 = __float2half_rn(65504.0f);
     const float s = __half2float(s16);
-    const float4 xi = dither4(a.seed, a.layer, h, a.pos0 + t, lane, tensor);
+    // round to nearest is the dithered quantizer with xi = 0
+    const float4 xi = DITHER ? dither4(a.seed, a.layer, h, a.pos0 + t, lane, tensor) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
     uint32_t packed = 0;
     int codes[4];
@@ -263,7 +264,7 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
 
 // One warp per (sequence, token, KV head) of tokens tok_begin .. tok_begin + tok_count - 1:
 // appends and the parts of a write that do not fill whole blocks.
-template <typename T, bool INT8>
+template <typename T, int SCH>
 __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -271,20 +272,20 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   if (wid >= a.B * a.tok_count * a.Hkv) return;
   const int h = wid % a.Hkv, n = a.tok_begin + (wid / a.Hkv) % a.tok_count, i = wid / (a.Hkv * a.tok_count);
   const int blk = (a.t0 + n) >> 4;
-  constexpr int kBytes = INT8 ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  constexpr int kBytes = int8_layout(SCH) ? Int8Layout::BYTES : Fp8Layout::BYTES;
   uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * kBytes;
-  if constexpr (INT8) int8_token<T>(a, bp, i, h, n, lane);
+  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, n, lane);
   else fp8_token<T>(a, bp, i, h, n, lane);
 }
 
 // One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
 // completely: the warp builds the block's image in shared memory token by token and stores
 // it with 16-byte writes.
-template <typename T, bool INT8>
+template <typename T, int SCH>
 __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
   pdl_wait();
   pdl_trigger();
-  constexpr int kBytes = INT8 ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  constexpr int kBytes = int8_layout(SCH) ? Int8Layout::BYTES : Fp8Layout::BYTES;
   __shared__ __align__(16) uint8_t img[4][kBytes];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 4 + warp;       // (i * Hkv + h) * nblocks + b
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int
   uint8_t* im = img[warp];
   for (int r = 0; r < kBlk; ++r) {
     const int n = blk * kBlk + r - a.t0;
-    if constexpr (INT8) int8_token<T>(a, im, i, h, n, lane);
+    if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, im, i, h, n, lane);
     else fp8_token<T>(a, im, i, h, n, lane);
   }
   __syncwarp();
@@ -448,7 +449,7 @@ template <typename T>
 cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   const int warps = a.B * a.n_tok * a.Hkv;
   const dim3 blocks((warps * 32 + 127) / 128);
-  if (scheme == kInt8 || scheme == kFp8) {
+  if (int8_layout(scheme) || scheme == kFp8) {
     // whole blocks through shared-memory images, the rest token by token
     const int t_end = a.t0 + a.n_tok;
     const int lo_full = (a.t0 + kBlk - 1) / kBlk * kBlk, hi_full = t_end / kBlk * kBlk;
@@ -458,16 +459,18 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
       b.tok_begin = begin;
       b.tok_count = count;
       const dim3 g(((unsigned)(a.B * count * a.Hkv) * 32u + 127u) / 128u);
-      return scheme == kInt8 ? launch_pdl(write_token_kernel<T, true>, g, dim3(128), st, pdl, b)
-                             : launch_pdl(write_token_kernel<T, false>, g, dim3(128), st, pdl, b);
+      return scheme == kInt8  ? launch_pdl(write_token_kernel<T, kInt8>, g, dim3(128), st, pdl, b)
+             : scheme == kRtn ? launch_pdl(write_token_kernel<T, kRtn>, g, dim3(128), st, pdl, b)
+                              : launch_pdl(write_token_kernel<T, kFp8>, g, dim3(128), st, pdl, b);
     };
     if (hi_full <= lo_full) return tokens(0, a.n_tok);
     cudaError_t e = tokens(0, lo_full - a.t0);
     if (e != cudaSuccess) return e;
     const int nblocks = (hi_full - lo_full) / kBlk;
     const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + 3) / 4));
-    e = scheme == kInt8 ? launch_pdl(write_block_kernel<T, true>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
-                        : launch_pdl(write_block_kernel<T, false>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
+    e = scheme == kInt8  ? launch_pdl(write_block_kernel<T, kInt8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
+        : scheme == kRtn ? launch_pdl(write_block_kernel<T, kRtn>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
+                         : launch_pdl(write_block_kernel<T, kFp8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
     if (e != cudaSuccess) return e;
     return tokens(hi_full - a.t0, t_end - hi_full);
   }

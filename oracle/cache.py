@@ -18,7 +18,7 @@ from .philox import dither
 from .quant import (BLOCK, D, witness, witness_stored, write_fp8, write_int8_dither,
                     write_kivi2_k, write_kivi2_v)
 
-SCHEMES = ("int8_dither", "fp8_e4m3", "kivi2")
+SCHEMES = ("int8_dither", "fp8_e4m3", "kivi2", "int8_rtn")
 
 
 class OracleCache:
@@ -63,9 +63,13 @@ class OracleCache:
         vs = np.zeros((B, n, H, 4), np.float16)
         vz = np.zeros((B, n, H, 4), np.float16)
         for h in range(H):
-            if self.scheme == "int8_dither":
-                xik = dither(self.seed, layer, h, pos, 0)
-                xiv = dither(self.seed, layer, h, pos, 1)
+            if self.scheme in ("int8_dither", "int8_rtn"):
+                # round to nearest is the dithered quantizer with xi = 0
+                if self.scheme == "int8_dither":
+                    xik = dither(self.seed, layer, h, pos, 0)
+                    xiv = dither(self.seed, layer, h, pos, 1)
+                else:
+                    xik = xiv = np.zeros((n, D), np.float32)
                 for i in range(B):
                     c, s, xh, cl = write_int8_dither(K[i, :, h], xik)
                     kc[i, :, h], ks[i, :, h], kh[i, :, h] = c, s, xh

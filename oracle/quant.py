@@ -138,6 +138,7 @@ def write_kivi2_v(x):
 BYTES_PER_TOKEN_HEAD = {
     # K codes + V codes + K scales + V scales + K witness
     "int8_dither": 128 + 128 + 8 + 8 + 32,
+    "int8_rtn": 128 + 128 + 8 + 8 + 32,
     # K codes + V codes + K witness
     "fp8_e4m3": 128 + 128 + 32,
     # K codes + K (scale, zero) per channel per 16 tokens + V codes + V (scale, zero) per group + K witness

@@ -51,7 +51,7 @@ def check_write(gpu, ref, layer, scheme):
     S = ref.length(layer)
     kc = gpu.export(layer, _lib.X_K_CODES).cpu().numpy()
     vc = gpu.export(layer, _lib.X_V_CODES).cpu().numpy()
-    if scheme == "int8_dither":
+    if scheme in ("int8_dither", "int8_rtn"):
         np.testing.assert_array_equal(kc.view(np.int8).astype(np.int16), ref.kcode[layer])
         np.testing.assert_array_equal(vc.view(np.int8).astype(np.int16), ref.vcode[layer])
         ks = gpu.export(layer, _lib.X_K_SCALES).cpu().numpy()

@@ -49,7 +49,7 @@ def test_tiny_write_and_metered_decode_with_appends(n_splits):
     assert st["int8_clamps"] == 0 and st["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
 def test_qwen_shaped_bf16_ragged(scheme):
     """28q/4kv, bf16, planted keys and x50 outliers; 3 sequences (a partial sequence group),
     1000 tokens (several splits and a ragged 8-token tail), two steps with an append."""
@@ -80,7 +80,7 @@ def test_more_split_ctas_than_the_gpu_holds(scheme):
     assert gpu.witcert_stats()["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
 def test_kivi_and_all_schemes_across_block_boundaries(scheme):
     """Appends one token at a time across two 16-token boundaries (KIVI closes blocks)."""
     w = WORKLOADS["tiny"].with_(context=29, steps=20, scheme=scheme, batch=2)
@@ -97,7 +97,7 @@ def test_kivi_and_all_schemes_across_block_boundaries(scheme):
             check_decode(gpu, ref, 0, gen_q(w, 0, step), w, w.delta_req)
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
 def test_meter_off_output_is_bit_identical(scheme):
     w = WORKLOADS["qwen_1l"].with_(batch=5, context=700, scheme=scheme)
     gpu, _ = make_pair(w)
@@ -205,7 +205,7 @@ def test_errors_are_reported_not_raised_on_device():
     assert gpu.witcert_stats()["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2"])
+@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
 def test_witness_fallback_on_extreme_keys(scheme):
     """Keys near 1e-20 and near 1e25 push the writers' fp32 double-float witness outside its
     safe range, so those bands take the fp64 computation; keys near 1e-9 give witnesses in

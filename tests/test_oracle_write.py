@@ -254,4 +254,22 @@ def test_theorem2_is_tight_for_band_aligned_residuals():
 
 
 def test_bytes_per_token_head():
-    assert quant.BYTES_PER_TOKEN_HEAD == {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144}
+    assert quant.BYTES_PER_TOKEN_HEAD == {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304}
+
+
+def test_rtn_writer_is_the_nearest_code_and_idempotent():
+    """INT8 round to nearest (the dithered writer with xi = 0): every code is the nearest of the
+    256 codes under its group's scale (brute force), and requantizing x_hat returns the same
+    codes and values."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((6, 128)) * rng.uniform(0.01, 30, (6, 1))).astype(np.float32)
+    x[:, 10] *= 50
+    c, s, xh, _ = quant.write_int8_dither(x, np.zeros_like(x))
+    sg = np.repeat(s.astype(np.float64), 32, axis=1)
+    allc = np.arange(-128, 128, dtype=np.float64)
+    dist = np.abs(x.astype(np.float64)[..., None] - sg[..., None] * allc)      # [6, 128, 256]
+    best = dist.min(-1)
+    mine = np.abs(x.astype(np.float64) - sg * c)
+    assert np.all(mine <= best * (1 + 1e-12) + 1e-300)
+    c2, s2, xh2, _ = quant.write_int8_dither(xh.astype(np.float32), np.zeros_like(x))
+    assert np.array_equal(s2, s) and np.array_equal(c2, c) and np.array_equal(xh2, xh)
