@@ -4,6 +4,9 @@
   round-to-nearest-even, which is what the quantizer specification states.
 * fp16 conversions: numpy's float32 -> float16 cast rounds to nearest even;
   round-toward-+inf is that cast stepped up by one ulp when it fell below.
+* bfloat16: the upper 16 bits of a binary32; rounding to nearest with ties to
+  the even upper half, done on the bit pattern (finite inputs; values that
+  round past the largest bfloat16 become infinities, as in the format).
 * OCP FP8 E4M3 ("e4m3fn"): sign, 4 exponent bits (bias 7), 3 mantissa bits,
   no infinities, 0x7F/0xFF are NaN, largest finite 448, smallest subnormal
   2^-9.  Rounding is to the nearest finite value, ties to the even code, and
@@ -42,6 +45,14 @@ def fp32_ru(x) -> np.ndarray:
     f = x.astype(np.float32)
     low = f.astype(np.float64) < x
     return np.where(low, np.nextafter(f, np.float32(np.inf)), f).astype(np.float32)
+
+
+def bf16_rn(x) -> np.ndarray:
+    """Nearest-even bfloat16 of float32 values, returned as float32 (exact)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
 
 
 def _e4m3_table():

@@ -13,6 +13,12 @@ Notation (per sequence, layer, decode step and query head):
 with c_t = eps_t (Tier A) or u_t (Tier B).  The oracle evaluates A as 1 + D with
 D = sum_t p~_t expm1(c_t), and (A^2 - 1)/2 as D + D^2/2: the same numbers,
 without the cancellation of A^2 - 1 when every c_t is small.
+
+Value side (this build's reading; the pages define no value bound): with the
+stored value witness wv_t >= ||v_t - v^_t||,
+    E_V = sum_t p~_t wv_t >= || sum_t p~_t v_t - sum_t p~_t v^_t ||
+by the triangle inequality: the output error the value compression adds at the
+compressed attention weights.
 """
 from __future__ import annotations
 
@@ -70,6 +76,11 @@ def tv_meter(p_tilde, c):
     return np.minimum(1.0, raw), raw, Dv
 
 
+def value_meter(p_tilde, wv) -> np.ndarray:
+    """E_V = sum_t p~_t wv_t.   p_tilde: [g, S]; wv: [S] stored value witnesses."""
+    return np.asarray(p_tilde, np.float64) @ np.asarray(wv, np.float64)
+
+
 def tv_exact(p, p_tilde) -> np.ndarray:
     """Total variation between exact and compressed attention: (1/2) sum_t |p_t - p~_t|."""
     return 0.5 * np.sum(np.abs(np.asarray(p) - np.asarray(p_tilde)), axis=-1)
@@ -84,13 +95,14 @@ def block_risk(p_tilde, c, S: int) -> np.ndarray:
     return terms.reshape(terms.shape[:-1] + (nblk, BLOCK)).sum(-1)
 
 
-def decode_ref(q, khat, vhat, w, k_scales=None, repaired=None, dloc=None):
+def decode_ref(q, khat, vhat, w, k_scales=None, repaired=None, dloc=None, wv=None):
     """Metered decode of one (sequence, KV head) group over its whole context.
 
     q: [g, d] query heads of the group; khat/vhat: [S, d] keys/values the decode
     attends to (dequantized, or exact for repaired tokens); w: [S, 16] witness
     (zero for repaired tokens); k_scales: [S, 4] INT8 key scales (dither scheme
-    only, enables Tier B); repaired: [S] bool.
+    only, enables Tier B); repaired: [S] bool; wv: [S] value witnesses (enables
+    the value meter E_V).
     """
     q = np.asarray(q, dtype=np.float64)
     S = khat.shape[0]
@@ -100,14 +112,15 @@ def decode_ref(q, khat, vhat, w, k_scales=None, repaired=None, dloc=None):
         return dict(out=np.zeros((g, D)), p=np.zeros((g, 0)), eps=np.zeros((g, 0)), u=None,
                     meter_a=z, raw_a=z, D_a=z, meter_b=z if k_scales is not None else None,
                     raw_b=z if k_scales is not None else None, D_b=z if k_scales is not None else None,
-                    risk=np.zeros((g, 0)))
+                    meter_v=z if wv is not None else None, risk=np.zeros((g, 0)))
     rep = np.zeros(S, bool) if repaired is None else np.asarray(repaired, bool)
     _, p, out = attention(q, khat, vhat)
     eps = tier_a(q, w)
     eps[:, rep] = 0.0
     meter_a, raw_a, D_a = tv_meter(p, eps)
     res = dict(out=out, p=p, eps=eps, u=None, meter_a=meter_a, raw_a=raw_a, D_a=D_a,
-               meter_b=None, raw_b=None, D_b=None)
+               meter_b=None, raw_b=None, D_b=None,
+               meter_v=value_meter(p, wv) if wv is not None else None)
     c_gate = eps
     if k_scales is not None:
         u = tier_b(q, k_scales, S, dloc)
@@ -121,20 +134,23 @@ def decode_ref(q, khat, vhat, w, k_scales=None, repaired=None, dloc=None):
 
 # --------------------------------------------------------------------------- split-KV states
 
-def partial_state(q, khat, vhat, c_a, c_b, lo: int, hi: int):
+def partial_state(q, khat, vhat, c_a, c_b, lo: int, hi: int, wv=None):
     """Unnormalized state of tokens [lo, hi): running max m, Z = sum e^(l-m),
-    S_X = sum e^(l-m) expm1(c_X), acc = sum e^(l-m) v^ [WitCert summary,
-    implementation: LSE-merged certificate accumulation across KV splits]."""
+    S_X = sum e^(l-m) expm1(c_X), S_V = sum e^(l-m) wv, acc = sum e^(l-m) v^
+    [WitCert summary, implementation: LSE-merged certificate accumulation across
+    KV splits]."""
     q = np.asarray(q, np.float64)
     g = q.shape[0]
+    wv = np.zeros(khat.shape[0]) if wv is None else np.asarray(wv, np.float64)
     if hi <= lo:
         return dict(m=np.full(g, -np.inf), Z=np.zeros(g), SA=np.zeros(g), SB=np.zeros(g),
-                    acc=np.zeros((g, D)))
+                    SV=np.zeros(g), acc=np.zeros((g, D)))
     logits = q @ np.asarray(khat[lo:hi], np.float64).T / math.sqrt(D)
     m = logits.max(-1)
     e = np.exp(logits - m[:, None])
     return dict(m=m, Z=e.sum(-1), SA=(e * np.expm1(c_a[:, lo:hi])).sum(-1),
-                SB=(e * np.expm1(c_b[:, lo:hi])).sum(-1), acc=e @ np.asarray(vhat[lo:hi], np.float64))
+                SB=(e * np.expm1(c_b[:, lo:hi])).sum(-1), SV=e @ wv[lo:hi],
+                acc=e @ np.asarray(vhat[lo:hi], np.float64))
 
 
 def merge_states(states):
@@ -143,14 +159,16 @@ def merge_states(states):
     Z = np.zeros_like(M)
     SA = np.zeros_like(M)
     SB = np.zeros_like(M)
+    SV = np.zeros_like(M)
     acc = np.zeros(M.shape + (D,))
     for s in states:
         f = np.where(np.isfinite(s["m"]), np.exp(s["m"] - np.where(np.isfinite(M), M, 0.0)), 0.0)
         Z += f * s["Z"]
         SA += f * s["SA"]
         SB += f * s["SB"]
+        SV += f * s["SV"]
         acc += f[:, None] * s["acc"]
     DA = SA / Z
     DB = SB / Z
     return dict(out=acc / Z[:, None], D_a=DA, D_b=DB, meter_a=np.minimum(1.0, DA + 0.5 * DA * DA),
-                meter_b=np.minimum(1.0, DB + 0.5 * DB * DB))
+                meter_b=np.minimum(1.0, DB + 0.5 * DB * DB), meter_v=SV / Z)

@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fp import FP16_MAX, e4m3_decode, e4m3_rn_satfinite, fp16_rn, fp16_ru
+from .fp import FP16_MAX, bf16_rn, e4m3_decode, e4m3_rn_satfinite, fp16_rn, fp16_ru
 
 D = 128
 N_BANDS = 16
@@ -44,6 +44,17 @@ def witness_stored(w64: np.ndarray) -> np.ndarray:
     of a float64 norm.
     """
     return fp16_ru(np.asarray(w64, dtype=np.float64) * (1.0 + WITNESS_MARGIN))
+
+
+def value_witness(resid: np.ndarray) -> np.ndarray:
+    """wv_t = ||r_t||_2 over all 128 dims of a value row's residual r = v - v_hat.
+
+    The value side of the witness idea: the output error the value compression
+    adds at the compressed weights is bounded by sum_t p~_t wv_t (triangle
+    inequality), with no query involved, so one norm per token suffices.
+    """
+    r = np.asarray(resid, dtype=np.float64)
+    return np.sqrt(np.sum(r ** 2, axis=-1))
 
 
 # --------------------------------------------------------------------------- INT8 + subtractive dither
@@ -88,6 +99,17 @@ def write_fp8(x):
     [WitCert summary, gate results: raw-cast fp8].  Returns codes uint8 and x_hat."""
     code = e4m3_rn_satfinite(np.asarray(x, dtype=np.float32))
     return code, e4m3_decode(code)
+
+
+# --------------------------------------------------------------------------- black-box tensor function
+
+def write_blackbox(x_hat):
+    """Any scheme given as one tensor function f [WitCert abstract: any scheme
+    registered as one tensor function is measured; Tier A is sound for any
+    cache-preserving black-box quantizer].  The caller applies f; the cache keeps
+    its output as bfloat16 (nearest even of the float32 value), and the decode and
+    the witness both use that stored value.  x_hat: float32 [n, 128]."""
+    return bf16_rn(np.asarray(x_hat, dtype=np.float32)).astype(np.float64)
 
 
 # --------------------------------------------------------------------------- KIVI-style 2-bit
@@ -143,4 +165,8 @@ BYTES_PER_TOKEN_HEAD = {
     "fp8_e4m3": 128 + 128 + 32,
     # K codes + K (scale, zero) per channel per 16 tokens + V codes + V (scale, zero) per group + K witness
     "kivi2": 32 + (128 * 2 * 2) // BLOCK + 32 + 4 * 2 * 2 + 32,
+    # K_hat + V_hat as bfloat16 + K witness
+    "blackbox": 256 + 256 + 32,
 }
+# optional value witness: one fp16 norm per token and head
+V_WITNESS_BYTES = 2

@@ -52,13 +52,14 @@ def test_single_process_reduction_is_identity():
 # ----------------------------------------------------------------------------- context-parallel exchange
 
 def _pack(st, g):
-    """Oracle partial state -> records [g, 132] (m, Z, S_A, S_B, acc)."""
-    rec = torch.zeros((g, 132), dtype=torch.float64)
+    """Oracle partial state -> records [g, 136] (m, Z, S_A, S_B, S_V, 3 unused, acc)."""
+    rec = torch.zeros((g, 136), dtype=torch.float64)
     rec[:, 0] = torch.from_numpy(st["m"])
     rec[:, 1] = torch.from_numpy(st["Z"])
     rec[:, 2] = torch.from_numpy(st["SA"])
     rec[:, 3] = torch.from_numpy(st["SB"])
-    rec[:, 4:] = torch.from_numpy(st["acc"])
+    rec[:, 4] = torch.from_numpy(st["SV"])
+    rec[:, 8:] = torch.from_numpy(st["acc"])
     return rec
 
 
@@ -75,18 +76,21 @@ def _cp_worker(rank, world, port, q):
     vh = rng.standard_normal((S, d))
     ca = rng.uniform(0, 0.3, (g, S))
     cb = rng.uniform(0, 0.1, (g, S))
+    wv = rng.uniform(0, 0.2, S)
     bounds = [0, 137, S]                                 # rank r holds positions bounds[r] .. bounds[r+1]-1
-    local = _pack(meter.partial_state(qv, kh, vh, ca, cb, bounds[rank], bounds[rank + 1]), g)
-    allp = wdist.gather_partials(local.unsqueeze(0)).squeeze(0)     # [g, world, 132]
+    local = _pack(meter.partial_state(qv, kh, vh, ca, cb, bounds[rank], bounds[rank + 1], wv), g)
+    allp = wdist.gather_partials(local.unsqueeze(0)).squeeze(0)     # [g, world, 136]
     states = [dict(m=allp[:, r, 0].numpy(), Z=allp[:, r, 1].numpy(), SA=allp[:, r, 2].numpy(),
-                   SB=allp[:, r, 3].numpy(), acc=allp[:, r, 4:].numpy()) for r in range(world)]
+                   SB=allp[:, r, 3].numpy(), SV=allp[:, r, 4].numpy(), acc=allp[:, r, 8:].numpy())
+              for r in range(world)]
     merged = meter.merge_states(states)
-    whole = meter.merge_states([meter.partial_state(qv, kh, vh, ca, cb, 0, S)])
+    whole = meter.merge_states([meter.partial_state(qv, kh, vh, ca, cb, 0, S, wv)])
     _, p, out = meter.attention(qv, kh, vh)
     ok = (torch.equal(allp[:, rank], local)
           and np.allclose(merged["out"], out, rtol=1e-12, atol=1e-12)
           and np.allclose(merged["D_a"], whole["D_a"], rtol=1e-12)
-          and np.allclose(merged["D_b"], whole["D_b"], rtol=1e-12))
+          and np.allclose(merged["D_b"], whole["D_b"], rtol=1e-12)
+          and np.allclose(merged["meter_v"], p @ wv, rtol=1e-12))
     q.put((rank, bool(ok)))
     dist.barrier()
     dist.destroy_process_group()

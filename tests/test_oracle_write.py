@@ -254,7 +254,9 @@ def test_theorem2_is_tight_for_band_aligned_residuals():
 
 
 def test_bytes_per_token_head():
-    assert quant.BYTES_PER_TOKEN_HEAD == {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304}
+    assert quant.BYTES_PER_TOKEN_HEAD == {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304,
+                                          "blackbox": 544}
+    assert quant.V_WITNESS_BYTES == 2
 
 
 def test_rtn_writer_is_the_nearest_code_and_idempotent():
