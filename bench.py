@@ -33,8 +33,9 @@ import numpy as np  # noqa: E402
 
 from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload  # noqa: E402
 
-BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304}
-CODE_KIND = {"int8_dither": "int8", "fp8_e4m3": "e4m3", "kivi2": "2-bit", "int8_rtn": "int8"}
+BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304, "blackbox": 544}
+V_WITNESS_BYTES = 2        # per token and KV head, with --v-witness
+CODE_KIND = {"int8_dither": "int8", "fp8_e4m3": "e4m3", "kivi2": "2-bit", "int8_rtn": "int8", "blackbox": "bf16"}
 DISTINCT_LAYERS = 4        # prefill K/V sets generated on the host; layer l uses set l % 4
 METRIC = "metered decode attended-KV-tokens/s"
 UNIT = "tokens/s"
@@ -53,6 +54,7 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (small profiling runs)")
     ap.add_argument("--taus", default="0.5,1,2", help="gate thresholds of the gated workload")
     ap.add_argument("--gated-steps", type=int, default=256, help="decode steps per threshold (gated workload)")
+    ap.add_argument("--v-witness", action="store_true", help="keep value witnesses and report the value meter")
     return ap.parse_args()
 
 
@@ -67,14 +69,29 @@ def workload_of(name, scheme):
     return w
 
 
+def tok_head_bytes(scheme, v_witness):
+    return BYTES_PER_TOK_HEAD[scheme] + (V_WITNESS_BYTES if v_witness else 0)
+
+
+def tensor_function(x):
+    """The black-box scheme's tensor function in this benchmark: a raw cast to FP8-E4M3 and back
+    (a caller's quantize-dequantize step; applied with torch before any timed region)."""
+    import torch
+    return x.to(torch.float8_e4m3fn).to(x.dtype)
+
+
 def config_of(w, args, n_splits, world):
+    vw = getattr(args, "v_witness", False)
     return {"workload": f"{w.name}: {w.n_layers} layers, {w.n_q_heads}q/{w.n_kv_heads}kv heads, d=128, "
-                        f"batch {w.batch} x {w.context} context per GPU, {w.scheme}",
+                        f"batch {w.batch} x {w.context} context per GPU, {w.scheme}"
+                        + (" (f = raw FP8 cast)" if w.scheme == "blackbox" else "")
+                        + (", value witnesses" if vw else ""),
             "model": w.name, "global_batch": w.batch * world, "seq_len": w.context, "layers": w.n_layers,
             "scheme": w.scheme, "delta_req": w.delta_req, "n_splits": n_splits,
             "parallelism": f"replicas x{world} (independent sequence shards)",
+            "v_witness": bool(vw),
             "l2": "inputs larger than L2: every step reads the whole cache "
-                  f"({w.n_layers * w.batch * w.n_kv_heads * w.context * BYTES_PER_TOK_HEAD[w.scheme] / 1e9:.2f} GB)",
+                  f"({w.n_layers * w.batch * w.n_kv_heads * w.context * tok_head_bytes(w.scheme, vw) / 1e9:.2f} GB)",
             "prefill_data": f"{DISTINCT_LAYERS} generated K/V sets reused across layers"}
 
 
@@ -134,13 +151,13 @@ def measured_peak():
 def recorded_traffic(w):
     """Per-launch DRAM bytes of the decode split kernel from the committed ncu summary, if it was
     taken on the current kernel source (null otherwise)."""
-    src = os.path.join(ROOT, "kv_cache_quantization_witcert_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "kv_cache_quantization_witcert_gb300", "csrc", "decode_split.cuh")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     path = os.path.join(ROOT, "profiles", f"decode_{w.scheme}_{w.name}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    m = re.search(r"decode\.cu sha256\[:16\]:\s*([0-9a-f]{16})", txt)
+    m = re.search(r"decode_split\.cuh sha256\[:16\]:\s*([0-9a-f]{16})", txt)
     t = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", txt)
     if not m or not t or m.group(1) != digest:
         return None
@@ -149,9 +166,9 @@ def recorded_traffic(w):
 
 # ----------------------------------------------------------------------------- reference arm (CPU oracle)
 
-def cpu_oracle_rate(w, seconds):
+def cpu_oracle_rate(w, seconds, v_witness=False):
     """Oracle decode of (sequence, KV head) groups of one layer, repeated for about `seconds`."""
-    from oracle import meter, quant
+    from oracle import fp, meter, quant
     from oracle.philox import dither
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
     wl = w.with_(batch=1)
@@ -169,15 +186,22 @@ def cpu_oracle_rate(w, seconds):
             _, ks, kh, _ = quant.write_int8_dither(k, dither(w.seed, 0, h, pos, 0))
             _, _, vh, _ = quant.write_int8_dither(v, dither(w.seed, 0, h, pos, 1))
             kss = ks.astype(np.float64)
+        elif w.scheme == "int8_rtn":
+            zero = np.zeros_like(k)
+            kh, vh, kss = quant.write_int8_dither(k, zero)[2], quant.write_int8_dither(v, zero)[2], None
         elif w.scheme == "fp8_e4m3":
             kh, vh, kss = quant.write_fp8(k)[1], quant.write_fp8(v)[1], None
+        elif w.scheme == "blackbox":     # f = raw FP8 cast, as in the GPU run
+            f = lambda x: fp.e4m3_decode(fp.e4m3_rn_satfinite(x)).astype(np.float32)
+            kh, vh, kss = quant.write_blackbox(f(k)), quant.write_blackbox(f(v)), None
         else:
             kh = k.astype(np.float64)
             vh = quant.write_kivi2_v(v)[3]
             kss = None
         wst = quant.witness_stored(quant.witness(k - kh)).astype(np.float64)
+        wv = quant.witness_stored(quant.value_witness(v - vh)).astype(np.float64) if v_witness else None
         js = slice((h % w.n_kv_heads) * w.group, (h % w.n_kv_heads + 1) * w.group)
-        meter.decode_ref(q[0, js], kh, vh, wst, kss, None, dl)
+        meter.decode_ref(q[0, js], kh, vh, wst, kss, None, dl, wv)
         groups += 1
         h += 1
         el = time.perf_counter() - t0
@@ -197,7 +221,7 @@ def run_reference(args, w):
     rates = []
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
     for k in range(args.warmup + args.steps):
-        r, cores, sample = cpu_oracle_rate(w, per_step)
+        r, cores, sample = cpu_oracle_rate(w, per_step, getattr(args, "v_witness", False))
         if k >= args.warmup:
             rates.append(r)
     value = statistics.median(rates)
@@ -229,8 +253,11 @@ def run_ours(args, w):
     total = args.warmup + args.steps
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, args.steps // 2)
     n_app = total + args.steps + e2e_steps + 1
+    vw = args.v_witness
+    bb = wl.scheme == "blackbox"
+    tbytes = tok_head_bytes(wl.scheme, vw)
     cache = wc.Cache(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.batch, wl.context + n_app, wl.scheme,
-                     dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0)
+                     dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0, v_witness=vw)
     stream = torch.cuda.current_stream()
 
     # prefill every layer (outside the step timing; its write throughput is reported on its own)
@@ -238,17 +265,24 @@ def run_ours(args, w):
     for sid in range(min(DISTINCT_LAYERS, wl.n_layers)):
         K, V = gen_kv(wl, sid)
         sets[sid] = (torch.from_numpy(K).to(dev, dt), torch.from_numpy(V).to(dev, dt))
+        if bb:
+            sets[sid] += (tensor_function(sets[sid][0]), tensor_function(sets[sid][1]))
     torch.cuda.synchronize()
     pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pf0.record(stream)
     for layer in range(wl.n_layers):
-        cache.witcert_write(layer, *sets[layer % DISTINCT_LAYERS])
+        if bb:
+            cache.witcert_write_hat(layer, *sets[layer % DISTINCT_LAYERS])
+        else:
+            cache.witcert_write(layer, *sets[layer % DISTINCT_LAYERS])
     pf1.record(stream)
     torch.cuda.synchronize()
     prefill_ms = pf0.elapsed_time(pf1)
     prefill_tok_heads = wl.n_layers * wl.batch * wl.context * wl.n_kv_heads
-    # bytes per token-head: bf16 K and V read (512 B), the compressed token written
-    prefill_gbs = prefill_tok_heads * (512 + BYTES_PER_TOK_HEAD[wl.scheme]) / (prefill_ms / 1e3) / 1e9
+    # bytes per token-head: bf16 K and V read (512 B; the black-box scheme also reads f(K), f(V)),
+    # the compressed token written
+    prefill_read = 1024 if bb else 512
+    prefill_gbs = prefill_tok_heads * (prefill_read + tbytes) / (prefill_ms / 1e3) / 1e9
     del sets
 
     # per-step inputs resident in HBM: appended token and queries of every layer
@@ -260,12 +294,15 @@ def run_ours(args, w):
             vs.append(v)
             qs.append(gen_q(wl, layer % DISTINCT_LAYERS, step % 8))
         arr = [np.stack(ks), np.stack(vs), np.stack(qs)]
-        return [torch.from_numpy(a).to(dt) for a in arr]
+        t = [torch.from_numpy(a).to(dt) for a in arr]
+        if bb:     # f(K), f(V) of the appended tokens come with the step's inputs
+            t += [tensor_function(t[0]), tensor_function(t[1])]
+        return t
 
     host_inputs = [step_inputs(s) for s in range(8)]
     dev_inputs = [[t.to(dev) for t in hi] for hi in host_inputs]
     out = torch.empty((wl.n_layers, wl.batch, wl.n_q_heads, 128), dtype=torch.float32, device=dev)
-    mtr = torch.empty((wl.n_layers, 4, wl.batch, wl.n_q_heads), dtype=torch.float32, device=dev)
+    mtr = torch.empty((wl.n_layers, 5 if vw else 4, wl.batch, wl.n_q_heads), dtype=torch.float32, device=dev)
 
     # Per-layer C-ABI arguments are built once, outside every timed region, so the timed loops
     # issue nothing but the library calls (Python tensor indexing per call would otherwise cost
@@ -275,20 +312,26 @@ def run_ours(args, w):
     handle = cache._h
     sptr = ctypes.c_void_p(int(stream.cuda_stream))
     vp = lambda t: ctypes.c_void_p(t.data_ptr())
-    out_args = [(vp(out[l]), vp(mtr[l, 0]), vp(mtr[l, 1]), vp(mtr[l, 2]), vp(mtr[l, 3])) for l in range(wl.n_layers)]
+    out_args = [(vp(out[l]), vp(mtr[l, 0]), vp(mtr[l, 1]), vp(mtr[l, 2]), vp(mtr[l, 3]), vp(mtr[l, 4]) if vw else None)
+                for l in range(wl.n_layers)]
 
     def make_args(inp):
-        K1, V1, Q = inp
-        return [(vp(K1[l]), vp(V1[l]), vp(Q[l])) for l in range(wl.n_layers)], inp
+        K1, V1, Q = inp[:3]
+        hats = inp[3:] if bb else (None, None)
+        return [(vp(K1[l]), vp(V1[l]), vp(Q[l]), vp(hats[0][l]) if bb else None, vp(hats[1][l]) if bb else None)
+                for l in range(wl.n_layers)], inp
 
     def one_step(prepared):
         args_l, _keepalive = prepared
         dreq = ctypes.c_double(wl.delta_req)
         for layer in range(wl.n_layers):
-            kp, vpp, qp = args_l[layer]
-            st1 = lib.witcert_write(handle, layer, kp, vpp, 1, sptr)
-            o, ma, mb, ra, rb = out_args[layer]
-            st2 = lib.witcert_decode(handle, layer, qp, dreq, o, ma, mb, ra, rb, sptr)
+            kp, vpp, qp, khp, vhp = args_l[layer]
+            if bb:
+                st1 = lib.witcert_write_hat(handle, layer, kp, vpp, khp, vhp, 1, sptr)
+            else:
+                st1 = lib.witcert_write(handle, layer, kp, vpp, 1, sptr)
+            o, ma, mb, ra, rb, mv = out_args[layer]
+            st2 = lib.witcert_decode(handle, layer, qp, dreq, o, ma, mb, ra, rb, mv, sptr)
             if st1 or st2:
                 wc.check(st1 or st2, "bench step")
 
@@ -335,10 +378,10 @@ def run_ours(args, w):
     n_launch = st["decode_kernel_launches"]
     avg_ms = st["decode_kernel_ms"] / max(1, n_launch)
     avg_S = prof_len0 + 1 + (args.steps - 1) / 2.0
-    alg_bytes = wl.batch * wl.n_kv_heads * avg_S * BYTES_PER_TOK_HEAD[wl.scheme]
+    alg_bytes = wl.batch * wl.n_kv_heads * avg_S * tbytes
     achieved = alg_bytes / (avg_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = recorded_traffic(wl)
+    traffic = recorded_traffic(wl) if not vw else None
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     pinned = [[t.pin_memory() for t in hi] for hi in host_inputs]
@@ -365,7 +408,7 @@ def run_ours(args, w):
 
     cpu = None
     if rank == 0 and world == 1:
-        r, cores, sample = cpu_oracle_rate(w, args.cpu_seconds)
+        r, cores, sample = cpu_oracle_rate(w, args.cpu_seconds, vw)
         cpu = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -373,7 +416,7 @@ def run_ours(args, w):
                 "scaling": "weak", "vs_baseline": None, "dtype": f"fp16-mma/fp32 ({CODE_KIND[wl.scheme]} codes)",
                 "data": "synthetic (seeded numpy; bf16 N(0,1) K/V/q, x50 outlier RoPE pair, planted keys)",
                 "config": config_of(wl, args, f"auto ({st['last_n_splits']})", world),
-                "hbm_gbs_decode": achieved, "bytes_per_attended_token": wl.n_kv_heads * BYTES_PER_TOK_HEAD[wl.scheme],
+                "hbm_gbs_decode": achieved, "bytes_per_attended_token": wl.n_kv_heads * tbytes,
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                              "kernel": "decode_split_kernel", "avg_launch_ms": avg_ms, "launches": n_launch,
@@ -384,7 +427,7 @@ def run_ours(args, w):
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": 3 * wl.n_layers * args.steps,
                 "prefill_write": {"gbs": prefill_gbs, "frac": prefill_gbs / peak, "ms": prefill_ms,
-                                  "tok_heads": prefill_tok_heads, "bytes_per_tok_head": 512 + BYTES_PER_TOK_HEAD[wl.scheme]},
+                                  "tok_heads": prefill_tok_heads, "bytes_per_tok_head": prefill_read + tbytes},
                 "clocks": clk,
                 "device_errors": st["device_errors"], "int8_clamps": st["int8_clamps"]}
         print(json.dumps(line), flush=True)

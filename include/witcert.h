@@ -6,7 +6,10 @@
  *   [summary]   technical summary page: witness paragraph with Lemma 1,
  *               Theorem 2, the Tier B paragraph, the implementation
  *               paragraph, the closing improvements list (TV bound);
- *   [Lean page] paperswithlean.com page: Approach, Figure 2 and Figure 5.
+ *   [Lean page] paperswithlean.com page: Approach, Figure 2 and Figure 5;
+ *   [abstract]  arXiv abstract: the meter is sound for any cache-preserving
+ *               black-box quantizer, and any scheme given as one tensor
+ *               function is measured.
  *
  * Conventions for every call:
  *   - Pointers documented as "device" must be CUDA device pointers (or managed
@@ -46,8 +49,11 @@ typedef enum {
   WITCERT_INT8_DITHER = 0, /* subtractively dithered INT8, per-(token, 32-channel) fp16 scales [summary, Tier B] */
   WITCERT_FP8_E4M3 = 1,    /* black-box raw cast to OCP E4M3, no scale [summary, gate results] */
   WITCERT_KIVI2 = 2,       /* KIVI-style asymmetric 2-bit: K per channel over 16 tokens, V per token per 32 channels */
-  WITCERT_INT8_RTN = 3     /* INT8 with the same scales, rounded to nearest without dither (the dithered
+  WITCERT_INT8_RTN = 3,    /* INT8 with the same scales, rounded to nearest without dither (the dithered
                               quantizer with xi = 0); Tier A only */
+  WITCERT_BLACKBOX = 4     /* any tensor function f [abstract]: the caller passes f(K), f(V) with every
+                              write (witcert_write_hat); the cache keeps them as bfloat16 (544 B per token
+                              and KV head with the witness); Tier A only */
 } witcert_scheme;
 
 typedef enum {
@@ -72,6 +78,11 @@ typedef struct {
   int pos_offset;          /* global position of the cache's first token: a cache holding one slice of
                               a longer context (one shard of a context-parallel decode) keys its dither
                               on global positions; 0 for a whole context */
+  int v_witness;           /* nonzero: also keep the value witness wv_t >= ||v_t - v^_t|| (whole row,
+                              fp16 rounded up; 2 B per token and KV head) and report the value meter
+                              E_V = sum_t p~_t wv_t, which bounds || sum_t p~_t (v_t - v^_t) || by the
+                              triangle inequality.  The pages define no value-side bound: this is the
+                              value counterpart of the key witness, a reading of this library. */
 } witcert_config;
 
 typedef struct witcert_cache witcert_cache;
@@ -118,6 +129,16 @@ witcert_status witcert_destroy(witcert_cache* cache);
 witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, const void* V,
                              int n_tok, void* stream);
 
+/* Write path of the black-box scheme [abstract: any scheme registered as one tensor
+ * function is measured; Tier A holds for any cache-preserving black-box quantizer].
+ * K, V as in witcert_write; K_hat, V_hat are the tensor function's outputs f(K), f(V)
+ * in the same layout and dtype.  The cache stores bf16(K_hat), bf16(V_hat) (nearest
+ * even; unchanged for bf16 inputs), and the key witness w_{t,b} = ||K - bf16(K_hat)||
+ * of each band, so the decode and the bound use exactly what is stored.  EINVAL on a
+ * cache of another scheme (which takes witcert_write) and as witcert_write otherwise. */
+witcert_status witcert_write_hat(witcert_cache* cache, int layer, const void* K, const void* V,
+                                 const void* K_hat, const void* V_hat, int n_tok, void* stream);
+
 /* Fused metered split-KV decode [summary, implementation paragraph (output
  * and meter produced by one kernel reading the cache once, with the
  * certificate terms merged across KV splits by log-sum-exp); Theorem 2
@@ -132,8 +153,10 @@ witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, con
  *                                    s2_t = (1/d) sum_c q_c^2 s_{c,t}^2/12,
  *                                    delta_loc = delta_req/(L*Hq*T); NaN unless INT8_DITHER
  *   raw_a, raw_b                      the unclamped (A^2-1)/2 of each tier
+ *   meter_v [batch][n_q_heads]       value meter E_V = sum_t p~_t wv_t (v_witness caches;
+ *                                    EINVAL if non-NULL on a cache without value witnesses)
  * Meters are rounded upward (never below the exact value of the formula).
- * Any meter pointer may be NULL; if all four are NULL the meter work is
+ * Any meter pointer may be NULL; if all five are NULL the meter work is
  * compiled out and `out` is bit-identical to the metered run's.
  * With the gate enabled, per-16-token-block risks of the gate's tier
  * (Tier B for INT8_DITHER, Tier A otherwise) are kept for witcert_gate.
@@ -141,7 +164,7 @@ witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, con
  * (len 0) yields zero output and zero meters.  EINVAL on bad arguments. */
 witcert_status witcert_decode(witcert_cache* cache, int layer, const void* q, double delta_req,
                               float* out, float* meter_a, float* meter_b, float* raw_a,
-                              float* raw_b, void* stream);
+                              float* raw_b, float* meter_v, void* stream);
 
 /* Metered decode that allocates nothing.  The paper has no counterpart; this
  * entry point exists for callers that cannot call cudaMalloc while they serve:
@@ -151,7 +174,7 @@ witcert_status witcert_decode(witcert_cache* cache, int layer, const void* q, do
  * start-up.  Arguments, results and ordering are those of witcert_decode.  The
  * split-KV partial results live in one static device array of 16 MiB that
  * every GPU loading the library keeps until the process exits; the call rejects
- * with EINVAL a shape whose batch x n_q_heads x KV splits x 528 bytes exceeds
+ * with EINVAL a shape whose batch x n_q_heads x KV splits x 544 bytes exceeds
  * it.  The array's device address is looked up (cudaGetSymbolAddress) on the
  * first call made on each device, with that device current; make that first
  * call before any stream capture.  All calls share the array and each call
@@ -160,7 +183,7 @@ witcert_status witcert_decode(witcert_cache* cache, int layer, const void* q, do
  * the caller.  No cudaMalloc, cudaFree or allocating library routine is used. */
 witcert_status witcert_decode_noalloc(witcert_cache* cache, int layer, const void* q, double delta_req,
                                       float* out, float* meter_a, float* meter_b, float* raw_a,
-                                      float* raw_b, void* stream);
+                                      float* raw_b, float* meter_v, void* stream);
 
 /* Meter-driven gate [summary, implementation paragraph (exact blocks come
  * back from host memory once the meter passes a threshold); Lean page,
@@ -185,12 +208,13 @@ witcert_status witcert_gate_stats(witcert_cache* cache, witcert_gate_counters* o
 /* Context-parallel decode, one shard: this cache holds one slice of a longer context (its
  * tokens at global positions pos_offset, pos_offset + 1, ...; see witcert_config).  The
  * shard's decode of `layer` is merged over the shard's own splits but not normalized: for
- * every (sequence, query head) cell it writes one record of kPartStride = 132 floats to
- * `part` (device, [batch][n_q_heads][132]): the running maximum m of the logits in log2 units,
- * Z = sum 2^(l - m), S_A and S_B = sum 2^(l - m) expm1(c) of the Tier A and Tier B bounds,
- * and the 128 value sums relative to m.  Tier B's kappa uses s_total, the whole context's
+ * every (sequence, query head) cell it writes one record of 136 floats to `part` (device,
+ * [batch][n_q_heads][136]): the running maximum m of the logits in log2 units, Z = sum
+ * 2^(l - m), S_A and S_B = sum 2^(l - m) expm1(c) of the Tier A and Tier B bounds, S_V =
+ * sum 2^(l - m) wv (0 without value witnesses), three unused floats, and the 128 value sums
+ * relative to m.  Tier B's kappa uses s_total, the whole context's
  * length (>= this slice's), so the shards of one decode share delta_loc.  The records of all
- * shards, gathered in any order into [batch][n_q_heads][n_parts][132], are merged by
+ * shards, gathered in any order into [batch][n_q_heads][n_parts][136], are merged by
  * witcert_merge_partials into the same output and meters a single cache holding the whole
  * context would give (up to floating-point summation order).  Block risks are not kept
  * (gating needs a whole-context decode).  Same-stream ordering as witcert_decode. */
@@ -199,12 +223,12 @@ witcert_status witcert_decode_partial(witcert_cache* cache, int layer, const voi
 
 /* Merge of context-parallel shard records (see witcert_decode_partial; the log-sum-exp merge
  * of the pages' split-KV decode, applied across shards): parts is device [batch][n_q_heads]
- * [n_parts][132]; out [batch][n_q_heads][128] fp32 and the optional meters [batch][n_q_heads]
- * as in witcert_decode (meter_b NaN unless scheme is WITCERT_INT8_DITHER).  Asynchronous on
- * `stream`; no cache is involved. */
+ * [n_parts][136]; out [batch][n_q_heads][128] fp32 and the optional meters [batch][n_q_heads]
+ * as in witcert_decode (meter_b NaN unless scheme is WITCERT_INT8_DITHER; meter_v from the
+ * records' S_V).  Asynchronous on `stream`; no cache is involved. */
 witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch, int n_q_heads,
                                       witcert_scheme scheme, float* out, float* meter_a, float* meter_b,
-                                      float* raw_a, float* raw_b, void* stream);
+                                      float* raw_a, float* raw_b, float* meter_v, void* stream);
 
 /* Library counters.  Synchronizes the device. */
 witcert_status witcert_stats(witcert_cache* cache, witcert_stats_t* out);
@@ -226,20 +250,22 @@ witcert_status witcert_length(const witcert_cache* cache, int layer, int* len);
 typedef enum {
   WITCERT_X_K_CODES = 0, WITCERT_X_V_CODES = 1, WITCERT_X_K_SCALES = 2, WITCERT_X_V_SCALES = 3,
   WITCERT_X_V_ZEROS = 4, WITCERT_X_KIVI_K_SCALE = 5, WITCERT_X_KIVI_K_ZERO = 6,
-  WITCERT_X_WITNESS = 7, WITCERT_X_SLOTS = 8, WITCERT_X_BLOCK_RISK = 9
+  WITCERT_X_WITNESS = 7, WITCERT_X_SLOTS = 8, WITCERT_X_BLOCK_RISK = 9, WITCERT_X_V_WITNESS = 10
 } witcert_export_kind;
 
 /* Cache contents in a canonical layout, for inspection and tests.  Writes
  * into a caller-owned device buffer of `bytes` bytes (EINVAL if too small):
  *   WITCERT_X_K_CODES, V_CODES  uint8 [batch][len][n_kv_heads][128]
  *                               (INT8: two's-complement int8; FP8: E4M3 bits;
- *                               KIVI: 0..3, keys of an unfinished block 0)
+ *                               KIVI: 0..3, keys of an unfinished block 0);
+ *                               BLACKBOX: the stored bf16 values [batch][len][n_kv_heads][128]
  *   WITCERT_X_K_SCALES, V_SCALES fp16 [batch][len][n_kv_heads][4] (INT8; KIVI V scales)
  *   WITCERT_X_V_ZEROS           fp16 [batch][len][n_kv_heads][4] (KIVI)
  *   WITCERT_X_KIVI_K_SCALE, _ZERO fp16 [batch][nblk][n_kv_heads][128] (KIVI, full blocks)
  *   WITCERT_X_WITNESS           fp16 [batch][len][n_kv_heads][16]
  *   WITCERT_X_SLOTS             int32 [batch][n_kv_heads][nblk] (-1 = not repaired)
  *   WITCERT_X_BLOCK_RISK        float [batch][n_q_heads][nblk] (last decode; gate enabled)
+ *   WITCERT_X_V_WITNESS         fp16 [batch][len][n_kv_heads] (v_witness caches)
  * nblk = ceil(len/16).  Asynchronous on `stream`. */
 witcert_status witcert_export(witcert_cache* cache, int layer, witcert_export_kind what,
                               void* dst, size_t bytes, void* stream);

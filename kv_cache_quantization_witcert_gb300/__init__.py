@@ -11,8 +11,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (BF16, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER, INT8_RTN, KIVI2,  # noqa: F401
-                   SCHEMES, WitcertError, check, load)
+from ._lib import (BF16, BLACKBOX, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER,  # noqa: F401
+                   INT8_RTN, KIVI2, SCHEMES, WitcertError, check, load)
 
 __all__ = ["Cache", "witcert_dither", "witcert_merge_partials", "WitcertError", "load", "SCHEMES", "PART_STRIDE"]
 
@@ -33,14 +33,16 @@ class Cache:
     """One WitCert cache: compressed K/V store, witnesses, optional gate state."""
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, batch, max_tokens, scheme="int8_dither",
-                 dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0, pos_offset=0):
+                 dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0, pos_offset=0,
+                 v_witness=False):
         lib = load()
         self.dtype = dtype
         self.cfg = _lib.witcert_config(n_layers, n_q_heads, n_kv_heads, 128, batch, max_tokens,
                                        SCHEMES[scheme] if isinstance(scheme, str) else scheme,
                                        BF16 if dtype == torch.bfloat16 else F32, seed, total_steps, n_splits,
-                                       max_repair_blocks, pos_offset)
+                                       max_repair_blocks, pos_offset, int(bool(v_witness)))
         self.scheme = scheme
+        self.v_witness = bool(v_witness)
         h = ctypes.c_void_p()
         check(lib.witcert_create(ctypes.byref(self.cfg), ctypes.byref(h)), "witcert_create")
         self._h = h
@@ -51,19 +53,26 @@ class Cache:
         n_tok = K.shape[1]
         check(load().witcert_write(self._h, layer, _ptr(K), _ptr(V), n_tok, _stream_ptr(stream)), "witcert_write")
 
+    def witcert_write_hat(self, layer, K, V, K_hat, V_hat, stream=None):
+        """Black-box scheme: K_hat, V_hat are the tensor function's outputs f(K), f(V)."""
+        for t in (K, V, K_hat, V_hat):
+            assert t.is_contiguous() and t.dtype == self.dtype and t.shape == K.shape
+        check(load().witcert_write_hat(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), K.shape[1],
+                                       _stream_ptr(stream)), "witcert_write_hat")
+
     def witcert_decode(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
-                       stream=None):
+                       meter_v=None, stream=None):
         assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
         check(load().witcert_decode(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
-                                    _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
+                                    _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _ptr(meter_v), _stream_ptr(stream)),
               "witcert_decode")
 
     def witcert_decode_noalloc(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
-                               stream=None):
+                               meter_v=None, stream=None):
         assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
         check(load().witcert_decode_noalloc(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
-                                            _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _stream_ptr(stream)),
-              "witcert_decode_noalloc")
+                                            _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _ptr(meter_v),
+                                            _stream_ptr(stream)), "witcert_decode_noalloc")
 
     def witcert_decode_partial(self, layer, q, delta_req, s_total, part, stream=None):
         assert q.is_contiguous() and q.dtype == self.dtype and part.dtype == torch.float32 and part.is_contiguous()
@@ -71,7 +80,7 @@ class Cache:
                                             _stream_ptr(stream)), "witcert_decode_partial")
 
     def decode_partial(self, layer, q, delta_req, s_total, stream=None):
-        """This shard's per-cell records [B, Hq, 132] (see witcert_decode_partial)."""
+        """This shard's per-cell records [B, Hq, 136] (see witcert_decode_partial)."""
         part = torch.empty((q.shape[0], q.shape[1], PART_STRIDE), dtype=torch.float32, device=q.device)
         self.witcert_decode_partial(layer, q, delta_req, s_total, part, stream=stream)
         return part
@@ -122,23 +131,28 @@ class Cache:
         if not meters:
             self.witcert_decode(layer, q, delta_req, out, stream=stream)
             return out, None
-        m = torch.empty((4, B, Hq), dtype=torch.float32, device=q.device)
-        self.witcert_decode(layer, q, delta_req, out, m[0], m[1], m[2], m[3], stream=stream)
-        return out, {"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3]}
+        m = torch.empty((5, B, Hq), dtype=torch.float32, device=q.device)
+        self.witcert_decode(layer, q, delta_req, out, m[0], m[1], m[2], m[3], m[4] if self.v_witness else None,
+                            stream=stream)
+        meters = {"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3]}
+        if self.v_witness:
+            meters["meter_v"] = m[4]
+        return out, meters
 
     def export(self, layer, what, stream=None):
         B, Hkv, Hq = self.cfg.batch, self.cfg.n_kv_heads, self.cfg.n_q_heads
         S = self.witcert_length(layer)
         nblk = (S + 15) // 16
         dev = torch.device("cuda", torch.cuda.current_device())
+        code_dt = torch.bfloat16 if self.cfg.scheme == BLACKBOX else torch.uint8
         shapes = {
-            _lib.X_K_CODES: ((B, S, Hkv, 128), torch.uint8), _lib.X_V_CODES: ((B, S, Hkv, 128), torch.uint8),
+            _lib.X_K_CODES: ((B, S, Hkv, 128), code_dt), _lib.X_V_CODES: ((B, S, Hkv, 128), code_dt),
             _lib.X_K_SCALES: ((B, S, Hkv, 4), torch.float16), _lib.X_V_SCALES: ((B, S, Hkv, 4), torch.float16),
             _lib.X_V_ZEROS: ((B, S, Hkv, 4), torch.float16),
             _lib.X_KIVI_K_SCALE: ((B, nblk, Hkv, 128), torch.float16),
             _lib.X_KIVI_K_ZERO: ((B, nblk, Hkv, 128), torch.float16),
             _lib.X_WITNESS: ((B, S, Hkv, 16), torch.float16), _lib.X_SLOTS: ((B, Hkv, nblk), torch.int32),
-            _lib.X_BLOCK_RISK: ((B, Hq, nblk), torch.float32),
+            _lib.X_BLOCK_RISK: ((B, Hq, nblk), torch.float32), _lib.X_V_WITNESS: ((B, S, Hkv), torch.float16),
         }
         shape, dt = shapes[what]
         dst = torch.empty(shape, dtype=dt, device=dev)
@@ -147,21 +161,22 @@ class Cache:
         return dst
 
 
-PART_STRIDE = 132     # floats per (sequence, query head) record: m, Z, S_A, S_B, 128 value sums
+PART_STRIDE = 136     # floats per (sequence, query head) record: m, Z, S_A, S_B, S_V, 3 unused, 128 value sums
 
 
 def witcert_merge_partials(parts, scheme, out=None, meters=True, stream=None):
-    """Merge shard records parts [B, Hq, n_parts, 132] (device fp32) into the output [B, Hq, 128]
-    and, with meters, {"meter_a", "meter_b", "raw_a", "raw_b"} (see witcert_merge_partials)."""
+    """Merge shard records parts [B, Hq, n_parts, 136] (device fp32) into the output [B, Hq, 128]
+    and, with meters, {"meter_a", "meter_b", "raw_a", "raw_b", "meter_v"} (see witcert_merge_partials)."""
     assert parts.dtype == torch.float32 and parts.is_contiguous() and parts.shape[-1] == PART_STRIDE
     B, Hq, n = parts.shape[0], parts.shape[1], parts.shape[2]
     if out is None:
         out = torch.empty((B, Hq, 128), dtype=torch.float32, device=parts.device)
-    m = torch.empty((4, B, Hq), dtype=torch.float32, device=parts.device) if meters else None
-    ptrs = (_ptr(m[0]), _ptr(m[1]), _ptr(m[2]), _ptr(m[3])) if meters else (None,) * 4
+    m = torch.empty((5, B, Hq), dtype=torch.float32, device=parts.device) if meters else None
+    ptrs = tuple(_ptr(m[k]) for k in range(5)) if meters else (None,) * 5
     check(load().witcert_merge_partials(_ptr(parts), n, B, Hq, SCHEMES[scheme] if isinstance(scheme, str) else scheme,
                                         _ptr(out), *ptrs, _stream_ptr(stream)), "witcert_merge_partials")
-    return out, ({"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3]} if meters else None)
+    return out, ({"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3], "meter_v": m[4]}
+                 if meters else None)
 
 
 def witcert_wait_selftest(limit_ns, stream=None):

@@ -8,12 +8,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libwitcert.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ETIMEDOUT, EPAGEIN, ESTATE = 0, -1, -2, -3, -4, -5, -6
-INT8_DITHER, FP8_E4M3, KIVI2, INT8_RTN = 0, 1, 2, 3
+INT8_DITHER, FP8_E4M3, KIVI2, INT8_RTN, BLACKBOX = 0, 1, 2, 3, 4
 F32, BF16 = 0, 1
 (X_K_CODES, X_V_CODES, X_K_SCALES, X_V_SCALES, X_V_ZEROS, X_KIVI_K_SCALE, X_KIVI_K_ZERO, X_WITNESS,
- X_SLOTS, X_BLOCK_RISK) = range(10)
+ X_SLOTS, X_BLOCK_RISK, X_V_WITNESS) = range(11)
 
-SCHEMES = {"int8_dither": INT8_DITHER, "fp8_e4m3": FP8_E4M3, "kivi2": KIVI2, "int8_rtn": INT8_RTN}
+SCHEMES = {"int8_dither": INT8_DITHER, "fp8_e4m3": FP8_E4M3, "kivi2": KIVI2, "int8_rtn": INT8_RTN,
+           "blackbox": BLACKBOX}
 STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ETIMEDOUT: "ETIMEDOUT",
                 EPAGEIN: "EPAGEIN", ESTATE: "ESTATE"}
 
@@ -23,7 +24,7 @@ class witcert_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("batch", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("scheme", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("total_steps", ctypes.c_int), ("n_splits", ctypes.c_int), ("max_repair_blocks", ctypes.c_int),
-                ("pos_offset", ctypes.c_int)]
+                ("pos_offset", ctypes.c_int), ("v_witness", ctypes.c_int)]
 
 
 class witcert_gate_counters(ctypes.Structure):
@@ -45,10 +46,11 @@ SIGNATURES = {
     "witcert_create": [ctypes.POINTER(witcert_config), ctypes.POINTER(_vp)],
     "witcert_destroy": [_vp],
     "witcert_write": [_vp, _int, _vp, _vp, _int, _vp],
-    "witcert_decode": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
-    "witcert_decode_noalloc": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp],
+    "witcert_write_hat": [_vp, _int, _vp, _vp, _vp, _vp, _int, _vp],
+    "witcert_decode": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "witcert_decode_noalloc": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_decode_partial": [_vp, _int, _vp, ctypes.c_double, ctypes.c_longlong, _vp, _vp],
-    "witcert_merge_partials": [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp],
+    "witcert_merge_partials": [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_gate": [_vp, _int, ctypes.c_float, _vp],
     "witcert_gate_stats": [_vp, ctypes.POINTER(witcert_gate_counters), _int],
     "witcert_stats": [_vp, ctypes.POINTER(witcert_stats_t)],

@@ -7,6 +7,10 @@
 //   INT8_DITHER (4864 B = 16 x 304):  K codes 2048 | V codes 2048 | K scales 128 | V scales 128 | witness 512
 //   FP8_E4M3    (4608 B = 16 x 288):  K codes 2048 | V codes 2048 | witness 512
 //   KIVI2       (2304 B = 16 x 144):  K codes 512 | K scale,zero 512 | V codes 512 | V scale,zero 256 | witness 512
+//   BLACKBOX    (8704 B = 16 x 544):  K_hat bf16 4096 | V_hat bf16 4096 | witness 512
+//
+// With the value witness on, a separate array holds one fp16 norm per token:
+// 32 bytes per block, [B][Hkv][nblk_max][16] per layer.
 //
 // Codes are stored in "fragment order": the byte a lane of a warp needs for
 // the A operand of mma.m16n8k16 sits where one 16-byte shared-memory load per
@@ -27,19 +31,24 @@ constexpr int kGroupCh = 32;
 constexpr int kGroups = 4;
 constexpr int kMaxGroupHeads = 8;
 
-enum SchemeId : int { kInt8 = 0, kFp8 = 1, kKivi = 2, kRtn = 3 };
+enum SchemeId : int { kInt8 = 0, kFp8 = 1, kKivi = 2, kRtn = 3, kBbox = 4 };
 // INT8 round-to-nearest (kRtn) keeps the dithered scheme's block layout without the dither.
 __host__ __device__ constexpr bool int8_layout(int scheme) { return scheme == kInt8 || scheme == kRtn; }
 
 struct Int8Layout { static constexpr int KC = 0, VC = 2048, KS = 4096, VS = 4224, W = 4352, BYTES = 4864; };
 struct Fp8Layout  { static constexpr int KC = 0, VC = 2048, W = 4096, BYTES = 4608; };
 struct KiviLayout { static constexpr int KC = 0, KP = 512, VC = 1024, VP = 1536, W = 1792, BYTES = 2304; };
+struct BboxLayout { static constexpr int KH = 0, VH = 4096, W = 8192, BYTES = 8704; };
+constexpr int kVwBytes = kBlk * 2;   // value witnesses of one block
 
 __host__ __device__ constexpr int block_bytes(int scheme) {
-  return int8_layout(scheme) ? Int8Layout::BYTES : scheme == kFp8 ? Fp8Layout::BYTES : KiviLayout::BYTES;
+  return int8_layout(scheme) ? Int8Layout::BYTES
+         : scheme == kFp8    ? Fp8Layout::BYTES
+         : scheme == kKivi   ? KiviLayout::BYTES
+                             : BboxLayout::BYTES;
 }
 __host__ __device__ constexpr int witness_off(int scheme) {
-  return int8_layout(scheme) ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : KiviLayout::W;
+  return int8_layout(scheme) ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : scheme == kKivi ? KiviLayout::W : BboxLayout::W;
 }
 
 // ------------------------------------------------------------------ fragment-order index maps
@@ -92,6 +101,18 @@ __host__ __device__ inline void kivi_v_pos(int r, int c, int& word_off, int& bit
   int L = 4 * g + t, j = mt >> 1, reg = h + 2 * (e >> 1), p = (mt & 1) * 4 + reg;
   word_off = L * 16 + j * 4;
   bit = 2 * p + 16 * (e & 1);
+}
+// bf16 key of token r, channel c (black-box store): the QK A operand with two-byte
+// elements, 16 bytes per (k-step, lane): register h + 2 (e >> 1), half e & 1.
+__host__ __device__ inline int kbf_off(int r, int c) {
+  int g = r & 7, h = r >> 3, kk = c >> 4, t = (c >> 2) & 3, e = c & 3;
+  return (kk * 32 + 4 * g + t) * 16 + (h + 2 * (e >> 1)) * 4 + (e & 1) * 2;
+}
+// bf16 value of token r, channel c: the P.V A operand (channels as rows, tokens as k),
+// 16 bytes per (m-tile, lane).
+__host__ __device__ inline int vbf_off(int r, int c) {
+  int mt = c >> 4, g = c & 7, h = (c >> 3) & 1, t = pv_lane(r), e = pv_slot(r);
+  return (mt * 32 + 4 * g + t) * 16 + (h + 2 * (e >> 1)) * 4 + (e & 1) * 2;
 }
 // KIVI K per-channel scale (fp16) index; the zero point sits 256 bytes later.
 __host__ __device__ inline int kivi_kparam_idx(int c) { return ((c >> 2) & 3) * 32 + (c >> 4) * 4 + (c & 3); }
@@ -175,6 +196,14 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Transpose of an 8x8 fp16 matrix held as mma fragments (lane 4g + t holds row g,
 // columns 2t, 2t+1; afterwards it holds row g of the transpose).
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
@@ -187,6 +216,7 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) { return h2_bits(__halves2half2(lo, hi)); }
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // Two biased INT8 codes (code + 128 in bytes b, b+1 of w) -> exact fp16x2 codes.
 // 0x64XX is the fp16 1024 + XX; subtracting 1152 = 1024 + 128 leaves the code.

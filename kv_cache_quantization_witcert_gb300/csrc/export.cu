@@ -7,7 +7,7 @@ namespace witcert {
 
 namespace {
 
-enum { X_KC = 0, X_VC, X_KS, X_VS, X_VZ, X_KIVI_KS, X_KIVI_KZ, X_W, X_SLOTS, X_RISK };
+enum { X_KC = 0, X_VC, X_KS, X_VS, X_VZ, X_KIVI_KS, X_KIVI_KZ, X_W, X_SLOTS, X_RISK, X_VW };
 
 __global__ void export_kernel(const ExportArgs a, size_t n) {
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -21,6 +21,11 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
       const int i = idx / ((size_t)kD * a.Hkv * a.S);
       const uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * bb;
       const int r = t & 15;
+      if (a.scheme == kBbox) {   // the stored bf16 values
+        const int off = a.what == X_KC ? BboxLayout::KH + kbf_off(r, c) : BboxLayout::VH + vbf_off(r, c);
+        reinterpret_cast<uint16_t*>(a.dst)[idx] = *reinterpret_cast<const uint16_t*>(bp + off);
+        break;
+      }
       uint8_t v;
       if (a.scheme == kKivi) {
         int off, bit;
@@ -81,6 +86,12 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
       reinterpret_cast<float*>(a.dst)[idx] = a.risk[cell * a.nblk_max + b];
       break;
     }
+    case X_VW: {  // [B][S][Hkv]
+      const int h = idx % a.Hkv, t = (idx / a.Hkv) % a.S;
+      const int i = idx / ((size_t)a.Hkv * a.S);
+      reinterpret_cast<__half*>(a.dst)[idx] = a.vwit[(((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * kBlk + (t & 15)];
+      break;
+    }
   }
 }
 
@@ -126,6 +137,7 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t st) {
     case X_W: n = (size_t)a.B * a.S * a.Hkv * kBands; break;
     case X_SLOTS: n = (size_t)a.B * a.Hkv * nblk; break;
     case X_RISK: n = (size_t)a.B * a.Hq * nblk; break;
+    case X_VW: n = (size_t)a.B * a.S * a.Hkv; break;
   }
   if (n == 0) return cudaSuccess;
   export_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a, n);

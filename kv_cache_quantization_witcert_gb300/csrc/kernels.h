@@ -2,17 +2,23 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace witcert {
 
-constexpr int kPartStride = 132;   // m (log2 units), Z, S_A, S_B, acc[128]
+// Split record: m (log2 units), Z, S_A, S_B, S_V, three unused, acc[128]
+constexpr int kPartStride = 136;
+constexpr int kPartAcc = 8;
 
 struct WriteArgs {
   uint8_t* blocks;           // layer base: [B][Hkv][nblk_max][block_bytes]
   int nblk_max;
   const void* K;             // [B][n_tok][Hkv][128]
   const void* V;
+  const void* Kh;            // black-box scheme: the tensor function's outputs, same layout as K, V
+  const void* Vh;
+  __half* vwit;              // layer base [B][Hkv][nblk_max][16] value witnesses, or null
   int B, Hkv, n_tok, t0, layer, backing_rows;   // backing_rows: rows per (seq, KV head) in the backing store
   int tok_begin, tok_count;  // tokens of this write a per-token launch covers
   int pos0;                  // global position of the cache's first token (dither key)
@@ -44,6 +50,8 @@ struct DecodeArgs {
   float* risk;               // [B][Hq][nblk_max] normalized block risk, or null
   float* out;                // [B][Hq][128]
   float *meter_a, *meter_b, *raw_a, *raw_b;
+  const __half* vwit;        // layer base [B][Hkv][nblk_max][16] value witnesses, or null
+  float* meter_v;            // [B][Hq] value meter, or null
   int* err;                  // device error word (spin limits)
   const uint8_t* next_blocks;  // the next layer's base: its first blocks are prefetched into L2, or null
   int pos0;                  // global position of the cache's first token (dither key)
@@ -64,7 +72,7 @@ cudaError_t launch_decode(int scheme, const DecodeArgs& a, int sm_count, cudaStr
 int decode_ctas_per_sm(int scheme, const DecodeArgs& a);
 // Merge kernel alone over caller-given records a.part [B][Hq][a.n_splits][kPartStride].
 cudaError_t launch_merge_records(int scheme, const DecodeArgs& a, cudaStream_t st);
-int decode_auto_splits(int B, int Hkv, int nblk, int sm_count, int per_sm);
+int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count, int per_sm);
 // Device address (current device) and size of the library's static split scratch,
 // used by witcert_decode_noalloc; the first call on a device looks the address up.
 cudaError_t decode_static_scratch(float** ptr, size_t* bytes);
@@ -90,6 +98,7 @@ struct ExportArgs {
   int nblk_max, B, Hkv, Hq, S, scheme;
   const int32_t* slots;
   const float* risk;
+  const __half* vwit;        // layer base [B][Hkv][nblk_max][16], or null
   void* dst;
   int what;
 };

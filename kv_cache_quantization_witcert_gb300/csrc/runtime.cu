@@ -46,6 +46,7 @@ struct witcert_cache {
   size_t layer_blocks = 0;          // bytes of one layer's block store
   uint8_t* blocks = nullptr;
   float* kivi_tail = nullptr;       // [L][B][Hkv][16][128]
+  __half* vwit = nullptr;           // [L][B][Hkv][nblk_max][16] value witnesses (v_witness caches)
   int32_t* slots = nullptr;         // [L][B][Hkv][nblk_max]
   void* pool = nullptr;             // [cap][16][128] kv dtype
   void* backing_host = nullptr;     // [L][B][Hkv][max_tokens][128] kv dtype, pinned + mapped
@@ -84,6 +85,8 @@ size_t layer_rows(const witcert_cache* c) { return (size_t)c->cfg.batch * c->cfg
 // Backing-store rows per (sequence, KV head): capacity rounded up to whole 16-token blocks,
 // so page-in can always copy a full block.
 size_t backing_rows(const witcert_cache* c) { return (size_t)c->nblk_max * kBlk; }
+// Value witnesses of one layer: [B][Hkv][nblk_max][16].
+size_t vwit_layer(const witcert_cache* c) { return layer_rows(c) * c->nblk_max * kBlk; }
 
 witcert_status check_layer(const witcert_cache* c, int layer) {
   if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
@@ -92,7 +95,7 @@ witcert_status check_layer(const witcert_cache* c, int layer) {
 }
 
 void free_all(witcert_cache* c) {
-  cudaFree(c->blocks); cudaFree(c->kivi_tail); cudaFree(c->slots); cudaFree(c->pool);
+  cudaFree(c->blocks); cudaFree(c->kivi_tail); cudaFree(c->vwit); cudaFree(c->slots); cudaFree(c->pool);
   if (c->backing_host) cudaFreeHost(c->backing_host);
   cudaFree(c->risk_raw); cudaFree(c->risk); cudaFree(c->part); cudaFree(c->selmask); cudaFree(c->todo);
   cudaFree(c->todo_count); cudaFree(c->pool_next); cudaFree(c->gstats); cudaFree(c->clamps); cudaFree(c->err);
@@ -144,7 +147,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
     return fail(WITCERT_EINVAL, "n_q_heads must be a positive multiple of n_kv_heads");
   if (f.n_q_heads / f.n_kv_heads > kMaxGroupHeads) return fail(WITCERT_EINVAL, "at most %d query heads per KV head", kMaxGroupHeads);
   if (f.batch <= 0 || f.max_tokens <= 0) return fail(WITCERT_EINVAL, "batch and max_tokens must be positive");
-  if (f.scheme < WITCERT_INT8_DITHER || f.scheme > WITCERT_INT8_RTN) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)f.scheme);
+  if (f.scheme < WITCERT_INT8_DITHER || f.scheme > WITCERT_BLACKBOX) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)f.scheme);
   if (f.kv_dtype != WITCERT_F32 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "unknown dtype %d", (int)f.kv_dtype);
   if (f.total_steps <= 0) return fail(WITCERT_EINVAL, "total_steps must be positive");
   if (f.n_splits < 0 || f.max_repair_blocks < 0) return fail(WITCERT_EINVAL, "n_splits and max_repair_blocks must be >= 0");
@@ -174,6 +177,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
 #define TRY(x, what) do { e = (x); if (e != cudaSuccess) { free_all(c); delete c; return cuda_fail(e, what); } } while (0)
   TRY(dalloc(&c->blocks, L * c->layer_blocks), "allocating the block store");
   if (c->scheme == kKivi) TRY(dalloc(&c->kivi_tail, L * layer_rows(c) * kBlk * kD * sizeof(float)), "allocating the KIVI tail");
+  if (f.v_witness) TRY(dalloc(&c->vwit, L * vwit_layer(c) * sizeof(__half)), "allocating value witnesses");
   TRY(dalloc(&c->part, cells * c->max_splits * kPartStride * sizeof(float)), "allocating split scratch");
   TRY(dalloc(&c->clamps, sizeof(unsigned long long)), "allocating counters");
   TRY(dalloc(&c->err, sizeof(int)), "allocating the error word");
@@ -212,10 +216,12 @@ witcert_status witcert_destroy(witcert_cache* c) {
   return WITCERT_OK;
 }
 
-witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const void* V, int n_tok, void* stream) {
+static witcert_status write_impl(witcert_cache* c, int layer, const void* K, const void* V, const void* Kh,
+                                 const void* Vh, int n_tok, void* stream) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (n_tok < 0) return fail(WITCERT_EINVAL, "n_tok must be >= 0");
   if (n_tok > 0 && (!K || !V)) return fail(WITCERT_EINVAL, "K and V must not be NULL");
+  if (n_tok > 0 && c->scheme == kBbox && (!Kh || !Vh)) return fail(WITCERT_EINVAL, "K_hat and V_hat must not be NULL");
   if ((long long)c->len[layer] + n_tok > c->cfg.max_tokens)
     return fail(WITCERT_EINVAL, "layer %d would hold %lld tokens, capacity %d", layer,
                 (long long)c->len[layer] + n_tok, c->cfg.max_tokens);
@@ -225,7 +231,8 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   WriteArgs a{};
   a.blocks = c->blocks + layer * c->layer_blocks;
   a.nblk_max = c->nblk_max;
-  a.K = K; a.V = V;
+  a.K = K; a.V = V; a.Kh = Kh; a.Vh = Vh;
+  if (c->vwit) a.vwit = c->vwit + layer * vwit_layer(c);
   a.B = c->cfg.batch; a.Hkv = c->cfg.n_kv_heads; a.n_tok = n_tok; a.t0 = c->len[layer]; a.layer = layer;
   a.backing_rows = (int)backing_rows(c);
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
@@ -264,6 +271,17 @@ witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const v
   return WITCERT_OK;
 }
 
+witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const void* V, int n_tok, void* stream) {
+  if (c && c->scheme == kBbox) return fail(WITCERT_EINVAL, "a black-box cache is written with witcert_write_hat");
+  return write_impl(c, layer, K, V, nullptr, nullptr, n_tok, stream);
+}
+
+witcert_status witcert_write_hat(witcert_cache* c, int layer, const void* K, const void* V, const void* K_hat,
+                                 const void* V_hat, int n_tok, void* stream) {
+  if (c && c->scheme != kBbox) return fail(WITCERT_EINVAL, "witcert_write_hat needs a WITCERT_BLACKBOX cache");
+  return write_impl(c, layer, K, V, K_hat, V_hat, n_tok, stream);
+}
+
 // Automatic split count for a decode of nblk blocks: sized by how many split-kernel CTAs of
 // this configuration fit on an SM, and never above the scratch sized at create time.
 static int auto_splits(const witcert_cache* c, int nblk, bool meter, int cap) {
@@ -273,7 +291,7 @@ static int auto_splits(const witcert_cache* c, int nblk, bool meter, int cap) {
   a.meter = meter;
   a.slots = c->slots;
   const int per_sm = decode_ctas_per_sm(c->scheme, a);
-  int s = decode_auto_splits(c->cfg.batch, c->cfg.n_kv_heads, nblk > 0 ? nblk : 1, c->sm_count, per_sm);
+  int s = decode_auto_splits(c->scheme, c->cfg.batch, c->cfg.n_kv_heads, nblk > 0 ? nblk : 1, c->sm_count, per_sm);
   if (cap > 0 && s > cap) s = cap;
   return s;
 }
@@ -310,14 +328,17 @@ static void fill_decode(witcert_cache* c, int layer, const void* q, double delta
   a.kappa = kappa;
   a.err = c->err;
   if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
+  if (c->vwit && meter) a.vwit = c->vwit + layer * vwit_layer(c);
   a.meter = meter;
 }
 
 witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
-                              float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
+                              float* meter_a, float* meter_b, float* raw_a, float* raw_b, float* meter_v,
+                              void* stream) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
-  const bool meter = meter_a || meter_b || raw_a || raw_b;
+  if (meter_v && !c->vwit) return fail(WITCERT_EINVAL, "meter_v needs a cache created with v_witness");
+  const bool meter = meter_a || meter_b || raw_a || raw_b || meter_v;
   if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
   auto st = static_cast<cudaStream_t>(stream);
   const bool waited = order_after_gate(c, layer, st);
@@ -329,7 +350,7 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
     a.risk_raw = c->risk_raw;
     a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
   }
-  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b; a.meter_v = meter_v;
   ProfPair pp{nullptr, nullptr};
   if (c->profiling) {
     if (c->prof_free.empty()) {
@@ -353,10 +374,12 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
 }
 
 witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q, double delta_req, float* out,
-                                      float* meter_a, float* meter_b, float* raw_a, float* raw_b, void* stream) {
+                                      float* meter_a, float* meter_b, float* raw_a, float* raw_b, float* meter_v,
+                                      void* stream) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (!q || !out) return fail(WITCERT_EINVAL, "q and out must not be NULL");
-  const bool meter = meter_a || meter_b || raw_a || raw_b;
+  if (meter_v && !c->vwit) return fail(WITCERT_EINVAL, "meter_v needs a cache created with v_witness");
+  const bool meter = meter_a || meter_b || raw_a || raw_b || meter_v;
   if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
   DecodeArgs a{};
   fill_decode(c, layer, q, delta_req, meter, 0, a);
@@ -377,7 +400,7 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
     a.risk_raw = c->risk_raw;
     a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
   }
-  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b; a.meter_v = meter_v;
   e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (gate && meter) c->risk_len[layer] = a.S;
@@ -410,16 +433,16 @@ witcert_status witcert_decode_partial(witcert_cache* c, int layer, const void* q
 
 witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch, int n_q_heads,
                                       witcert_scheme scheme, float* out, float* meter_a, float* meter_b,
-                                      float* raw_a, float* raw_b, void* stream) {
+                                      float* raw_a, float* raw_b, float* meter_v, void* stream) {
   if (!parts || !out) return fail(WITCERT_EINVAL, "parts and out must not be NULL");
   if (n_parts < 1 || batch < 1 || n_q_heads < 1) return fail(WITCERT_EINVAL, "n_parts, batch and n_q_heads must be >= 1");
-  if (scheme < WITCERT_INT8_DITHER || scheme > WITCERT_INT8_RTN) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)scheme);
+  if (scheme < WITCERT_INT8_DITHER || scheme > WITCERT_BLACKBOX) return fail(WITCERT_EINVAL, "unknown scheme %d", (int)scheme);
   DecodeArgs a{};
   a.part = const_cast<float*>(parts);
   a.n_splits = n_parts;
   a.B = batch; a.Hq = n_q_heads;
-  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b;
-  a.meter = meter_a || meter_b || raw_a || raw_b;
+  a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b; a.meter_v = meter_v;
+  a.meter = meter_a || meter_b || raw_a || raw_b || meter_v;
   cudaError_t e = launch_merge_records((int)scheme, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   ok();
@@ -540,12 +563,13 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
   const size_t B = c->cfg.batch, Hkv = c->cfg.n_kv_heads, Hq = c->cfg.n_q_heads;
   size_t need = 0;
   switch (what) {
-    case WITCERT_X_K_CODES: case WITCERT_X_V_CODES: need = B * S * Hkv * kD; break;
+    case WITCERT_X_K_CODES: case WITCERT_X_V_CODES: need = B * S * Hkv * kD * (c->scheme == kBbox ? 2 : 1); break;
     case WITCERT_X_K_SCALES: case WITCERT_X_V_SCALES: case WITCERT_X_V_ZEROS: need = B * S * Hkv * 4 * 2; break;
     case WITCERT_X_KIVI_K_SCALE: case WITCERT_X_KIVI_K_ZERO: need = B * nblk * Hkv * kD * 2; break;
     case WITCERT_X_WITNESS: need = B * S * Hkv * kBands * 2; break;
     case WITCERT_X_SLOTS: need = B * Hkv * nblk * 4; break;
     case WITCERT_X_BLOCK_RISK: need = B * Hq * nblk * 4; break;
+    case WITCERT_X_V_WITNESS: need = B * S * Hkv * 2; break;
     default: return fail(WITCERT_EINVAL, "unknown export kind %d", (int)what);
   }
   const bool int8 = int8_layout(c->scheme), kivi = c->scheme == kKivi;
@@ -553,6 +577,7 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
       ((what == WITCERT_X_V_ZEROS || what == WITCERT_X_KIVI_K_SCALE || what == WITCERT_X_KIVI_K_ZERO) && !kivi))
     return fail(WITCERT_EINVAL, "export kind %d does not exist for this scheme", (int)what);
   if (what == WITCERT_X_BLOCK_RISK && !c->risk) return fail(WITCERT_ESTATE, "block risks need the gate enabled");
+  if (what == WITCERT_X_V_WITNESS && !c->vwit) return fail(WITCERT_EINVAL, "value witnesses need a cache created with v_witness");
   if (!dst || bytes < need) return fail(WITCERT_EINVAL, "export needs %zu bytes, got %zu", need, bytes);
   auto st = static_cast<cudaStream_t>(stream);
   order_after_gate(c, layer, st);
@@ -561,6 +586,7 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
   a.nblk_max = c->nblk_max; a.B = (int)B; a.Hkv = (int)Hkv; a.Hq = (int)Hq; a.S = S; a.scheme = c->scheme;
   a.slots = c->slots ? c->slots + layer * layer_rows(c) * c->nblk_max : nullptr;
   a.risk = c->risk ? c->risk + (size_t)layer * B * Hq * c->nblk_max : nullptr;
+  a.vwit = c->vwit ? c->vwit + layer * vwit_layer(c) : nullptr;
   a.dst = dst;
   a.what = (int)what;
   cudaError_t e = launch_export(a, st);

@@ -10,6 +10,9 @@
 // KIVI keys are quantized per channel over a 16-token block when the block's
 // last token arrives (one warp per (sequence, KV head) walks the blocks in
 // order); until then they wait, exact, in a per-(sequence, head) tail buffer.
+// The black-box scheme stores a caller's tensor-function outputs K_hat, V_hat as
+// bfloat16 and takes the witness against them.  With the value witness on, every
+// writer also stores ||v - v_hat|| over the whole row, rounded up to fp16 the same way.
 #include <cmath>
 
 #include "common.cuh"
@@ -102,13 +105,33 @@ __device__ __forceinline__ __half f16_ru_df(float hi, float lo) {
   return h;
 }
 
-// Lanes 0..15 store band `lane` of token r from the lane's four residuals (double-float, with
-// absolute error bound `err` summed over them) and its partner lane's (lane ^ 16).  Returns
-// false, storing nothing, when the warp must fall back to the fp64 computation.
-__device__ __forceinline__ bool store_witness_df(uint8_t* wreg, int r, const Df (&res)[4], float err, int lane,
-                                                 bool zero) {
+// fp16_ru(w (1 + 2^-48)) of w = sqrt(ss), ss a double-float sum of squares whose norm carries
+// an absolute error of at most `err` from the residuals and a relative error of at most `arith`
+// from the double-float arithmetic.  Returns false when an fp16 value lies within that error
+// band (or ss is too small for the band to mean anything): the caller then takes the fp64 path.
+__device__ __forceinline__ bool norm_f16_ru(Df ss, float err, float arith, __half& w16) {
+  w16 = __float2half_rn(0.f);
+  if (!(ss.hi > 0.f)) return !(err > 0.f);      // an exact zero only when the residuals are exact
+  // w = sqrt(ss): correctly rounded root, one correction from the exact remainder
+  const float y = __fsqrt_rn(ss.hi);
+  const float rem = __fmaf_rn(-y, y, ss.hi);
+  const Df w = fast_two_sum(y, __fdividef(__fadd_rn(rem, ss.lo), 2.0f * y));
+  // z = w (1 + 2^-48)
+  const Df z = fast_two_sum(w.hi, __fmaf_rn(w.hi, 0x1p-48f, w.lo));
+  w16 = f16_ru_df(z.hi, z.lo);
+  const float band = __fadd_ru(arith, __fdiv_ru(__fmul_ru(4.0f, err), w.hi));
+  const float up = __fsub_rn(__fsub_rn(__half2float(w16), z.hi), z.lo);         // >= 0
+  const unsigned short bits = __half_as_ushort(w16);
+  const float down = bits ? __fadd_rn(__fsub_rn(z.hi, __half2float(__ushort_as_half((unsigned short)(bits - 1)))), z.lo)
+                          : INFINITY;
+  const float lim = __fmul_ru(__fmul_ru(2.0f, band), z.hi);
+  return up > lim && down > lim && ss.hi >= 0x1p-90f;
+}
+
+// Sum of squares of the lane's four residuals as a double-float; `bad` flags magnitudes
+// outside the range where the double-float error bounds hold.
+__device__ __forceinline__ Df lane_sumsq(const Df (&res)[4], bool& bad) {
   Df ss = {0.f, 0.f};
-  bool bad = false;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float a = fabsf(res[e].hi);
@@ -117,33 +140,50 @@ __device__ __forceinline__ bool store_witness_df(uint8_t* wreg, int r, const Df 
     sq.lo = __fmaf_rn(2.0f * res[e].hi, res[e].lo, sq.lo);
     ss = df_add(ss, sq);
   }
+  return ss;
+}
+
+// Lanes 0..15 store band `lane` of token r from the lane's four residuals (double-float, with
+// absolute error bound `err` summed over them) and its partner lane's (lane ^ 16).  Returns
+// false, storing nothing, when the warp must fall back to the fp64 computation.
+__device__ __forceinline__ bool store_witness_df(uint8_t* wreg, int r, const Df (&res)[4], float err, int lane,
+                                                 bool zero) {
+  bool bad = false;
+  Df ss = lane_sumsq(res, bad);
   ss = df_add(ss, {__shfl_xor_sync(0xffffffffu, ss.hi, 16), __shfl_xor_sync(0xffffffffu, ss.lo, 16)});
   err = __fadd_ru(err, __shfl_xor_sync(0xffffffffu, err, 16));
   __half w16 = __float2half_rn(0.f);
-  if (lane < 16 && !zero) {
-    if (ss.hi > 0.f) {
-      // w = sqrt(ss): correctly rounded root, one correction from the exact remainder
-      const float y = __fsqrt_rn(ss.hi);
-      const float rem = __fmaf_rn(-y, y, ss.hi);
-      const Df w = fast_two_sum(y, __fdividef(__fadd_rn(rem, ss.lo), 2.0f * y));
-      // z = w (1 + 2^-48)
-      const Df z = fast_two_sum(w.hi, __fmaf_rn(w.hi, 0x1p-48f, w.lo));
-      w16 = f16_ru_df(z.hi, z.lo);
-      // relative error band of z: double-float arithmetic plus the residuals' own error
-      const float band = __fadd_ru(0x1p-40f, __fdiv_ru(__fmul_ru(4.0f, err), w.hi));
-      const float up = __fsub_rn(__fsub_rn(__half2float(w16), z.hi), z.lo);         // >= 0
-      const unsigned short bits = __half_as_ushort(w16);
-      const float down = bits ? __fadd_rn(__fsub_rn(z.hi, __half2float(__ushort_as_half((unsigned short)(bits - 1)))), z.lo)
-                              : INFINITY;
-      const float lim = __fmul_ru(__fmul_ru(2.0f, band), z.hi);
-      bad |= !(up > lim) || !(down > lim) || ss.hi < 0x1p-90f;
-    } else {
-      bad |= err > 0.f;            // an exact zero only when the residuals are exact
-    }
-  }
+  if (lane < 16 && !zero) bad |= !norm_f16_ru(ss, err, 0x1p-40f, w16);
   if (__any_sync(0xffffffffu, bad)) return false;
   if (lane < 16) *reinterpret_cast<__half*>(wreg + wit_off(r, lane)) = w16;
   return true;
+}
+
+// Value witness: lane 0 stores the norm of the whole row (all 32 lanes' residuals) at *dst,
+// by the same rule; false (nothing stored) when the warp must take the fp64 path.
+__device__ __forceinline__ bool store_rownorm_df(__half* dst, const Df (&res)[4], float err, int lane) {
+  bool bad = false;
+  Df ss = lane_sumsq(res, bad);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ss = df_add(ss, {__shfl_xor_sync(0xffffffffu, ss.hi, o), __shfl_xor_sync(0xffffffffu, ss.lo, o)});
+    err = __fadd_ru(err, __shfl_xor_sync(0xffffffffu, err, o));
+  }
+  __half w16 = __float2half_rn(0.f);
+  if (lane == 0) bad |= !norm_f16_ru(ss, err, 0x1p-34f, w16);
+  if (__any_sync(0xffffffffu, bad)) return false;
+  if (lane == 0) *dst = w16;
+  return true;
+}
+__device__ __forceinline__ void store_rownorm(__half* dst, const double (&res)[4], int lane) {
+  double ss = res[0] * res[0] + res[1] * res[1] + res[2] * res[2] + res[3] * res[3];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) *dst = __float2half_ru(__double2float_ru(sqrt(ss) * kWitMargin));
+}
+// Where token t of (sequence i, KV head h) keeps its value witness.
+__device__ __forceinline__ __half* vwit_at(const WriteArgs& a, int i, int h, int t) {
+  return a.vwit + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * kBlk + (t & 15);
 }
 
 // Exact-key side effects shared by all schemes: backing store and repaired blocks.
@@ -187,6 +227,7 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     Df rdf[4];
     float err = 0.f;
     int clamps = 0;
+    const bool resid = tensor == 0 || a.vwit;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int code = 0;
@@ -198,7 +239,7 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
         code = (int)rz;
       }
       codes[e] = code;
-      if (tensor == 0) {
+      if (resid) {
         // residual x - s (code - xi) = x - s code + s xi, as exact fp32 terms (s code has at most
         // 19 significant bits; s xi is an exact product pair)
         const float sc = __fmul_rn(s, (float)code);
@@ -222,6 +263,11 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
         store_witness(bp + Int8Layout::W, r, res, lane, repaired);
       }
+    } else if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
+      double res[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
+      store_rownorm(vwit_at(a, i, h, t), res, lane);
     }
   }
 }
@@ -257,8 +303,64 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xhs[e];
         store_witness(bp + Fp8Layout::W, r, res, lane, repaired);
       }
+    } else if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
+      double res[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xhs[e];
+      store_rownorm(vwit_at(a, i, h, t), res, lane);
     }
   }
+}
+
+// Black-box scheme: the caller's K_hat, V_hat rows rounded to bfloat16 (nearest even) are the
+// store; the key witness (and the value witness) are taken against those stored values.
+template <typename T>
+__device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
+  const int t = a.t0 + n, r = t & 15;
+  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+  const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
+#pragma unroll
+  for (int tensor = 0; tensor < 2; ++tensor) {
+    float x[4], y[4];
+    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
+    load4f<T>(reinterpret_cast<const T*>(tensor ? a.Vh : a.Kh) + row + 4 * lane, y);
+    const __nv_bfloat162 p01 = __floats2bfloat162_rn(y[0], y[1]), p23 = __floats2bfloat162_rn(y[2], y[3]);
+    const float xh[4] = {__low2float(p01), __high2float(p01), __low2float(p23), __high2float(p23)};
+    Df rdf[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rdf[e] = residual_df(x[e], -xh[e], 0.f, 0.f);   // exact: one error-free sum
+    if (tensor == 0) {
+      // channels 4 lane .. 4 lane + 3: registers h (e = 0, 1) and h + 2 (e = 2, 3) of one (k-step, lane) slot
+      *reinterpret_cast<uint32_t*>(bp + BboxLayout::KH + kbf_off(r, 4 * lane)) = bf2_bits(p01);
+      *reinterpret_cast<uint32_t*>(bp + BboxLayout::KH + kbf_off(r, 4 * lane + 2)) = bf2_bits(p23);
+      if (!store_witness_df(bp + BboxLayout::W, r, rdf, 0.f, lane, repaired)) {
+        double res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xh[e];
+        store_witness(bp + BboxLayout::W, r, res, lane, repaired);
+      }
+    } else {
+      __nv_bfloat16* vh = reinterpret_cast<__nv_bfloat16*>(bp + BboxLayout::VH);
+      vh[vbf_off(r, 4 * lane) / 2] = __low2bfloat16(p01);
+      vh[vbf_off(r, 4 * lane + 1) / 2] = __high2bfloat16(p01);
+      vh[vbf_off(r, 4 * lane + 2) / 2] = __low2bfloat16(p23);
+      vh[vbf_off(r, 4 * lane + 3) / 2] = __high2bfloat16(p23);
+      if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
+        double res[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xh[e];
+        store_rownorm(vwit_at(a, i, h, t), res, lane);
+      }
+    }
+  }
+}
+
+// One token of a write into the block image at bp, by scheme.
+template <typename T, int SCH>
+__device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
+  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, n, lane);
+  else if constexpr (SCH == kFp8) fp8_token<T>(a, bp, i, h, n, lane);
+  else bbox_token<T>(a, bp, i, h, n, lane);
 }
 
 
@@ -272,10 +374,9 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   if (wid >= a.B * a.tok_count * a.Hkv) return;
   const int h = wid % a.Hkv, n = a.tok_begin + (wid / a.Hkv) % a.tok_count, i = wid / (a.Hkv * a.tok_count);
   const int blk = (a.t0 + n) >> 4;
-  constexpr int kBytes = int8_layout(SCH) ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  constexpr int kBytes = block_bytes(SCH);
   uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * kBytes;
-  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, n, lane);
-  else fp8_token<T>(a, bp, i, h, n, lane);
+  write_token<T, SCH>(a, bp, i, h, n, lane);
 }
 
 // One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
@@ -285,7 +386,7 @@ template <typename T, int SCH>
 __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
   pdl_wait();
   pdl_trigger();
-  constexpr int kBytes = int8_layout(SCH) ? Int8Layout::BYTES : Fp8Layout::BYTES;
+  constexpr int kBytes = block_bytes(SCH);
   __shared__ __align__(16) uint8_t img[4][kBytes];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 4 + warp;       // (i * Hkv + h) * nblocks + b
@@ -293,11 +394,7 @@ __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int
   const int b = (int)(unit % nblocks), sh = (int)(unit / nblocks);
   const int i = sh / a.Hkv, h = sh % a.Hkv, blk = blk0 + b;
   uint8_t* im = img[warp];
-  for (int r = 0; r < kBlk; ++r) {
-    const int n = blk * kBlk + r - a.t0;
-    if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, im, i, h, n, lane);
-    else fp8_token<T>(a, im, i, h, n, lane);
-  }
+  for (int r = 0; r < kBlk; ++r) write_token<T, SCH>(a, im, i, h, blk * kBlk + r - a.t0, lane);
   __syncwarp();
   uint4* dst = reinterpret_cast<uint4*>(a.blocks + ((size_t)sh * a.nblk_max + blk) * kBytes);
   const uint4* src = reinterpret_cast<const uint4*>(im);
@@ -332,17 +429,31 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
   const __half sc16 = f16_sat_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
   const __half zr16 = f16_sat_rn(mn);
   const float sc = __half2float(sc16), zr = __half2float(zr16);
+  int codes[4];
+  Df rdf[4];
+  float err = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const int code = kivi_code(x[e], zr, sc);
+    codes[e] = code;
     int off, bit;
     kivi_v_pos(r, 4 * lane + e, off, bit);
     if (code) atomicOr(reinterpret_cast<unsigned int*>(bp + KiviLayout::VC + off), (unsigned int)code << bit);
+    // residual x - (zero + scale code): scale code is exact (at most 13 significant bits)
+    const float scc = __fmul_rn(sc, (float)code);
+    rdf[e] = residual_df(x[e], -zr, -scc, 0.f);
+    err = __fadd_ru(err, __fmul_ru(0x1p-46f, __fadd_ru(__fadd_ru(fabsf(x[e]), fabsf(zr)), fabsf(scc))));
   }
   if ((lane & 7) == 0) {
     __half* vp = reinterpret_cast<__half*>(bp + KiviLayout::VP) + (r * 4 + (lane >> 3)) * 2;
     vp[0] = sc16;
     vp[1] = zr16;
+  }
+  if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
+    double res[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - ((double)zr + (double)sc * (double)codes[e]);
+    store_rownorm(vwit_at(a, i, h, t), res, lane);
   }
 }
 
@@ -449,7 +560,7 @@ template <typename T>
 cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   const int warps = a.B * a.n_tok * a.Hkv;
   const dim3 blocks((warps * 32 + 127) / 128);
-  if (int8_layout(scheme) || scheme == kFp8) {
+  if (scheme != kKivi) {
     // whole blocks through shared-memory images, the rest token by token
     const int t_end = a.t0 + a.n_tok;
     const int lo_full = (a.t0 + kBlk - 1) / kBlk * kBlk, hi_full = t_end / kBlk * kBlk;
@@ -461,7 +572,8 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
       const dim3 g(((unsigned)(a.B * count * a.Hkv) * 32u + 127u) / 128u);
       return scheme == kInt8  ? launch_pdl(write_token_kernel<T, kInt8>, g, dim3(128), st, pdl, b)
              : scheme == kRtn ? launch_pdl(write_token_kernel<T, kRtn>, g, dim3(128), st, pdl, b)
-                              : launch_pdl(write_token_kernel<T, kFp8>, g, dim3(128), st, pdl, b);
+             : scheme == kFp8 ? launch_pdl(write_token_kernel<T, kFp8>, g, dim3(128), st, pdl, b)
+                              : launch_pdl(write_token_kernel<T, kBbox>, g, dim3(128), st, pdl, b);
     };
     if (hi_full <= lo_full) return tokens(0, a.n_tok);
     cudaError_t e = tokens(0, lo_full - a.t0);
@@ -470,7 +582,8 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
     const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + 3) / 4));
     e = scheme == kInt8  ? launch_pdl(write_block_kernel<T, kInt8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
         : scheme == kRtn ? launch_pdl(write_block_kernel<T, kRtn>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
-                         : launch_pdl(write_block_kernel<T, kFp8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
+        : scheme == kFp8 ? launch_pdl(write_block_kernel<T, kFp8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
+                         : launch_pdl(write_block_kernel<T, kBbox>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
     if (e != cudaSuccess) return e;
     return tokens(hi_full - a.t0, t_end - hi_full);
   }

@@ -25,14 +25,39 @@ def to_dev(x, w):
     return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(torch_dtype(w))
 
 
-def make_pair(w, scheme=None, n_splits=None, extra_tokens=None, gate_blocks=0):
+def make_pair(w, scheme=None, n_splits=None, extra_tokens=None, gate_blocks=0, v_witness=False):
     scheme = scheme or w.scheme
     cap = w.context + (w.steps if extra_tokens is None else extra_tokens)
     gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, cap, scheme, dtype=torch_dtype(w),
                    seed=w.seed, total_steps=w.steps, n_splits=w.n_splits if n_splits is None else n_splits,
-                   max_repair_blocks=gate_blocks)
-    ref = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, scheme, w.seed, w.steps)
+                   max_repair_blocks=gate_blocks, v_witness=v_witness)
+    ref = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, scheme, w.seed, w.steps, v_witness=v_witness)
     return gpu, ref
+
+
+def tensor_function(x, seed=0):
+    """A caller's quantize-dequantize function for the black-box scheme (test input): keep five
+    mantissa bits, and move 1% of the entries by a seeded N(0, 1) amount."""
+    x = np.asarray(x, np.float32)
+    m, e = np.frexp(x)
+    y = np.ldexp(np.trunc(m * 32.0) / 32.0, e).astype(np.float32)
+    rng = np.random.default_rng(seed)
+    mask = rng.random(x.shape) < 0.01
+    y[mask] += rng.standard_normal(int(mask.sum())).astype(np.float32)
+    return y
+
+
+def write_both(gpu, ref, layer, K, V, w, seed=0):
+    """Append K, V to both caches; the black-box scheme also gets f(K), f(V), and the oracle gets
+    exactly the values the device received."""
+    if ref.scheme != "blackbox":
+        gpu.witcert_write(layer, to_dev(K, w), to_dev(V, w))
+        ref.write(layer, K, V)
+        return
+    kh = to_dev(tensor_function(K, seed), w)
+    vh = to_dev(tensor_function(V, seed + 1), w)
+    gpu.witcert_write_hat(layer, to_dev(K, w), to_dev(V, w), kh, vh)
+    ref.write(layer, K, V, kh.float().cpu().numpy(), vh.float().cpu().numpy())
 
 
 def check_meter(gpu, ref, rel=METER_REL, what=""):
@@ -49,8 +74,14 @@ def check_meter(gpu, ref, rel=METER_REL, what=""):
 def check_write(gpu, ref, layer, scheme):
     """Codes and scales bit-exact; stored witness bit-exact and bracketing the float64 norm."""
     S = ref.length(layer)
-    kc = gpu.export(layer, _lib.X_K_CODES).cpu().numpy()
-    vc = gpu.export(layer, _lib.X_V_CODES).cpu().numpy()
+    if scheme == "blackbox":     # the stored bf16 values are the oracle's bf16(f(x)), bit for bit
+        kc = gpu.export(layer, _lib.X_K_CODES).float().cpu().numpy().astype(np.float64)
+        vc = gpu.export(layer, _lib.X_V_CODES).float().cpu().numpy().astype(np.float64)
+        np.testing.assert_array_equal(kc, ref.khat[layer])
+        np.testing.assert_array_equal(vc, ref.vhat[layer])
+    else:
+        kc = gpu.export(layer, _lib.X_K_CODES).cpu().numpy()
+        vc = gpu.export(layer, _lib.X_V_CODES).cpu().numpy()
     if scheme in ("int8_dither", "int8_rtn"):
         np.testing.assert_array_equal(kc.view(np.int8).astype(np.int16), ref.kcode[layer])
         np.testing.assert_array_equal(vc.view(np.int8).astype(np.int16), ref.vcode[layer])
@@ -61,7 +92,7 @@ def check_write(gpu, ref, layer, scheme):
     elif scheme == "fp8_e4m3":
         np.testing.assert_array_equal(kc.astype(np.int16), ref.kcode[layer])
         np.testing.assert_array_equal(vc.astype(np.int16), ref.vcode[layer])
-    else:
+    elif scheme == "kivi2":
         full = (S // 16) * 16
         np.testing.assert_array_equal(kc[:, :full].astype(np.int16), ref.kcode[layer][:, :full])
         np.testing.assert_array_equal(vc.astype(np.int16), ref.vcode[layer])
@@ -81,6 +112,12 @@ def check_write(gpu, ref, layer, scheme):
     assert np.all(wg >= w64)
     # above fp16's largest value the rounded-up witness is +inf
     assert np.all((wg <= np.maximum(w64 * (1 + 1e-3), w64 + 2.0 ** -24)) | (np.isinf(wg) & (w64 > 65504.0)))
+    if ref.v_witness:
+        wv = gpu.export(layer, _lib.X_V_WITNESS).cpu().numpy()
+        np.testing.assert_array_equal(wv.view(np.uint16), ref.wv16[layer].view(np.uint16))
+        wvg, wv64 = wv.astype(np.float64), ref.wv64[layer]
+        assert np.all(wvg >= wv64)
+        assert np.all((wvg <= np.maximum(wv64 * (1 + 1e-3), wv64 + 2.0 ** -24)) | (np.isinf(wvg) & (wv64 > 65504.0)))
     return w
 
 
@@ -88,6 +125,8 @@ def check_decode(gpu, ref, layer, q_host, w, delta_req, rel=METER_REL):
     """Decode both sides on the same query; the oracle uses the GPU's stored witness."""
     out, m = gpu.decode(layer, to_dev(q_host, w), delta_req)
     ref.w16[layer] = gpu.export(layer, _lib.X_WITNESS).cpu().numpy()
+    if ref.v_witness:
+        ref.wv16[layer] = gpu.export(layer, _lib.X_V_WITNESS).cpu().numpy()
     r = ref.decode(layer, q_host, delta_req)
     o = out.cpu().numpy().astype(np.float64)
     g = ref.g
@@ -103,6 +142,8 @@ def check_decode(gpu, ref, layer, q_host, w, delta_req, rel=METER_REL):
         check_meter(m["meter_b"].cpu().numpy(), r["meter_b"], rel, "meter_b")
     else:
         assert np.all(np.isnan(m["meter_b"].cpu().numpy()))
+    if ref.v_witness:
+        check_meter(m["meter_v"].cpu().numpy(), r["meter_v"], rel, "meter_v")
     return out, m, r
 
 

@@ -11,7 +11,8 @@ from oracle import meter
 from oracle.philox import dither
 from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload
 
-from gpu_helpers import check_decode, check_meter, check_write, make_pair, oracle_group, to_dev
+from gpu_helpers import (check_decode, check_meter, check_write, make_pair, oracle_group, tensor_function, to_dev,
+                         write_both)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,22 +50,82 @@ def test_tiny_write_and_metered_decode_with_appends(n_splits):
     assert st["int8_clamps"] == 0 and st["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
-def test_qwen_shaped_bf16_ragged(scheme):
+ALL_SCHEMES = ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn", "blackbox"]
+
+
+@pytest.mark.parametrize("v_witness", [False, True])
+@pytest.mark.parametrize("scheme", ALL_SCHEMES)
+def test_qwen_shaped_bf16_ragged(scheme, v_witness):
     """28q/4kv, bf16, planted keys and x50 outliers; 3 sequences (a partial sequence group),
-    1000 tokens (several splits and a ragged 8-token tail), two steps with an append."""
+    1000 tokens (several splits and a ragged 8-token tail), two steps with an append; with and
+    without value witnesses (value meter E_V)."""
     w = WORKLOADS["qwen_1l"].with_(batch=3, context=1000, steps=2, scheme=scheme)
-    gpu, ref = make_pair(w)
+    gpu, ref = make_pair(w, v_witness=v_witness)
     K, V = gen_kv(w, 0)
-    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
-    ref.write(0, K, V)
+    write_both(gpu, ref, 0, K, V, w)
     check_write(gpu, ref, 0, scheme)
     check_decode(gpu, ref, 0, gen_q(w, 0, 0), w, w.delta_req)
     k1, v1 = gen_append_kv(w, 0, 0)
-    gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
-    ref.write(0, k1, v1)
+    write_both(gpu, ref, 0, k1, v1, w, seed=5)
     check_write(gpu, ref, 0, scheme)
     check_decode(gpu, ref, 0, gen_q(w, 0, 1), w, 1e-3)
+
+
+@pytest.mark.parametrize("n_splits", [0, 3])
+def test_tiny_blackbox_fp32_with_appends_and_value_witness(n_splits):
+    """fp32 keys and function outputs (rounded to bf16 by the cache), sixteen single-token appends
+    across a block boundary, value witnesses on."""
+    w = WORKLOADS["tiny"].with_(scheme="blackbox", steps=16)
+    gpu, ref = make_pair(w, n_splits=n_splits, v_witness=True)
+    K, V = gen_kv(w, 0)
+    write_both(gpu, ref, 0, K, V, w)
+    check_write(gpu, ref, 0, "blackbox")
+    for step in range(w.steps):
+        k1, v1 = gen_append_kv(w, 0, step)
+        write_both(gpu, ref, 0, k1, v1, w, seed=100 + step)
+        if step % 4 == 3:
+            check_write(gpu, ref, 0, "blackbox")
+            check_decode(gpu, ref, 0, gen_q(w, 0, step), w, w.delta_req)
+    assert gpu.witcert_stats()["device_errors"] == 0
+
+
+def test_blackbox_identity_function_is_plain_attention():
+    """f = identity: zero witnesses and meters, and the output is softmax attention on the exact
+    bf16 keys and values."""
+    w = WORKLOADS["qwen_1l"].with_(batch=2, context=300, scheme="blackbox")
+    gpu, _ = make_pair(w, v_witness=True)
+    K, V = gen_kv(w, 0)
+    Kd, Vd = to_dev(K, w), to_dev(V, w)
+    gpu.witcert_write_hat(0, Kd, Vd, Kd, Vd)
+    q = gen_q(w, 0, 0)
+    out, m = gpu.decode(0, to_dev(q, w), w.delta_req)
+    assert torch.count_nonzero(gpu.export(0, _lib.X_WITNESS)) == 0
+    for k in ("meter_a", "raw_a", "meter_v"):
+        assert torch.count_nonzero(m[k]) == 0
+    o = out.cpu().numpy()
+    for i in range(2):
+        for j in range(w.n_q_heads):
+            _, _, ref = meter.attention(q[i, j:j + 1], K[i, :, j // w.group], V[i, :, j // w.group])
+            assert np.abs(o[i, j] - ref[0]).max() <= 2e-3 * np.abs(V[i, :, j // w.group]).max()
+
+
+def test_write_entry_points_match_the_scheme():
+    w = WORKLOADS["tiny"]
+    bb, _ = make_pair(w, scheme="blackbox")
+    K, V = gen_kv(w, 0)
+    with pytest.raises(wc.WitcertError) as e:
+        bb.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    assert e.value.status == _lib.EINVAL
+    i8, _ = make_pair(w)
+    with pytest.raises(wc.WitcertError) as e:
+        i8.witcert_write_hat(0, to_dev(K, w), to_dev(V, w), to_dev(K, w), to_dev(V, w))
+    assert e.value.status == _lib.EINVAL
+    i8.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float32, device="cuda")
+    mv = torch.empty((w.batch, w.n_q_heads), dtype=torch.float32, device="cuda")
+    with pytest.raises(wc.WitcertError) as e:     # no value witnesses in this cache
+        i8.witcert_decode(0, to_dev(gen_q(w, 0, 0), w), w.delta_req, out, meter_v=mv)
+    assert e.value.status == _lib.EINVAL
 
 
 @pytest.mark.parametrize("scheme", ["int8_dither", "kivi2"])
@@ -80,29 +141,28 @@ def test_more_split_ctas_than_the_gpu_holds(scheme):
     assert gpu.witcert_stats()["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
+@pytest.mark.parametrize("scheme", ALL_SCHEMES)
 def test_kivi_and_all_schemes_across_block_boundaries(scheme):
-    """Appends one token at a time across two 16-token boundaries (KIVI closes blocks)."""
+    """Appends one token at a time across two 16-token boundaries (KIVI closes blocks); value
+    witnesses on."""
     w = WORKLOADS["tiny"].with_(context=29, steps=20, scheme=scheme, batch=2)
-    gpu, ref = make_pair(w)
+    gpu, ref = make_pair(w, v_witness=True)
     K, V = gen_kv(w, 0)
-    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
-    ref.write(0, K, V)
+    write_both(gpu, ref, 0, K, V, w)
     for step in range(w.steps):
         k1, v1 = gen_append_kv(w, 0, step)
-        gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
-        ref.write(0, k1, v1)
+        write_both(gpu, ref, 0, k1, v1, w, seed=7 + step)
         if step % 5 == 4:
             check_write(gpu, ref, 0, scheme)
             check_decode(gpu, ref, 0, gen_q(w, 0, step), w, w.delta_req)
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
+@pytest.mark.parametrize("scheme", ALL_SCHEMES)
 def test_meter_off_output_is_bit_identical(scheme):
     w = WORKLOADS["qwen_1l"].with_(batch=5, context=700, scheme=scheme)
-    gpu, _ = make_pair(w)
+    gpu, ref = make_pair(w, v_witness=True)
     K, V = gen_kv(w, 0)
-    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
+    write_both(gpu, ref, 0, K, V, w)
     q = to_dev(gen_q(w, 0, 0), w)
     on, _ = gpu.decode(0, q, w.delta_req, meters=True)
     off, _ = gpu.decode(0, q, w.delta_req, meters=False)
@@ -136,14 +196,15 @@ def test_empty_layer_decodes_to_zero():
     assert torch.count_nonzero(m["meter_a"]) == 0 and torch.count_nonzero(m["meter_b"]) == 0
 
 
-def test_gate_decisions_bit_exact_and_repaired_decode():
-    """Raw-cast FP8: the oracle's gate, fed the GPU's block risks, picks exactly the blocks the
-    GPU pages in; the next decode matches the oracle on the repaired cache."""
-    w = WORKLOADS["qwen_1l"].with_(batch=2, context=400, steps=3, scheme="fp8_e4m3")
-    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32)
+@pytest.mark.parametrize("scheme,v_witness", [("fp8_e4m3", False), ("blackbox", True)])
+def test_gate_decisions_bit_exact_and_repaired_decode(scheme, v_witness):
+    """Raw-cast FP8 and the black-box store: the oracle's gate, fed the GPU's block risks, picks
+    exactly the blocks the GPU pages in; the next decode matches the oracle on the repaired cache
+    (value witnesses stay: the gate pages in keys only)."""
+    w = WORKLOADS["qwen_1l"].with_(batch=2, context=400, steps=3, scheme=scheme)
+    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32, v_witness=v_witness)
     K, V = gen_kv(w, 0)
-    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
-    ref.write(0, K, V)
+    write_both(gpu, ref, 0, K, V, w)
     for step, tau in enumerate((0.5, 0.2, 0.05)):
         q = gen_q(w, 0, step)
         check_decode(gpu, ref, 0, q, w, w.delta_req)
@@ -159,8 +220,7 @@ def test_gate_decisions_bit_exact_and_repaired_decode():
     assert st["bytes_paged_in"] == st["blocks_paged_in"] * 16 * 128 * 2
     # appends into a repaired partial block keep the exact pool row in step
     k1, v1 = gen_append_kv(w, 0, 0)
-    gpu.witcert_write(0, to_dev(k1, w), to_dev(v1, w))
-    ref.write(0, k1, v1)
+    write_both(gpu, ref, 0, k1, v1, w, seed=3)
     check_decode(gpu, ref, 0, gen_q(w, 0, 10), w, w.delta_req)
 
 
@@ -205,18 +265,22 @@ def test_errors_are_reported_not_raised_on_device():
     assert gpu.witcert_stats()["device_errors"] == 0
 
 
-@pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn"])
+@pytest.mark.parametrize("scheme", ALL_SCHEMES)
 def test_witness_fallback_on_extreme_keys(scheme):
     """Keys near 1e-20 and near 1e25 push the writers' fp32 double-float witness outside its
     safe range, so those bands take the fp64 computation; keys near 1e-9 give witnesses in
-    fp16's subnormal range.  Every stored witness must still equal the oracle's bit for bit."""
+    fp16's subnormal range.  Values scaled the same way do this to the value witnesses.  Every
+    stored witness must still equal the oracle's bit for bit."""
     w = WORKLOADS["tiny"].with_(scheme=scheme)
-    gpu, ref = make_pair(w)
     K, V = gen_kv(w, 0)
     K = K.copy()
     K[:, 0:5] *= 1e-20         # residuals far below 2^-45
     K[:, 5:9] *= 1e25          # residuals above 2^60
     K[:, 9:13] *= 1e-9         # witnesses below fp16's smallest normal
-    gpu.witcert_write(0, to_dev(K, w), to_dev(V, w))
-    ref.write(0, K, V)
+    V = V.copy()               # the same for the value witnesses
+    V[:, 0:5] *= 1e-20
+    V[:, 5:9] *= 1e25
+    V[:, 9:13] *= 1e-9
+    gpu, ref = make_pair(w, v_witness=True)
+    write_both(gpu, ref, 0, K, V, w)
     check_write(gpu, ref, 0, scheme)

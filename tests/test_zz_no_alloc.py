@@ -54,7 +54,7 @@ def test_noalloc_decode_matches_decode_on_two_calls(scheme):
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_array():
-    # 64 sequences x 32 query heads x 64 splits x 528 bytes = 69 MB > 16 MiB
+    # 64 sequences x 32 query heads x 64 splits x 544 bytes = 71 MB > 16 MiB
     cache = wc.Cache(1, 32, 4, 64, 64, "fp8_e4m3", dtype=torch.bfloat16, n_splits=64)
     q = torch.zeros((64, 32, 128), dtype=torch.bfloat16, device="cuda")
     out = torch.empty((64, 32, 128), dtype=torch.float32, device="cuda")
