@@ -66,7 +66,7 @@ typedef struct {
   int n_q_heads;           /* Hq (H in delta_loc) */
   int n_kv_heads;          /* Hkv; Hq must be a multiple, Hq/Hkv <= 8 */
   int head_dim;            /* must be 128 */
-  int batch;               /* sequences held by the cache (all share one length per layer) */
+  int batch;               /* sequences held by the cache; each has its own length per layer */
   int max_tokens;          /* capacity per sequence per layer */
   witcert_scheme scheme;   /* fixed for the cache's lifetime */
   witcert_dtype kv_dtype;  /* dtype of K, V and q passed to write/decode, and of the backing store */
@@ -139,12 +139,30 @@ witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, con
 witcert_status witcert_write_hat(witcert_cache* cache, int layer, const void* K, const void* V,
                                  const void* K_hat, const void* V_hat, int n_tok, void* stream);
 
+/* Ragged append (serving batches whose sequences have different lengths; the pages'
+ * implementation paragraph describes the write side per token and head, which this applies
+ * to each sequence at its own position).  n_tok: host [batch], entries >= 0 (0 leaves a
+ * sequence as it is).  K, V (and, for black-box caches, K_hat, V_hat; NULL otherwise) are
+ * device arrays of the appended tokens packed sequence by sequence: [sum n_tok][n_kv_heads]
+ * [128] of kv_dtype, sequence 0's tokens first.  Sequence i's tokens take positions
+ * len_i .. len_i + n_tok[i] - 1.  Once lengths differ the cache keeps per-sequence lengths on
+ * the device and every decode attends each sequence over its own length (Tier B's S is that
+ * length).  EINVAL if a sequence would exceed max_tokens (nothing is written then). */
+witcert_status witcert_write_ragged(witcert_cache* cache, int layer, const void* K, const void* V,
+                                    const void* K_hat, const void* V_hat, const int32_t* n_tok,
+                                    void* stream);
+
+/* Empty sequence `seq` in every layer so the slot can serve a new request (continuous
+ * batching).  Its repairs are dropped too (their slots in the exact-key pool are not
+ * reused).  Asynchronous on `stream`; decodes issued after it see the sequence empty. */
+witcert_status witcert_reset_sequence(witcert_cache* cache, int seq, void* stream);
+
 /* Fused metered split-KV decode [summary, implementation paragraph (output
  * and meter produced by one kernel reading the cache once, with the
  * certificate terms merged across KV splits by log-sum-exp); Theorem 2
  * (Tier A); Tier B paragraph; improvements list (TV aggregation)].
  * q: device [batch][n_q_heads][128] of kv_dtype, post-RoPE.  Query head j
- * reads KV head j / (Hq/Hkv).  Attends to all len tokens of `layer`.
+ * reads KV head j / (Hq/Hkv).  Each sequence attends to all its tokens of `layer`.
  * Outputs (device, caller-owned, float32):
  *   out     [batch][n_q_heads][128]  attention output
  *   meter_a [batch][n_q_heads]       min(1, (A^2-1)/2), A = sum_t p~_t exp(eps_t),
@@ -243,8 +261,11 @@ witcert_status witcert_set_profiling(witcert_cache* cache, int on);
  * predecessor's results.  Results are identical either way. */
 witcert_status witcert_set_launch_overlap(witcert_cache* cache, int on);
 
-/* Current length of `layer` (host, synchronous, no device work). */
+/* Length of `layer`'s longest sequence (host, synchronous, no device work). */
 witcert_status witcert_length(const witcert_cache* cache, int layer, int* len);
+
+/* Length of sequence `seq` in `layer` (host, synchronous, no device work). */
+witcert_status witcert_seq_length(const witcert_cache* cache, int layer, int seq, int* len);
 
 /* What witcert_export copies out (layouts below). */
 typedef enum {

@@ -60,6 +60,25 @@ class Cache:
         check(load().witcert_write_hat(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), K.shape[1],
                                        _stream_ptr(stream)), "witcert_write_hat")
 
+    def witcert_write_ragged(self, layer, K, V, n_tok, K_hat=None, V_hat=None, stream=None):
+        """Ragged append: n_tok[i] tokens to sequence i; K, V (and K_hat, V_hat for black-box
+        caches) packed sequence by sequence, [sum(n_tok), Hkv, 128]."""
+        counts = [int(x) for x in n_tok]
+        assert len(counts) == self.cfg.batch
+        for t in (K, V) + tuple(x for x in (K_hat, V_hat) if x is not None):
+            assert t.is_contiguous() and t.dtype == self.dtype and t.shape[0] == sum(counts)
+        arr = (ctypes.c_int32 * len(counts))(*counts)
+        check(load().witcert_write_ragged(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), arr,
+                                          _stream_ptr(stream)), "witcert_write_ragged")
+
+    def witcert_reset_sequence(self, seq, stream=None):
+        check(load().witcert_reset_sequence(self._h, int(seq), _stream_ptr(stream)), "witcert_reset_sequence")
+
+    def witcert_seq_length(self, layer, seq):
+        n = ctypes.c_int()
+        check(load().witcert_seq_length(self._h, layer, int(seq), ctypes.byref(n)), "witcert_seq_length")
+        return n.value
+
     def witcert_decode(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
                        meter_v=None, stream=None):
         assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32

@@ -47,6 +47,9 @@ SIGNATURES = {
     "witcert_destroy": [_vp],
     "witcert_write": [_vp, _int, _vp, _vp, _int, _vp],
     "witcert_write_hat": [_vp, _int, _vp, _vp, _vp, _vp, _int, _vp],
+    "witcert_write_ragged": [_vp, _int, _vp, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int32), _vp],
+    "witcert_reset_sequence": [_vp, _int, _vp],
+    "witcert_seq_length": [_vp, _int, _int, ctypes.POINTER(_int)],
     "witcert_decode": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_decode_noalloc": [_vp, _int, _vp, ctypes.c_double, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "witcert_decode_partial": [_vp, _int, _vp, ctypes.c_double, ctypes.c_longlong, _vp, _vp],

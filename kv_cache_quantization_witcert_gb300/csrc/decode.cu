@@ -88,10 +88,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   }
   if (RISK) {
     const int nblk = (p.S + kBlk - 1) / kBlk;
+    const int S_c = p.seq_len ? p.seq_len[cell / p.Hq] : p.S;      // this cell's sequence
+    const int nblk_c = (S_c + kBlk - 1) / kBlk;
     const float2* rr = p.risk_raw + (size_t)cell * p.nblk_max;
     float* ro = p.risk + (size_t)cell * p.nblk_max;
     for (int b = threadIdx.x; b < nblk; b += kMergeWarps * 32) {
-      const float2 v = rr[b];
+      const float2 v = b < nblk_c ? rr[b] : make_float2(0.f, 0.f);
       ro[b] = (v.y == 0.f || Zt == 0.f) ? 0.f : v.y * ex2(v.x - Mx) * inv;
     }
   }

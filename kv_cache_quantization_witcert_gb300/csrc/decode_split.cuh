@@ -240,6 +240,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     b_end = (int)(((long long)(split + 1) * nblk) / p.n_splits);
   }
   const int nb = b_end - b_begin;
+  // The warp's own sequence length (sequences of a ragged batch differ; the splits cut the
+  // longest one's blocks, so block b holds the same positions for every warp and the dither
+  // stays shared) and how many of the split's blocks the sequence has.  Every warp still
+  // walks all nb blocks for the dither hand-over.
+  __shared__ int s_len[NW];                        // read back once per block: keeps a register free
+  const int S_w = (p.seq_len && active) ? p.seq_len[i] : p.S;
+  const int nbw = min(nb, max(0, (S_w + kBlk - 1) / kBlk - b_begin));
+  if (lane == 0) s_len[warp] = S_w;
 
   constexpr int STB = SM::STB;
   uint8_t* ring = smem + SM::kRingOff + warp * NST * STB;
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // the first blocks' copies go out before anything else; blocks from p.dirty_blk on may
   // still be written by the immediately preceding kernel
   if (active && lane == 0) {
-    for (int s = 0; s < NST && s < nb; ++s) {
+    for (int s = 0; s < NST && s < nbw; ++s) {
       if (b_begin + s >= p.dirty_blk) pdl_wait();
       stage_copy(s, s);
     }
@@ -398,7 +406,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   const float lscale = kLog2e * 0x1.6a09e6p-4f;   // log2(e) / sqrt(128), 1/sqrt(128) to nearest
   // Tier B: u = kappa * sqrt(var).  var is summed with nearest rounding (4 terms) and the
   // SFU square root is within 2^-22 relative; this factor covers both.
-  const float kappa_up = p.kappa * (1.0f + 1.9073486328125e-6f);
+  float kappa = p.kappa;
+  if (METER && SCHEME == kInt8 && p.seq_len) {
+    // per sequence: sqrt(2 ln(2 S / delta_loc)) in fp64 (log and sqrt within a few units of
+    // 2^-53), raised by 2^-40 and rounded up to fp32
+    kappa = S_w > 0 ? __double2float_ru(sqrt(2.0 * (log((double)S_w) + p.log2dl)) * (1.0 + 0x1p-40)) : 0.f;
+  }
+  const float kappa_up = kappa * (1.0f + 1.9073486328125e-6f);
   float2 qgp[4];
 #pragma unroll
   for (int G = 0; G < 4; ++G) qgp[G] = make_float2(qg2[0][G], qg2[1][G]);
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     const bool gen_next = SCHEME == kInt8 && n + SM::XD < nb;
     if (gen_next && gen_early) produce(n + SM::XD);
 
-    if (active && !fault) {
+    if (active && !fault && n < nbw) {
       if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs) ||
           (SCHEME == kInt8 && !mbar_wait(smem_addr(&xfull[xs]), (uint32_t)((n / SM::NXI) & 1), kWaitLimitNs))) {
         fault = true;
@@ -423,12 +437,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
     }
     if (blk >= p.dirty_blk) pdl_wait();             // also covers the exact pool and KIVI tail rows
-    const bool live = active && !fault;
+    const bool live = active && !fault && n < nbw;
     const uint8_t* sb = ring + stage * STB;
     uint32_t P0 = 0u, P1 = 0u, P0l = 0u, P1l = 0u;
     if (live) {
       const int slot = GATE ? p.slots[seq_base + blk] : -1;
-      const bool ragged = (blk + 1) * kBlk > p.S;      // the context ends inside this block
+      const int S_blk = s_len[warp];
+      const bool ragged = (blk + 1) * kBlk > S_blk;    // the context ends inside this block
       const bool kivi_tail = SCHEME == kKivi && ragged;
       float2 lgA, lgB, epsA = f2(0.f), epsB = f2(0.f), ubA = f2(0.f), ubB = f2(0.f);
 
@@ -588,8 +603,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
       if (ragged) {   // tokens past the context: no weight, no meter term
         const int tok0 = blk * kBlk + g, tok1 = tok0 + 8;
-        if (tok0 >= p.S) { lgA = f2(-INFINITY); epsA = f2(0.f); ubA = f2(0.f); }
-        if (tok1 >= p.S) { lgB = f2(-INFINITY); epsB = f2(0.f); ubB = f2(0.f); }
+        if (tok0 >= S_blk) { lgA = f2(-INFINITY); epsA = f2(0.f); ubA = f2(0.f); }
+        if (tok1 >= S_blk) { lgB = f2(-INFINITY); epsB = f2(0.f); ubB = f2(0.f); }
       }
 
       // ------------------------------------------------------------ online softmax + meters
@@ -750,7 +765,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
       __syncwarp();
       // refill this stage with the block NST ahead
-      if (lane == 0 && n + NST < nb) {
+      if (lane == 0 && n + NST < nbw) {
         if (blk + NST >= p.dirty_blk) pdl_wait();
         fence_proxy_async();
         stage_copy(stage, n + NST);
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // Layers are decoded in order: the first blocks this warp will stream in the next layer go
   // to L2 now, so the next decode's pipeline fill overlaps this one's merge and the next write.
   if (p.next_blocks && active && !fault && lane == 0)
-    for (int s = 0; s < NST && s < nb; ++s)
+    for (int s = 0; s < NST && s < nbw; ++s)
       prefetch_l2(p.next_blocks + (seq_base + b_begin + s) * L::BYTES, L::BYTES);
   pdl_wait();     // partial results overwrite scratch the preceding merge may still read
   if (fault) {

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateArgs
   __shared__ int s_n, s_jmax;
   const int cell = blockIdx.x;                 // i * Hq + j
   const int i = cell / a.Hq, j = cell % a.Hq, h = j / a.grp;
-  const int nblk = (a.S + kBlk - 1) / kBlk;
+  const int nblk = ((a.seq_len ? a.seq_len[i] : a.S) + kBlk - 1) / kBlk;
   const float* risk = a.risk + (size_t)cell * a.nblk_max;
   const int32_t* slots = a.slots + ((size_t)i * a.Hkv + h) * a.nblk_max;
   if (threadIdx.x == 0) { s_n = 0; s_jmax = -1; }

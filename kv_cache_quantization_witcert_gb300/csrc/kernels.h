@@ -39,7 +39,9 @@ struct DecodeArgs {
   const float* kivi_tail;    // layer base (KIVI)
   const void* q;             // [B][Hq][128]
   int is_bf16;
-  int B, Hq, Hkv, grp, S, n_splits, seqs_per_cta;
+  int B, Hq, Hkv, grp, S, n_splits, seqs_per_cta;   // S: the longest sequence's length
+  const int* seq_len;        // [B] per-sequence lengths of a ragged batch (device), or null (all S)
+  double log2dl;             // ln(2 / delta_loc): Tier B's kappa per sequence when seq_len is set
   int dirty_blk;             // first block the immediately preceding kernel may write (INT_MAX: none)
   uint64_t seed;
   uint32_t rk0[10], rk1[10]; // Philox round keys of `seed` (key words advanced by the Weyl increments)
@@ -60,8 +62,29 @@ struct DecodeArgs {
   bool meter;
 };
 
+// Sequences of one ragged append launch, passed by value: sequence seq[k] appends the
+// off[k+1] - off[k] tokens that start at packed input row row0[k] (inputs [rows][Hkv][128]),
+// at positions t0[k], t0[k] + 1, ...; off is the launch's running token count.
+constexpr int kRaggedPerLaunch = 128;
+struct RaggedArgs {
+  int n_seq;
+  int seq[kRaggedPerLaunch], t0[kRaggedPerLaunch], row0[kRaggedPerLaunch], off[kRaggedPerLaunch + 1];
+};
+// New per-sequence lengths, up to kRaggedPerLaunch of them: dst[idx[k]] = len[k] (idx indexes
+// the [layer][sequence] array).
+struct LengthArgs {
+  int* dst;
+  int n;
+  int idx[kRaggedPerLaunch], len[kRaggedPerLaunch];
+};
+
 // pdl: launch with programmatic stream serialization (off right after an event wait).
 cudaError_t launch_write(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl);
+// Ragged appends of the sequences in g (KIVI: values and the key backing store only).
+cudaError_t launch_write_ragged(int scheme, const WriteArgs& a, const RaggedArgs& g, cudaStream_t st, bool pdl);
+cudaError_t launch_set_lengths(const LengthArgs& u, cudaStream_t st, bool pdl);
+// KIVI key blocks a (uniform) write completes, then its unfinished block's exact tail.
+cudaError_t launch_kivi_keys(const WriteArgs& a, cudaStream_t st, bool pdl);
 // Philox4x32-10 round keys of a 64-bit seed: key (seed mod 2^32, seed div 2^32) advanced
 // by 0x9E3779B9 / 0xBB67AE85 before every round but the first.
 void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]);
@@ -89,6 +112,7 @@ struct GateArgs {
   const void* backing;       // device-mapped pinned host, layer base
   void* pool;
   int nblk_max, B, Hq, Hkv, grp, S, backing_rows, pool_capacity, scheme, elem_bytes;
+  const int* seq_len;        // [B] per-sequence lengths (ragged batch), or null (all S)
   double d_star;
 };
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t st);

@@ -61,7 +61,12 @@ struct witcert_cache {
   unsigned long long* gstats = nullptr;   // [6]
   unsigned long long* clamps = nullptr;
   int* err = nullptr;
-  std::vector<int> len, risk_len;
+  int* dlen = nullptr;              // [L][B] per-sequence lengths on the device (ragged batches)
+  std::vector<int> len;             // per layer: the longest sequence
+  std::vector<std::vector<int>> slen;   // per layer and sequence
+  std::vector<uint64_t> write_gen, risk_gen;   // per layer: writes / resets so far; at the last metered decode
+  bool ragged = false;              // sequence lengths may differ: kernels read dlen
+  bool lengths_last = false;        // the most recent launch on the cache's stream set dlen
   std::vector<cudaEvent_t> gate_done;
   std::vector<char> gate_pending;
   cudaStream_t side = nullptr;
@@ -99,6 +104,7 @@ void free_all(witcert_cache* c) {
   if (c->backing_host) cudaFreeHost(c->backing_host);
   cudaFree(c->risk_raw); cudaFree(c->risk); cudaFree(c->part); cudaFree(c->selmask); cudaFree(c->todo);
   cudaFree(c->todo_count); cudaFree(c->pool_next); cudaFree(c->gstats); cudaFree(c->clamps); cudaFree(c->err);
+  cudaFree(c->dlen);
   for (auto e : c->gate_done) if (e) cudaEventDestroy(e);
   for (auto& p : c->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto& p : c->prof_free) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
@@ -168,7 +174,9 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   const int auto_max = auto_on > auto_off ? auto_on : auto_off;
   c->max_splits = f.n_splits > auto_max ? f.n_splits : auto_max;
   c->len.assign(f.n_layers, 0);
-  c->risk_len.assign(f.n_layers, -1);
+  c->slen.assign(f.n_layers, std::vector<int>(f.batch, 0));
+  c->write_gen.assign(f.n_layers, 0);
+  c->risk_gen.assign(f.n_layers, ~uint64_t(0));
   c->gate_done.assign(f.n_layers, nullptr);
   c->gate_pending.assign(f.n_layers, 0);
   const size_t L = f.n_layers, cells = (size_t)f.batch * f.n_q_heads;
@@ -181,6 +189,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   TRY(dalloc(&c->part, cells * c->max_splits * kPartStride * sizeof(float)), "allocating split scratch");
   TRY(dalloc(&c->clamps, sizeof(unsigned long long)), "allocating counters");
   TRY(dalloc(&c->err, sizeof(int)), "allocating the error word");
+  TRY(dalloc(&c->dlen, L * f.batch * sizeof(int)), "allocating sequence lengths");
   if (gate) {
     TRY(dalloc(&c->slots, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "allocating repair slots");
     TRY(cudaMemset(c->slots, 0xFF, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "clearing repair slots");
@@ -216,24 +225,15 @@ witcert_status witcert_destroy(witcert_cache* c) {
   return WITCERT_OK;
 }
 
-static witcert_status write_impl(witcert_cache* c, int layer, const void* K, const void* V, const void* Kh,
-                                 const void* Vh, int n_tok, void* stream) {
-  if (witcert_status s = check_layer(c, layer)) return s;
-  if (n_tok < 0) return fail(WITCERT_EINVAL, "n_tok must be >= 0");
-  if (n_tok > 0 && (!K || !V)) return fail(WITCERT_EINVAL, "K and V must not be NULL");
-  if (n_tok > 0 && c->scheme == kBbox && (!Kh || !Vh)) return fail(WITCERT_EINVAL, "K_hat and V_hat must not be NULL");
-  if ((long long)c->len[layer] + n_tok > c->cfg.max_tokens)
-    return fail(WITCERT_EINVAL, "layer %d would hold %lld tokens, capacity %d", layer,
-                (long long)c->len[layer] + n_tok, c->cfg.max_tokens);
-  if (n_tok == 0) { ok(); return WITCERT_OK; }
-  auto st = static_cast<cudaStream_t>(stream);
-  const bool waited = order_after_gate(c, layer, st);
+// Write arguments of `layer` for all sequences: appends of n_tok tokens at t0.
+static WriteArgs layer_write_args(const witcert_cache* c, int layer, const void* K, const void* V, const void* Kh,
+                                  const void* Vh, int n_tok, int t0) {
   WriteArgs a{};
   a.blocks = c->blocks + layer * c->layer_blocks;
   a.nblk_max = c->nblk_max;
   a.K = K; a.V = V; a.Kh = Kh; a.Vh = Vh;
   if (c->vwit) a.vwit = c->vwit + layer * vwit_layer(c);
-  a.B = c->cfg.batch; a.Hkv = c->cfg.n_kv_heads; a.n_tok = n_tok; a.t0 = c->len[layer]; a.layer = layer;
+  a.B = c->cfg.batch; a.Hkv = c->cfg.n_kv_heads; a.n_tok = n_tok; a.t0 = t0; a.layer = layer;
   a.backing_rows = (int)backing_rows(c);
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.seed = c->cfg.seed;
@@ -244,42 +244,220 @@ static witcert_status write_impl(witcert_cache* c, int layer, const void* K, con
   a.pool = c->pool;
   if (c->kivi_tail) a.kivi_tail = c->kivi_tail + layer * layer_rows(c) * kBlk * kD;
   a.clamps = c->clamps;
-  cudaError_t e = cudaSuccess;
-  bool pdl = c->overlap && !waited;
-  if (c->backing_host && n_tok >= kBulkBackingTokens) {
-    // bulk writes copy their exact keys to the pinned backing store with the copy engines,
-    // one strided copy per (sequence, KV head), instead of the kernels' stores over C2C
-    const size_t row = (size_t)kD * c->elem;
-    uint8_t* host = static_cast<uint8_t*>(c->backing_host) + layer * layer_rows(c) * backing_rows(c) * row;
-    for (int i = 0; i < a.B && e == cudaSuccess; ++i)
-      for (int h = 0; h < a.Hkv && e == cudaSuccess; ++h)
-        e = cudaMemcpy2DAsync(host + (((size_t)i * a.Hkv + h) * backing_rows(c) + a.t0) * row, row,
-                              static_cast<const uint8_t*>(K) + ((size_t)i * n_tok * a.Hkv + h) * row, a.Hkv * row,
-                              row, n_tok, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
-    a.backing = nullptr;
-    pdl = false;                     // the copies sit between this write and its predecessor
+  return a;
+}
+
+// The same arguments narrowed to sequence i alone (B = 1): its n tokens sit at packed input
+// row in_row (tokens, each n_kv_heads x 128 elements) and are appended at position t0.
+static WriteArgs seq_write_args(const witcert_cache* c, const WriteArgs& all, int i, size_t in_row, int n, int t0) {
+  WriteArgs a = all;
+  const size_t rows = (size_t)i * c->cfg.n_kv_heads;          // (sequence, KV head) rows before i
+  const size_t in_bytes = in_row * c->cfg.n_kv_heads * kD * c->elem;
+  a.blocks += rows * c->nblk_max * c->bblk;
+  if (a.vwit) a.vwit += rows * c->nblk_max * kBlk;
+  if (a.backing) a.backing = static_cast<uint8_t*>(a.backing) + rows * backing_rows(c) * kD * c->elem;
+  if (a.slots) a.slots += rows * c->nblk_max;
+  if (a.kivi_tail) a.kivi_tail += rows * kBlk * kD;
+  a.K = static_cast<const uint8_t*>(all.K) + in_bytes;
+  a.V = static_cast<const uint8_t*>(all.V) + in_bytes;
+  if (all.Kh) a.Kh = static_cast<const uint8_t*>(all.Kh) + in_bytes;
+  if (all.Vh) a.Vh = static_cast<const uint8_t*>(all.Vh) + in_bytes;
+  a.B = 1; a.n_tok = n; a.t0 = t0;
+  return a;
+}
+
+// Device copies of per-sequence lengths: entries (layer * batch + sequence, length), sent as
+// kernel parameters (no host buffer outlives the call).
+static cudaError_t push_lengths(witcert_cache* c, const std::vector<std::pair<int, int>>& upd, cudaStream_t st,
+                                bool& pdl) {
+  for (size_t k0 = 0; k0 < upd.size(); k0 += kRaggedPerLaunch) {
+    LengthArgs u{};
+    u.dst = c->dlen;
+    for (size_t k = k0; k < upd.size() && k < k0 + kRaggedPerLaunch; ++k) {
+      u.idx[u.n] = upd[k].first;
+      u.len[u.n] = upd[k].second;
+      ++u.n;
+    }
+    cudaError_t e = launch_set_lengths(u, st, pdl);
+    if (e != cudaSuccess) return e;
   }
-  e = launch_write(c->scheme, a, st, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "write launch");
+  return cudaSuccess;
+}
+
+// From now on the sequences' lengths may differ: the device gets every layer's lengths.
+static cudaError_t enter_ragged(witcert_cache* c, cudaStream_t st, bool& pdl) {
+  if (c->ragged) return cudaSuccess;
+  std::vector<std::pair<int, int>> upd;
+  for (int l = 0; l < c->cfg.n_layers; ++l)
+    for (int i = 0; i < c->cfg.batch; ++i) upd.emplace_back(l * c->cfg.batch + i, c->slen[l][i]);
+  cudaError_t e = push_lengths(c, upd, st, pdl);
+  if (e == cudaSuccess) c->ragged = true;
+  return e;
+}
+
+// Exact keys of n tokens of sequence i (packed input row in_row) to the pinned backing store
+// at position t0, one strided copy-engine transfer per KV head.
+static cudaError_t backing_copy(witcert_cache* c, int layer, const void* K, int i, size_t in_row, int n, int t0,
+                                cudaStream_t st) {
+  const size_t row = (size_t)kD * c->elem;
+  const int Hkv = c->cfg.n_kv_heads;
+  uint8_t* host = static_cast<uint8_t*>(c->backing_host) + layer * layer_rows(c) * backing_rows(c) * row;
+  cudaError_t e = cudaSuccess;
+  for (int h = 0; h < Hkv && e == cudaSuccess; ++h)
+    e = cudaMemcpy2DAsync(host + (((size_t)i * Hkv + h) * backing_rows(c) + t0) * row, row,
+                          static_cast<const uint8_t*>(K) + (in_row * Hkv + h) * row, Hkv * row, row, n,
+                          cudaMemcpyDeviceToHost, st);
+  return e;
+}
+
+// Appends counts[i] tokens (n_uniform each when counts is NULL) to every sequence of `layer`;
+// inputs are packed sequence-major.  Equal appends to equal lengths take the batched writers;
+// anything else marks the cache ragged and writes each sequence at its own position.
+static witcert_status write_impl(witcert_cache* c, int layer, const void* K, const void* V, const void* Kh,
+                                 const void* Vh, const int32_t* counts, int n_uniform, void* stream) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  const int B = c->cfg.batch;
+  std::vector<int> n(B, n_uniform);
+  long long total = 0;
+  for (int i = 0; i < B; ++i) {
+    if (counts) n[i] = counts[i];
+    if (n[i] < 0) return fail(WITCERT_EINVAL, "token counts must be >= 0 (sequence %d: %d)", i, n[i]);
+    if ((long long)c->slen[layer][i] + n[i] > c->cfg.max_tokens)
+      return fail(WITCERT_EINVAL, "layer %d sequence %d would hold %lld tokens, capacity %d", layer, i,
+                  (long long)c->slen[layer][i] + n[i], c->cfg.max_tokens);
+    total += n[i];
+  }
+  if (total > 0 && (!K || !V)) return fail(WITCERT_EINVAL, "K and V must not be NULL");
+  if (total > 0 && c->scheme == kBbox && (!Kh || !Vh)) return fail(WITCERT_EINVAL, "K_hat and V_hat must not be NULL");
+  if (total == 0) { ok(); return WITCERT_OK; }
+  bool uniform = !c->ragged;
+  for (int i = 1; i < B && uniform; ++i) uniform = n[i] == n[0];
+  auto st = static_cast<cudaStream_t>(stream);
+  const bool waited = order_after_gate(c, layer, st);
+  bool pdl = c->overlap && !waited;
+  cudaError_t e = cudaSuccess;
+  int first_blk = INT_MAX;
+  if (uniform) {
+    const int n_tok = n[0], t0 = c->len[layer];
+    WriteArgs a = layer_write_args(c, layer, K, V, Kh, Vh, n_tok, t0);
+    if (c->backing_host && n_tok >= kBulkBackingTokens) {
+      // bulk writes copy their exact keys to the pinned backing store with the copy engines
+      // instead of the kernels' stores over C2C
+      for (int i = 0; i < B && e == cudaSuccess; ++i) e = backing_copy(c, layer, K, i, (size_t)i * n_tok, n_tok, t0, st);
+      if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
+      a.backing = nullptr;
+      pdl = false;                     // the copies sit between this write and its predecessor
+    }
+    e = launch_write(c->scheme, a, st, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "write launch");
+    first_blk = t0 / kBlk;
+  } else {
+    if ((e = enter_ragged(c, st, pdl)) != cudaSuccess) return cuda_fail(e, "sequence lengths");
+    std::vector<std::pair<int, int>> upd;
+    for (int i = 0; i < B; ++i)
+      if (n[i] > 0) upd.emplace_back(layer * B + i, c->slen[layer][i] + n[i]);
+    if ((e = push_lengths(c, upd, st, pdl)) != cudaSuccess) return cuda_fail(e, "sequence lengths");
+    const WriteArgs all = layer_write_args(c, layer, K, V, Kh, Vh, 0, 0);
+    // long appends: the batched writers on that sequence alone; short ones: ragged launches
+    // of up to kRaggedPerLaunch sequences
+    RaggedArgs g{};
+    auto flush = [&]() -> cudaError_t {
+      if (g.n_seq == 0) return cudaSuccess;
+      cudaError_t r = launch_write_ragged(c->scheme, all, g, st, pdl);
+      // KIVI keys close per 16-token block: each sequence's blocks by its own launch
+      for (int k = 0; k < g.n_seq && r == cudaSuccess && c->scheme == kKivi; ++k)
+        r = launch_kivi_keys(seq_write_args(c, all, g.seq[k], (size_t)g.row0[k], g.off[k + 1] - g.off[k], g.t0[k]),
+                             st, pdl);
+      g = RaggedArgs{};
+      return r;
+    };
+    size_t row = 0;
+    for (int i = 0; i < B && e == cudaSuccess; ++i) {
+      if (n[i] == 0) continue;
+      const int t0 = c->slen[layer][i];
+      first_blk = t0 / kBlk < first_blk ? t0 / kBlk : first_blk;
+      if (n[i] >= kBlk) {
+        WriteArgs a = seq_write_args(c, all, i, row, n[i], t0);
+        if (c->backing_host && n[i] >= kBulkBackingTokens) {
+          e = backing_copy(c, layer, K, i, row, n[i], t0, st);
+          if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
+          a.backing = nullptr;
+          pdl = false;
+        }
+        e = launch_write(c->scheme, a, st, pdl);
+      } else {
+        g.seq[g.n_seq] = i;
+        g.t0[g.n_seq] = t0;
+        g.row0[g.n_seq] = (int)row;
+        g.off[g.n_seq + 1] = g.off[g.n_seq] + n[i];
+        if (++g.n_seq == kRaggedPerLaunch) e = flush();
+      }
+      row += n[i];
+    }
+    if (e == cudaSuccess) e = flush();
+    if (e != cudaSuccess) return cuda_fail(e, "ragged write launch");
+  }
   c->last_write_layer = layer;
-  c->last_write_blk = a.t0 / kBlk;
-  c->len[layer] += n_tok;
-  c->risk_len[layer] = -1;
-  c->tokens_written += (uint64_t)n_tok * layer_rows(c);
+  c->last_write_blk = first_blk;
+  c->lengths_last = false;
+  for (int i = 0; i < B; ++i) c->slen[layer][i] += n[i];
+  int mx = 0;
+  for (int i = 0; i < B; ++i) mx = c->slen[layer][i] > mx ? c->slen[layer][i] : mx;
+  c->len[layer] = mx;
+  ++c->write_gen[layer];
+  c->tokens_written += (uint64_t)total * c->cfg.n_kv_heads;
   ok();
   return WITCERT_OK;
 }
 
 witcert_status witcert_write(witcert_cache* c, int layer, const void* K, const void* V, int n_tok, void* stream) {
   if (c && c->scheme == kBbox) return fail(WITCERT_EINVAL, "a black-box cache is written with witcert_write_hat");
-  return write_impl(c, layer, K, V, nullptr, nullptr, n_tok, stream);
+  if (n_tok < 0) return fail(WITCERT_EINVAL, "n_tok must be >= 0");
+  return write_impl(c, layer, K, V, nullptr, nullptr, nullptr, n_tok, stream);
 }
 
 witcert_status witcert_write_hat(witcert_cache* c, int layer, const void* K, const void* V, const void* K_hat,
                                  const void* V_hat, int n_tok, void* stream) {
   if (c && c->scheme != kBbox) return fail(WITCERT_EINVAL, "witcert_write_hat needs a WITCERT_BLACKBOX cache");
-  return write_impl(c, layer, K, V, K_hat, V_hat, n_tok, stream);
+  if (n_tok < 0) return fail(WITCERT_EINVAL, "n_tok must be >= 0");
+  return write_impl(c, layer, K, V, K_hat, V_hat, nullptr, n_tok, stream);
+}
+
+witcert_status witcert_write_ragged(witcert_cache* c, int layer, const void* K, const void* V, const void* K_hat,
+                                    const void* V_hat, const int32_t* n_tok, void* stream) {
+  if (!c || !n_tok) return fail(WITCERT_EINVAL, "cache and n_tok must not be NULL");
+  if (c->scheme != kBbox && (K_hat || V_hat)) return fail(WITCERT_EINVAL, "K_hat and V_hat belong to black-box caches");
+  return write_impl(c, layer, K, V, K_hat, V_hat, n_tok, 0, stream);
+}
+
+witcert_status witcert_reset_sequence(witcert_cache* c, int seq, void* stream) {
+  if (!c) return fail(WITCERT_EINVAL, "cache is NULL");
+  if (seq < 0 || seq >= c->cfg.batch) return fail(WITCERT_EINVAL, "sequence %d out of range [0, %d)", seq, c->cfg.batch);
+  auto st = static_cast<cudaStream_t>(stream);
+  bool waited = false;
+  for (int l = 0; l < c->cfg.n_layers; ++l) waited |= order_after_gate(c, l, st);
+  bool pdl = c->overlap && !waited;
+  cudaError_t e = enter_ragged(c, st, pdl);
+  std::vector<std::pair<int, int>> upd;
+  for (int l = 0; l < c->cfg.n_layers; ++l) upd.emplace_back(l * c->cfg.batch + seq, 0);
+  if (e == cudaSuccess) e = push_lengths(c, upd, st, pdl);
+  // the sequence's repairs go with it (their pool slots are not reused)
+  const size_t rows = (size_t)c->cfg.n_kv_heads * c->nblk_max;
+  for (int l = 0; l < c->cfg.n_layers && e == cudaSuccess && c->slots; ++l)
+    e = cudaMemsetAsync(c->slots + (size_t)l * layer_rows(c) * c->nblk_max + (size_t)seq * rows, 0xFF,
+                        rows * sizeof(int32_t), st);
+  if (e != cudaSuccess) return cuda_fail(e, "reset");
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    c->slen[l][seq] = 0;
+    int mx = 0;
+    for (int i = 0; i < c->cfg.batch; ++i) mx = c->slen[l][i] > mx ? c->slen[l][i] : mx;
+    c->len[l] = mx;
+    ++c->write_gen[l];
+  }
+  c->last_write_layer = -1;
+  c->lengths_last = true;
+  ok();
+  return WITCERT_OK;
 }
 
 // Automatic split count for a decode of nblk blocks: sized by how many split-kernel CTAs of
@@ -311,6 +489,7 @@ static void fill_decode(witcert_cache* c, int layer, const void* q, double delta
   a.q = q;
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
+  if (c->ragged) a.seq_len = c->dlen + (size_t)layer * c->cfg.batch;
   a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits : auto_splits(c, nblk, meter, c->max_splits);
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
@@ -325,6 +504,7 @@ static void fill_decode(witcert_cache* c, int layer, const void* q, double delta
     kappa = (float)k;
     if ((double)kappa < k) kappa = std::nextafter(kappa, INFINITY);
   }
+  if (meter) a.log2dl = std::log(2.0 * (double)c->cfg.n_layers * c->cfg.n_q_heads * c->cfg.total_steps / delta_req);
   a.kappa = kappa;
   a.err = c->err;
   if (layer + 1 < c->cfg.n_layers && c->len[layer + 1] > 0) a.next_blocks = c->blocks + (layer + 1) * c->layer_blocks;
@@ -362,10 +542,12 @@ witcert_status witcert_decode(witcert_cache* c, int layer, const void* q, double
     pp = c->prof_free.back();
     c->prof_free.pop_back();
   }
-  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b, c->overlap && !waited);
+  // the split kernel reads the sequence lengths before it waits for its predecessor
+  cudaError_t e = launch_decode(c->scheme, a, c->sm_count, st, pp.a, pp.b, c->overlap && !waited && !c->lengths_last);
   if (pp.a) c->prof_pending.push_back(pp);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (gate && meter) c->risk_len[layer] = a.S;
+  c->lengths_last = false;
+  if (gate && meter) c->risk_gen[layer] = c->write_gen[layer];
   c->last_write_layer = -1;
   c->last_n_splits = a.n_splits;
   ++c->decode_calls;
@@ -401,9 +583,10 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
     a.risk = c->risk + (size_t)layer * a.B * a.Hq * c->nblk_max;
   }
   a.out = out; a.meter_a = meter_a; a.meter_b = meter_b; a.raw_a = raw_a; a.raw_b = raw_b; a.meter_v = meter_v;
-  e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited);
+  e = launch_decode(c->scheme, a, c->sm_count, st, nullptr, nullptr, c->overlap && !waited && !c->lengths_last);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (gate && meter) c->risk_len[layer] = a.S;
+  c->lengths_last = false;
+  if (gate && meter) c->risk_gen[layer] = c->write_gen[layer];
   c->last_write_layer = -1;
   ok();
   return WITCERT_OK;
@@ -416,6 +599,7 @@ witcert_status witcert_decode_partial(witcert_cache* c, int layer, const void* q
   if (!(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
   if (s_total < c->len[layer]) return fail(WITCERT_EINVAL, "s_total %lld is below the slice's own %d tokens",
                                            s_total, c->len[layer]);
+  if (c->ragged) return fail(WITCERT_ESTATE, "context-parallel shards hold equal-length sequences");
   auto st = static_cast<cudaStream_t>(stream);
   const bool waited = order_after_gate(c, layer, st);
   DecodeArgs a{};
@@ -453,7 +637,7 @@ witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream
   if (witcert_status s = check_layer(c, layer)) return s;
   if (c->cfg.max_repair_blocks <= 0) return fail(WITCERT_ESTATE, "the gate is disabled (max_repair_blocks = 0)");
   if (!(tau >= 0.f) || !std::isfinite(tau)) return fail(WITCERT_EINVAL, "tau must be finite and >= 0");
-  if (c->risk_len[layer] != c->len[layer] || c->len[layer] == 0)
+  if (c->risk_gen[layer] != c->write_gen[layer] || c->len[layer] == 0)
     return fail(WITCERT_ESTATE, "layer %d has no metered decode since its last write", layer);
   auto st = static_cast<cudaStream_t>(stream);
   cudaEvent_t ready = c->gate_done[layer];
@@ -472,6 +656,7 @@ witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream
   a.pool = c->pool;
   a.nblk_max = c->nblk_max; a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads;
   a.grp = a.Hq / a.Hkv; a.S = c->len[layer]; a.backing_rows = (int)backing_rows(c);
+  if (c->ragged) a.seq_len = c->dlen + (size_t)layer * c->cfg.batch;
   a.pool_capacity = c->cfg.max_repair_blocks; a.scheme = c->scheme; a.elem_bytes = c->elem;
   a.d_star = std::sqrt(1.0 + 2.0 * (double)tau) - 1.0;
   e = launch_gate(a, c->side);
@@ -552,6 +737,15 @@ witcert_status witcert_length(const witcert_cache* c, int layer, int* len) {
   if (witcert_status s = check_layer(c, layer)) return s;
   if (!len) return fail(WITCERT_EINVAL, "len is NULL");
   *len = c->len[layer];
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_seq_length(const witcert_cache* c, int layer, int seq, int* len) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (!len) return fail(WITCERT_EINVAL, "len is NULL");
+  if (seq < 0 || seq >= c->cfg.batch) return fail(WITCERT_EINVAL, "sequence %d out of range [0, %d)", seq, c->cfg.batch);
+  *len = c->slen[layer][seq];
   ok();
   return WITCERT_OK;
 }

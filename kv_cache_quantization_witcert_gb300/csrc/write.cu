@@ -201,12 +201,12 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
   return false;
 }
 
-// Token n of the write (position t = t0 + n, row r = t mod 16 of its block) of sequence i,
-// KV head h, quantized into the block image at bp (device memory or shared memory).
+// The token at position t (row r = t mod 16 of its block) of sequence i, KV head h, whose
+// input row starts at element `row` of K and V, quantized into the block image at bp (device
+// memory or shared memory).
 template <typename T, bool DITHER>
-__device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
-  const int t = a.t0 + n, r = t & 15;
-  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+__device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+  const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
   const int G = lane >> 3;
 #pragma unroll
@@ -272,12 +272,10 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
   }
 }
 
-// Token n of the write (position t = t0 + n, row r = t mod 16 of its block) of sequence i,
-// KV head h, quantized into the block image at bp (device memory or shared memory).
+// As int8_token, for the raw FP8 cast.
 template <typename T>
-__device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
-  const int t = a.t0 + n, r = t & 15;
-  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+__device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+  const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
 #pragma unroll
   for (int tensor = 0; tensor < 2; ++tensor) {
@@ -315,9 +313,8 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
 // Black-box scheme: the caller's K_hat, V_hat rows rounded to bfloat16 (nearest even) are the
 // store; the key witness (and the value witness) are taken against those stored values.
 template <typename T>
-__device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
-  const int t = a.t0 + n, r = t & 15;
-  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+__device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+  const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
 #pragma unroll
   for (int tensor = 0; tensor < 2; ++tensor) {
@@ -355,12 +352,18 @@ __device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int 
   }
 }
 
+// Input row (element offset into K, V) of token n of a write that appends n_tok tokens to
+// every sequence, sequence-major.
+__device__ __forceinline__ size_t uniform_row(const WriteArgs& a, int i, int n, int h) {
+  return (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+}
+
 // One token of a write into the block image at bp, by scheme.
 template <typename T, int SCH>
-__device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int i, int h, int n, int lane) {
-  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, n, lane);
-  else if constexpr (SCH == kFp8) fp8_token<T>(a, bp, i, h, n, lane);
-  else bbox_token<T>(a, bp, i, h, n, lane);
+__device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, t, row, lane);
+  else if constexpr (SCH == kFp8) fp8_token<T>(a, bp, i, h, t, row, lane);
+  else bbox_token<T>(a, bp, i, h, t, row, lane);
 }
 
 
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   const int blk = (a.t0 + n) >> 4;
   constexpr int kBytes = block_bytes(SCH);
   uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * kBytes;
-  write_token<T, SCH>(a, bp, i, h, n, lane);
+  write_token<T, SCH>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
 }
 
 // One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
@@ -394,7 +397,10 @@ __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int
   const int b = (int)(unit % nblocks), sh = (int)(unit / nblocks);
   const int i = sh / a.Hkv, h = sh % a.Hkv, blk = blk0 + b;
   uint8_t* im = img[warp];
-  for (int r = 0; r < kBlk; ++r) write_token<T, SCH>(a, im, i, h, blk * kBlk + r - a.t0, lane);
+  for (int r = 0; r < kBlk; ++r) {
+    const int t = blk * kBlk + r;
+    write_token<T, SCH>(a, im, i, h, t, uniform_row(a, i, t - a.t0, h), lane);
+  }
   __syncwarp();
   uint4* dst = reinterpret_cast<uint4*>(a.blocks + ((size_t)sh * a.nblk_max + blk) * kBytes);
   const uint4* src = reinterpret_cast<const uint4*>(im);
@@ -410,17 +416,11 @@ __device__ __forceinline__ int kivi_code(float x, float zr, float sc) {
 }
 __device__ __forceinline__ __half f16_sat_rn(float v) { return __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f)); }
 
-// KIVI values (per token, per 32-channel group) + backing store of keys.
+// KIVI values of one token (per 32-channel group) + backing store of its key; bp is the
+// token's block in device memory.
 template <typename T>
-__global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
-  pdl_wait();
-  pdl_trigger();
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (wid >= a.B * a.n_tok * a.Hkv) return;
-  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
-  const int t = a.t0 + n, blk = t >> 4, r = t & 15;
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * KiviLayout::BYTES;
-  const size_t row = (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
+__device__ __forceinline__ void kivi_v_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+  const int r = t & 15;
   exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
   float x[4];
   load4f<T>(reinterpret_cast<const T*>(a.V) + row + 4 * lane, x);
@@ -438,7 +438,11 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
     codes[e] = code;
     int off, bit;
     kivi_v_pos(r, 4 * lane + e, off, bit);
-    if (code) atomicOr(reinterpret_cast<unsigned int*>(bp + KiviLayout::VC + off), (unsigned int)code << bit);
+    // the word's other fields belong to other tokens and channels: clear this field (a
+    // sequence that was reset leaves old bits), then set it
+    unsigned int* word = reinterpret_cast<unsigned int*>(bp + KiviLayout::VC + off);
+    atomicAnd(word, ~(3u << bit));
+    if (code) atomicOr(word, (unsigned int)code << bit);
     // residual x - (zero + scale code): scale code is exact (at most 13 significant bits)
     const float scc = __fmul_rn(sc, (float)code);
     rdf[e] = residual_df(x[e], -zr, -scc, 0.f);
@@ -455,6 +459,48 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
     for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - ((double)zr + (double)sc * (double)codes[e]);
     store_rownorm(vwit_at(a, i, h, t), res, lane);
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= a.B * a.n_tok * a.Hkv) return;
+  const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
+  const int t = a.t0 + n;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * KiviLayout::BYTES;
+  kivi_v_token<T>(a, bp, i, h, t, uniform_row(a, i, n, h), lane);
+}
+
+// Ragged appends: sequence seq[k] (k < n_seq) gets its off[k+1] - off[k] tokens, packed from
+// input row row0[k] on, at positions t0[k], t0[k] + 1, ...  One warp per (token of the launch,
+// KV head); KIVI keys are handled per sequence by write_kivi_k_kernel.
+template <typename T, int SCH>
+__global__ void __launch_bounds__(128) write_ragged_kernel(const WriteArgs a, const RaggedArgs g) {
+  pdl_wait();
+  pdl_trigger();
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int total = g.off[g.n_seq];
+  if (wid >= total * a.Hkv) return;
+  const int h = wid % a.Hkv, tok = wid / a.Hkv;
+  int lo = 0, hi = g.n_seq - 1;                     // the k with off[k] <= tok < off[k + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (g.off[mid] <= tok) lo = mid; else hi = mid - 1;
+  }
+  const int i = g.seq[lo], t = g.t0[lo] + (tok - g.off[lo]);
+  const size_t row = ((size_t)(g.row0[lo] + (tok - g.off[lo])) * a.Hkv + h) * kD;
+  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * block_bytes(SCH);
+  if constexpr (SCH == kKivi) kivi_v_token<T>(a, bp, i, h, t, row, lane);
+  else write_token<T, SCH>(a, bp, i, h, t, row, lane);
+}
+
+// Per-sequence lengths on the device ([B] of one layer), set from the launch's parameters.
+__global__ void __launch_bounds__(128) set_lengths_kernel(const LengthArgs u) {
+  pdl_wait();
+  pdl_trigger();
+  for (int k = threadIdx.x; k < u.n; k += blockDim.x) u.dst[u.idx[k]] = u.len[k];
 }
 
 // KIVI keys: one warp per (sequence, KV head, block) this write touches.  Blocks the write
@@ -474,10 +520,13 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int
     const int blk = blk0 + blockIdx.y;
     const int lo = blk * kBlk;
     if (lo + kBlk > t_end) {   // unfinished block: keep the new keys exact in the tail
+      uint8_t* wreg = a.blocks + ((size_t)sh * a.nblk_max + blk) * KiviLayout::BYTES + KiviLayout::W;
       for (int t = (a.t0 > lo ? a.t0 : lo); t < t_end; ++t) {
         float x[4];
         load4f<T>(reinterpret_cast<const T*>(a.K) + (((size_t)i * a.n_tok + (t - a.t0)) * a.Hkv + h) * kD + 4 * lane, x);
         *reinterpret_cast<float4*>(tail + (t - lo) * kD + 4 * lane) = make_float4(x[0], x[1], x[2], x[3]);
+        // exact keys: zero witness (the row may hold a witness of a sequence that was reset)
+        if (lane < kBands) *reinterpret_cast<__half*>(wreg + wit_off(t - lo, lane)) = __float2half_rn(0.f);
       }
       __syncwarp();
       return;
@@ -556,6 +605,19 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t st, bool pd
   return cudaLaunchKernelEx(&cfg, kernel, a, extra...);
 }
 
+// KIVI keys of a write: the blocks it completes, then the unfinished one (if any).
+template <typename T>
+cudaError_t kivi_keys_t(const WriteArgs& a, cudaStream_t st, bool pdl) {
+  cudaError_t e = cudaSuccess;
+  const int t_end = a.t0 + a.n_tok, b0 = a.t0 / kBlk, nfull = t_end / kBlk - b0;
+  if (nfull > 0) {
+    e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, nfull), dim3(32), st, pdl, a, b0);
+    if (e != cudaSuccess) return e;
+  }
+  if (t_end % kBlk) e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, 1), dim3(32), st, pdl, a, t_end / kBlk);
+  return e;
+}
+
 template <typename T>
 cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) {
   const int warps = a.B * a.n_tok * a.Hkv;
@@ -589,17 +651,47 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
   }
   cudaError_t e = launch_pdl(write_kivi_v_kernel<T>, blocks, dim3(128), st, pdl, a);
   if (e != cudaSuccess) return e;
-  // blocks this write completes, then the unfinished one (if any)
-  const int t_end = a.t0 + a.n_tok, b0 = a.t0 / kBlk, nfull = t_end / kBlk - b0;
-  if (nfull > 0) {
-    e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, nfull), dim3(32), st, pdl, a, b0);
-    if (e != cudaSuccess) return e;
+  return kivi_keys_t<T>(a, st, pdl);
+}
+
+template <typename T>
+cudaError_t launch_ragged_t(int scheme, const WriteArgs& a, const RaggedArgs& g, cudaStream_t st, bool pdl) {
+  const int total = g.off[g.n_seq];
+  if (total == 0) return cudaSuccess;
+  const dim3 grid((unsigned)(((long long)total * a.Hkv * 32 + 127) / 128));
+  switch (scheme) {
+    case kInt8: return launch_pdl(write_ragged_kernel<T, kInt8>, grid, dim3(128), st, pdl, a, g);
+    case kRtn: return launch_pdl(write_ragged_kernel<T, kRtn>, grid, dim3(128), st, pdl, a, g);
+    case kFp8: return launch_pdl(write_ragged_kernel<T, kFp8>, grid, dim3(128), st, pdl, a, g);
+    case kKivi: return launch_pdl(write_ragged_kernel<T, kKivi>, grid, dim3(128), st, pdl, a, g);
+    default: return launch_pdl(write_ragged_kernel<T, kBbox>, grid, dim3(128), st, pdl, a, g);
   }
-  if (t_end % kBlk) e = launch_pdl(write_kivi_k_kernel<T>, dim3(a.B * a.Hkv, 1), dim3(32), st, pdl, a, t_end / kBlk);
-  return e;
 }
 
 }  // namespace
+
+cudaError_t launch_write_ragged(int scheme, const WriteArgs& a, const RaggedArgs& g, cudaStream_t st, bool pdl) {
+  return a.is_bf16 ? launch_ragged_t<__nv_bfloat16>(scheme, a, g, st, pdl) : launch_ragged_t<float>(scheme, a, g, st, pdl);
+}
+
+cudaError_t launch_kivi_keys(const WriteArgs& a, cudaStream_t st, bool pdl) {
+  if (a.B * a.n_tok * a.Hkv == 0) return cudaSuccess;
+  return a.is_bf16 ? kivi_keys_t<__nv_bfloat16>(a, st, pdl) : kivi_keys_t<float>(a, st, pdl);
+}
+
+cudaError_t launch_set_lengths(const LengthArgs& u, cudaStream_t st, bool pdl) {
+  if (u.n <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(128);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, set_lengths_kernel, u);
+}
 
 void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]) {
   uint32_t k0 = (uint32_t)(seed & 0xFFFFFFFFull), k1 = (uint32_t)(seed >> 32);

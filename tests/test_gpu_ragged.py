@@ -1,0 +1,212 @@
+"""Ragged batches on the GPU: sequences of different lengths in one cache.
+
+Each sequence of the GPU cache is checked against its own single-sequence oracle
+cache (the oracle of one sequence is the plain definition: its tokens, its
+positions, its length as S in Tier B).  Covers a ragged prefill (an empty
+sequence, a ragged tail, lengths spanning several splits), ragged appends with
+some sequences idle, a sequence reset and refill (continuous batching), the gate
+on ragged lengths, and every scheme with value witnesses on.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kv_cache_quantization_witcert_gb300 as wc
+from kv_cache_quantization_witcert_gb300 import _lib
+from oracle import OracleCache
+from workload import WORKLOADS, gen_kv, gen_q
+
+from gpu_helpers import METER_REL, check_meter, tensor_function, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+ALL_SCHEMES = ["int8_dither", "fp8_e4m3", "kivi2", "int8_rtn", "blackbox"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    wc.load()
+
+
+class Ragged:
+    """A GPU cache of B sequences and one oracle cache per sequence."""
+
+    def __init__(self, w, scheme, cap, v_witness=True, gate_blocks=0, n_splits=0):
+        self.w, self.scheme, self.B = w, scheme, w.batch
+        self.gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, cap, scheme, dtype=torch_dtype(w),
+                            seed=w.seed, total_steps=w.steps, max_repair_blocks=gate_blocks, v_witness=v_witness,
+                            n_splits=n_splits)
+        self.refs = [OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps,
+                                 v_witness=v_witness) for _ in range(w.batch)]
+        self.fseed = 0
+
+    def dev(self, x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(torch_dtype(self.w))
+
+    def write(self, layer, parts):
+        """parts[i]: (K_i, V_i) of shape [n_i, Hkv, d] (n_i may be 0)."""
+        counts = [p[0].shape[0] for p in parts]
+        K = np.concatenate([p[0] for p in parts], 0)
+        V = np.concatenate([p[1] for p in parts], 0)
+        Kd, Vd = self.dev(K), self.dev(V)
+        if self.scheme == "blackbox":
+            self.fseed += 2
+            Kh, Vh = self.dev(tensor_function(K, self.fseed)), self.dev(tensor_function(V, self.fseed + 1))
+            self.gpu.witcert_write_ragged(layer, Kd, Vd, counts, Kh, Vh)
+            Kh, Vh = Kh.float().cpu().numpy(), Vh.float().cpu().numpy()
+        else:
+            self.gpu.witcert_write_ragged(layer, Kd, Vd, counts)
+        row = 0
+        for i, n in enumerate(counts):
+            if n:
+                sl = slice(row, row + n)
+                if self.scheme == "blackbox":
+                    self.refs[i].write(layer, K[None, sl], V[None, sl], Kh[None, sl], Vh[None, sl])
+                else:
+                    self.refs[i].write(layer, K[None, sl], V[None, sl])
+            row += n
+        for i in range(self.B):
+            assert self.gpu.witcert_seq_length(layer, i) == self.refs[i].length(layer)
+
+    def check_store(self, layer):
+        """Stored witnesses (and value witnesses) of every sequence's own rows, bit for bit."""
+        w16 = self.gpu.export(layer, _lib.X_WITNESS).cpu().numpy()
+        wv = self.gpu.export(layer, _lib.X_V_WITNESS).cpu().numpy() if self.gpu.v_witness else None
+        for i, ref in enumerate(self.refs):
+            S = ref.length(layer)
+            np.testing.assert_array_equal(w16[i, :S].view(np.uint16), ref.w16[layer][0].view(np.uint16))
+            if wv is not None:
+                np.testing.assert_array_equal(wv[i, :S].view(np.uint16), ref.wv16[layer][0].view(np.uint16))
+
+    def check_decode(self, layer, q, delta_req):
+        out, m = self.gpu.decode(layer, self.dev(q), delta_req)
+        o = out.cpu().numpy()
+        mm = {k: v.cpu().numpy() for k, v in m.items()}
+        w16 = self.gpu.export(layer, _lib.X_WITNESS).cpu().numpy()
+        risks = []
+        for i, ref in enumerate(self.refs):
+            S = ref.length(layer)
+            ref.w16[layer] = w16[i:i + 1, :S]
+            r = ref.decode(layer, q[i:i + 1], delta_req)
+            vmax = np.abs(ref.v[layer]).max() if S else 1.0
+            assert np.abs(o[i] - r["out"][0]).max() <= 2e-3 * vmax, f"sequence {i} (S={S})"
+            check_meter(mm["raw_a"][i], r["raw_a"][0], METER_REL, f"raw_a seq {i}")
+            if self.scheme == "int8_dither":
+                check_meter(mm["raw_b"][i], r["raw_b"][0], METER_REL, f"raw_b seq {i}")
+            if self.gpu.v_witness:
+                check_meter(mm["meter_v"][i], r["meter_v"][0], METER_REL, f"meter_v seq {i}")
+            if S == 0:
+                assert not np.any(o[i]) and mm["raw_a"][i].max() == 0
+            risks.append(r["risk"][0])
+        return out, mm, risks
+
+
+def _split(arr, lens, start=None):
+    """Per-sequence slices [n_i, Hkv, d] of arr [B, S, Hkv, d], from start[i] (0) on."""
+    start = start or [0] * len(lens)
+    return [arr[i, start[i]:start[i] + n] for i, n in enumerate(lens)]
+
+
+@pytest.mark.parametrize("scheme", ALL_SCHEMES)
+def test_ragged_prefill_appends_and_reset(scheme):
+    """Four sequences of lengths 0 / 37 / 300 / 1000 (an empty one, ragged tails, several
+    splits), then appends of 1 / 0 / 3 / 1 tokens, then sequence 2 reset and refilled."""
+    w = WORKLOADS["qwen_1l"].with_(batch=4, context=1000, steps=3, scheme=scheme)
+    rg = Ragged(w, scheme, cap=1100)
+    K, V = gen_kv(w, 0)
+    lens = [0, 37, 300, 1000]
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    rg.check_store(0)
+    rg.check_decode(0, gen_q(w, 0, 0), w.delta_req)
+    K2, V2 = gen_kv(w.with_(context=16), 5)
+    app = [1, 0, 3, 1]
+    rg.write(0, list(zip(_split(K2, app), _split(V2, app))))
+    rg.check_store(0)
+    rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
+    rg.gpu.witcert_reset_sequence(2)
+    rg.refs[2] = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps, v_witness=True)
+    assert rg.gpu.witcert_seq_length(0, 2) == 0
+    rg.check_decode(0, gen_q(w, 0, 2), w.delta_req)
+    K3, V3 = gen_kv(w.with_(context=64), 6)
+    refill = [0, 0, 50, 0]
+    rg.write(0, list(zip(_split(K3, refill), _split(V3, refill))))
+    rg.check_store(0)
+    rg.check_decode(0, gen_q(w, 0, 2), 1e-3)
+    assert rg.gpu.witcert_stats()["device_errors"] == 0
+
+
+def test_ragged_single_token_appends_cross_block_boundaries():
+    """Tiny fp32 INT8-dither, three sequences at different offsets inside a block, 20 rounds
+    of single-token appends to a changing subset (KIVI-free path of the ragged kernel and the
+    dither of each sequence's own positions)."""
+    w = WORKLOADS["tiny"].with_(batch=3, context=40, steps=20)
+    rg = Ragged(w, "int8_dither", cap=80, n_splits=3)
+    K, V = gen_kv(w, 0)
+    lens = [5, 16, 29]
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    Ka, Va = gen_kv(w.with_(context=40), 3)
+    pos = [0, 0, 0]
+    for step in range(20):
+        app = [1 if (step + i) % (i + 1) == 0 else 0 for i in range(3)]
+        rg.write(0, list(zip(_split(Ka, app, pos), _split(Va, app, pos))))
+        pos = [p + a for p, a in zip(pos, app)]
+        if step % 5 == 4:
+            rg.check_store(0)
+            rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
+
+
+def test_ragged_kivi_appends_close_blocks_per_sequence():
+    w = WORKLOADS["tiny"].with_(batch=3, context=40, steps=20, scheme="kivi2")
+    rg = Ragged(w, "kivi2", cap=80)
+    K, V = gen_kv(w, 0)
+    lens = [14, 15, 31]
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    Ka, Va = gen_kv(w.with_(context=40), 3)
+    pos = [0, 0, 0]
+    for step in range(6):
+        app = [2, 1, 3]
+        rg.write(0, list(zip(_split(Ka, app, pos), _split(Va, app, pos))))
+        pos = [p + a for p, a in zip(pos, app)]
+        rg.check_store(0)
+        rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
+
+
+def test_ragged_gate_decisions_match_each_sequence():
+    """FP8 with the gate on ragged lengths: each sequence's block risks (its own blocks; the
+    GPU's rows past its length are zero) drive that sequence's oracle gate, and the GPU pages in
+    exactly those blocks."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=500, steps=3, scheme="fp8_e4m3")
+    rg = Ragged(w, "fp8_e4m3", cap=520, v_witness=False, gate_blocks=3 * 4 * 40)
+    K, V = gen_kv(w, 0)
+    lens = [500, 130, 257]
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    for step, tau in enumerate((0.5, 0.1)):
+        rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
+        risk = rg.gpu.export(0, _lib.X_BLOCK_RISK).cpu().numpy()
+        rg.gpu.witcert_gate(0, tau)
+        slots = rg.gpu.export(0, _lib.X_SLOTS).cpu().numpy()
+        for i, ref in enumerate(rg.refs):
+            nblk = (lens[i] + 15) // 16
+            assert not np.any(risk[i, :, nblk:])
+            ref.gate(0, tau, risk[i:i + 1, :, :nblk])
+            np.testing.assert_array_equal(slots[i, :, :nblk] >= 0, ref.repaired[0][0])
+            assert not np.any(slots[i, :, nblk:] >= 0)
+    rg.check_decode(0, gen_q(w, 0, 7), w.delta_req)
+    assert rg.gpu.witcert_gate_stats()["blocks_paged_in"] > 0
+
+
+def test_ragged_rejects_overflow_and_partial_decode():
+    w = WORKLOADS["tiny"].with_(batch=2)
+    rg = Ragged(w, "int8_dither", cap=40)
+    K, V = gen_kv(w, 0)
+    with pytest.raises(wc.WitcertError) as e:
+        rg.gpu.witcert_write_ragged(0, rg.dev(K[0, :41]), rg.dev(V[0, :41]), [41, 0])
+    assert e.value.status == _lib.EINVAL
+    assert rg.gpu.witcert_seq_length(0, 0) == 0
+    rg.write(0, [(K[0, :10], V[0, :10]), (K[1, :3], V[1, :3])])
+    with pytest.raises(wc.WitcertError) as e:
+        rg.gpu.decode_partial(0, rg.dev(gen_q(w, 0, 0)), w.delta_req, 10)
+    assert e.value.status == _lib.ESTATE
