@@ -83,6 +83,13 @@ typedef struct {
                               E_V = sum_t p~_t wv_t, which bounds || sum_t p~_t (v_t - v^_t) || by the
                               triangle inequality.  The pages define no value-side bound: this is the
                               value counterpart of the key witness, a reading of this library. */
+  int max_pages;           /* > 0: paged block store.  Each layer holds a pool of max_pages pages, a page
+                              being one 16-token block of every KV head of one sequence; a per-sequence
+                              page table (shared by the layers) maps a sequence's blocks to pages, taken
+                              as writes reach new blocks and given back by witcert_reset_sequence, so
+                              sequences of different lengths share the pool instead of each reserving
+                              max_tokens.  max_tokens stays the per-sequence cap.  bf16 caches only.
+                              0: every sequence owns max_tokens of contiguous blocks. */
 } witcert_config;
 
 typedef struct witcert_cache witcert_cache;
@@ -104,6 +111,7 @@ typedef struct {
   double decode_kernel_ms;    /* summed split-kernel time while profiling is on */
   uint64_t decode_kernel_launches;
   int last_n_splits;          /* KV splits used by the most recent decode */
+  uint64_t pages_used;        /* paged store: pages held by sequences (0 for a contiguous store) */
 } witcert_stats_t;
 
 /* Create a cache.  Allocates the compressed store, the witness store, the
@@ -147,7 +155,8 @@ witcert_status witcert_write_hat(witcert_cache* cache, int layer, const void* K,
  * [128] of kv_dtype, sequence 0's tokens first.  Sequence i's tokens take positions
  * len_i .. len_i + n_tok[i] - 1.  Once lengths differ the cache keeps per-sequence lengths on
  * the device and every decode attends each sequence over its own length (Tier B's S is that
- * length).  EINVAL if a sequence would exceed max_tokens (nothing is written then). */
+ * length).  EINVAL if a sequence would exceed max_tokens, ENOMEM if a paged cache's pool has
+ * no page left for a new block (nothing is written either way). */
 witcert_status witcert_write_ragged(witcert_cache* cache, int layer, const void* K, const void* V,
                                     const void* K_hat, const void* V_hat, const int32_t* n_tok,
                                     void* stream);

@@ -34,13 +34,13 @@ class Cache:
 
     def __init__(self, n_layers, n_q_heads, n_kv_heads, batch, max_tokens, scheme="int8_dither",
                  dtype=torch.bfloat16, seed=0, total_steps=1, n_splits=0, max_repair_blocks=0, pos_offset=0,
-                 v_witness=False):
+                 v_witness=False, max_pages=0):
         lib = load()
         self.dtype = dtype
         self.cfg = _lib.witcert_config(n_layers, n_q_heads, n_kv_heads, 128, batch, max_tokens,
                                        SCHEMES[scheme] if isinstance(scheme, str) else scheme,
                                        BF16 if dtype == torch.bfloat16 else F32, seed, total_steps, n_splits,
-                                       max_repair_blocks, pos_offset, int(bool(v_witness)))
+                                       max_repair_blocks, pos_offset, int(bool(v_witness)), max_pages)
         self.scheme = scheme
         self.v_witness = bool(v_witness)
         h = ctypes.c_void_p()

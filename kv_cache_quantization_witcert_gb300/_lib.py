@@ -24,7 +24,7 @@ class witcert_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("batch", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("scheme", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("seed", ctypes.c_uint64),
                 ("total_steps", ctypes.c_int), ("n_splits", ctypes.c_int), ("max_repair_blocks", ctypes.c_int),
-                ("pos_offset", ctypes.c_int), ("v_witness", ctypes.c_int)]
+                ("pos_offset", ctypes.c_int), ("v_witness", ctypes.c_int), ("max_pages", ctypes.c_int)]
 
 
 class witcert_gate_counters(ctypes.Structure):
@@ -36,7 +36,7 @@ class witcert_stats_t(ctypes.Structure):
     _fields_ = [("tokens_written", ctypes.c_uint64), ("decode_calls", ctypes.c_uint64),
                 ("int8_clamps", ctypes.c_uint64), ("device_errors", ctypes.c_uint64),
                 ("decode_kernel_ms", ctypes.c_double), ("decode_kernel_launches", ctypes.c_uint64),
-                ("last_n_splits", ctypes.c_int)]
+                ("last_n_splits", ctypes.c_int), ("pages_used", ctypes.c_uint64)]
 
 
 _vp, _int, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t

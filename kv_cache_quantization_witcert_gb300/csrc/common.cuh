@@ -10,7 +10,8 @@
 //   BLACKBOX    (8704 B = 16 x 544):  K_hat bf16 4096 | V_hat bf16 4096 | witness 512
 //
 // With the value witness on, a separate array holds one fp16 norm per token:
-// 32 bytes per block, [B][Hkv][nblk_max][16] per layer.
+// 32 bytes per block, [B][Hkv][nblk_max][16] per layer.  A paged cache keeps the blocks
+// in a pool of pages instead (see block_index); every other array stays per sequence.
 //
 // Codes are stored in "fragment order": the byte a lane of a warp needs for
 // the A operand of mma.m16n8k16 sits where one 16-byte shared-memory load per
@@ -49,6 +50,13 @@ __host__ __device__ constexpr int block_bytes(int scheme) {
 }
 __host__ __device__ constexpr int witness_off(int scheme) {
   return int8_layout(scheme) ? Int8Layout::W : scheme == kFp8 ? Fp8Layout::W : scheme == kKivi ? KiviLayout::W : BboxLayout::W;
+}
+
+// Index of block b of (sequence i, KV head h) in a layer's block store: [B][Hkv][nblk_max]
+// blocks in a contiguous store, or page table[i][b] of a paged store ([pages][Hkv] blocks;
+// a page holds one 16-token block of every KV head of one sequence).
+__host__ __device__ inline size_t block_index(const int32_t* table, int Hkv, int nblk_max, int i, int h, int b) {
+  return table ? (size_t)table[(size_t)i * nblk_max + b] * Hkv + h : ((size_t)i * Hkv + h) * nblk_max + b;
 }
 
 // ------------------------------------------------------------------ fragment-order index maps

@@ -216,7 +216,7 @@ __device__ __forceinline__ void exact_block_logits(const KT* ex, const uint32_t 
   }
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW, int NW>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW, bool PAGED, int NW>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_kernel(const DecodeArgs p) {
   using L = Lay<SCHEME>;
   using SM = Smem<NW, SCHEME>;
@@ -258,10 +258,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
   const size_t seq_base = active ? ((size_t)(i * p.Hkv + h) * p.nblk_max) : 0;
   const uint8_t* src = p.blocks + (seq_base + b_begin) * L::BYTES;
+  // block m of the split: consecutive in a contiguous store, looked up in the page table of a
+  // paged one (the same pages serve every layer)
+  auto block_src = [&](const uint8_t* base, int m) -> const uint8_t* {
+    if constexpr (PAGED) return base + ((size_t)p.table[(size_t)i * p.nblk_max + b_begin + m] * p.Hkv + h) * L::BYTES;
+    else return base + (seq_base + b_begin + m) * L::BYTES;
+  };
   // one stage: the block and (value witnesses on) its 32 bytes of value witnesses
   auto stage_copy = [&](int s, int m) {
     mbar_expect_tx(smem_addr(&bars[s]), L::BYTES + (VW ? kVwBytes : 0));
-    bulk_g2s(smem_addr(ring + s * STB), src + (size_t)m * L::BYTES, L::BYTES, smem_addr(&bars[s]));
+    bulk_g2s(smem_addr(ring + s * STB), PAGED ? block_src(p.blocks, m) : src + (size_t)m * L::BYTES, L::BYTES,
+             smem_addr(&bars[s]));
     if (VW)
       bulk_g2s(smem_addr(ring + s * STB + L::BYTES), p.vwit + (seq_base + b_begin + m) * kBlk, kVwBytes,
                smem_addr(&bars[s]));
@@ -780,8 +787,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // Layers are decoded in order: the first blocks this warp will stream in the next layer go
   // to L2 now, so the next decode's pipeline fill overlaps this one's merge and the next write.
   if (p.next_blocks && active && !fault && lane == 0)
-    for (int s = 0; s < NST && s < nbw; ++s)
-      prefetch_l2(p.next_blocks + (seq_base + b_begin + s) * L::BYTES, L::BYTES);
+    for (int s = 0; s < NST && s < nbw; ++s) prefetch_l2(block_src(p.next_blocks, s), L::BYTES);
   pdl_wait();     // partial results overwrite scratch the preceding merge may still read
   if (fault) {
     // drain copies still in flight before the CTA's shared memory is released
@@ -866,12 +872,12 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done) {
 }
 
 // Launches the split kernel, or (occ != nullptr) reports how many of its CTAs fit on an SM.
-template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW, int NW>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW, bool PAGED, int NW>
 cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
   using SM = Smem<NW, SCHEME>;
   static std::atomic<uint64_t> smem_done{0};
   static std::atomic<int> resident{0};
-  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, GATE, VW, NW>;
+  auto k = decode_split_kernel<SCHEME, QT, METER, RISK, GATE, VW, PAGED, NW>;
   cudaError_t e = allow_smem(k, SM::kBytes, smem_done);
   if (e != cudaSuccess) return e;
   if (occ) {
@@ -887,32 +893,40 @@ cudaError_t run_split(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl,
   return launch_pdl(k, grid, dim3(NW * 32), SM::kBytes, st, pdl, a);
 }
 
-template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW>
+template <int SCHEME, typename QT, bool METER, bool RISK, bool GATE, bool VW, bool PAGED>
 cudaError_t dispatch_nw(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
   switch (a.seqs_per_cta) {
-    case 1: return run_split<SCHEME, QT, METER, RISK, GATE, VW, 1>(a, grid, st, pdl, occ);
-    case 2: return run_split<SCHEME, QT, METER, RISK, GATE, VW, 2>(a, grid, st, pdl, occ);
-    case 4: return run_split<SCHEME, QT, METER, RISK, GATE, VW, 4>(a, grid, st, pdl, occ);
-    case 8: return run_split<SCHEME, QT, METER, RISK, GATE, VW, 8>(a, grid, st, pdl, occ);
+    case 1: return run_split<SCHEME, QT, METER, RISK, GATE, VW, PAGED, 1>(a, grid, st, pdl, occ);
+    case 2: return run_split<SCHEME, QT, METER, RISK, GATE, VW, PAGED, 2>(a, grid, st, pdl, occ);
+    case 4: return run_split<SCHEME, QT, METER, RISK, GATE, VW, PAGED, 4>(a, grid, st, pdl, occ);
+    case 8: return run_split<SCHEME, QT, METER, RISK, GATE, VW, PAGED, 8>(a, grid, st, pdl, occ);
     default:
       // the black-box store's blocks are too large for 16 warps' rings (seqs_per_cta_for caps it at 8)
       if constexpr (SCHEME == kBbox) return cudaErrorInvalidValue;
-      else return run_split<SCHEME, QT, METER, RISK, GATE, VW, 16>(a, grid, st, pdl, occ);
+      else return run_split<SCHEME, QT, METER, RISK, GATE, VW, PAGED, 16>(a, grid, st, pdl, occ);
   }
 }
 
 // Instantiated combinations: meters off with and without a gate; meters on without a gate;
 // meters on with a gate, which always keeps block risks; each meters-on case with and
 // without value witnesses.
+template <int SCHEME, typename QT, bool PAGED>
+cudaError_t dispatch_combo(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
+  const bool gate = a.slots != nullptr, vw = a.vwit != nullptr;
+  if (!a.meter) return gate ? dispatch_nw<SCHEME, QT, false, false, true, false, PAGED>(a, grid, st, pdl, occ)
+                            : dispatch_nw<SCHEME, QT, false, false, false, false, PAGED>(a, grid, st, pdl, occ);
+  if (gate) return vw ? dispatch_nw<SCHEME, QT, true, true, true, true, PAGED>(a, grid, st, pdl, occ)
+                      : dispatch_nw<SCHEME, QT, true, true, true, false, PAGED>(a, grid, st, pdl, occ);
+  return vw ? dispatch_nw<SCHEME, QT, true, false, false, true, PAGED>(a, grid, st, pdl, occ)
+            : dispatch_nw<SCHEME, QT, true, false, false, false, PAGED>(a, grid, st, pdl, occ);
+}
+
+// Paged stores are instantiated for bf16 caches only (the runtime rejects fp32 paged caches).
 template <int SCHEME, typename QT>
 cudaError_t dispatch_qt(const DecodeArgs& a, dim3 grid, cudaStream_t st, bool pdl, int* occ) {
-  const bool gate = a.slots != nullptr, vw = a.vwit != nullptr;
-  if (!a.meter) return gate ? dispatch_nw<SCHEME, QT, false, false, true, false>(a, grid, st, pdl, occ)
-                            : dispatch_nw<SCHEME, QT, false, false, false, false>(a, grid, st, pdl, occ);
-  if (gate) return vw ? dispatch_nw<SCHEME, QT, true, true, true, true>(a, grid, st, pdl, occ)
-                      : dispatch_nw<SCHEME, QT, true, true, true, false>(a, grid, st, pdl, occ);
-  return vw ? dispatch_nw<SCHEME, QT, true, false, false, true>(a, grid, st, pdl, occ)
-            : dispatch_nw<SCHEME, QT, true, false, false, false>(a, grid, st, pdl, occ);
+  if (a.table == nullptr) return dispatch_combo<SCHEME, QT, false>(a, grid, st, pdl, occ);
+  if constexpr (sizeof(QT) == 2) return dispatch_combo<SCHEME, QT, true>(a, grid, st, pdl, occ);
+  else return cudaErrorInvalidValue;
 }
 
 template <int SCHEME>

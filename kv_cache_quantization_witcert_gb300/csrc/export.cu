@@ -19,7 +19,7 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
     case X_VC: {  // [B][S][Hkv][128]
       const int c = idx % kD, h = (idx / kD) % a.Hkv, t = (idx / ((size_t)kD * a.Hkv)) % a.S;
       const int i = idx / ((size_t)kD * a.Hkv * a.S);
-      const uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * bb;
+      const uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * bb;
       const int r = t & 15;
       if (a.scheme == kBbox) {   // the stored bf16 values
         const int off = a.what == X_KC ? BboxLayout::KH + kbf_off(r, c) : BboxLayout::VH + vbf_off(r, c);
@@ -45,7 +45,7 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
     case X_VZ: {  // [B][S][Hkv][4]
       const int G = idx % 4, h = (idx / 4) % a.Hkv, t = (idx / (4 * (size_t)a.Hkv)) % a.S;
       const int i = idx / (4 * (size_t)a.Hkv * a.S);
-      const uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * bb;
+      const uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * bb;
       const int r = t & 15;
       __half v;
       if (a.scheme == kKivi) {
@@ -61,7 +61,7 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
     case X_KIVI_KZ: {  // [B][nblk][Hkv][128]
       const int c = idx % kD, h = (idx / kD) % a.Hkv, b = (idx / ((size_t)kD * a.Hkv)) % nblk;
       const int i = idx / ((size_t)kD * a.Hkv * nblk);
-      const uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + b) * bb;
+      const uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, b) * bb;
       reinterpret_cast<__half*>(a.dst)[idx] =
           reinterpret_cast<const __half*>(bp + KiviLayout::KP + (a.what == X_KIVI_KZ ? 256 : 0))[kivi_kparam_idx(c)];
       break;
@@ -69,7 +69,7 @@ __global__ void export_kernel(const ExportArgs a, size_t n) {
     case X_W: {  // [B][S][Hkv][16]
       const int b = idx % kBands, h = (idx / kBands) % a.Hkv, t = (idx / ((size_t)kBands * a.Hkv)) % a.S;
       const int i = idx / ((size_t)kBands * a.Hkv * a.S);
-      const uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * bb;
+      const uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * bb;
       reinterpret_cast<__half*>(a.dst)[idx] =
           *reinterpret_cast<const __half*>(bp + witness_off(a.scheme) + wit_off(t & 15, b));
       break;

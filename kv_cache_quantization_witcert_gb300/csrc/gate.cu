@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(256) gate_pagein_kernel(const GateArgs a) {
       *reinterpret_cast<uint4*>(dst + k) = *reinterpret_cast<const uint4*>(src + k);
     __syncthreads();
     if (threadIdx.x < 32) {
-      uint8_t* wreg = a.blocks + ((sh * a.nblk_max) + b) * block_bytes(a.scheme) + witness_off(a.scheme);
+      uint8_t* wreg = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, b) * block_bytes(a.scheme) +
+                      witness_off(a.scheme);
       reinterpret_cast<uint4*>(wreg)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     }
     __threadfence();

@@ -12,7 +12,8 @@ constexpr int kPartStride = 136;
 constexpr int kPartAcc = 8;
 
 struct WriteArgs {
-  uint8_t* blocks;           // layer base: [B][Hkv][nblk_max][block_bytes]
+  uint8_t* blocks;           // layer base: [B][Hkv][nblk_max][block_bytes], or the layer's page pool
+  const int32_t* table;      // paged store: [B][nblk_max] page of each block (shared by layers), or null
   int nblk_max;
   const void* K;             // [B][n_tok][Hkv][128]
   const void* V;
@@ -32,7 +33,8 @@ struct WriteArgs {
 };
 
 struct DecodeArgs {
-  const uint8_t* blocks;     // layer base
+  const uint8_t* blocks;     // layer base (contiguous store or page pool)
+  const int32_t* table;      // paged store: [B][nblk_max] pages, or null
   int nblk_max;
   const int32_t* slots;      // layer base or null
   const void* pool;
@@ -108,7 +110,8 @@ struct GateArgs {
   unsigned int* todo_count;  // device counter (reset per call)
   unsigned int* pool_next;   // device counter (persistent)
   unsigned long long* stats; // [6] device counters (witcert_gate_stats order)
-  uint8_t* blocks;           // layer base
+  uint8_t* blocks;           // layer base (contiguous store or page pool)
+  const int32_t* table;      // paged store: [B][nblk_max] pages, or null
   const void* backing;       // device-mapped pinned host, layer base
   void* pool;
   int nblk_max, B, Hq, Hkv, grp, S, backing_rows, pool_capacity, scheme, elem_bytes;
@@ -119,6 +122,7 @@ cudaError_t launch_gate(const GateArgs& a, cudaStream_t st);
 
 struct ExportArgs {
   const uint8_t* blocks;
+  const int32_t* table;      // paged store, or null
   int nblk_max, B, Hkv, Hq, S, scheme;
   const int32_t* slots;
   const float* risk;

@@ -62,6 +62,9 @@ struct witcert_cache {
   unsigned long long* clamps = nullptr;
   int* err = nullptr;
   int* dlen = nullptr;              // [L][B] per-sequence lengths on the device (ragged batches)
+  int32_t* table = nullptr;         // paged store: [B][nblk_max] page of each block (all layers), -1 = none
+  std::vector<int32_t> table_host;  // host copy of the page table
+  std::vector<int32_t> free_pages;  // paged store: pages no sequence holds
   std::vector<int> len;             // per layer: the longest sequence
   std::vector<std::vector<int>> slen;   // per layer and sequence
   std::vector<uint64_t> write_gen, risk_gen;   // per layer: writes / resets so far; at the last metered decode
@@ -104,7 +107,7 @@ void free_all(witcert_cache* c) {
   if (c->backing_host) cudaFreeHost(c->backing_host);
   cudaFree(c->risk_raw); cudaFree(c->risk); cudaFree(c->part); cudaFree(c->selmask); cudaFree(c->todo);
   cudaFree(c->todo_count); cudaFree(c->pool_next); cudaFree(c->gstats); cudaFree(c->clamps); cudaFree(c->err);
-  cudaFree(c->dlen);
+  cudaFree(c->dlen); cudaFree(c->table);
   for (auto e : c->gate_done) if (e) cudaEventDestroy(e);
   for (auto& p : c->prof_pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
   for (auto& p : c->prof_free) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
@@ -158,6 +161,8 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   if (f.total_steps <= 0) return fail(WITCERT_EINVAL, "total_steps must be positive");
   if (f.n_splits < 0 || f.max_repair_blocks < 0) return fail(WITCERT_EINVAL, "n_splits and max_repair_blocks must be >= 0");
   if (f.pos_offset < 0) return fail(WITCERT_EINVAL, "pos_offset must be >= 0");
+  if (f.max_pages < 0) return fail(WITCERT_EINVAL, "max_pages must be >= 0");
+  if (f.max_pages > 0 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "a paged cache holds bf16 keys and values");
 
   auto* c = new (std::nothrow) witcert_cache();
   if (!c) return fail(WITCERT_ENOMEM, "host allocation failed");
@@ -169,7 +174,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   c->bblk = block_bytes(c->scheme);
   c->nblk_max = (f.max_tokens + kBlk - 1) / kBlk;
   c->elem = f.kv_dtype == WITCERT_BF16 ? 2 : 4;
-  c->layer_blocks = layer_rows(c) * c->nblk_max * c->bblk;
+  c->layer_blocks = f.max_pages > 0 ? (size_t)f.max_pages * f.n_kv_heads * c->bblk : layer_rows(c) * c->nblk_max * c->bblk;
   const int auto_on = auto_splits(c, c->nblk_max, true, 0), auto_off = auto_splits(c, c->nblk_max, false, 0);
   const int auto_max = auto_on > auto_off ? auto_on : auto_off;
   c->max_splits = f.n_splits > auto_max ? f.n_splits : auto_max;
@@ -190,6 +195,13 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   TRY(dalloc(&c->clamps, sizeof(unsigned long long)), "allocating counters");
   TRY(dalloc(&c->err, sizeof(int)), "allocating the error word");
   TRY(dalloc(&c->dlen, L * f.batch * sizeof(int)), "allocating sequence lengths");
+  if (f.max_pages > 0) {
+    const size_t entries = (size_t)f.batch * c->nblk_max;
+    TRY(dalloc(&c->table, entries * sizeof(int32_t)), "allocating the page table");
+    TRY(cudaMemset(c->table, 0xFF, entries * sizeof(int32_t)), "clearing the page table");
+    c->table_host.assign(entries, -1);
+    for (int pg = f.max_pages - 1; pg >= 0; --pg) c->free_pages.push_back(pg);
+  }
   if (gate) {
     TRY(dalloc(&c->slots, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "allocating repair slots");
     TRY(cudaMemset(c->slots, 0xFF, L * layer_rows(c) * c->nblk_max * sizeof(int32_t)), "clearing repair slots");
@@ -230,6 +242,7 @@ static WriteArgs layer_write_args(const witcert_cache* c, int layer, const void*
                                   const void* Vh, int n_tok, int t0) {
   WriteArgs a{};
   a.blocks = c->blocks + layer * c->layer_blocks;
+  a.table = c->table;
   a.nblk_max = c->nblk_max;
   a.K = K; a.V = V; a.Kh = Kh; a.Vh = Vh;
   if (c->vwit) a.vwit = c->vwit + layer * vwit_layer(c);
@@ -253,7 +266,8 @@ static WriteArgs seq_write_args(const witcert_cache* c, const WriteArgs& all, in
   WriteArgs a = all;
   const size_t rows = (size_t)i * c->cfg.n_kv_heads;          // (sequence, KV head) rows before i
   const size_t in_bytes = in_row * c->cfg.n_kv_heads * kD * c->elem;
-  a.blocks += rows * c->nblk_max * c->bblk;
+  if (a.table) a.table += (size_t)i * c->nblk_max;            // paged: the sequence's row of the table
+  else a.blocks += rows * c->nblk_max * c->bblk;
   if (a.vwit) a.vwit += rows * c->nblk_max * kBlk;
   if (a.backing) a.backing = static_cast<uint8_t*>(a.backing) + rows * backing_rows(c) * kD * c->elem;
   if (a.slots) a.slots += rows * c->nblk_max;
@@ -268,11 +282,10 @@ static WriteArgs seq_write_args(const witcert_cache* c, const WriteArgs& all, in
 
 // Device copies of per-sequence lengths: entries (layer * batch + sequence, length), sent as
 // kernel parameters (no host buffer outlives the call).
-static cudaError_t push_lengths(witcert_cache* c, const std::vector<std::pair<int, int>>& upd, cudaStream_t st,
-                                bool& pdl) {
+static cudaError_t push_ints(int* dst, const std::vector<std::pair<int, int>>& upd, cudaStream_t st, bool& pdl) {
   for (size_t k0 = 0; k0 < upd.size(); k0 += kRaggedPerLaunch) {
     LengthArgs u{};
-    u.dst = c->dlen;
+    u.dst = dst;
     for (size_t k = k0; k < upd.size() && k < k0 + kRaggedPerLaunch; ++k) {
       u.idx[u.n] = upd[k].first;
       u.len[u.n] = upd[k].second;
@@ -282,6 +295,38 @@ static cudaError_t push_lengths(witcert_cache* c, const std::vector<std::pair<in
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+static cudaError_t push_lengths(witcert_cache* c, const std::vector<std::pair<int, int>>& upd, cudaStream_t st,
+                                bool& pdl) {
+  return push_ints(c->dlen, upd, st, pdl);
+}
+
+// Paged store: pages for every block the appends of n touch that has none yet (the table is
+// shared by the layers, so the first layer to reach a block takes its page).  Fails, taking
+// back what it took, when the pool runs out.
+static witcert_status take_pages(witcert_cache* c, int layer, const std::vector<int>& n,
+                                 std::vector<std::pair<int, int>>& upd) {
+  if (!c->table) return WITCERT_OK;
+  for (int i = 0; i < c->cfg.batch; ++i) {
+    if (n[i] == 0) continue;
+    const int t0 = c->slen[layer][i];
+    for (int b = t0 / kBlk; b <= (t0 + n[i] - 1) / kBlk; ++b) {
+      int32_t& e = c->table_host[(size_t)i * c->nblk_max + b];
+      if (e >= 0) continue;
+      if (c->free_pages.empty()) {
+        for (auto& u : upd) {
+          c->free_pages.push_back(u.second);
+          c->table_host[u.first] = -1;
+        }
+        upd.clear();
+        return fail(WITCERT_ENOMEM, "the page pool (%d pages) is exhausted", c->cfg.max_pages);
+      }
+      e = c->free_pages.back();
+      c->free_pages.pop_back();
+      upd.emplace_back((int)((size_t)i * c->nblk_max + b), e);
+    }
+  }
+  return WITCERT_OK;
 }
 
 // From now on the sequences' lengths may differ: the device gets every layer's lengths.
@@ -332,10 +377,13 @@ static witcert_status write_impl(witcert_cache* c, int layer, const void* K, con
   if (total == 0) { ok(); return WITCERT_OK; }
   bool uniform = !c->ragged;
   for (int i = 1; i < B && uniform; ++i) uniform = n[i] == n[0];
+  std::vector<std::pair<int, int>> pages;
+  if (witcert_status ps = take_pages(c, layer, n, pages)) return ps;
   auto st = static_cast<cudaStream_t>(stream);
   const bool waited = order_after_gate(c, layer, st);
   bool pdl = c->overlap && !waited;
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = push_ints(c->table, pages, st, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "page table");
   int first_blk = INT_MAX;
   if (uniform) {
     const int n_tok = n[0], t0 = c->len[layer];
@@ -441,6 +489,17 @@ witcert_status witcert_reset_sequence(witcert_cache* c, int seq, void* stream) {
   std::vector<std::pair<int, int>> upd;
   for (int l = 0; l < c->cfg.n_layers; ++l) upd.emplace_back(l * c->cfg.batch + seq, 0);
   if (e == cudaSuccess) e = push_lengths(c, upd, st, pdl);
+  if (c->table && e == cudaSuccess) {       // its pages go back to the pool
+    std::vector<std::pair<int, int>> freed;
+    for (int b = 0; b < c->nblk_max; ++b) {
+      int32_t& pg = c->table_host[(size_t)seq * c->nblk_max + b];
+      if (pg < 0) continue;
+      c->free_pages.push_back(pg);
+      pg = -1;
+      freed.emplace_back((int)((size_t)seq * c->nblk_max + b), -1);
+    }
+    e = push_ints(c->table, freed, st, pdl);
+  }
   // the sequence's repairs go with it (their pool slots are not reused)
   const size_t rows = (size_t)c->cfg.n_kv_heads * c->nblk_max;
   for (int l = 0; l < c->cfg.n_layers && e == cudaSuccess && c->slots; ++l)
@@ -490,6 +549,7 @@ static void fill_decode(witcert_cache* c, int layer, const void* q, double delta
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads; a.grp = a.Hq / a.Hkv; a.S = S;
   if (c->ragged) a.seq_len = c->dlen + (size_t)layer * c->cfg.batch;
+  a.table = c->table;
   a.n_splits = c->cfg.n_splits > 0 ? c->cfg.n_splits : auto_splits(c, nblk, meter, c->max_splits);
   a.seed = c->cfg.seed;
   philox_round_keys(a.seed, a.rk0, a.rk1);
@@ -657,6 +717,7 @@ witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream
   a.nblk_max = c->nblk_max; a.B = c->cfg.batch; a.Hq = c->cfg.n_q_heads; a.Hkv = c->cfg.n_kv_heads;
   a.grp = a.Hq / a.Hkv; a.S = c->len[layer]; a.backing_rows = (int)backing_rows(c);
   if (c->ragged) a.seq_len = c->dlen + (size_t)layer * c->cfg.batch;
+  a.table = c->table;
   a.pool_capacity = c->cfg.max_repair_blocks; a.scheme = c->scheme; a.elem_bytes = c->elem;
   a.d_star = std::sqrt(1.0 + 2.0 * (double)tau) - 1.0;
   e = launch_gate(a, c->side);
@@ -710,6 +771,7 @@ witcert_status witcert_stats(witcert_cache* c, witcert_stats_t* out) {
   out->decode_kernel_ms = c->prof_ms;
   out->decode_kernel_launches = c->prof_n;
   out->last_n_splits = c->last_n_splits;
+  out->pages_used = c->table ? (uint64_t)c->cfg.max_pages - c->free_pages.size() : 0;
   ok();
   return WITCERT_OK;
 }
@@ -781,6 +843,7 @@ witcert_status witcert_export(witcert_cache* c, int layer, witcert_export_kind w
   a.slots = c->slots ? c->slots + layer * layer_rows(c) * c->nblk_max : nullptr;
   a.risk = c->risk ? c->risk + (size_t)layer * B * Hq * c->nblk_max : nullptr;
   a.vwit = c->vwit ? c->vwit + layer * vwit_layer(c) : nullptr;
+  a.table = c->table;
   a.dst = dst;
   a.what = (int)what;
   cudaError_t e = launch_export(a, st);

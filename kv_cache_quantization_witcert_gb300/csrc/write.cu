@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   const int h = wid % a.Hkv, n = a.tok_begin + (wid / a.Hkv) % a.tok_count, i = wid / (a.Hkv * a.tok_count);
   const int blk = (a.t0 + n) >> 4;
   constexpr int kBytes = block_bytes(SCH);
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + blk) * kBytes;
+  uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes;
   write_token<T, SCH>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
 }
 
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int
     write_token<T, SCH>(a, im, i, h, t, uniform_row(a, i, t - a.t0, h), lane);
   }
   __syncwarp();
-  uint4* dst = reinterpret_cast<uint4*>(a.blocks + ((size_t)sh * a.nblk_max + blk) * kBytes);
+  uint4* dst = reinterpret_cast<uint4*>(a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes);
   const uint4* src = reinterpret_cast<const uint4*>(im);
   for (int k = lane; k < kBytes / 16; k += 32) dst[k] = src[k];
 }
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
   if (wid >= a.B * a.n_tok * a.Hkv) return;
   const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
   const int t = a.t0 + n;
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * KiviLayout::BYTES;
+  uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * KiviLayout::BYTES;
   kivi_v_token<T>(a, bp, i, h, t, uniform_row(a, i, n, h), lane);
 }
 
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(128) write_ragged_kernel(const WriteArgs a, co
   }
   const int i = g.seq[lo], t = g.t0[lo] + (tok - g.off[lo]);
   const size_t row = ((size_t)(g.row0[lo] + (tok - g.off[lo])) * a.Hkv + h) * kD;
-  uint8_t* bp = a.blocks + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * block_bytes(SCH);
+  uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * block_bytes(SCH);
   if constexpr (SCH == kKivi) kivi_v_token<T>(a, bp, i, h, t, row, lane);
   else write_token<T, SCH>(a, bp, i, h, t, row, lane);
 }
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int
     const int blk = blk0 + blockIdx.y;
     const int lo = blk * kBlk;
     if (lo + kBlk > t_end) {   // unfinished block: keep the new keys exact in the tail
-      uint8_t* wreg = a.blocks + ((size_t)sh * a.nblk_max + blk) * KiviLayout::BYTES + KiviLayout::W;
+      uint8_t* wreg = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * KiviLayout::BYTES + KiviLayout::W;
       for (int t = (a.t0 > lo ? a.t0 : lo); t < t_end; ++t) {
         float x[4];
         load4f<T>(reinterpret_cast<const T*>(a.K) + (((size_t)i * a.n_tok + (t - a.t0)) * a.Hkv + h) * kD + 4 * lane, x);
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int
     }
     for (int k = lane; k < 128; k += 32) img[k] = 0u;
     __syncwarp();
-    uint8_t* bp = a.blocks + ((size_t)sh * a.nblk_max + blk) * KiviLayout::BYTES;
+    uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * KiviLayout::BYTES;
     __half* ksc = reinterpret_cast<__half*>(bp + KiviLayout::KP);
     __half* kzr = reinterpret_cast<__half*>(bp + KiviLayout::KP + 256);
     float sc[4], zr[4];

@@ -1,11 +1,13 @@
-"""Ragged batches on the GPU: sequences of different lengths in one cache.
+"""Ragged batches on the GPU: sequences of different lengths in one cache, in a contiguous
+store and in a paged one (a shared pool of pages behind a per-sequence page table).
 
 Each sequence of the GPU cache is checked against its own single-sequence oracle
 cache (the oracle of one sequence is the plain definition: its tokens, its
 positions, its length as S in Tier B).  Covers a ragged prefill (an empty
 sequence, a ragged tail, lengths spanning several splits), ragged appends with
 some sequences idle, a sequence reset and refill (continuous batching), the gate
-on ragged lengths, and every scheme with value witnesses on.
+on ragged lengths, and every scheme with value witnesses on; the paged store must
+give the same results with a pool far smaller than batch x max_tokens.
 """
 import numpy as np
 import pytest
@@ -34,11 +36,11 @@ def _cuda():
 class Ragged:
     """A GPU cache of B sequences and one oracle cache per sequence."""
 
-    def __init__(self, w, scheme, cap, v_witness=True, gate_blocks=0, n_splits=0):
+    def __init__(self, w, scheme, cap, v_witness=True, gate_blocks=0, n_splits=0, max_pages=0):
         self.w, self.scheme, self.B = w, scheme, w.batch
         self.gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, cap, scheme, dtype=torch_dtype(w),
                             seed=w.seed, total_steps=w.steps, max_repair_blocks=gate_blocks, v_witness=v_witness,
-                            n_splits=n_splits)
+                            n_splits=n_splits, max_pages=max_pages)
         self.refs = [OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps,
                                  v_witness=v_witness) for _ in range(w.batch)]
         self.fseed = 0
@@ -110,12 +112,14 @@ def _split(arr, lens, start=None):
     return [arr[i, start[i]:start[i] + n] for i, n in enumerate(lens)]
 
 
+@pytest.mark.parametrize("pages", [0, 100])
 @pytest.mark.parametrize("scheme", ALL_SCHEMES)
-def test_ragged_prefill_appends_and_reset(scheme):
+def test_ragged_prefill_appends_and_reset(scheme, pages):
     """Four sequences of lengths 0 / 37 / 300 / 1000 (an empty one, ragged tails, several
-    splits), then appends of 1 / 0 / 3 / 1 tokens, then sequence 2 reset and refilled."""
+    splits), then appends of 1 / 0 / 3 / 1 tokens, then sequence 2 reset and refilled; with a
+    contiguous store and with a pool of 100 pages (4 x 1100 tokens would take 276)."""
     w = WORKLOADS["qwen_1l"].with_(batch=4, context=1000, steps=3, scheme=scheme)
-    rg = Ragged(w, scheme, cap=1100)
+    rg = Ragged(w, scheme, cap=1100, max_pages=pages)
     K, V = gen_kv(w, 0)
     lens = [0, 37, 300, 1000]
     rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
@@ -126,9 +130,13 @@ def test_ragged_prefill_appends_and_reset(scheme):
     rg.write(0, list(zip(_split(K2, app), _split(V2, app))))
     rg.check_store(0)
     rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
+    if pages:
+        assert rg.gpu.witcert_stats()["pages_used"] == 1 + 3 + 19 + 63
     rg.gpu.witcert_reset_sequence(2)
     rg.refs[2] = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps, v_witness=True)
     assert rg.gpu.witcert_seq_length(0, 2) == 0
+    if pages:
+        assert rg.gpu.witcert_stats()["pages_used"] == 1 + 3 + 63
     rg.check_decode(0, gen_q(w, 0, 2), w.delta_req)
     K3, V3 = gen_kv(w.with_(context=64), 6)
     refill = [0, 0, 50, 0]
@@ -174,12 +182,13 @@ def test_ragged_kivi_appends_close_blocks_per_sequence():
         rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
 
 
-def test_ragged_gate_decisions_match_each_sequence():
+@pytest.mark.parametrize("pages", [0, 60])
+def test_ragged_gate_decisions_match_each_sequence(pages):
     """FP8 with the gate on ragged lengths: each sequence's block risks (its own blocks; the
     GPU's rows past its length are zero) drive that sequence's oracle gate, and the GPU pages in
-    exactly those blocks."""
+    exactly those blocks (witnesses zeroed in the page that holds each block when paged)."""
     w = WORKLOADS["qwen_1l"].with_(batch=3, context=500, steps=3, scheme="fp8_e4m3")
-    rg = Ragged(w, "fp8_e4m3", cap=520, v_witness=False, gate_blocks=3 * 4 * 40)
+    rg = Ragged(w, "fp8_e4m3", cap=520, v_witness=False, gate_blocks=3 * 4 * 40, max_pages=pages)
     K, V = gen_kv(w, 0)
     lens = [500, 130, 257]
     rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
@@ -210,3 +219,31 @@ def test_ragged_rejects_overflow_and_partial_decode():
     with pytest.raises(wc.WitcertError) as e:
         rg.gpu.decode_partial(0, rg.dev(gen_q(w, 0, 0)), w.delta_req, 10)
     assert e.value.status == _lib.ESTATE
+
+
+@pytest.mark.parametrize("scheme", ["int8_dither", "kivi2"])
+def test_paged_uniform_writes_and_pool_exhaustion(scheme):
+    """Equal appends to a paged cache take the batched writers through the page table; a write
+    the pool cannot hold fails with ENOMEM and changes nothing; after a reset frees pages the
+    same write succeeds.  Every result matches the oracle."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=200, steps=2, scheme=scheme)
+    rg = Ragged(w, scheme, cap=400, max_pages=3 * 13 + 5)
+    K, V = gen_kv(w, 0)
+    lens = [200, 200, 200]                      # 13 blocks each
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    assert rg.gpu.witcert_stats()["pages_used"] == 39
+    rg.check_store(0)
+    rg.check_decode(0, gen_q(w, 0, 0), w.delta_req)
+    K2, V2 = gen_kv(w.with_(context=120), 4)
+    big = [0, 120, 0]                           # blocks 13..19: 7 new pages > 5 free
+    with pytest.raises(wc.WitcertError) as e:
+        rg.gpu.witcert_write_ragged(0, rg.dev(K2[1, :120]), rg.dev(V2[1, :120]), big)
+    assert e.value.status == _lib.ENOMEM
+    assert rg.gpu.witcert_seq_length(0, 1) == 200 and rg.gpu.witcert_stats()["pages_used"] == 39
+    rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
+    rg.gpu.witcert_reset_sequence(0)
+    rg.refs[0] = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps, v_witness=True)
+    rg.write(0, list(zip(_split(K2, big), _split(V2, big))))
+    assert rg.gpu.witcert_stats()["pages_used"] == 26 + 7
+    rg.check_store(0)
+    rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
