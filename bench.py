@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--taus", default="0.5,1,2", help="gate thresholds of the gated workload")
     ap.add_argument("--gated-steps", type=int, default=256, help="decode steps per threshold (gated workload)")
     ap.add_argument("--v-witness", action="store_true", help="keep value witnesses and report the value meter")
+    ap.add_argument("--paged", action="store_true", help="paged block store (a pool that fits the run exactly)")
+    ap.add_argument("--ragged", default=None, metavar="LO:HI",
+                    help="ragged batch: sequence i's context drawn uniformly from [LO, HI] (seeded); HI <= context")
     return ap.parse_args()
 
 
@@ -80,12 +83,24 @@ def tensor_function(x):
     return x.to(torch.float8_e4m3fn).to(x.dtype)
 
 
+def ragged_lengths(w, spec):
+    """Per-sequence contexts of a ragged run: seeded uniform draws in [LO, HI]."""
+    if not spec:
+        return [w.context] * w.batch
+    lo, hi = (int(x) for x in spec.split(":"))
+    assert 1 <= lo <= hi <= w.context
+    return [int(x) for x in np.random.default_rng(w.seed + 7).integers(lo, hi + 1, size=w.batch)]
+
+
 def config_of(w, args, n_splits, world):
     vw = getattr(args, "v_witness", False)
+    rg = getattr(args, "ragged", None)
+    ctx = f"contexts uniform in [{rg.replace(':', ', ')}] (seeded)" if rg else f"{w.context} context"
     return {"workload": f"{w.name}: {w.n_layers} layers, {w.n_q_heads}q/{w.n_kv_heads}kv heads, d=128, "
-                        f"batch {w.batch} x {w.context} context per GPU, {w.scheme}"
+                        f"batch {w.batch} x {ctx} per GPU, {w.scheme}"
                         + (" (f = raw FP8 cast)" if w.scheme == "blackbox" else "")
-                        + (", value witnesses" if vw else ""),
+                        + (", value witnesses" if vw else "")
+                        + (", paged store" if getattr(args, "paged", False) else ""),
             "model": w.name, "global_batch": w.batch * world, "seq_len": w.context, "layers": w.n_layers,
             "scheme": w.scheme, "delta_req": w.delta_req, "n_splits": n_splits,
             "parallelism": f"replicas x{world} (independent sequence shards)",
@@ -256,14 +271,19 @@ def run_ours(args, w):
     vw = args.v_witness
     bb = wl.scheme == "blackbox"
     tbytes = tok_head_bytes(wl.scheme, vw)
+    lens = ragged_lengths(wl, args.ragged)
+    pages = sum((n + n_app + 15) // 16 for n in lens) if args.paged else 0
     cache = wc.Cache(wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.batch, wl.context + n_app, wl.scheme,
-                     dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0, v_witness=vw)
+                     dtype=dt, seed=wl.seed, total_steps=wl.steps, n_splits=0, v_witness=vw, max_pages=pages)
     stream = torch.cuda.current_stream()
 
     # prefill every layer (outside the step timing; its write throughput is reported on its own)
     sets = {}
     for sid in range(min(DISTINCT_LAYERS, wl.n_layers)):
         K, V = gen_kv(wl, sid)
+        if args.ragged:      # sequence i keeps its first lens[i] tokens, packed sequence by sequence
+            K = np.concatenate([K[i, :n] for i, n in enumerate(lens)])
+            V = np.concatenate([V[i, :n] for i, n in enumerate(lens)])
         sets[sid] = (torch.from_numpy(K).to(dev, dt), torch.from_numpy(V).to(dev, dt))
         if bb:
             sets[sid] += (tensor_function(sets[sid][0]), tensor_function(sets[sid][1]))
@@ -271,14 +291,17 @@ def run_ours(args, w):
     pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pf0.record(stream)
     for layer in range(wl.n_layers):
-        if bb:
-            cache.witcert_write_hat(layer, *sets[layer % DISTINCT_LAYERS])
+        kv = sets[layer % DISTINCT_LAYERS]
+        if args.ragged:
+            cache.witcert_write_ragged(layer, kv[0], kv[1], lens, *(kv[2:] if bb else ()))
+        elif bb:
+            cache.witcert_write_hat(layer, *kv)
         else:
-            cache.witcert_write(layer, *sets[layer % DISTINCT_LAYERS])
+            cache.witcert_write(layer, *kv)
     pf1.record(stream)
     torch.cuda.synchronize()
     prefill_ms = pf0.elapsed_time(pf1)
-    prefill_tok_heads = wl.n_layers * wl.batch * wl.context * wl.n_kv_heads
+    prefill_tok_heads = wl.n_layers * sum(lens) * wl.n_kv_heads
     # bytes per token-head: bf16 K and V read (512 B; the black-box scheme also reads f(K), f(V)),
     # the compressed token written
     prefill_read = 1024 if bb else 512
@@ -351,7 +374,7 @@ def run_ours(args, w):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    s_len0 = cache.witcert_length(0)
+    lens0 = [cache.witcert_seq_length(0, i) for i in range(wl.batch)]
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -364,24 +387,24 @@ def run_ours(args, w):
     # (the events sit on the launching stream; they also break the launch overlap, so the
     # step time above comes from the pass without them)
     cache.witcert_set_profiling(True)
-    prof_len0 = cache.witcert_length(0)
+    prof_lens = [cache.witcert_seq_length(0, i) for i in range(wl.batch)]
     for s in range(args.steps):
         one_step(dev_inputs[(args.warmup + args.steps + s) % 8])
     st = cache.witcert_stats()
     cache.witcert_set_profiling(False)
     clk = clocks.stop()
-    attended = sum(wl.batch * (s_len0 + 1 + s) for s in range(args.steps)) * wl.n_layers
+    attended = sum(n + 1 + s for n in lens0 for s in range(args.steps)) * wl.n_layers
     ms, attended = reduce_timing(ms, attended, dev)
     value = attended / (ms / 1e3)
 
     # roofline of the dominant kernel (decode split kernel), timed by the library's events
     n_launch = st["decode_kernel_launches"]
     avg_ms = st["decode_kernel_ms"] / max(1, n_launch)
-    avg_S = prof_len0 + 1 + (args.steps - 1) / 2.0
-    alg_bytes = wl.batch * wl.n_kv_heads * avg_S * tbytes
+    sum_S = sum(n + 1 + (args.steps - 1) / 2.0 for n in prof_lens)      # mean over the launches
+    alg_bytes = wl.n_kv_heads * sum_S * tbytes
     achieved = alg_bytes / (avg_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
-    traffic = recorded_traffic(wl) if not vw else None
+    traffic = recorded_traffic(wl) if not (vw or args.paged or args.ragged) else None
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     pinned = [[t.pin_memory() for t in hi] for hi in host_inputs]
@@ -390,7 +413,7 @@ def run_ours(args, w):
     h2d = sum(t.numel() * t.element_size() for t in pinned[0])
     d2h = out_h.numel() * 4 + mtr_h.numel() * 4
     barrier()
-    l0 = cache.witcert_length(0)
+    l0s = [cache.witcert_seq_length(0, i) for i in range(wl.batch)]
     t0 = time.perf_counter()
     e2e_dev = [[torch.empty_like(t, device=dev) for t in pinned[0]] for _ in range(2)]
     e2e_args = [make_args(buf) for buf in e2e_dev]
@@ -403,7 +426,7 @@ def run_ours(args, w):
         mtr_h.copy_(mtr, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_s = time.perf_counter() - t0
-    e2e_tokens = sum(wl.batch * (l0 + 1 + s) for s in range(e2e_steps)) * wl.n_layers
+    e2e_tokens = sum(n + 1 + s for n in l0s for s in range(e2e_steps)) * wl.n_layers
     e2e_s, e2e_tokens = reduce_timing(e2e_s, e2e_tokens, dev)
 
     cpu = None
