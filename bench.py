@@ -163,11 +163,22 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+def kernel_digest(path):
+    """sha256[:16] of a kernel source with its // comments and blank lines removed (a comment
+    edit leaves the recorded counters valid; any code edit invalidates them)."""
+    lines = []
+    for ln in open(path).read().splitlines():
+        code = re.sub(r"//.*$", "", ln).rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def recorded_traffic(w):
     """Per-launch DRAM bytes of the decode split kernel from the committed ncu summary, if it was
     taken on the current kernel source (null otherwise)."""
     src = os.path.join(ROOT, "kv_cache_quantization_witcert_gb300", "csrc", "decode_split.cuh")
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = kernel_digest(src)
     path = os.path.join(ROOT, "profiles", f"decode_{w.scheme}_{w.name}.md")
     if not os.path.exists(path):
         return None

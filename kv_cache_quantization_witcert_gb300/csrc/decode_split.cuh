@@ -27,15 +27,20 @@
 // aggregation min(1, (A^2-1)/2) with A = 1 + S_X/Z [WitCert summary,
 // improvements list] is applied after the merge.
 //
-// Launches chain through programmatic dependent launch.  Every kernel of the chain
-// except the split kernel waits for its predecessor before it lets its successor
-// start, so when a split kernel starts, everything but its immediate predecessor is
-// complete.  The split kernel lets its successor start at once and waits for that
-// predecessor only where it depends on it: before staging a block the preceding
-// write may touch (p.dirty_blk on; for a one-token append that is the final block),
-// before writing its partial results, and, with block risks on, before its first
-// risk store.  Older blocks, the dither and the queries are used without waiting,
-// so the write's latency overlaps the decode.
+// Launches chain through programmatic dependent launch.  Every kernel waits for its
+// predecessor at some point, so a kernel's completion implies that of everything before
+// it.  The merge and most writers wait before they let their successor start; the split
+// kernel, and the writers of equal appends to a contiguous store, let their successor start
+// at once (such a writer waits on its way out).  So when a split kernel starts, its
+// preceding write and the merge before that may still run; neither touches what the split
+// reads before it waits: the split waits for its predecessor before staging a block the
+// preceding write may touch (p.dirty_blk on; for a one-token append that is the final
+// block; this also covers the exact pool, the KIVI tail and value-witness rows), before
+// writing its partial results (the merge before may still read the scratch), and, with
+// block risks on, before its first risk store.  Older blocks, the dither and the queries
+// are used without waiting, so the write's and the previous merge's latency overlap the
+// decode.  Per-sequence lengths and page tables, which the split reads at once, are set by
+// kernels that precede a writer that waits before its successor starts.
 #pragma once
 #include <atomic>
 #include <cfloat>

@@ -24,6 +24,8 @@ struct WriteArgs {
   int tok_begin, tok_count;  // tokens of this write a per-token launch covers
   int pos0;                  // global position of the cache's first token (dither key)
   int is_bf16;
+  int late_wait;             // token, block and KIVI value kernels wait for their predecessor at
+                             // their end instead of their start (see ChainEntry in write.cu)
   uint64_t seed;
   void* backing;             // device-mapped pinned host, layer base [B][Hkv][backing_rows][128], or null
   const int32_t* slots;      // layer base [B][Hkv][nblk_max], or null

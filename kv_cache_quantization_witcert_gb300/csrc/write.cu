@@ -186,6 +186,23 @@ __device__ __forceinline__ __half* vwit_at(const WriteArgs& a, int i, int h, int
   return a.vwit + (((size_t)i * a.Hkv + h) * a.nblk_max + (t >> 4)) * kBlk + (t & 15);
 }
 
+// Entry of a write kernel into the launch chain.  Normally it waits for its predecessor, then
+// lets its successor start.  With late_wait (equal appends to a contiguous store) it lets the
+// successor start at once, does its work alongside the predecessor (a merge, or a write
+// kernel of the same call on other blocks: none of them touches what this kernel touches),
+// and waits for the predecessor on its way out, so its completion still implies the
+// predecessor's and every later kernel finds all earlier work done.
+struct ChainEntry {
+  bool late;
+  __device__ explicit ChainEntry(bool late_wait) : late(late_wait) {
+    if (!late) pdl_wait();
+    pdl_trigger();
+  }
+  __device__ ~ChainEntry() {
+    if (late) pdl_wait();
+  }
+};
+
 // Exact-key side effects shared by all schemes: backing store and repaired blocks.
 template <typename T>
 __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int t, int lane, const T* krow) {
@@ -371,8 +388,7 @@ __device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int
 // appends and the parts of a write that do not fill whole blocks.
 template <typename T, int SCH>
 __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  const ChainEntry chain(a.late_wait != 0);
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.B * a.tok_count * a.Hkv) return;
   const int h = wid % a.Hkv, n = a.tok_begin + (wid / a.Hkv) % a.tok_count, i = wid / (a.Hkv * a.tok_count);
@@ -387,8 +403,7 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
 // it with 16-byte writes.
 template <typename T, int SCH>
 __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
-  pdl_wait();
-  pdl_trigger();
+  const ChainEntry chain(a.late_wait != 0);
   constexpr int kBytes = block_bytes(SCH);
   __shared__ __align__(16) uint8_t img[4][kBytes];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -463,8 +478,7 @@ __device__ __forceinline__ void kivi_v_token(const WriteArgs& a, uint8_t* bp, in
 
 template <typename T>
 __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  const ChainEntry chain(a.late_wait != 0);
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= a.B * a.n_tok * a.Hkv) return;
   const int h = wid % a.Hkv, n = (wid / a.Hkv) % a.n_tok, i = wid / (a.Hkv * a.n_tok);
