@@ -5,8 +5,8 @@ back from host memory a block at a time and clears the witnesses of what it
 repaired; it ranks by risk when the threshold is 1 or more and certifies below
 1, and repairs accumulate and persist
 [WitCert summary, implementation paragraph; WitCert Lean page, Approach and
-Figures 2 and 5].  The ranking and stopping rule below are this build's
-reading of those sentences:
+Figures 2 and 5].  The ranking and stopping rule below are a reading of
+those sentences (the pages state the behavior, not the rule):
 
 * a (sequence, query head) cell triggers when its unclamped meter
   D + D^2/2 exceeds tau, i.e. when D > D*(tau) = sqrt(1 + 2 tau) - 1;

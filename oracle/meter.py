@@ -14,7 +14,7 @@ with c_t = eps_t (Tier A) or u_t (Tier B).  The oracle evaluates A as 1 + D with
 D = sum_t p~_t expm1(c_t), and (A^2 - 1)/2 as D + D^2/2: the same numbers,
 without the cancellation of A^2 - 1 when every c_t is small.
 
-Value side (this build's reading; the pages define no value bound): with the
+Value side (a reading of this library; the pages define no value bound): with the
 stored value witness wv_t >= ||v_t - v^_t||,
     E_V = sum_t p~_t wv_t >= || sum_t p~_t v_t - sum_t p~_t v^_t ||
 by the triangle inequality: the output error the value compression adds at the

@@ -8,7 +8,7 @@ bfloat16 rounding against torch's cast and hand-worked ties; Theorem 2
 tensor functions; the identity function giving zero witness, zero meter and
 plain attention.
 
-The value meter E_V = sum_t p~_t wv_t (this build's reading: the pages define
+The value meter E_V = sum_t p~_t wv_t (a reading of this library: the pages define
 no value bound) is pinned by the triangle inequality it rests on, checked by
 brute force on every scheme, by a residual shared by all tokens (where the
 inequality is an equality) and by uniform weights (q = 0: E_V is the mean).
