@@ -79,6 +79,7 @@ template <int NW> struct XiSlots { static constexpr int value = NW == 8 ? 3 : 4;
 template <int NW, int SCHEME> struct Smem {
   static constexpr int NST = Stages<NW>::value;
   static constexpr int NXI = SCHEME == kInt8 ? XiSlots<NW>::value : 0;
+  static constexpr int NXI_DIV = NXI > 0 ? NXI : 1;      // slot arithmetic (used only when NXI > 0)
   static constexpr int XD = NXI > 2 ? NXI - 2 : 1;
   static constexpr int STB = Lay<SCHEME>::BYTES + kVwBytes;
   static constexpr int kRing = NW * NST * STB;
@@ -314,8 +315,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // Dither of block b_begin + m into its slot: wait until every warp is done with the block
   // that used the slot before, write this thread's share, then count the warp in.
   auto produce = [&](int m) {
-    const int ps = m % SM::NXI;
-    if (m >= SM::NXI && !mbar_wait(smem_addr(&xfree[ps]), (uint32_t)((m / SM::NXI - 1) & 1), kWaitLimitNs)) {
+    const int ps = m % SM::NXI_DIV;
+    if (m >= SM::NXI && !mbar_wait(smem_addr(&xfree[ps]), (uint32_t)((m / SM::NXI_DIV - 1) & 1), kWaitLimitNs)) {
       if (!fault && lane == 0) atomicAdd(p.err, 1);
       fault = true;
     }
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   for (int n = 0; n < nb; ++n) {
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
-    const int xs = SCHEME == kInt8 ? n % SM::NXI : 0;
+    const int xs = SCHEME == kInt8 ? n % SM::NXI_DIV : 0;
     const uint8_t* xb = xib + xs * kXiBytes;
     // The dither XD blocks ahead: half of the warps (two per scheduler) make their share before
     // this block's logits, the other half between its softmax and its P.V product, so that the
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
     if (active && !fault && n < nbw) {
       if (!mbar_wait(smem_addr(&bars[stage]), par, kWaitLimitNs) ||
-          (SCHEME == kInt8 && !mbar_wait(smem_addr(&xfull[xs]), (uint32_t)((n / SM::NXI) & 1), kWaitLimitNs))) {
+          (SCHEME == kInt8 && !mbar_wait(smem_addr(&xfull[xs]), (uint32_t)((n / SM::NXI_DIV) & 1), kWaitLimitNs))) {
         fault = true;
         if (lane == 0) atomicAdd(p.err, 1);
       }

@@ -388,8 +388,8 @@ static witcert_status write_impl(witcert_cache* c, int layer, const void* K, con
   if (uniform) {
     const int n_tok = n[0], t0 = c->len[layer];
     WriteArgs a = layer_write_args(c, layer, K, V, Kh, Vh, n_tok, t0);
-    // a paged store's table update precedes the write kernels, which must see it complete
-    a.late_wait = c->table == nullptr;
+    // a page-table update launched just before must be complete before the writers read it
+    a.late_wait = pages.empty();
     if (c->backing_host && n_tok >= kBulkBackingTokens) {
       // bulk writes copy their exact keys to the pinned backing store with the copy engines
       // instead of the kernels' stores over C2C
