@@ -221,7 +221,7 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
 // The token at position t (row r = t mod 16 of its block) of sequence i, KV head h, whose
 // input row starts at element `row` of K and V, quantized into the block image at bp (device
 // memory or shared memory).
-template <typename T, bool DITHER>
+template <typename T, bool DITHER, bool VW>
 __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
   const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
@@ -244,7 +244,7 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     Df rdf[4];
     float err = 0.f;
     int clamps = 0;
-    const bool resid = tensor == 0 || a.vwit;
+    const bool resid = tensor == 0 || VW;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int code = 0;
@@ -280,7 +280,7 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
         store_witness(bp + Int8Layout::W, r, res, lane, repaired);
       }
-    } else if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
+    } else if (VW && !store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
       double res[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
@@ -375,10 +375,10 @@ __device__ __forceinline__ size_t uniform_row(const WriteArgs& a, int i, int n, 
   return (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
 }
 
-// One token of a write into the block image at bp, by scheme.
-template <typename T, int SCH>
+// One token of a write into the block image at bp, by scheme (VW: with value witnesses).
+template <typename T, int SCH, bool VW>
 __device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
-  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8>(a, bp, i, h, t, row, lane);
+  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8, VW>(a, bp, i, h, t, row, lane);
   else if constexpr (SCH == kFp8) fp8_token<T>(a, bp, i, h, t, row, lane);
   else bbox_token<T>(a, bp, i, h, t, row, lane);
 }
@@ -386,7 +386,7 @@ __device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int
 
 // One warp per (sequence, token, KV head) of tokens tok_begin .. tok_begin + tok_count - 1:
 // appends and the parts of a write that do not fill whole blocks.
-template <typename T, int SCH>
+template <typename T, int SCH, bool VW>
 __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   const ChainEntry chain(a.late_wait != 0);
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -395,14 +395,14 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   const int blk = (a.t0 + n) >> 4;
   constexpr int kBytes = block_bytes(SCH);
   uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes;
-  write_token<T, SCH>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
+  write_token<T, SCH, VW>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
 }
 
 // One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
 // completely: the warp builds the block's image in shared memory token by token and stores
 // it with 16-byte writes.
-template <typename T, int SCH>
-__global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
+template <typename T, int SCH, bool VW>
+__global__ void __launch_bounds__(128, 6) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
   const ChainEntry chain(a.late_wait != 0);
   constexpr int kBytes = block_bytes(SCH);
   __shared__ __align__(16) uint8_t img[4][kBytes];
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(128) write_block_kernel(const WriteArgs a, int
   uint8_t* im = img[warp];
   for (int r = 0; r < kBlk; ++r) {
     const int t = blk * kBlk + r;
-    write_token<T, SCH>(a, im, i, h, t, uniform_row(a, i, t - a.t0, h), lane);
+    write_token<T, SCH, VW>(a, im, i, h, t, uniform_row(a, i, t - a.t0, h), lane);
   }
   __syncwarp();
   uint4* dst = reinterpret_cast<uint4*>(a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes);
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(128) write_kivi_v_kernel(const WriteArgs a) {
 // Ragged appends: sequence seq[k] (k < n_seq) gets its off[k+1] - off[k] tokens, packed from
 // input row row0[k] on, at positions t0[k], t0[k] + 1, ...  One warp per (token of the launch,
 // KV head); KIVI keys are handled per sequence by write_kivi_k_kernel.
-template <typename T, int SCH>
+template <typename T, int SCH, bool VW>
 __global__ void __launch_bounds__(128) write_ragged_kernel(const WriteArgs a, const RaggedArgs g) {
   pdl_wait();
   pdl_trigger();
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(128) write_ragged_kernel(const WriteArgs a, co
   const size_t row = ((size_t)(g.row0[lo] + (tok - g.off[lo])) * a.Hkv + h) * kD;
   uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * block_bytes(SCH);
   if constexpr (SCH == kKivi) kivi_v_token<T>(a, bp, i, h, t, row, lane);
-  else write_token<T, SCH>(a, bp, i, h, t, row, lane);
+  else write_token<T, SCH, VW>(a, bp, i, h, t, row, lane);
 }
 
 // Per-sequence lengths on the device ([B] of one layer), set from the launch's parameters.
@@ -646,20 +646,27 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
       b.tok_begin = begin;
       b.tok_count = count;
       const dim3 g(((unsigned)(a.B * count * a.Hkv) * 32u + 127u) / 128u);
-      return scheme == kInt8  ? launch_pdl(write_token_kernel<T, kInt8>, g, dim3(128), st, pdl, b)
-             : scheme == kRtn ? launch_pdl(write_token_kernel<T, kRtn>, g, dim3(128), st, pdl, b)
-             : scheme == kFp8 ? launch_pdl(write_token_kernel<T, kFp8>, g, dim3(128), st, pdl, b)
-                              : launch_pdl(write_token_kernel<T, kBbox>, g, dim3(128), st, pdl, b);
+      const bool vw = a.vwit != nullptr;        // the INT8 writers compile the value witness in or out
+      return scheme == kInt8  ? (vw ? launch_pdl(write_token_kernel<T, kInt8, true>, g, dim3(128), st, pdl, b)
+                                    : launch_pdl(write_token_kernel<T, kInt8, false>, g, dim3(128), st, pdl, b))
+             : scheme == kRtn ? (vw ? launch_pdl(write_token_kernel<T, kRtn, true>, g, dim3(128), st, pdl, b)
+                                    : launch_pdl(write_token_kernel<T, kRtn, false>, g, dim3(128), st, pdl, b))
+             : scheme == kFp8 ? launch_pdl(write_token_kernel<T, kFp8, false>, g, dim3(128), st, pdl, b)
+                              : launch_pdl(write_token_kernel<T, kBbox, false>, g, dim3(128), st, pdl, b);
     };
     if (hi_full <= lo_full) return tokens(0, a.n_tok);
     cudaError_t e = tokens(0, lo_full - a.t0);
     if (e != cudaSuccess) return e;
     const int nblocks = (hi_full - lo_full) / kBlk;
     const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + 3) / 4));
-    e = scheme == kInt8  ? launch_pdl(write_block_kernel<T, kInt8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
-        : scheme == kRtn ? launch_pdl(write_block_kernel<T, kRtn>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
-        : scheme == kFp8 ? launch_pdl(write_block_kernel<T, kFp8>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks)
-                         : launch_pdl(write_block_kernel<T, kBbox>, g, dim3(128), st, pdl, a, lo_full / kBlk, nblocks);
+    const int b0 = lo_full / kBlk;
+    const bool vw = a.vwit != nullptr;
+    e = scheme == kInt8  ? (vw ? launch_pdl(write_block_kernel<T, kInt8, true>, g, dim3(128), st, pdl, a, b0, nblocks)
+                               : launch_pdl(write_block_kernel<T, kInt8, false>, g, dim3(128), st, pdl, a, b0, nblocks))
+        : scheme == kRtn ? (vw ? launch_pdl(write_block_kernel<T, kRtn, true>, g, dim3(128), st, pdl, a, b0, nblocks)
+                               : launch_pdl(write_block_kernel<T, kRtn, false>, g, dim3(128), st, pdl, a, b0, nblocks))
+        : scheme == kFp8 ? launch_pdl(write_block_kernel<T, kFp8, false>, g, dim3(128), st, pdl, a, b0, nblocks)
+                         : launch_pdl(write_block_kernel<T, kBbox, false>, g, dim3(128), st, pdl, a, b0, nblocks);
     if (e != cudaSuccess) return e;
     return tokens(hi_full - a.t0, t_end - hi_full);
   }
@@ -674,11 +681,13 @@ cudaError_t launch_ragged_t(int scheme, const WriteArgs& a, const RaggedArgs& g,
   if (total == 0) return cudaSuccess;
   const dim3 grid((unsigned)(((long long)total * a.Hkv * 32 + 127) / 128));
   switch (scheme) {
-    case kInt8: return launch_pdl(write_ragged_kernel<T, kInt8>, grid, dim3(128), st, pdl, a, g);
-    case kRtn: return launch_pdl(write_ragged_kernel<T, kRtn>, grid, dim3(128), st, pdl, a, g);
-    case kFp8: return launch_pdl(write_ragged_kernel<T, kFp8>, grid, dim3(128), st, pdl, a, g);
-    case kKivi: return launch_pdl(write_ragged_kernel<T, kKivi>, grid, dim3(128), st, pdl, a, g);
-    default: return launch_pdl(write_ragged_kernel<T, kBbox>, grid, dim3(128), st, pdl, a, g);
+    case kInt8: return a.vwit ? launch_pdl(write_ragged_kernel<T, kInt8, true>, grid, dim3(128), st, pdl, a, g)
+                              : launch_pdl(write_ragged_kernel<T, kInt8, false>, grid, dim3(128), st, pdl, a, g);
+    case kRtn: return a.vwit ? launch_pdl(write_ragged_kernel<T, kRtn, true>, grid, dim3(128), st, pdl, a, g)
+                             : launch_pdl(write_ragged_kernel<T, kRtn, false>, grid, dim3(128), st, pdl, a, g);
+    case kFp8: return launch_pdl(write_ragged_kernel<T, kFp8, false>, grid, dim3(128), st, pdl, a, g);
+    case kKivi: return launch_pdl(write_ragged_kernel<T, kKivi, false>, grid, dim3(128), st, pdl, a, g);
+    default: return launch_pdl(write_ragged_kernel<T, kBbox, false>, grid, dim3(128), st, pdl, a, g);
   }
 }
 
