@@ -1,0 +1,45 @@
+"""Host-side helpers of bench.py (no GPU): the kernel-source digest that keys recorded
+profile counters, the ragged-context draw and the per-token byte accounting."""
+import importlib.util
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_module", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_kernel_digest_ignores_comments_but_not_code(bench, tmp_path):
+    a = tmp_path / "a.cuh"
+    a.write_text("// header\nint f(int x) {\n  return x + 1;   // one more\n}\n")
+    b = tmp_path / "b.cuh"
+    b.write_text("int f(int x) {\n\n  return x + 1;\n}\n// trailing note\n")
+    c = tmp_path / "c.cuh"
+    c.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.kernel_digest(a) == bench.kernel_digest(b)
+    assert bench.kernel_digest(a) != bench.kernel_digest(c)
+    assert len(bench.kernel_digest(a)) == 16
+
+
+def test_ragged_lengths_are_seeded_and_in_range(bench):
+    from workload import WORKLOADS
+    w = WORKLOADS["qwen_28l"]
+    lens = bench.ragged_lengths(w, "512:4096")
+    assert lens == bench.ragged_lengths(w, "512:4096")
+    assert len(lens) == w.batch and all(512 <= n <= 4096 for n in lens) and len(set(lens)) > 1
+    assert bench.ragged_lengths(w, None) == [w.context] * w.batch
+    with pytest.raises(AssertionError):
+        bench.ragged_lengths(w, "512:99999")
+
+
+def test_bytes_per_token_head_match_the_oracle_accounting(bench):
+    from oracle import quant
+    assert bench.BYTES_PER_TOK_HEAD == quant.BYTES_PER_TOKEN_HEAD
+    assert bench.tok_head_bytes("int8_dither", True) == 304 + quant.V_WITNESS_BYTES
