@@ -270,14 +270,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     if constexpr (PAGED) return base + ((size_t)p.table[(size_t)i * p.nblk_max + b_begin + m] * p.Hkv + h) * L::BYTES;
     else return base + (seq_base + b_begin + m) * L::BYTES;
   };
-  // one stage: the block and (value witnesses on) its 32 bytes of value witnesses
-  auto stage_copy = [&](int s, int m) {
+  // one stage: the block (from g) and (value witnesses on) its 32 bytes of value witnesses
+  auto stage_copy_from = [&](int s, int m, const uint8_t* g) {
     mbar_expect_tx(smem_addr(&bars[s]), L::BYTES + (VW ? kVwBytes : 0));
-    bulk_g2s(smem_addr(ring + s * STB), PAGED ? block_src(p.blocks, m) : src + (size_t)m * L::BYTES, L::BYTES,
-             smem_addr(&bars[s]));
+    bulk_g2s(smem_addr(ring + s * STB), g, L::BYTES, smem_addr(&bars[s]));
     if (VW)
       bulk_g2s(smem_addr(ring + s * STB + L::BYTES), p.vwit + (seq_base + b_begin + m) * kBlk, kVwBytes,
                smem_addr(&bars[s]));
+  };
+  auto stage_copy = [&](int s, int m) {
+    stage_copy_from(s, m, PAGED ? block_src(p.blocks, m) : src + (size_t)m * L::BYTES);
   };
 
   // ---------------------------------------------------------------- prologue
@@ -431,7 +433,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   for (int G = 0; G < 4; ++G) qgp[G] = make_float2(qg2[0][G], qg2[1][G]);
 
   const bool gen_early = ((warp >> 2) & 1) == 0;
+  // paged store: the page of the block the refill will stage, loaded a block ahead so its
+  // latency is off the refill's path
+  int32_t page_ahead = 0;
   for (int n = 0; n < nb; ++n) {
+    if constexpr (PAGED) {
+      if (active && lane == 0 && n + NST < nbw) page_ahead = p.table[(size_t)i * p.nblk_max + b_begin + n + NST];
+    }
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
     const int xs = SCHEME == kInt8 ? n % SM::NXI_DIV : 0;
@@ -781,7 +789,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       if (lane == 0 && n + NST < nbw) {
         if (blk + NST >= p.dirty_blk) pdl_wait();
         fence_proxy_async();
-        stage_copy(stage, n + NST);
+        if constexpr (PAGED)
+          stage_copy_from(stage, n + NST, p.blocks + ((size_t)page_ahead * p.Hkv + h) * L::BYTES);
+        else
+          stage_copy(stage, n + NST);
       }
     }
     if (SCHEME == kInt8) {            // this warp is done with the block's dither slot
