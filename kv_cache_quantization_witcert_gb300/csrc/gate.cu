@@ -21,7 +21,7 @@ namespace witcert {
 
 namespace {
 
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
 constexpr int kRun = 32;
 
 __device__ __forceinline__ double key_risk(unsigned long long key) {
