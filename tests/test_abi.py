@@ -66,3 +66,29 @@ def test_header_documents_each_entry_point():
         while prev >= 0 and not lines[prev].strip():
             prev -= 1
         assert lines[prev].strip().endswith("*/") or "/*" in lines[k], f"{n} has no comment"
+
+
+def test_new_entry_points_reject_bad_arguments_without_the_gpu(lib_path):
+    """Argument checks of the ragged, reset, paged and merge entry points come before any CUDA call."""
+    import ctypes
+
+    import kv_cache_quantization_witcert_gb300 as w
+    from kv_cache_quantization_witcert_gb300 import _lib
+    lib = w.load()
+    h = ctypes.c_void_p()
+    neg_pages = _lib.witcert_config(1, 4, 2, 128, 1, 16, 0, _lib.BF16, 0, 1, 0, 0, 0, 0, -1)
+    assert lib.witcert_create(ctypes.byref(neg_pages), ctypes.byref(h)) == _lib.EINVAL
+    paged_f32 = _lib.witcert_config(1, 4, 2, 128, 1, 16, 0, _lib.F32, 0, 1, 0, 0, 0, 0, 8)
+    assert lib.witcert_create(ctypes.byref(paged_f32), ctypes.byref(h)) == _lib.EINVAL
+    assert b"bf16" in lib.witcert_last_error()
+    bad_scheme = _lib.witcert_config(1, 4, 2, 128, 1, 16, 9, _lib.BF16, 0, 1, 0, 0, 0, 0, 0)
+    assert lib.witcert_create(ctypes.byref(bad_scheme), ctypes.byref(h)) == _lib.EINVAL
+    counts = (ctypes.c_int32 * 1)(1)
+    assert lib.witcert_write_ragged(None, 0, None, None, None, None, counts, None) == _lib.EINVAL
+    assert lib.witcert_reset_sequence(None, 0, None) == _lib.EINVAL
+    n = ctypes.c_int()
+    assert lib.witcert_seq_length(None, 0, 0, ctypes.byref(n)) == _lib.EINVAL
+    assert lib.witcert_write_hat(None, 0, None, None, None, None, 1, None) == _lib.EINVAL
+    assert lib.witcert_merge_partials(None, 1, 1, 1, 0, None, None, None, None, None, None, None) == _lib.EINVAL
+    fake = ctypes.c_void_p(1)
+    assert lib.witcert_merge_partials(fake, 1, 1, 1, 7, fake, None, None, None, None, None, None) == _lib.EINVAL
