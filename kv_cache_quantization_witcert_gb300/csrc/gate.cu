@@ -41,21 +41,32 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateArgs
   const float* risk = a.risk + (size_t)cell * a.nblk_max;
   const int32_t* slots = a.slots + ((size_t)i * a.Hkv + h) * a.nblk_max;
   if (threadIdx.x == 0) { s_n = 0; s_jmax = -1; }
+  __syncthreads();
+  // the cell's candidate keys, packed to the front in any order (the sort ranks them), so the
+  // sort covers the next power of two above the candidates rather than above the blocks
   double part = 0.0;
-  int cnt = 0;
-  for (int b = threadIdx.x; b < npow2; b += blockDim.x) {
-    unsigned long long key = ~0ull;
-    if (b < nblk && slots[b] < 0) {
+  const int lane = threadIdx.x & 31;
+  for (int b0 = 0; b0 < nblk; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    const bool cand = b < nblk && slots[b] < 0;
+    unsigned long long key = 0ull;
+    if (cand) {
       const float r = risk[b];
       part += (double)r;
-      ++cnt;
       key = ((unsigned long long)(~__float_as_uint(r)) << 32) | (unsigned int)b;
     }
-    keys[b] = key;
+    const unsigned int ballot = __ballot_sync(0xffffffffu, cand);
+    int base = 0;
+    if (lane == 0 && ballot) base = atomicAdd(&s_n, __popc(ballot));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (cand) keys[base + __popc(ballot & ((1u << lane) - 1u))] = key;
   }
   red[threadIdx.x] = part;
   __syncthreads();
-  if (cnt) atomicAdd(&s_n, cnt);
+  const int n = s_n;
+  int npc = 1;
+  while (npc < n) npc <<= 1;                   // <= npow2: n <= nblk
+  for (int k = n + threadIdx.x; k < npc; k += blockDim.x) keys[k] = ~0ull;
   for (int s = blockDim.x / 2; s; s >>= 1) {
     if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
@@ -63,12 +74,11 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(const GateArgs
   // a parallel sum differs from the run-ordered one by far less than 1e-9 relative:
   // cells clearly below D* skip the ordered sums
   if (red[0] <= a.d_star * (1.0 - 1e-9)) return;
-  const int n = s_n;
   // bitonic sort, ascending keys = descending risk then ascending block; each thread
   // takes compare-exchange pairs (x, x + jj) directly, x having bit jj clear
-  for (int k = 2; k <= npow2; k <<= 1) {
+  for (int k = 2; k <= npc; k <<= 1) {
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int pr = threadIdx.x; pr < (npow2 >> 1); pr += blockDim.x) {
+      for (int pr = threadIdx.x; pr < (npc >> 1); pr += blockDim.x) {
         const int x = ((pr & ~(jj - 1)) << 1) | (pr & (jj - 1)), y = x + jj;
         const unsigned long long kx = keys[x], ky = keys[y];
         const bool up = (x & k) == 0;
