@@ -188,10 +188,11 @@ cudaError_t launch_decode(int scheme, const DecodeArgs& a0, int sm_count, cudaSt
   dim3 grid(a.n_splits, a.Hkv, groups);
   // event boundaries around a timed split (and an event wait before it) get a plain launch
   const bool pdl = pdl_allowed && split_start == nullptr;
-  if (split_start) cudaEventRecord(split_start, st);
-  cudaError_t e = dispatch_scheme(scheme, a, grid, st, pdl, nullptr);
-  if (split_stop) cudaEventRecord(split_stop, st);
+  cudaError_t e = split_start ? cudaEventRecord(split_start, st) : cudaSuccess;
   if (e != cudaSuccess) return e;
+  e = dispatch_scheme(scheme, a, grid, st, pdl, nullptr);
+  if (e != cudaSuccess) return e;
+  if (split_stop && (e = cudaEventRecord(split_stop, st)) != cudaSuccess) return e;
   const dim3 mg(a.B * a.Hq);
   const bool risk = a.risk_raw != nullptr && a.meter;
   if (scheme == kInt8)
