@@ -507,6 +507,9 @@ witcert_status witcert_reset_sequence(witcert_cache* c, int seq, void* stream) {
   for (int l = 0; l < c->cfg.n_layers && e == cudaSuccess && c->slots; ++l)
     e = cudaMemsetAsync(c->slots + (size_t)l * layer_rows(c) * c->nblk_max + (size_t)seq * rows, 0xFF,
                         rows * sizeof(int32_t), st);
+  // value witnesses past the next occupant's length are read (with weight 0): keep them zero
+  for (int l = 0; l < c->cfg.n_layers && e == cudaSuccess && c->vwit; ++l)
+    e = cudaMemsetAsync(c->vwit + l * vwit_layer(c) + (size_t)seq * rows * kBlk, 0, rows * kBlk * sizeof(__half), st);
   if (e != cudaSuccess) return cuda_fail(e, "reset");
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     c->slen[l][seq] = 0;
