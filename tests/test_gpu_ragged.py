@@ -247,3 +247,28 @@ def test_paged_uniform_writes_and_pool_exhaustion(scheme):
     assert rg.gpu.witcert_stats()["pages_used"] == 26 + 7
     rg.check_store(0)
     rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
+
+
+def test_reset_clears_value_witnesses_of_the_last_block():
+    """Black-box scheme: a sequence whose value witnesses overflowed to +inf (the caller's f(V)
+    is 1e5 off in channel 0) is reset and refilled with 10 tokens.  Rows 10..15 of its last block
+    are read with weight 0, so they must hold zero, not the stale +inf (0 x inf would make the
+    value meter NaN)."""
+    w = WORKLOADS["qwen_1l"].with_(batch=2, context=40, steps=2, scheme="blackbox")
+    rg = Ragged(w, "blackbox", cap=64)
+    K, V = gen_kv(w, 0)
+    Kd, Vd = rg.dev(K[1, :40]), rg.dev(V[1, :40])
+    Vh = V[1, :40].copy()
+    Vh[..., 0] += 1e5
+    rg.gpu.witcert_write_ragged(0, Kd, Vd, [0, 40], rg.dev(tensor_function(K[1, :40], 3)), rg.dev(Vh))
+    wv = rg.gpu.export(0, _lib.X_V_WITNESS).cpu().numpy()
+    assert np.all(np.isposinf(wv[1, :40]))
+    rg.gpu.witcert_reset_sequence(1)
+    rg.refs[1] = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, "blackbox", w.seed, w.steps, v_witness=True)
+    K2, V2 = gen_kv(w.with_(context=20), 4)
+    rg.write(0, list(zip(_split(K2, [20, 10]), _split(V2, [20, 10]))))
+    rg.check_store(0)
+    wv = rg.gpu.export(0, _lib.X_V_WITNESS).cpu().numpy()
+    assert not np.any(wv[1, 10:16])
+    _, mm, _ = rg.check_decode(0, gen_q(w, 0, 0), w.delta_req)
+    assert np.all(np.isfinite(mm["meter_v"]))
