@@ -12,7 +12,7 @@ from oracle import OracleCache, meter, quant
 from oracle.philox import dither
 
 # Meters: GPU >= oracle (one fp32 ulp of slack for rounding the oracle's value to fp32)
-# and GPU <= oracle * (1 + 1e-4).
+# and GPU <= oracle * (1 + 1e-4); a GPU NaN where the oracle has a number fails.
 METER_REL = 1e-4
 FP32_ULP = 2.0 ** -23
 
@@ -65,10 +65,11 @@ def check_meter(gpu, ref, rel=METER_REL, what=""):
     r = np.asarray(ref, np.float64)
     low = g < r * (1 - FP32_ULP)
     high = g > r * (1 + rel) + 1e-30
-    if low.any() or high.any():
-        idx = np.argwhere(low | high)[:5]
+    nan = np.isnan(g) & ~np.isnan(r)          # a NaN bounds nothing and fails both comparisons
+    if low.any() or high.any() or nan.any():
+        idx = np.argwhere(low | high | nan)[:5]
         detail = [(tuple(ix), g[tuple(ix)], r[tuple(ix)]) for ix in idx]
-        raise AssertionError(f"{what}: {low.sum()} below, {high.sum()} above tolerance: {detail}")
+        raise AssertionError(f"{what}: {low.sum()} below, {high.sum()} above tolerance, {nan.sum()} NaN: {detail}")
 
 
 def check_write(gpu, ref, layer, scheme):
