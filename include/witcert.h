@@ -142,8 +142,12 @@ witcert_status witcert_write(witcert_cache* cache, int layer, const void* K, con
  * K, V as in witcert_write; K_hat, V_hat are the tensor function's outputs f(K), f(V)
  * in the same layout and dtype.  The cache stores bf16(K_hat), bf16(V_hat) (nearest
  * even; unchanged for bf16 inputs), and the key witness w_{t,b} = ||K - bf16(K_hat)||
- * of each band, so the decode and the bound use exactly what is stored.  EINVAL on a
- * cache of another scheme (which takes witcert_write) and as witcert_write otherwise. */
+ * of each band, so the decode and the bound use exactly what is stored.  K_hat and V_hat
+ * must be finite: the rows of a sequence's last block past its length take part in the
+ * decode's P.V product with weight 0, and a non-finite value left there (by the rows'
+ * occupant before a reset, or in a page that held another sequence) makes 0 x inf a NaN in
+ * that later sequence's output.  EINVAL on a cache of another scheme (which takes
+ * witcert_write) and as witcert_write otherwise. */
 witcert_status witcert_write_hat(witcert_cache* cache, int layer, const void* K, const void* V,
                                  const void* K_hat, const void* V_hat, int n_tok, void* stream);
 
@@ -163,7 +167,10 @@ witcert_status witcert_write_ragged(witcert_cache* cache, int layer, const void*
 
 /* Empty sequence `seq` in every layer so the slot can serve a new request (continuous
  * batching).  Its repairs are dropped too (their slots in the exact-key pool are not
- * reused).  Asynchronous on `stream`; decodes issued after it see the sequence empty. */
+ * reused), a paged cache returns its pages to the pool, and its value witnesses are zeroed
+ * (the decode weighs the rows past a length by 0, which needs finite values there).
+ * Asynchronous on `stream`; decodes issued after it see the sequence empty.  EINVAL if
+ * seq is out of range. */
 witcert_status witcert_reset_sequence(witcert_cache* cache, int seq, void* stream);
 
 /* Fused metered split-KV decode [summary, implementation paragraph (output
