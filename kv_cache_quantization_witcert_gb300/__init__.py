@@ -29,6 +29,37 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _extent(t, i):
+    """Extent i of a tensor argument, or None when it has none (_need then rejects it)."""
+    return t.shape[i] if isinstance(t, torch.Tensor) and t.dim() > i else None
+
+
+def _need(*specs):
+    """Check the tensors a call hands the library, each spec (name, tensor, dtype, shape[,
+    optional]) with None in shape for any extent: contiguous tensors of that dtype and shape,
+    then all on a CUDA device.  The C ABI takes bare pointers, so a host tensor or a short
+    buffer would reach a kernel; the binding raises ValueError instead."""
+    given = []
+    for name, t, dtype, shape, *opt in specs:
+        if t is None:
+            if opt and opt[0]:
+                continue
+            raise ValueError(f"{name} must not be None")
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name} must be a torch.Tensor, got {type(t).__name__}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+        if t.dim() != len(shape) or any(e is not None and e != x for e, x in zip(shape, t.shape)):
+            want = tuple("*" if e is None else e for e in shape)
+            raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+        given.append((name, t))
+    for name, t in given:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
 class Cache:
     """One WitCert cache: compressed K/V store, witnesses, optional gate state."""
 
@@ -48,25 +79,40 @@ class Cache:
         self._h = h
 
     # ------------------------------------------------------------------ ABI calls
+    def _kv_shape(self, n_tok=None):
+        return (self.cfg.batch, n_tok, self.cfg.n_kv_heads, 128)
+
+    def _q_shape(self, last=128):
+        return (self.cfg.batch, self.cfg.n_q_heads, last)
+
+    def _decode_args(self, q, out, meters):
+        names = ("meter_a", "meter_b", "raw_a", "raw_b", "meter_v")
+        _need(("q", q, self.dtype, self._q_shape()), ("out", out, torch.float32, self._q_shape()),
+              *((n, m, torch.float32, self._q_shape()[:2], True) for n, m in zip(names, meters)))
+
     def witcert_write(self, layer, K, V, stream=None):
-        assert K.is_contiguous() and V.is_contiguous() and K.dtype == self.dtype and V.dtype == self.dtype
-        n_tok = K.shape[1]
+        """Append K, V [batch, n_tok, n_kv_heads, 128] to every sequence of `layer`."""
+        n_tok = _extent(K, 1)
+        _need(("K", K, self.dtype, self._kv_shape(n_tok)), ("V", V, self.dtype, self._kv_shape(n_tok)))
         check(load().witcert_write(self._h, layer, _ptr(K), _ptr(V), n_tok, _stream_ptr(stream)), "witcert_write")
 
     def witcert_write_hat(self, layer, K, V, K_hat, V_hat, stream=None):
         """Black-box scheme: K_hat, V_hat are the tensor function's outputs f(K), f(V)."""
-        for t in (K, V, K_hat, V_hat):
-            assert t.is_contiguous() and t.dtype == self.dtype and t.shape == K.shape
-        check(load().witcert_write_hat(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), K.shape[1],
+        n_tok = _extent(K, 1)
+        _need(*((name, t, self.dtype, self._kv_shape(n_tok)) for name, t in
+                (("K", K), ("V", V), ("K_hat", K_hat), ("V_hat", V_hat))))
+        check(load().witcert_write_hat(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), n_tok,
                                        _stream_ptr(stream)), "witcert_write_hat")
 
     def witcert_write_ragged(self, layer, K, V, n_tok, K_hat=None, V_hat=None, stream=None):
         """Ragged append: n_tok[i] tokens to sequence i; K, V (and K_hat, V_hat for black-box
         caches) packed sequence by sequence, [sum(n_tok), Hkv, 128]."""
         counts = [int(x) for x in n_tok]
-        assert len(counts) == self.cfg.batch
-        for t in (K, V) + tuple(x for x in (K_hat, V_hat) if x is not None):
-            assert t.is_contiguous() and t.dtype == self.dtype and t.shape[0] == sum(counts)
+        if len(counts) != self.cfg.batch:
+            raise ValueError(f"n_tok needs one count per sequence ({self.cfg.batch}), got {len(counts)}")
+        shape = (sum(counts), self.cfg.n_kv_heads, 128)
+        _need(("K", K, self.dtype, shape), ("V", V, self.dtype, shape), ("K_hat", K_hat, self.dtype, shape, True),
+              ("V_hat", V_hat, self.dtype, shape, True))
         arr = (ctypes.c_int32 * len(counts))(*counts)
         check(load().witcert_write_ragged(self._h, layer, _ptr(K), _ptr(V), _ptr(K_hat), _ptr(V_hat), arr,
                                           _stream_ptr(stream)), "witcert_write_ragged")
@@ -81,20 +127,20 @@ class Cache:
 
     def witcert_decode(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
                        meter_v=None, stream=None):
-        assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
+        self._decode_args(q, out, (meter_a, meter_b, raw_a, raw_b, meter_v))
         check(load().witcert_decode(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
                                     _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _ptr(meter_v), _stream_ptr(stream)),
               "witcert_decode")
 
     def witcert_decode_noalloc(self, layer, q, delta_req, out, meter_a=None, meter_b=None, raw_a=None, raw_b=None,
                                meter_v=None, stream=None):
-        assert q.is_contiguous() and q.dtype == self.dtype and out.dtype == torch.float32
+        self._decode_args(q, out, (meter_a, meter_b, raw_a, raw_b, meter_v))
         check(load().witcert_decode_noalloc(self._h, layer, _ptr(q), float(delta_req), _ptr(out), _ptr(meter_a),
                                             _ptr(meter_b), _ptr(raw_a), _ptr(raw_b), _ptr(meter_v),
                                             _stream_ptr(stream)), "witcert_decode_noalloc")
 
     def witcert_decode_partial(self, layer, q, delta_req, s_total, part, stream=None):
-        assert q.is_contiguous() and q.dtype == self.dtype and part.dtype == torch.float32 and part.is_contiguous()
+        _need(("q", q, self.dtype, self._q_shape()), ("part", part, torch.float32, self._q_shape(PART_STRIDE)))
         check(load().witcert_decode_partial(self._h, layer, _ptr(q), float(delta_req), int(s_total), _ptr(part),
                                             _stream_ptr(stream)), "witcert_decode_partial")
 
@@ -129,6 +175,7 @@ class Cache:
         return n.value
 
     def witcert_export(self, layer, what, dst, stream=None):
+        _need(("dst", dst, getattr(dst, "dtype", None), tuple(getattr(dst, "shape", ()))))   # the library checks the size
         check(load().witcert_export(self._h, layer, what, _ptr(dst), dst.numel() * dst.element_size(),
                                     _stream_ptr(stream)), "witcert_export")
 
@@ -186,10 +233,11 @@ PART_STRIDE = 136     # floats per (sequence, query head) record: m, Z, S_A, S_B
 def witcert_merge_partials(parts, scheme, out=None, meters=True, stream=None):
     """Merge shard records parts [B, Hq, n_parts, 136] (device fp32) into the output [B, Hq, 128]
     and, with meters, {"meter_a", "meter_b", "raw_a", "raw_b", "meter_v"} (see witcert_merge_partials)."""
-    assert parts.dtype == torch.float32 and parts.is_contiguous() and parts.shape[-1] == PART_STRIDE
+    _need(("parts", parts, torch.float32, (None, None, None, PART_STRIDE)))
     B, Hq, n = parts.shape[0], parts.shape[1], parts.shape[2]
     if out is None:
         out = torch.empty((B, Hq, 128), dtype=torch.float32, device=parts.device)
+    _need(("out", out, torch.float32, (B, Hq, 128)))
     m = torch.empty((5, B, Hq), dtype=torch.float32, device=parts.device) if meters else None
     ptrs = tuple(_ptr(m[k]) for k in range(5)) if meters else (None,) * 5
     check(load().witcert_merge_partials(_ptr(parts), n, B, Hq, SCHEMES[scheme] if isinstance(scheme, str) else scheme,
@@ -207,6 +255,7 @@ def witcert_dither(seed, layer, kv_head, t0, n, tensor, out=None, stream=None):
     """Device dither xi [n, 128] float32 (see witcert_dither in include/witcert.h)."""
     if out is None:
         out = torch.empty((n, 128), dtype=torch.float32, device="cuda")
+    _need(("out", out, torch.float32, (n, 128)))
     check(load().witcert_dither(seed, layer, kv_head, t0, n, tensor, _ptr(out), _stream_ptr(stream)),
           "witcert_dither")
     return out
