@@ -92,6 +92,25 @@ def ragged_lengths(w, spec):
     return [int(x) for x in np.random.default_rng(w.seed + 7).integers(lo, hi + 1, size=w.batch)]
 
 
+def timed_launches(scheme, n_layers, lens0, steps, ragged, paged):
+    """Kernels the library launches over `steps` decode steps of one appended token per
+    sequence, from the per-sequence lengths lens0 at the first step.  Per layer and step: the
+    writer (KIVI: the values, then the keys of the block the token lands in), the split kernel
+    and the merge.  A cache whose sequences have different lengths instead pushes the new
+    lengths and writes through the ragged kernel, up to 128 sequences per launch (KIVI adds one
+    key launch per sequence).  A paged cache pushes page-table entries in the first layer of
+    every step in which a sequence starts a new 16-token block."""
+    B, kivi = len(lens0), scheme == "kivi2"
+    per128 = -(-B // 128)
+    write = 2 * per128 + (B if kivi else 0) if ragged else (2 if kivi else 1)
+    n = steps * n_layers * (write + 2)
+    if paged:
+        for s in range(steps):
+            starts = sum(1 for n0 in lens0 if (n0 + s) % 16 == 0)
+            n += -(-starts // 128)
+    return n
+
+
 def config_of(w, args, n_splits, world):
     vw = getattr(args, "v_witness", False)
     rg = getattr(args, "ragged", None)
@@ -371,7 +390,6 @@ def run_ours(args, w):
 
     dev_inputs = [make_args(di) for di in dev_inputs]
 
-    lens = []
     for s in range(args.warmup):
         one_step(dev_inputs[s % 8])
     torch.cuda.synchronize()
@@ -459,7 +477,8 @@ def run_ours(args, w):
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_tokens / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-                "gpu_launches": 3 * wl.n_layers * args.steps,
+                "gpu_launches": timed_launches(wl.scheme, wl.n_layers, lens0, args.steps, len(set(lens)) > 1,
+                                               bool(args.paged)),
                 "prefill_write": {"gbs": prefill_gbs, "frac": prefill_gbs / peak, "ms": prefill_ms,
                                   "tok_heads": prefill_tok_heads, "bytes_per_tok_head": prefill_read + tbytes},
                 "clocks": clk,

@@ -43,3 +43,19 @@ def test_bytes_per_token_head_match_the_oracle_accounting(bench):
     from oracle import quant
     assert bench.BYTES_PER_TOK_HEAD == quant.BYTES_PER_TOKEN_HEAD
     assert bench.tok_head_bytes("int8_dither", True) == 304 + quant.V_WITNESS_BYTES
+
+
+def test_timed_launch_count_follows_the_write_path(bench):
+    """Three launches per layer and step on the default path (writer, split, merge); KIVI adds
+    its key writer; a ragged cache adds the length push; a paged cache adds one page-table push
+    in each step where a sequence starts a block."""
+    t = bench.timed_launches
+    assert t("int8_dither", 28, [4096] * 16, 10, False, False) == 3 * 28 * 10
+    assert t("fp8_e4m3", 28, [4096] * 16, 10, False, False) == 3 * 28 * 10
+    assert t("kivi2", 28, [4096] * 16, 10, False, False) == 4 * 28 * 10
+    assert t("int8_dither", 28, [600, 4000], 10, True, False) == 4 * 28 * 10
+    assert t("kivi2", 2, [600, 4000], 10, True, False) == (4 + 2) * 2 * 10
+    # one sequence at 4096 starts a block at steps 0 and 16; two at 4100 both start one at
+    # step 12, which takes one push
+    assert t("int8_dither", 1, [4096], 20, False, True) == 3 * 20 + 2
+    assert t("int8_dither", 1, [4100, 4100], 20, True, True) == 4 * 20 + 1
