@@ -1,7 +1,7 @@
 """Parity at the full sizes of the long-context workloads, on sampled outputs.
 
-The 32768-token sweep points (Mistral-7B and Yi-1.5-6B shaped) and the gated-repair
-workload (Qwen2.5-7B shaped, batch 8 x 32768, raw-cast FP8 with the gate) are run at
+Long-context sweep points (Mistral-7B and Yi-1.5-6B shaped) at 32768 tokens and at the
+sweep's longest context, 131072 tokens, and the gated-repair workload (Qwen2.5-7B shaped, batch 8 x 32768, raw-cast FP8 with the gate) are run at
 their full batch, head and context sizes, one layer each: a layer's launch configuration
 (split count, CTAs, sequences per CTA) depends on the batch, heads and context, not on the
 layer count.  Sampled (sequence, KV head) groups are checked against the oracle computed
@@ -44,10 +44,12 @@ def check_group(w, o, m, r, i, h, V, tier_b):
         check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what=f"raw_b seq {i} head {h}")
 
 
-@pytest.mark.parametrize("model,batch,scheme", [("mistral", 16, "int8_dither"), ("yi", 8, "fp8_e4m3")])
-def test_long_context_sweep_point_sampled_groups(model, batch, scheme):
-    """One layer of a 32768-token sweep point (the bench sweeps four), automatic split count."""
-    w = sweep_workload(model, batch, LONG, scheme, n_layers=4)
+@pytest.mark.parametrize("model,batch,scheme,context", [("mistral", 16, "int8_dither", LONG), ("yi", 8, "fp8_e4m3", LONG),
+                                                         ("mistral", 1, "int8_dither", 4 * LONG)])
+def test_long_context_sweep_point_sampled_groups(model, batch, scheme, context):
+    """One layer of a sweep point (the bench sweeps four), automatic split count: two 32768-token
+    points and the sweep's longest context, 131072 tokens, for one sequence."""
+    w = sweep_workload(model, batch, context, scheme, n_layers=4)
     gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, w.context + 1, scheme, dtype=torch.bfloat16,
                    seed=w.seed, total_steps=w.steps)
     dl = meter.delta_loc(w.delta_req, w.n_layers, w.n_q_heads, w.steps)
