@@ -71,3 +71,11 @@ def test_merge_and_export_reject_host_buffers(cache):
         wc.witcert_merge_partials(parts, "int8_dither", out=torch.zeros((B, HQ, 128), dtype=torch.float32))
     with pytest.raises(ValueError, match="CUDA"):
         cache.witcert_export(0, _lib.X_WITNESS, torch.zeros(16, dtype=torch.float16))
+
+
+def test_non_tensor_arguments_are_named(cache):
+    import numpy as np
+    with pytest.raises(ValueError, match="K must be a torch.Tensor"):
+        cache.witcert_write(0, np.zeros((B, 3, HKV, 128), np.float32), kv())
+    with pytest.raises(ValueError, match="q must be a torch.Tensor"):
+        cache.witcert_decode(0, [[0.0]], 1e-2, torch.zeros((B, HQ, 128), dtype=torch.float32))
