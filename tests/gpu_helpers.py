@@ -1,8 +1,6 @@
 """Shared helpers of the GPU parity tests: run a workload through the library and the oracle."""
 from __future__ import annotations
 
-import math
-
 import numpy as np
 import torch
 

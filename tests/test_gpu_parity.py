@@ -1,6 +1,4 @@
 """GPU parity through the C ABI against the float64 oracle (needs a GB300)."""
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -9,10 +7,9 @@ import kv_cache_quantization_witcert_gb300 as wc
 from kv_cache_quantization_witcert_gb300 import _lib
 from oracle import meter
 from oracle.philox import dither
-from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload
+from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q
 
-from gpu_helpers import (check_decode, check_meter, check_write, make_pair, oracle_group, tensor_function, to_dev,
-                         write_both)
+from gpu_helpers import check_decode, check_meter, check_write, make_pair, oracle_group, to_dev, write_both
 
 pytestmark = pytest.mark.gpu
 
