@@ -18,7 +18,7 @@ import math
 import numpy as np
 import torch
 
-from oracle import OracleCache, fp, meter, quant
+from oracle import OracleCache, fp, meter
 
 
 # --------------------------------------------------------------------------- bfloat16 rounding

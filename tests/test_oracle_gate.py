@@ -3,7 +3,6 @@ import itertools
 import math
 
 import numpy as np
-import pytest
 
 from oracle import OracleCache, gate
 from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q

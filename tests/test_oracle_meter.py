@@ -6,7 +6,6 @@ import pytest
 import scipy.stats as st
 
 from oracle import OracleCache, meter, quant
-from oracle.philox import dither
 from workload import WORKLOADS, gen_kv, gen_q
 
 
