@@ -1,5 +1,8 @@
 """Meter-driven gate of the oracle: which exact key blocks to page in.
 
+Test infrastructure: a plain statement of the gate's selection rule, used by the tests,
+the smoke check and the benchmark's CPU baseline only, never by the library.
+
 Per the pages, once the meter passes a threshold the gate brings exact keys
 back from host memory a block at a time and clears the witnesses of what it
 repaired; it ranks by risk when the threshold is 1 or more and certifies below
@@ -16,69 +19,56 @@ those sentences (the pages state the behavior, not the rule):
   which brings the cell's meter to <= tau from the next step on;
 * a block is repaired once any query head of its KV head's group selects it.
 
-D and the remaining risks are suffix sums of the ranked risks in float64; the
-risks themselves are the fp32 values the decode reported.  Repaired blocks
-carry zero risk and are not ranked.  The pages fix no summation order; this
-reading fixes one so that the choice is reproducible bit for bit: the ranked
-list is cut into runs of RUN consecutive blocks, each run is summed from its
-lowest-ranked block upward, the run totals are summed from the last run
-upward, and the remaining risk after block j is (j's run-local suffix) + (the
-total of the runs after j's run).
+D and the remaining risks are the exact sums of the fp32 risks the decode
+reported (exact rationals: no summation order, no rounding), compared exactly
+with D*(tau) evaluated in float64 from tau as a float32 (the library's gate
+takes tau as a float).  Repaired blocks are not ranked.  A risk that is not a
+number counts as +infinity (such a block is always taken, first); a risk that
+is not positive counts as zero.
 """
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 
 import numpy as np
 
 
-def d_star(tau: float) -> float:
-    """Solution of D + D^2/2 = tau."""
-    return math.sqrt(1.0 + 2.0 * tau) - 1.0
+def d_star(tau) -> float:
+    """Solution of D + D^2/2 = tau, in float64, for tau rounded to float32."""
+    return math.sqrt(1.0 + 2.0 * float(np.float32(tau))) - 1.0
 
 
-RUN = 32
+def canonical_risk(r) -> float:
+    """The fp32 risk as the rule reads it: NaN -> +inf, anything not positive -> 0."""
+    x = float(np.float32(r))
+    if math.isnan(x):
+        return math.inf
+    return x if x > 0.0 else 0.0
 
 
-def suffix_sums(values):
-    """Remaining-risk sums of a ranked list: entry k = sum of values[k:], in the run order above;
-    entry len(values) = 0."""
-    n = len(values)
-    local = [0.0] * n
-    totals = []
-    for lo in range(0, n, RUN):
-        s = 0.0
-        for k in range(min(n, lo + RUN) - 1, lo - 1, -1):
-            s = s + float(values[k])
-            local[k] = s
-        totals.append(s)
-    after = [0.0] * len(totals)          # total of the runs after run c
-    u = 0.0
-    for c in range(len(totals) - 1, -1, -1):
-        after[c] = u
-        u = u + totals[c]
-    return [local[k] + after[k // RUN] for k in range(n)] + [0.0]
-
-
-def select_cell(risk_row, repaired, tau: float):
+def select_cell(risk_row, repaired, tau):
     """Blocks one (sequence, query head) cell asks for.  risk_row: fp32 [nblk]."""
-    r = np.asarray(risk_row, dtype=np.float32)
-    cand = np.nonzero(~np.asarray(repaired, bool))[0]
-    if cand.size == 0:
+    rep = np.asarray(repaired, bool)
+    r = [canonical_risk(x) for x in np.asarray(risk_row, dtype=np.float32)]
+    cand = [b for b in range(len(r)) if not rep[b]]
+    if not cand:
         return []
     # rank: larger risk first, ties to the lower block index
-    order = sorted(cand.tolist(), key=lambda b: (-float(r[b]), b))
-    suffix = suffix_sums([r[b] for b in order])
-    ds = d_star(tau)
-    if not suffix[0] > ds:
+    order = sorted(cand, key=lambda b: (-r[b], b))
+    n_inf = sum(1 for b in cand if r[b] == math.inf)
+    remaining = sum((Fraction(r[b]) for b in cand if r[b] != math.inf), Fraction(0))
+    ds = Fraction(d_star(tau))
+    if n_inf == 0 and not remaining > ds:
         return []
-    k = 0
-    while suffix[k] > ds:
+    k = n_inf                     # infinite risks come first and are always taken
+    while remaining > ds:
+        remaining -= Fraction(r[order[k]])
         k += 1
     return order[:k]
 
 
-def gate_group(risk, repaired, tau: float):
+def gate_group(risk, repaired, tau):
     """Union over the query heads of one KV head's group.  risk: [g, nblk]."""
     sel = set()
     for j in range(risk.shape[0]):

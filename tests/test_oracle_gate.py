@@ -11,7 +11,14 @@ from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q
 def test_d_star_solves_the_meter_equation():
     for tau in (0.0, 0.01, 0.5, 1.0, 2.0, 10.0):
         ds = gate.d_star(tau)
-        assert abs(ds + ds * ds / 2 - tau) < 1e-12 * max(1, tau)
+        t32 = float(np.float32(tau))
+        assert abs(ds + ds * ds / 2 - t32) < 1e-12 * max(1, t32)
+
+
+def exceeds(values, ds):
+    """Exact sign test of sum(values) - ds > 0 by Shewchuk's exactly rounded sum (math.fsum):
+    its result is zero only when the exact sum is, and otherwise has the exact sum's sign."""
+    return math.fsum([float(v) for v in values] + [-ds]) > 0.0
 
 
 def test_selection_is_a_minimum_cardinality_repair_by_brute_force():
@@ -26,22 +33,20 @@ def test_selection_is_a_minimum_cardinality_repair_by_brute_force():
         tau = float(rng.choice([0.02, 0.05, 0.1, 0.3]))
         ds = gate.d_star(tau)
         sel = gate.select_cell(risk, rep, tau)
-        total = float(np.sum(risk.astype(np.float64)))
-        if not total > ds:
+        cand = [b for b in range(n) if not rep[b]]
+        if not exceeds(risk[cand], ds):
             assert sel == []
             continue
-        cand = [b for b in range(n) if not rep[b]]
         best = None
         for k in range(len(cand) + 1):
             for sub in itertools.combinations(cand, k):
-                rest = total - sum(float(risk[b]) for b in sub)
-                if rest <= ds + 1e-12:
+                if not exceeds([risk[b] for b in cand if b not in sub], ds):
                     best = k
                     break
             if best is not None:
                 break
         assert len(sel) == best
-        assert total - sum(float(risk[b]) for b in sel) <= ds + 1e-12
+        assert not exceeds([risk[b] for b in cand if b not in sel], ds)
         assert not any(rep[b] for b in sel)
 
 
@@ -101,35 +106,60 @@ def test_oracle_cache_append_and_kivi_tail():
     assert np.any(wst[32:48] > 0) and not np.array_equal(kh[32:48], K[0, 32:48, 0])
 
 
-def test_run_order_suffix_sums_match_exact_sums_and_are_monotone():
-    """The fixed summation order stays within float64 rounding of the exact remaining risk
-    (math.fsum) and never increases down the ranked list, over several runs of 32."""
-    rng = np.random.default_rng(5)
-    for n in (1, 31, 32, 33, 100, 257, 2048):
-        vals = np.sort((rng.exponential(1.0, n) ** 4 * 10.0 ** rng.uniform(-12, 0, n)).astype(np.float32))[::-1]
-        suf = gate.suffix_sums(vals)
-        assert len(suf) == n + 1 and suf[n] == 0.0
-        for k in range(0, n, max(1, n // 50)):
-            exact = math.fsum(float(v) for v in vals[k:])
-            assert abs(suf[k] - exact) <= 1e-13 * exact
-        assert all(suf[k] >= suf[k + 1] for k in range(n))
-
-
-def test_selection_over_many_runs_is_the_exact_minimum_repair():
-    """Hundreds of blocks (many runs): the ranked prefix is the smallest whose exact remaining
-    risk (math.fsum) is <= D*; ranking by size makes a prefix the optimum."""
+def test_selection_over_many_blocks_is_the_exact_minimum_repair():
+    """Hundreds of blocks: the ranked prefix is the smallest whose exact remaining risk
+    (math.fsum sign test) is <= D*; ranking by size makes a prefix the optimum."""
     rng = np.random.default_rng(6)
     for trial in range(40):
         n = int(rng.integers(40, 400))
         risk = (rng.exponential(0.01, n) * (rng.random(n) < 0.9)).astype(np.float32)
         rep = rng.random(n) < 0.1
-        risk[rep] = 0.0
-        total = math.fsum(float(x) for x in risk)
-        tau = float(rng.uniform(0.05, 0.9)) * (total + total * total / 2)
+        total = math.fsum(float(x) for x in risk[~rep])
+        tau = float(np.float32(float(rng.uniform(0.05, 0.9)) * (total + total * total / 2)))
         ds = gate.d_star(tau)
         sel = gate.select_cell(risk, rep, tau)
         order = sorted((b for b in range(n) if not rep[b]), key=lambda b: (-float(risk[b]), b))
         k_exact = 0
-        while math.fsum(float(risk[b]) for b in order[k_exact:]) > ds:
+        while exceeds([risk[b] for b in order[k_exact:]], ds):
             k_exact += 1
         assert sel == order[:k_exact]
+
+
+def test_exact_ties_and_sums_that_float64_gets_wrong():
+    """tau = 1.5 gives D* = 1 exactly and tau = 4 gives D* = 2 (float32 and float64 exact)."""
+    assert gate.d_star(1.5) == 1.0 and gate.d_star(4.0) == 2.0
+    no = np.zeros(8, bool)
+    # the total equals D*: the cell does not trigger; one unit more and it does
+    assert gate.select_cell(np.array([0.5, 0.25, 0.25], np.float32), no[:3], 1.5) == []
+    tiny = np.float32(2.0 ** -149)
+    assert gate.select_cell(np.array([0.5, 0.25, 0.25, tiny], np.float32), no[:4], 1.5) == [0]
+    # remaining after the first block is exactly D*: the prefix stops there
+    assert gate.select_cell(np.array([0.75, 0.5, 0.5], np.float32), no[:3], 1.5) == [0]
+    # 1 + 4 * 2^-60 > 1 although a float64 running sum from the left rounds it to 1
+    r = np.array([1.0] + [2.0 ** -60] * 4, np.float32)
+    assert sum(float(x) for x in r) == 1.0                # the float64 running sum
+    assert gate.select_cell(r, no[:5], 1.5) == [0]
+    # equal risks: lower block index first; exactly D* = 2 left after three of five
+    r = np.array([0.5, 0.5, 1.0, 0.5, 1.0], np.float32)
+    assert gate.select_cell(r, no[:5], 4.0) == [2, 4]
+    assert gate.select_cell(r, no[:5], 1.5) == [2, 4, 0]
+
+
+def test_tau_zero_takes_every_positive_risk():
+    r = np.array([0.0, 1e-30, 0.0, 3.0, 2.0 ** -149], np.float32)
+    assert gate.d_star(0.0) == 0.0
+    assert gate.select_cell(r, np.zeros(5, bool), 0.0) == [3, 1, 4]
+
+
+def test_nan_counts_as_infinite_and_negative_as_zero():
+    r = np.array([0.1, np.nan, np.inf, -1.0, 0.2], np.float32)
+    # NaN and +inf are taken first (ties to the lower index), then by size until <= D*
+    assert gate.select_cell(r, np.zeros(5, bool), 0.05) == [1, 2, 4, 0]
+    assert gate.select_cell(r, np.zeros(5, bool), 10.0) == [1, 2]
+    assert gate.select_cell(np.array([-1.0, -0.0], np.float32), np.zeros(2, bool), 0.0) == []
+
+
+def test_tau_is_read_as_float32():
+    """The library's gate takes tau as a float: 0.2 means float32(0.2), not the double 0.2."""
+    assert gate.d_star(0.2) == math.sqrt(1.0 + 2.0 * float(np.float32(0.2))) - 1.0
+    assert gate.d_star(0.2) != math.sqrt(1.0 + 2.0 * 0.2) - 1.0

@@ -199,3 +199,33 @@ def test_meters_against_50_digit_arithmetic():
             A = mp.fsum(e[t] / Z * mp.exp(cvec[t]) for t in range(S))
             raw = (A * A - 1) / 2
             assert abs(float(raw) / r[key][0, j] - 1) < 1e-10
+
+
+@pytest.mark.parametrize("scheme", ["fp8_e4m3", "int8_dither"])
+@pytest.mark.parametrize("S", [256, 16 * 9 + 5])
+def test_block_risk_is_each_blocks_share_of_the_gate_tier(scheme, S):
+    """Block risks R_blk = sum_{t in blk} p~_t expm1(c_t): a brute force over tokens with
+    explicit loops, and their sum over the blocks (ragged tail included) equals D of the gate's
+    tier: Tier B for the dithered scheme, Tier A otherwise."""
+    w = WORKLOADS["tiny"].with_(scheme=scheme, context=S)
+    c = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, scheme, w.seed, w.steps)
+    K, V = gen_kv(w, 0)
+    c.write(0, K, V)
+    q = gen_q(w, 0, 0)
+    kh, vh, wst, ks, rep = c.group_view(0, 0, 1)
+    dl = meter.delta_loc(w.delta_req, w.n_layers, w.n_q_heads, w.steps)
+    r = meter.decode_ref(q[0, 2:4], kh, vh, wst, ks, rep, dl)
+    cg = r["u"] if scheme == "int8_dither" else r["eps"]
+    D = r["D_b"] if scheme == "int8_dither" else r["D_a"]
+    nblk = (S + 15) // 16
+    assert r["risk"].shape == (2, nblk)
+    for j in range(2):
+        for b in range(nblk):
+            want = 0.0
+            for t in range(16 * b, min(16 * b + 16, S)):
+                want += r["p"][j, t] * math.expm1(cg[j, t])
+            assert abs(r["risk"][j, b] - want) <= 1e-12 * max(want, 1e-300)
+        assert abs(math.fsum(r["risk"][j]) - D[j]) <= 1e-12 * D[j]
+    # the two tiers differ on the dithered scheme, so the identity picks out the tier
+    if scheme == "int8_dither":
+        assert np.all(np.abs(r["D_a"] - r["D_b"]) > 1e-6 * r["D_b"])
