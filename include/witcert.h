@@ -117,8 +117,9 @@ typedef struct {
 /* Create a cache.  Allocates the compressed store, the witness store, the
  * split scratch and, when max_repair_blocks > 0, the exact-key pool and a
  * pinned, device-mapped host backing store of exact keys.  Memory is zeroed.
- * Synchronous.  Returns EINVAL for unsupported shapes, ENOMEM on allocation
- * failure (nothing is leaked). */
+ * Synchronous.  Returns EINVAL for unsupported shapes (among them a cache with the gate
+ * enabled and max_tokens above 262144: the gate ranks at most 16384 blocks of a sequence),
+ * ENOMEM on allocation failure (nothing is leaked). */
 witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out);
 
 /* Free everything the cache owns.  Synchronizes the device first. */
@@ -189,7 +190,12 @@ witcert_status witcert_reset_sequence(witcert_cache* cache, int seq, void* strea
  *   raw_a, raw_b                      the unclamped (A^2-1)/2 of each tier
  *   meter_v [batch][n_q_heads]       value meter E_V = sum_t p~_t wv_t (v_witness caches;
  *                                    EINVAL if non-NULL on a cache without value witnesses)
- * Meters are rounded upward (never below the exact value of the formula).
+ * Meters are upper bounds of the formula's value on the stored cache: the sums over
+ * tokens, splits and warps are compensated (Kahan, two-sums), rescaled only by exact powers
+ * of two and rounded down (Z) or up (S) where they leave their compensated pairs, and the
+ * quotient, D + D^2/2 and a margin of 2^-15 on D are rounded up, so no error grows with the
+ * context length; the margin covers each token's own rounding (SFU exponentials and
+ * roots, tensor-core products, the expm1 series, which is itself an upper bound).
  * Any meter pointer may be NULL; if all five are NULL the meter work is
  * compiled out and `out` is bit-identical to the metered run's.
  * With the gate enabled, per-16-token-block risks of the gate's tier
@@ -224,15 +230,19 @@ witcert_status witcert_decode_noalloc(witcert_cache* cache, int layer, const voi
  * Figure 2 (repair works on whole blocks and clears their witnesses) and
  * Figure 5 (repairs accumulate and persist)].  Uses the block
  * risks of the layer's last decode: a (sequence, query head) cell whose
- * unclamped meter exceeds tau has its unrepaired blocks ranked by risk
- * (largest first, ties to the lower block) and takes the shortest prefix that
- * leaves remaining risk <= sqrt(1+2 tau)-1; the union over a KV head's query
- * heads is paged in from the pinned backing store into the exact-key pool,
- * marked repaired (persistently) and its witnesses zeroed.  Runs on the
- * cache's side stream after the work already queued on `stream`; later
- * writes and decodes of this layer wait for it on the device.  Repairs affect
- * decodes issued after this call.  ESTATE if the gate is disabled or the
- * layer has not been decoded since its last write. */
+ * unrepaired blocks' risks sum to more than D* = sqrt(1+2 tau)-1 (its unclamped
+ * meter exceeds tau) has those blocks ranked by risk (largest first, ties to the
+ * lower block; a NaN risk counts as +inf) and takes the shortest prefix that leaves
+ * remaining risk <= D*.  Sums and comparisons are exact: the fp32 risks are added as
+ * integers in units of 2^-149 and compared with D* (float64), so decisions depend on no
+ * summation order.  The union over a KV head's query heads is paged in from the pinned
+ * backing store into the exact-key pool, marked repaired (persistently) and its witnesses
+ * zeroed.  Runs on the cache's side stream after the work already queued on `stream`; later
+ * writes and decodes of this layer wait for it on the device.  Repairs affect decodes
+ * issued after this call.  ESTATE if the gate is disabled or the layer has not been decoded
+ * since its last write.  EPAGEIN, with nothing selected, paged in or zeroed, if the layer's
+ * backing store has lost exact keys (a host copy into it failed, or a fault was injected
+ * with witcert_inject_fault): its witnesses stay and keep bounding the error. */
 witcert_status witcert_gate(witcert_cache* cache, int layer, float tau, void* stream);
 
 /* Gate counters, summed over all gate calls.  Waits for outstanding gate work
@@ -243,10 +253,10 @@ witcert_status witcert_gate_stats(witcert_cache* cache, witcert_gate_counters* o
  * tokens at global positions pos_offset, pos_offset + 1, ...; see witcert_config).  The
  * shard's decode of `layer` is merged over the shard's own splits but not normalized: for
  * every (sequence, query head) cell it writes one record of 136 floats to `part` (device,
- * [batch][n_q_heads][136]): the running maximum m of the logits in log2 units, Z = sum
- * 2^(l - m), S_A and S_B = sum 2^(l - m) expm1(c) of the Tier A and Tier B bounds, S_V =
- * sum 2^(l - m) wv (0 without value witnesses), three unused floats, and the 128 value sums
- * relative to m.  Tier B's kappa uses s_total, the whole context's
+ * [batch][n_q_heads][136]): m, an integer (log2 units) at least the largest logit (-inf
+ * for an empty slice), Z = sum 2^(l - m) rounded down, S_A and S_B = sum 2^(l - m) expm1(c)
+ * of the Tier A and Tier B bounds rounded up, S_V = sum 2^(l - m) wv rounded up (0 without
+ * value witnesses), three unused floats, and the 128 value sums relative to m.  Tier B's kappa uses s_total, the whole context's
  * length (>= this slice's), so the shards of one decode share delta_loc.  The records of all
  * shards, gathered in any order into [batch][n_q_heads][n_parts][136], are merged by
  * witcert_merge_partials into the same output and meters a single cache holding the whole
@@ -259,10 +269,36 @@ witcert_status witcert_decode_partial(witcert_cache* cache, int layer, const voi
  * of the pages' split-KV decode, applied across shards): parts is device [batch][n_q_heads]
  * [n_parts][136]; out [batch][n_q_heads][128] fp32 and the optional meters [batch][n_q_heads]
  * as in witcert_decode (meter_b NaN unless scheme is WITCERT_INT8_DITHER; meter_v from the
- * records' S_V).  Asynchronous on `stream`; no cache is involved. */
+ * records' S_V).  Every record's m must be an integer or -inf, as witcert_decode_partial
+ * writes it.  Asynchronous on `stream`; no cache is involved. */
 witcert_status witcert_merge_partials(const float* parts, int n_parts, int batch, int n_q_heads,
                                       witcert_scheme scheme, float* out, float* meter_a, float* meter_b,
                                       float* raw_a, float* raw_b, float* meter_v, void* stream);
+
+/* The gate's block selection on its own [summary, implementation paragraph; Lean page,
+ * Figure 2], for risks computed elsewhere (the shards of a context-parallel decode combine
+ * theirs) and for tests: the rule of witcert_gate, applied to caller arrays.
+ *   risk      device float [batch][n_q_heads][nblk]  block risks of each cell
+ *   repaired  device uint8 [batch][n_kv_heads][nblk] nonzero = already repaired (not ranked),
+ *             or NULL (none repaired)
+ *   selected  device uint32 [batch][n_kv_heads][nblk/32 + 1] output bitmap: bit b % 32 of word
+ *             b / 32 is set when any query head of the KV head's group selects block b;
+ *             cleared by the call first
+ * Asynchronous on `stream`.  EINVAL for nblk outside [1, 16384] or bad shapes. */
+witcert_status witcert_gate_select(const float* risk, const uint8_t* repaired, int batch, int n_q_heads,
+                                   int n_kv_heads, int nblk, float tau, uint32_t* selected, void* stream);
+
+typedef enum {
+  WITCERT_FAULT_BACKING_LOST = 1   /* the layer's pinned backing store loses its exact keys, as
+                                      when a host copy into it fails */
+} witcert_fault;
+
+/* Host-side fault injection for failure-detection tests (no counterpart in the paper): puts
+ * `layer` of the cache into the state `fault` describes, as the failure itself would.  With
+ * WITCERT_FAULT_BACKING_LOST the layer's gate calls return WITCERT_EPAGEIN from then on and
+ * change nothing; decodes are unaffected.  No GPU work.  EINVAL for a bad layer or fault,
+ * ESTATE if the gate is disabled. */
+witcert_status witcert_inject_fault(witcert_cache* cache, witcert_fault fault, int layer);
 
 /* Library counters.  Synchronizes the device. */
 witcert_status witcert_stats(witcert_cache* cache, witcert_stats_t* out);
@@ -322,6 +358,14 @@ witcert_status witcert_dither(uint64_t seed, int layer, int kv_head, int t0, int
  * 1e10).  Returns WITCERT_ETIMEDOUT when the wait gives up as designed (the CUDA
  * context stays usable), WITCERT_OK if it was satisfied.  Synchronizes `stream`. */
 witcert_status witcert_wait_selftest(int64_t limit_ns, void* stream);
+
+/* Self test of the writers' quotient x / s (no counterpart in the paper): the INT8 writer
+ * divides by its fp16 scale s with a reciprocal and one exact correction instead of an IEEE
+ * division; this compares the two, on the GPU, for every positive fp16 scale against every
+ * bfloat16 x with |x| <= 127.5 s and n_f32 (<= 2^20) seeded float32 x per scale, wherever the
+ * quotient can move a code (|x / s| >= 2^-25).  Writes the number of differing quotients to
+ * host *mismatches (expected 0).  Synchronizes `stream`. */
+witcert_status witcert_quotient_selftest(int n_f32, uint64_t seed, uint64_t* mismatches, void* stream);
 
 /* Thread-local message of the last failing call on this thread ("" if none). */
 const char* witcert_last_error(void);

@@ -14,7 +14,7 @@ from . import _lib
 from ._lib import (BF16, BLACKBOX, EINVAL, ENOMEM, EPAGEIN, ESTATE, ETIMEDOUT, F32, FP8_E4M3, INT8_DITHER,  # noqa: F401
                    INT8_RTN, KIVI2, SCHEMES, WitcertError, check, load)
 
-__all__ = ["Cache", "witcert_dither", "witcert_merge_partials", "WitcertError", "load", "SCHEMES", "PART_STRIDE"]
+__all__ = ["Cache", "witcert_dither", "witcert_merge_partials", "witcert_gate_select", "WitcertError", "load", "SCHEMES", "PART_STRIDE"]
 
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -153,6 +153,10 @@ class Cache:
     def witcert_gate(self, layer, tau, stream=None):
         check(load().witcert_gate(self._h, layer, float(tau), _stream_ptr(stream)), "witcert_gate")
 
+    def witcert_inject_fault(self, fault, layer):
+        """Host-side fault injection (see witcert_inject_fault in include/witcert.h)."""
+        check(load().witcert_inject_fault(self._h, int(fault), int(layer)), "witcert_inject_fault")
+
     def witcert_gate_stats(self, timeout_ms=10000):
         s = _lib.witcert_gate_counters()
         check(load().witcert_gate_stats(self._h, ctypes.byref(s), timeout_ms), "witcert_gate_stats")
@@ -244,6 +248,30 @@ def witcert_merge_partials(parts, scheme, out=None, meters=True, stream=None):
                                         _ptr(out), *ptrs, _stream_ptr(stream)), "witcert_merge_partials")
     return out, ({"meter_a": m[0], "meter_b": m[1], "raw_a": m[2], "raw_b": m[3], "meter_v": m[4]}
                  if meters else None)
+
+
+def witcert_gate_select(risk, n_kv_heads, tau, repaired=None, selected=None, stream=None):
+    """The gate's block selection on caller arrays: risk [B, Hq, nblk] float32 (device), repaired
+    [B, Hkv, nblk] uint8 or None; returns the selection bitmap [B, Hkv, nblk // 32 + 1] int32
+    (see witcert_gate_select)."""
+    _need(("risk", risk, torch.float32, (None, None, None)))
+    B, Hq, nblk = risk.shape
+    _need(("repaired", repaired, torch.uint8, (B, n_kv_heads, nblk), True))
+    if selected is None:
+        selected = torch.empty((B, n_kv_heads, nblk // 32 + 1), dtype=torch.int32, device=risk.device)
+    _need(("selected", selected, torch.int32, (B, n_kv_heads, nblk // 32 + 1)))
+    check(load().witcert_gate_select(_ptr(risk), _ptr(repaired), B, Hq, n_kv_heads, nblk, float(tau), _ptr(selected),
+                                     _stream_ptr(stream)), "witcert_gate_select")
+    return selected
+
+
+def witcert_quotient_selftest(n_f32=4096, seed=0, stream=None):
+    """Differing quotients between the writers' x / s and the IEEE quotient over every positive
+    fp16 scale (see witcert_quotient_selftest); expected 0."""
+    n = ctypes.c_uint64()
+    check(load().witcert_quotient_selftest(int(n_f32), int(seed), ctypes.byref(n), _stream_ptr(stream)),
+          "witcert_quotient_selftest")
+    return n.value
 
 
 def witcert_wait_selftest(limit_ns, stream=None):

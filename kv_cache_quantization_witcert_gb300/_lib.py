@@ -13,6 +13,8 @@ F32, BF16 = 0, 1
 (X_K_CODES, X_V_CODES, X_K_SCALES, X_V_SCALES, X_V_ZEROS, X_KIVI_K_SCALE, X_KIVI_K_ZERO, X_WITNESS,
  X_SLOTS, X_BLOCK_RISK, X_V_WITNESS) = range(11)
 
+FAULT_BACKING_LOST = 1
+
 SCHEMES = {"int8_dither": INT8_DITHER, "fp8_e4m3": FP8_E4M3, "kivi2": KIVI2, "int8_rtn": INT8_RTN,
            "blackbox": BLACKBOX}
 STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ETIMEDOUT: "ETIMEDOUT",
@@ -63,6 +65,9 @@ SIGNATURES = {
     "witcert_export": [_vp, _int, _int, _vp, _sz, _vp],
     "witcert_dither": [ctypes.c_uint64, _int, _int, _int, _int, _int, _vp, _vp],
     "witcert_wait_selftest": [ctypes.c_int64, _vp],
+    "witcert_gate_select": [_vp, _vp, _int, _int, _int, _int, ctypes.c_float, _vp, _vp],
+    "witcert_inject_fault": [_vp, _int, _int],
+    "witcert_quotient_selftest": [_int, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64), _vp],
     "witcert_last_error": [],
 }
 

@@ -13,19 +13,38 @@ namespace {
 // w + kMergeWarps, ... into a running (max, Z, S_A, S_B, S_V, values) with online rescaling, so
 // that all its record loads are independent of one another; the warps' states meet in shared
 // memory, where thread j finishes channel j.  Then the meters and the block risks.
+//
+// The records' maxima are integers (log2 units), so every rescale is an exact power of two; the
+// sums are Kahan pairs within a warp and meet across warps through two-sums, and they leave their
+// pairs rounded down (Z) or up (S_X) before the quotient D = S_X / Z, its margin and D + D^2/2,
+// all rounded up.
 constexpr int kMergeWarps = 8;
+
+__device__ __forceinline__ void kahan_add(float& hi, float& lo, float x) {
+  const float y = x + lo;
+  const float t = hi + y;
+  lo = y - (t - hi);
+  hi = t;
+}
+
+// D = S / Z with the meters' margin, rounded up; D + D^2 / 2 rounded up.
+__device__ __forceinline__ float meter_ratio(float S_hi, float S_lo, float Z_dn) {
+  const float S_up = __fadd_ru(S_hi, S_lo);
+  if (!(S_up > 0.f) || !(Z_dn > 0.f)) return 0.f;
+  return __fadd_ru(__fmul_ru(__fdiv_ru(S_up, Z_dn), kMeterMargin), kMeterFloor);
+}
+__device__ __forceinline__ float meter_raw(float D) { return __fmaf_ru(__fmul_ru(0.5f, D), D, D); }
 
 template <bool INT8, bool RISK>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const DecodeArgs p) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float4 s_hdr[kMergeWarps];
-  __shared__ float s_sv[kMergeWarps];
+  __shared__ float s_hdr[kMergeWarps][9];       // M, then (hi, lo) of Z, S_A, S_B, S_V
   __shared__ __align__(16) float s_acc[kMergeWarps][kD];
   const int cell = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* recs = p.part + (size_t)cell * p.n_splits * kPartStride;
   const int ns = p.n_splits;
-  float M = -INFINITY, Z = 0.f, SA = 0.f, SB = 0.f, SV = 0.f;
+  float M = -INFINITY, Zh = 0.f, Zl = 0.f, Ah = 0.f, Al = 0.f, Bh = 0.f, Bl = 0.f, Vh = 0.f, Vl = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
   for (int s = warp; s < ns; s += kMergeWarps) {
@@ -34,67 +53,106 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
     const float sv = r[4];                                          // S_V
     const float4 a = *reinterpret_cast<const float4*>(r + kPartAcc + 4 * lane);
     if (h.x > M) {                                                  // same for every lane
-      const float sc = M == -INFINITY ? 0.f : ex2(M - h.x);
-      Z *= sc; SA *= sc; SB *= sc; SV *= sc;
-      acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+      const float k = M - h.x;                                      // -inf while M is
+      const float sd = pow2_dn(k), su = pow2_up(k);
+      Zh = __fmul_rd(Zh, sd); Zl = __fmul_rd(Zl, sd);
+      Ah = __fmul_ru(Ah, su); Al = __fmul_ru(Al, su);
+      Bh = __fmul_ru(Bh, su); Bl = __fmul_ru(Bl, su);
+      Vh = __fmul_ru(Vh, su); Vl = __fmul_ru(Vl, su);
+      acc.x *= sd; acc.y *= sd; acc.z *= sd; acc.w *= sd;
       M = h.x;
     }
-    const float f = h.x == -INFINITY ? 0.f : ex2(h.x - M);
-    Z = fmaf(f, h.y, Z); SA = fmaf(f, h.z, SA); SB = fmaf(f, h.w, SB); SV = fmaf(f, sv, SV);
-    acc.x = fmaf(f, a.x, acc.x); acc.y = fmaf(f, a.y, acc.y); acc.z = fmaf(f, a.z, acc.z); acc.w = fmaf(f, a.w, acc.w);
+    const float k = h.x == M ? 0.f : h.x - M;                       // -inf for an empty split
+    const float fd = pow2_dn(k), fu = pow2_up(k);
+    kahan_add(Zh, Zl, __fmul_rd(fd, h.y));
+    kahan_add(Ah, Al, __fmul_ru(fu, h.z));
+    kahan_add(Bh, Bl, __fmul_ru(fu, h.w));
+    kahan_add(Vh, Vl, __fmul_ru(fu, sv));
+    acc.x = fmaf(fd, a.x, acc.x); acc.y = fmaf(fd, a.y, acc.y); acc.z = fmaf(fd, a.z, acc.z); acc.w = fmaf(fd, a.w, acc.w);
   }
-  if (lane == 0) { s_hdr[warp] = make_float4(M, Z, SA, SB); s_sv[warp] = SV; }
+  if (lane == 0) {
+    float* hw = s_hdr[warp];
+    hw[0] = M; hw[1] = Zh; hw[2] = Zl; hw[3] = Ah; hw[4] = Al; hw[5] = Bh; hw[6] = Bl; hw[7] = Vh; hw[8] = Vl;
+  }
   *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
   __syncthreads();
+  // the warps' states meet at the largest maximum: warp 0 forms the sums and the meters, the
+  // first kD threads the output channels
+  __shared__ float s_tot[2];
   float Mx = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) Mx = fmaxf(Mx, s_hdr[w].x);
-  float Zt = 0.f, SAt = 0.f, SBt = 0.f, SVt = 0.f, o = 0.f;
-  if (Mx != -INFINITY) {
+  for (int w = 0; w < kMergeWarps; ++w) Mx = fmaxf(Mx, s_hdr[w][0]);
+  float o = 0.f;
+  if (threadIdx.x < kD && Mx != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      const float4 hw = s_hdr[w];
-      const float wt = hw.x == -INFINITY ? 0.f : ex2(hw.x - Mx);
-      Zt = fmaf(wt, hw.y, Zt); SAt = fmaf(wt, hw.z, SAt); SBt = fmaf(wt, hw.w, SBt); SVt = fmaf(wt, s_sv[w], SVt);
-      if (threadIdx.x < kD) o = fmaf(wt, s_acc[w][threadIdx.x], o);
+    for (int w = 0; w < kMergeWarps; ++w) o = fmaf(pow2_dn(s_hdr[w][0] == Mx ? 0.f : s_hdr[w][0] - Mx), s_acc[w][threadIdx.x], o);
+  }
+  // warp 0: lane 8q + w holds quantity q (Z, S_A, S_B, S_V) of warp w, scaled exactly to Mx (Z
+  // rounded down, the S rounded up where the scale leaves fp32's normal range); three rounds of
+  // two-sums add the warps, then the lane of each S forms its meter against Z
+  if (warp == 0) {
+    const int q = lane >> 3, w = lane & 7;
+    const float* hw = s_hdr[w];
+    const float k = hw[0] == Mx ? 0.f : hw[0] - Mx;
+    float hi = 0.f, lo = 0.f;
+    if (Mx != -INFINITY) {
+      if (q == 0) { const float f = pow2_dn(k); hi = __fmul_rd(f, hw[1]); lo = __fmul_rd(f, hw[2]); }
+      else { const float f = pow2_up(k); hi = __fmul_ru(f, hw[2 * q + 1]); lo = __fmul_ru(f, hw[2 * q + 2]); }
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+      const float ohi = __shfl_xor_sync(0xffffffffu, hi, m), olo = __shfl_xor_sync(0xffffffffu, lo, m);
+      pair_add(hi, lo, ohi, olo);
+    }
+    const float Zhi = __shfl_sync(0xffffffffu, hi, 0), Zlo = __shfl_sync(0xffffffffu, lo, 0);
+    const float Zdn = __fadd_rd(Zhi, Zlo);
+    const float S_up = __fadd_ru(hi, lo);
+    if (lane == 0) { s_tot[0] = Zhi + Zlo; s_tot[1] = Zdn; }
+    if (p.part_out) {         // context-parallel shard: the cell's combined record, unnormalized
+      float* rec = p.part_out + (size_t)cell * kPartStride;
+      if (lane == 0) { rec[0] = Mx; rec[1] = Zdn; rec[5] = 0.f; rec[6] = 0.f; rec[7] = 0.f; }
+      if (w == 0 && q > 0) rec[1 + q] = S_up;
+    } else if (p.meter && w == 0 && q > 0) {
+      const float D = meter_ratio(hi, lo, Zdn);
+      if (q == 3) {
+        if (p.meter_v) p.meter_v[cell] = D;                       // E_V = S_V / Z, rounded up
+      } else if (q == 1) {
+        const float rawA = meter_raw(D);
+        if (p.raw_a) p.raw_a[cell] = rawA;
+        if (p.meter_a) p.meter_a[cell] = fminf(1.0f, rawA);
+      } else {
+        const float rawB = INT8 ? meter_raw(D) : NAN;
+        if (p.raw_b) p.raw_b[cell] = rawB;
+        if (p.meter_b) p.meter_b[cell] = INT8 ? fminf(1.0f, rawB) : NAN;
+      }
     }
   }
-  if (p.part_out) {           // context-parallel shard: the cell's combined record, unnormalized
-    float* rec = p.part_out + (size_t)cell * kPartStride;
-    if (threadIdx.x == 0) {
-      *reinterpret_cast<float4*>(rec) = make_float4(Mx, Zt, SAt, SBt);
-      *reinterpret_cast<float4*>(rec + 4) = make_float4(SVt, 0.f, 0.f, 0.f);
-    }
-    if (threadIdx.x < kD) rec[kPartAcc + threadIdx.x] = o;
+  __syncthreads();
+  if (p.part_out) {
+    if (threadIdx.x < kD) p.part_out[(size_t)cell * kPartStride + kPartAcc + threadIdx.x] = o;
     return;
   }
+  const float Zt = s_tot[0], Zdn = s_tot[1];
   const float inv = Zt > 0.f ? 1.0f / Zt : 0.f;
   if (threadIdx.x < kD) p.out[(size_t)cell * kD + threadIdx.x] = o * inv;
   if (!p.meter) return;
-  if (threadIdx.x == 0 && p.meter_v)    // E_V = S_V / Z, rounded up with the meters' margin
-    p.meter_v[cell] = Zt > 0.f ? __fmul_ru(__fdiv_ru(SVt, Zt), kMeterMargin) : 0.f;
-  if (threadIdx.x == 0) {
-    const float DA = Zt > 0.f ? __fmul_ru(__fdiv_ru(SAt, Zt), kMeterMargin) : 0.f;
-    const float rawA = __fmaf_ru(__fmul_ru(0.5f, DA), DA, DA);
-    if (p.raw_a) p.raw_a[cell] = rawA;
-    if (p.meter_a) p.meter_a[cell] = fminf(1.0f, rawA);
-    float rawB = NAN;
-    if (INT8) {
-      const float DB = Zt > 0.f ? __fmul_ru(__fdiv_ru(SBt, Zt), kMeterMargin) : 0.f;
-      rawB = __fmaf_ru(__fmul_ru(0.5f, DB), DB, DB);
-    }
-    if (p.raw_b) p.raw_b[cell] = rawB;
-    if (p.meter_b) p.meter_b[cell] = INT8 ? fminf(1.0f, rawB) : NAN;
-  }
   if (RISK) {
+    // block share of D: r 2^(m_blk - M) / Z with the meters' margin, rounded up
     const int nblk = (p.S + kBlk - 1) / kBlk;
     const int S_c = p.seq_len ? p.seq_len[cell / p.Hq] : p.S;      // this cell's sequence
     const int nblk_c = (S_c + kBlk - 1) / kBlk;
     const float2* rr = p.risk_raw + (size_t)cell * p.nblk_max;
     float* ro = p.risk + (size_t)cell * p.nblk_max;
+    // margin / Z rounded up once: products of upward-rounded positive factors stay above
+    const float scale = Zdn > 0.f ? __fdiv_ru(kMeterMargin, Zdn) : 0.f;
     for (int b = threadIdx.x; b < nblk; b += kMergeWarps * 32) {
       const float2 v = b < nblk_c ? rr[b] : make_float2(0.f, 0.f);
-      ro[b] = (v.y == 0.f || Zt == 0.f) ? 0.f : v.y * ex2(v.x - Mx) * inv;
+      float r = 0.f;
+      if (v.y > 0.f && Zdn > 0.f) {
+        const float k = v.x == Mx ? 0.f : v.x - Mx;
+        r = __fadd_ru(__fmul_ru(__fmul_ru(v.y, pow2_up(k)), scale), kMeterFloor);
+      }
+      ro[b] = r;
     }
   }
 }

@@ -54,11 +54,12 @@ namespace witcert {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLog2eUp = 0x1.715478p+0f;          // log2(e) rounded up
+// c^4 coefficient of the expm1 series below c = 1/8: 1/24 raised to cover the dropped
+// terms, sum_{k>=5} c^(k-4)/k! < 0.042731 on [0, 1/8), so c(1 + c/2 + c^2/6 + a c^3) >= expm1(c)
+constexpr float kSeriesC4 = 0.0428f;
 constexpr int kXiKHi = 0, kXiKLo = 4096, kXiV = 8192, kXiBytes = 12288;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per barrier wait
-// Upward bias applied to every meter sum: covers the fp32 / tensor-core / SFU
-// rounding of the logits, exponentials and square roots relative to exact arithmetic.
-constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
 
 template <int SCHEME> struct Lay;
 template <> struct Lay<kInt8> : Int8Layout {};
@@ -105,19 +106,69 @@ __device__ __forceinline__ float sqrt_up(float x) {
 // Packed pairs (two query heads of a lane): fp32x2 arithmetic of sm_100+.
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 ex2x2(float2 v) { return make_float2(ex2(v.x), ex2(v.y)); }
-__device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+// a - b as one packed FMA, b * (-1) + a: the correctly rounded difference, without negating b first
+__device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a); }
 
-// p * expm1(c) for c >= 0, with p = e^(l - m) and d = l - m in log2 units.  Below c = 1/8
-// the series c + c^2/2 + c^3/6 + c^4/24 (truncation < 2e-6 relative); above it the term is
-// formed in the exponent, e^(l - m + c) - e^(l - m), which neither overflows for large c
-// nor loses a p that flushed to zero, and cancels at most a factor e^c/(e^c - 1) < 8.6 of
-// precision.  Tokens past the context arrive with d = -inf and c = 0 and give 0.
+// ------------------------------------------------------------------ meter arithmetic
+// The meter is D = S / Z with S = sum_t w_t expm1(c_t) and Z = sum_t w_t over the weights
+// w_t = 2^(l_t - m) of one cell.  Its value must never fall below the exact one, whatever
+// the length of the sums and the pattern of their roundings:
+//  * the running maximum m (log2 units) is kept integer-valued, so every rescale of the sums
+//    is a multiplication by an exact power of two;
+//  * a lane adds its per-block terms to Z and S with Kahan's compensated summation (a
+//    relative error of at most 2u + O(n u^2), u = 2^-24, for n non-negative terms, instead
+//    of the n u of a plain running sum);
+//  * lanes, splits and warps are combined with error-free two-sums, and whenever a sum
+//    leaves its (hi, lo) pair it is rounded down (Z) or up (S);
+//  * the quotient, the margin and D + D^2/2 are rounded up.
+// What remains is the rounding of each token's own term (exponentials, logits, witness
+// products, the series), a relative error independent of n that kMeterMargin covers.
+constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
+// Absolute allowance for terms the flush-to-zero exponentials drop: a dropped term is below
+// 2^-126 while Z >= 1/2, so fewer than 2^17 of them move D by less than 2^-108.
+constexpr float kMeterFloor = 0x1p-100f;
+
+// 2^k for an integer-valued k <= 0, or k = -inf: the largest float <= 2^k (pow2_dn) and the
+// smallest float >= 2^k (pow2_up); both are 2^k itself down to 2^-149.
+__device__ __forceinline__ float pow2_dn(float k) {
+  if (k >= -126.0f) return __int_as_float((int)(k + 127.0f) << 23);
+  if (k >= -149.0f) return __int_as_float(1 << (int)(k + 149.0f));
+  return 0.0f;
+}
+__device__ __forceinline__ float pow2_up(float k) {
+  if (k >= -149.0f) return pow2_dn(k);
+  return k == -INFINITY ? 0.0f : 0x1p-149f;
+}
+
+// Kahan's compensated summation in (hi, lo) form: hi + lo carries the running sum and lo the
+// rounding error hi has accumulated; two query heads at once.
+__device__ __forceinline__ void kahan_add2(float2& hi, float2& lo, float2 x) {
+  const float2 y = __fadd2_rn(x, lo);
+  const float2 t = __fadd2_rn(hi, y);
+  lo = f2sub(y, f2sub(t, hi));
+  hi = t;
+}
+// (hi, lo) += (ohi, olo) with an error-free two-sum of the high parts (Knuth).
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float ohi, float olo) {
+  const float s = hi + ohi;
+  const float bb = s - hi;
+  const float e = (hi - (s - bb)) + (ohi - bb);
+  lo = lo + olo + e;
+  hi = s;
+}
+
+// p * expm1(c) for c >= 0, with p = 2^d the token's weight and d = l - m in log2 units.  Below
+// c = 1/8 the series c (1 + c/2 + c^2/6 + a c^3), whose last coefficient a exceeds 1/24 by
+// enough that it never falls below expm1(c); above it the term is formed in the exponent,
+// 2^(d + c log2 e) - 2^d (log2 e rounded up), which neither overflows for large c nor loses a
+// p that flushed to zero, and cancels at most a factor e^c/(e^c - 1) < 8.6 of precision.
+// Tokens past the context arrive with d = -inf and c = 0 and give 0.
 __device__ __forceinline__ float2 meter_term2(float2 pe, float2 d, float2 c) {
-  float2 poly = __ffma2_rn(c, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
+  float2 poly = __ffma2_rn(c, f2(kSeriesC4), f2(1.0f / 6.0f));
   poly = __ffma2_rn(c, poly, f2(0.5f));
   poly = __ffma2_rn(c, poly, f2(1.0f));
   poly = __fmul2_rn(__fmul2_rn(c, poly), pe);
-  const float2 big = f2sub(ex2x2(__ffma2_rn(c, f2(kLog2e), d)), pe);
+  const float2 big = f2sub(ex2x2(__ffma2_rn(c, f2(kLog2eUp), d)), pe);
   return make_float2(c.x < 0.125f ? poly.x : big.x, c.y < 0.125f ? poly.y : big.y);
 }
 
@@ -412,8 +463,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   if (RISK) pdl_wait();    // block risks overwrite rows the preceding merge may still read
 
   // ---------------------------------------------------------------- state
-  // per lane: heads 2t (.x) and 2t+1 (.y); A = token g, B = token g+8 of the block
+  // per lane: heads 2t (.x) and 2t+1 (.y); A = token g, B = token g+8 of the block.  m2 is
+  // integer-valued; the sums are Kahan pairs (hi, lo).
   float2 m2 = f2(-INFINITY), Zp = f2(0.f), SAp = f2(0.f), SBp = f2(0.f), SVp = f2(0.f);
+  float2 Zl = f2(0.f), SAl = f2(0.f), SBl = f2(0.f), SVl = f2(0.f);
   float acco[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) acco[mt][0] = acco[mt][1] = acco[mt][2] = acco[mt][3] = 0.f;
@@ -629,8 +682,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       }
 
       // ------------------------------------------------------------ online softmax + meters
-      // The running max m2 moves only when a logit of the block exceeds it; otherwise the
-      // block's weights are taken against m2 as it stands (p <= 1 either way).
+      // The running max m2 (an integer in log2 units, at least every logit so far) moves only
+      // when a logit of the block exceeds it, to the ceiling of the block's largest logit;
+      // otherwise the block's weights are taken against m2 as it stands (p <= 1 either way).
+      // A move scales everything accumulated by the power of two 2^(old - new): exact, apart
+      // from results below 2^-126, which round down for Z and the output and up for the meter
+      // sums.
       float2 dA = f2sub(lgA, m2), dB = f2sub(lgB, m2);
       const bool grows = lgA.x > m2.x || lgA.y > m2.y || lgB.x > m2.x || lgB.y > m2.y;
       if (__any_sync(0xffffffffu, grows)) {
@@ -640,16 +697,39 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
           bm.x = fmaxf(bm.x, __shfl_xor_sync(0xffffffffu, bm.x, o));
           bm.y = fmaxf(bm.y, __shfl_xor_sync(0xffffffffu, bm.y, o));
         }
-        const float2 mn = make_float2(fmaxf(m2.x, bm.x), fmaxf(m2.y, bm.y));
-        const float2 scr = ex2x2(f2sub(m2, mn));
-        const float2 sc = make_float2(mn.x == -INFINITY ? 1.f : scr.x, mn.y == -INFINITY ? 1.f : scr.y);
+        const float2 mn = make_float2(fmaxf(m2.x, ceilf(bm.x)), fmaxf(m2.y, ceilf(bm.y)));
+        // exponent of the move: 0 where m2 stays or where nothing was accumulated yet (the sums
+        // are still zero)
+        const float kx = (mn.x == m2.x || m2.x == -INFINITY) ? 0.f : m2.x - mn.x;
+        const float ky = (mn.y == m2.y || m2.y == -INFINITY) ? 0.f : m2.y - mn.y;
         dA = f2sub(lgA, mn);
         dB = f2sub(lgB, mn);
         m2 = mn;
-        Zp = __fmul2_rn(Zp, sc);
-        SAp = __fmul2_rn(SAp, sc);
-        SBp = __fmul2_rn(SBp, sc);
-        if (VW) SVp = __fmul2_rn(SVp, sc);
+        float2 sc;
+        if (kx >= -100.f && ky >= -100.f) {
+          // the usual move: exact powers of two on packed pairs.  Z holds the old maximum's
+          // weight (>= 1/2), so it stays in fp32's normal range; an S or a low part that
+          // leaves it loses less than 2^-150, inside the meters' absolute allowance.
+          sc = make_float2(__int_as_float(((int)kx + 127) << 23), __int_as_float(((int)ky + 127) << 23));
+          Zp = __fmul2_rn(Zp, sc); Zl = __fmul2_rn(Zl, sc);
+          SAp = __fmul2_rn(SAp, sc); SAl = __fmul2_rn(SAl, sc);
+          SBp = __fmul2_rn(SBp, sc); SBl = __fmul2_rn(SBl, sc);
+          if (VW) { SVp = __fmul2_rn(SVp, sc); SVl = __fmul2_rn(SVl, sc); }
+        } else {
+          // a jump of more than 100 (log2 units): factors rounded down for Z and up for the S
+          sc = make_float2(pow2_dn(kx), pow2_dn(ky));
+          const float2 su = make_float2(pow2_up(kx), pow2_up(ky));
+          Zp = make_float2(__fmul_rd(Zp.x, sc.x), __fmul_rd(Zp.y, sc.y));
+          Zl = make_float2(__fmul_rd(Zl.x, sc.x), __fmul_rd(Zl.y, sc.y));
+          SAp = make_float2(__fmul_ru(SAp.x, su.x), __fmul_ru(SAp.y, su.y));
+          SAl = make_float2(__fmul_ru(SAl.x, su.x), __fmul_ru(SAl.y, su.y));
+          SBp = make_float2(__fmul_ru(SBp.x, su.x), __fmul_ru(SBp.y, su.y));
+          SBl = make_float2(__fmul_ru(SBl.x, su.x), __fmul_ru(SBl.y, su.y));
+          if (VW) {
+            SVp = make_float2(__fmul_ru(SVp.x, su.x), __fmul_ru(SVp.y, su.y));
+            SVl = make_float2(__fmul_ru(SVl.x, su.x), __fmul_ru(SVl.y, su.y));
+          }
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const float2 lo = __fmul2_rn(make_float2(acco[mt][0], acco[mt][1]), sc);
@@ -665,20 +745,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         }
       }
       const float2 peA = ex2x2(dA), peB = ex2x2(dB);
-      Zp = __fadd2_rn(Zp, __fadd2_rn(peA, peB));
+      kahan_add2(Zp, Zl, __fadd2_rn(peA, peB));
       if (METER) {
         const float2 taA = meter_term2(peA, dA, epsA), taB = meter_term2(peB, dB, epsB);
-        SAp = __fadd2_rn(SAp, __fadd2_rn(taA, taB));
+        kahan_add2(SAp, SAl, __fadd2_rn(taA, taB));
         if (VW) {       // value witnesses of tokens g and g + 8 (zero past the context, where p is 0)
           const __half* wv = reinterpret_cast<const __half*>(sb + L::BYTES);
-          SVp = __ffma2_rn(peA, f2(__half2float(wv[g])), SVp);
-          SVp = __ffma2_rn(peB, f2(__half2float(wv[g + 8])), SVp);
+          kahan_add2(SVp, SVl, __ffma2_rn(peA, f2(__half2float(wv[g])), __fmul2_rn(peB, f2(__half2float(wv[g + 8])))));
         }
         float2 tbA = f2(0.f), tbB = f2(0.f);
         if (SCHEME == kInt8) {
           tbA = meter_term2(peA, dA, ubA);
           tbB = meter_term2(peB, dB, ubB);
-          SBp = __fadd2_rn(SBp, __fadd2_rn(tbA, tbB));
+          kahan_add2(SBp, SBl, __fadd2_rn(tbA, tbB));
         }
         if (RISK) {
           float2 r = SCHEME == kInt8 ? __fadd2_rn(tbA, tbB) : __fadd2_rn(taA, taB);
@@ -815,18 +894,24 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   if (!active) return;
 
   // ---------------------------------------------------------------- partial state of this split
+  // Each lane's pair leaves rounded down (Z) or up (S_A, S_B, S_V); the eight lanes of a head
+  // pair then meet through adds rounded the same way (three one-sided roundings), so the record
+  // never understates a meter.
+  auto lane_sum = [&](float2 hi, float2 lo, bool up) -> float2 {
+    float2 v = up ? make_float2(__fadd_ru(hi.x, lo.x), __fadd_ru(hi.y, lo.y))
+                  : make_float2(__fadd_rd(hi.x, lo.x), __fadd_rd(hi.y, lo.y));
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    Zp.x += __shfl_xor_sync(0xffffffffu, Zp.x, o);
-    Zp.y += __shfl_xor_sync(0xffffffffu, Zp.y, o);
-    SAp.x += __shfl_xor_sync(0xffffffffu, SAp.x, o);
-    SAp.y += __shfl_xor_sync(0xffffffffu, SAp.y, o);
-    SBp.x += __shfl_xor_sync(0xffffffffu, SBp.x, o);
-    SBp.y += __shfl_xor_sync(0xffffffffu, SBp.y, o);
-    if (VW) {
-      SVp.x += __shfl_xor_sync(0xffffffffu, SVp.x, o);
-      SVp.y += __shfl_xor_sync(0xffffffffu, SVp.y, o);
+    for (int o = 4; o < 32; o <<= 1) {
+      const float ox = __shfl_xor_sync(0xffffffffu, v.x, o), oy = __shfl_xor_sync(0xffffffffu, v.y, o);
+      v = up ? make_float2(__fadd_ru(v.x, ox), __fadd_ru(v.y, oy)) : make_float2(__fadd_rd(v.x, ox), __fadd_rd(v.y, oy));
     }
+    return v;
+  };
+  Zp = lane_sum(Zp, Zl, false);
+  if (METER) {
+    SAp = lane_sum(SAp, SAl, true);
+    if (SCHEME == kInt8) SBp = lane_sum(SBp, SBl, true);
+    if (VW) SVp = lane_sum(SVp, SVl, true);
   }
   if (SCHEME == kKivi) {
     // add sum_t p_t zero_{t,G} of heads 2t, 2t+1 (held by lanes 4*head)

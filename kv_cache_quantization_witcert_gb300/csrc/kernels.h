@@ -27,6 +27,7 @@ struct WriteArgs {
   int late_wait;             // token, block and KIVI value kernels wait for their predecessor at
                              // their end instead of their start (see ChainEntry in write.cu)
   uint64_t seed;
+  uint32_t rk0[10], rk1[10]; // Philox round keys of `seed` (as in DecodeArgs)
   void* backing;             // device-mapped pinned host, layer base [B][Hkv][backing_rows][128], or null
   const int32_t* slots;      // layer base [B][Hkv][nblk_max], or null
   void* pool;                // exact-key pool [slots][16][128]
@@ -104,9 +105,16 @@ int decode_auto_splits(int scheme, int B, int Hkv, int nblk, int sm_count, int p
 // used by witcert_decode_noalloc; the first call on a device looks the address up.
 cudaError_t decode_static_scratch(float** ptr, size_t* bytes);
 
+// Exact fixed-point sums of the gate: 320 bits in units of 2^-149 (ten 32-bit limbs).
+constexpr int kBigLimbs = 10;
+// Keys a selection CTA sorts per thread, at most; with 512 threads the gate ranks up to
+// 16384 blocks (262144 tokens) per sequence.
+constexpr int kSelMaxKeysPerThread = 32;
+
 struct GateArgs {
   const float* risk;         // [B][Hq][nblk_max] (this layer)
-  int32_t* slots;            // [B][Hkv][nblk_max] (this layer)
+  int32_t* slots;            // [B][Hkv][nblk_max] (this layer), or null: candidacy from `repaired`
+  const uint8_t* repaired;   // [B][Hkv][nblk_max] nonzero = not a candidate (used when slots is null), or null
   uint32_t* selmask;         // [B][Hkv][nblk_max/32 + 1] scratch bitmap
   int4* todo;                // [capacity] (seq, kv head, block, slot)
   unsigned int* todo_count;  // device counter (reset per call)
@@ -118,9 +126,16 @@ struct GateArgs {
   void* pool;
   int nblk_max, B, Hq, Hkv, grp, S, backing_rows, pool_capacity, scheme, elem_bytes;
   const int* seq_len;        // [B] per-sequence lengths (ragged batch), or null (all S)
-  double d_star;
+  double d_star;             // sqrt(1 + 2 tau) - 1 in float64
+  uint32_t dstar[kBigLimbs]; // floor(d_star 2^149), filled by the launcher
 };
+// Selection, bitmap compaction and page-in of one layer.
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t st);
+// Selection alone: sets the bits of a.selmask ([B][Hkv][nblk_max/32 + 1], zeroed by the caller)
+// of the blocks the cells ask for; a.stats may be null.  Fails for more than gate_max_blocks().
+cudaError_t launch_gate_select(const GateArgs& a, cudaStream_t st);
+int gate_max_blocks();
+void fixed_limbs(double d, uint32_t (&w)[kBigLimbs]);
 
 struct ExportArgs {
   const uint8_t* blocks;
@@ -137,5 +152,9 @@ cudaError_t launch_export(const ExportArgs& a, cudaStream_t st);
 cudaError_t run_wait_selftest(uint64_t limit_ns, cudaStream_t st, int* timed_out);
 cudaError_t launch_dither(uint64_t seed, int layer, int kvh, int t0, int n, int tensor, float* out,
                           cudaStream_t st);
+// Writers' quotient x / s (reciprocal and one correction) against the IEEE quotient, for every
+// positive fp16 scale s and every bf16 x with |x| <= 127.5 s plus n_f32 seeded fp32 x per
+// scale; *mismatches counts the pairs that differ (synchronous).
+cudaError_t run_quotient_selftest(int n_f32, uint64_t seed, unsigned long long* mismatches, cudaStream_t st);
 
 }  // namespace witcert

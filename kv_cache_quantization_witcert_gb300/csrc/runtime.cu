@@ -72,6 +72,7 @@ struct witcert_cache {
   bool lengths_last = false;        // the most recent launch on the cache's stream set dlen
   std::vector<cudaEvent_t> gate_done;
   std::vector<char> gate_pending;
+  std::vector<char> backing_lost;   // per layer: the backing store misses exact keys (gate -> EPAGEIN)
   cudaStream_t side = nullptr;
   bool profiling = false;
   std::vector<ProfPair> prof_pending, prof_free;
@@ -163,6 +164,9 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   if (f.pos_offset < 0) return fail(WITCERT_EINVAL, "pos_offset must be >= 0");
   if (f.max_pages < 0) return fail(WITCERT_EINVAL, "max_pages must be >= 0");
   if (f.max_pages > 0 && f.kv_dtype != WITCERT_BF16) return fail(WITCERT_EINVAL, "a paged cache holds bf16 keys and values");
+  if (f.max_repair_blocks > 0 && (f.max_tokens + kBlk - 1) / kBlk > gate_max_blocks())
+    return fail(WITCERT_EINVAL, "with the gate enabled max_tokens must be at most %d (the gate ranks up to %d blocks)",
+                gate_max_blocks() * kBlk, gate_max_blocks());
 
   auto* c = new (std::nothrow) witcert_cache();
   if (!c) return fail(WITCERT_ENOMEM, "host allocation failed");
@@ -184,6 +188,7 @@ witcert_status witcert_create(const witcert_config* cfg, witcert_cache** out) {
   c->risk_gen.assign(f.n_layers, ~uint64_t(0));
   c->gate_done.assign(f.n_layers, nullptr);
   c->gate_pending.assign(f.n_layers, 0);
+  c->backing_lost.assign(f.n_layers, 0);
   const size_t L = f.n_layers, cells = (size_t)f.batch * f.n_q_heads;
   const bool gate = f.max_repair_blocks > 0;
 
@@ -250,6 +255,7 @@ static WriteArgs layer_write_args(const witcert_cache* c, int layer, const void*
   a.backing_rows = (int)backing_rows(c);
   a.is_bf16 = c->cfg.kv_dtype == WITCERT_BF16;
   a.seed = c->cfg.seed;
+  philox_round_keys(a.seed, a.rk0, a.rk1);
   a.pos0 = c->cfg.pos_offset;
   if (c->backing_dev)
     a.backing = static_cast<uint8_t*>(c->backing_dev) + layer * layer_rows(c) * backing_rows(c) * kD * c->elem;
@@ -394,7 +400,10 @@ static witcert_status write_impl(witcert_cache* c, int layer, const void* K, con
       // bulk writes copy their exact keys to the pinned backing store with the copy engines
       // instead of the kernels' stores over C2C
       for (int i = 0; i < B && e == cudaSuccess; ++i) e = backing_copy(c, layer, K, i, (size_t)i * n_tok, n_tok, t0, st);
-      if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
+      if (e != cudaSuccess) {
+        c->backing_lost[layer] = 1;
+        return cuda_fail(e, "backing-store copy");
+      }
       a.backing = nullptr;
       pdl = false;                     // the copies sit between this write and its predecessor
     }
@@ -430,7 +439,10 @@ static witcert_status write_impl(witcert_cache* c, int layer, const void* K, con
         WriteArgs a = seq_write_args(c, all, i, row, n[i], t0);
         if (c->backing_host && n[i] >= kBulkBackingTokens) {
           e = backing_copy(c, layer, K, i, row, n[i], t0, st);
-          if (e != cudaSuccess) return cuda_fail(e, "backing-store copy");
+          if (e != cudaSuccess) {
+            c->backing_lost[layer] = 1;
+            return cuda_fail(e, "backing-store copy");
+          }
           a.backing = nullptr;
           pdl = false;
         }
@@ -628,6 +640,9 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   if (meter_v && !c->vwit) return fail(WITCERT_EINVAL, "meter_v needs a cache created with v_witness");
   const bool meter = meter_a || meter_b || raw_a || raw_b || meter_v;
   if (meter && !(delta_req > 0.0 && delta_req <= 1.0)) return fail(WITCERT_EINVAL, "delta_req must be in (0, 1]");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device)
+    return fail(WITCERT_EINVAL, "the cache lives on device %d; make it current before this call", c->device);
   DecodeArgs a{};
   fill_decode(c, layer, q, delta_req, meter, 0, a);
   float* scratch = nullptr;
@@ -653,6 +668,8 @@ witcert_status witcert_decode_noalloc(witcert_cache* c, int layer, const void* q
   c->lengths_last = false;
   if (gate && meter) c->risk_gen[layer] = c->write_gen[layer];
   c->last_write_layer = -1;
+  c->last_n_splits = a.n_splits;
+  ++c->decode_calls;
   ok();
   return WITCERT_OK;
 }
@@ -704,6 +721,8 @@ witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream
   if (!(tau >= 0.f) || !std::isfinite(tau)) return fail(WITCERT_EINVAL, "tau must be finite and >= 0");
   if (c->risk_gen[layer] != c->write_gen[layer] || c->len[layer] == 0)
     return fail(WITCERT_ESTATE, "layer %d has no metered decode since its last write", layer);
+  if (c->backing_lost[layer])
+    return fail(WITCERT_EPAGEIN, "layer %d: the backing store lost exact keys; nothing was paged in", layer);
   auto st = static_cast<cudaStream_t>(stream);
   cudaEvent_t ready = c->gate_done[layer];
   cudaError_t e = cudaEventRecord(ready, st);   // reuse: marks the point the gate must follow
@@ -730,6 +749,37 @@ witcert_status witcert_gate(witcert_cache* c, int layer, float tau, void* stream
   if (e != cudaSuccess) return cuda_fail(e, "gate launch");
   c->gate_pending[layer] = 1;
   ++c->gate_calls;
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_gate_select(const float* risk, const uint8_t* repaired, int batch, int n_q_heads,
+                                   int n_kv_heads, int nblk, float tau, uint32_t* selected, void* stream) {
+  if (!risk || !selected) return fail(WITCERT_EINVAL, "risk and selected must not be NULL");
+  if (batch < 1 || n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads)
+    return fail(WITCERT_EINVAL, "batch >= 1 and n_q_heads a positive multiple of n_kv_heads");
+  if (nblk < 1 || nblk > gate_max_blocks()) return fail(WITCERT_EINVAL, "nblk must be in [1, %d]", gate_max_blocks());
+  if (!(tau >= 0.f) || !std::isfinite(tau)) return fail(WITCERT_EINVAL, "tau must be finite and >= 0");
+  auto st = static_cast<cudaStream_t>(stream);
+  GateArgs a{};
+  a.risk = risk;
+  a.repaired = repaired;
+  a.selmask = selected;
+  a.nblk_max = nblk; a.B = batch; a.Hq = n_q_heads; a.Hkv = n_kv_heads; a.grp = n_q_heads / n_kv_heads;
+  a.S = nblk * kBlk;
+  a.d_star = std::sqrt(1.0 + 2.0 * (double)tau) - 1.0;
+  cudaError_t e = cudaMemsetAsync(selected, 0, (size_t)batch * n_kv_heads * (nblk / 32 + 1) * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = launch_gate_select(a, st);
+  if (e != cudaSuccess) return cuda_fail(e, "gate selection");
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_inject_fault(witcert_cache* c, witcert_fault fault, int layer) {
+  if (witcert_status s = check_layer(c, layer)) return s;
+  if (fault != WITCERT_FAULT_BACKING_LOST) return fail(WITCERT_EINVAL, "unknown fault %d", (int)fault);
+  if (c->cfg.max_repair_blocks <= 0) return fail(WITCERT_ESTATE, "the gate is disabled: there is no backing store");
+  c->backing_lost[layer] = 1;
   ok();
   return WITCERT_OK;
 }
@@ -864,6 +914,16 @@ witcert_status witcert_wait_selftest(int64_t limit_ns, void* stream) {
   cudaError_t e = run_wait_selftest((uint64_t)limit_ns, static_cast<cudaStream_t>(stream), &timed_out);
   if (e != cudaSuccess) return cuda_fail(e, "wait self test");
   if (timed_out) return fail(WITCERT_ETIMEDOUT, "device wait gave up after %lld ns", (long long)limit_ns);
+  ok();
+  return WITCERT_OK;
+}
+
+witcert_status witcert_quotient_selftest(int n_f32, uint64_t seed, uint64_t* mismatches, void* stream) {
+  if (n_f32 < 0 || n_f32 > (1 << 20) || !mismatches) return fail(WITCERT_EINVAL, "n_f32 in [0, 2^20] and a result pointer");
+  unsigned long long m = 0;
+  cudaError_t e = run_quotient_selftest(n_f32, seed, &m, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quotient self test");
+  *mismatches = m;
   ok();
   return WITCERT_OK;
 }

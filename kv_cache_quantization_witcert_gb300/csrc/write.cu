@@ -13,6 +13,7 @@
 // The black-box scheme stores a caller's tensor-function outputs K_hat, V_hat as
 // bfloat16 and takes the witness against them.  With the value witness on, every
 // writer also stores ||v - v_hat|| over the whole row, rounded up to fp16 the same way.
+#include <cfloat>
 #include <cmath>
 
 #include "common.cuh"
@@ -159,6 +160,75 @@ __device__ __forceinline__ bool store_witness_df(uint8_t* wreg, int r, const Df 
   return true;
 }
 
+// ---------------------------------------------------------------- fp32 fast path of the witness
+// Most bands are decided in plain fp32: from residual estimates rr_e (each within err_e of the
+// exact residual, so the band norm is within the sum of the err_e) the norm is bracketed by
+// [w_lo, w_hi], widened by 2^-19 for the rounding of the squares, their sums and the square
+// root (together below 2^-21), and by 2^-47 more for the stored witness's 2^-48 margin.  When
+// both ends round up to the same fp16 value, that value is the stored witness; otherwise (an
+// fp16 value inside the bracket, about one band in a thousand) the double-float path decides.
+__device__ __forceinline__ bool bracket_f16_ru(float ss, float err, __half& w16) {
+  const float w = __fsqrt_rn(ss);
+  const float hi = __fmul_ru(__fadd_ru(w, err), 0x1.00002p+0f);       // (1 + 2^-19) above
+  const float lo = fmaxf(__fmul_rd(__fsub_rd(w, err), 0x1.ffffcp-1f), 0.0f);
+  const __half h_hi = __float2half_ru(hi);
+  w16 = h_hi;
+  return __half_as_ushort(h_hi) == __half_as_ushort(__float2half_ru(lo));
+}
+// Band witness (lanes 0..15 store band `lane`) from the lane's fp32 residual estimates and
+// their summed error bound; false, storing nothing, when some band of the warp is undecided.
+__device__ __forceinline__ bool store_witness_fast(uint8_t* wreg, int r, const float (&rr)[4], float err, int lane,
+                                                   bool zero) {
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ss = __fmaf_rn(rr[e], rr[e], ss);
+  ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 16));
+  err = __fadd_ru(err, __shfl_xor_sync(0xffffffffu, err, 16));
+  __half w16 = __float2half_rn(0.f);
+  const bool ok = lane >= 16 || zero || bracket_f16_ru(ss, err, w16);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  if (lane < 16) *reinterpret_cast<__half*>(wreg + wit_off(r, lane)) = zero ? __float2half_rn(0.f) : w16;
+  return true;
+}
+// Value witness of the whole row (lane 0 stores it) by the same rule; the 32-term sum of squares
+// stays within the 2^-19 widening.
+__device__ __forceinline__ bool store_rownorm_fast(__half* dst, const float (&rr)[4], float err, int lane) {
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ss = __fmaf_rn(rr[e], rr[e], ss);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    err = __fadd_ru(err, __shfl_xor_sync(0xffffffffu, err, o));
+  }
+  __half w16 = __float2half_rn(0.f);
+  const bool ok = bracket_f16_ru(ss, err, w16);
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+  if (lane == 0) *dst = w16;
+  return true;
+}
+// Error bound of an fp32 residual estimate rr = RN(d + p) formed from d = RN(u - v) (u - v
+// exact: the terms' sum has one rounding each) and an exact or rounded-once p: one unit of
+// each result, plus an absolute 2^-148 for results below fp32's normal range.
+__device__ __forceinline__ float resid_err(float d, float rr) {
+  return __fmaf_ru(0x1p-23f, __fadd_ru(fabsf(d), fabsf(rr)), 0x1p-148f);
+}
+
+// ---------------------------------------------------------------- quotients
+// x / s rounded to nearest from y = RN(1/s): q0 = RN(x y) is within one unit of x / s, the
+// remainder x - q0 s is then exact (one FMA), and RN(q0 + r y) is the correctly rounded
+// quotient (Markstein's theorem, as in Cornea, Golliver and Markstein, "Correctness proofs
+// outline for Newton-Raphson based floating-point divide and square root algorithms", 1999),
+// provided no intermediate leaves fp32's normal range.  The writers need the exact quotient
+// only where it can move a code: |x / s| >= 2^-25 with s >= 2^-24, far from that range.
+__device__ __forceinline__ float div_rn_by(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, s, x);
+  return __fmaf_rn(r, y, q0);
+}
+constexpr float kInv127 = 0x1.020408p-7f;          // RN(1/127)
+constexpr float kInv3 = 0x1.555556p-2f;            // RN(1/3)
+
 // Value witness: lane 0 stores the norm of the whole row (all 32 lanes' residuals) at *dst,
 // by the same rule; false (nothing stored) when the warp must take the fp64 path.
 __device__ __forceinline__ bool store_rownorm_df(__half* dst, const Df (&res)[4], float err, int lane) {
@@ -233,23 +303,25 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
     amax = grp_max8(amax);
     // s = fp16 round-up of fp32(amax / 127), at most 65504
-    __half s16 = __float2half_ru(__fdiv_rn(amax, 127.0f));
+    __half s16 = __float2half_ru(div_rn_by(amax, 127.0f, kInv127));
     if (__half2float(s16) > 65504.0f) s16 = __float2half_rn(65504.0f);
     const float s = __half2float(s16);
+    const float ys = s > 0.0f ? __frcp_rn(s) : 0.0f;
     // round to nearest is the dithered quantizer with xi = 0
-    const float4 xi = DITHER ? dither4(a.seed, a.layer, h, a.pos0 + t, lane, tensor) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 xi = DITHER ? dither4_rk(a.rk0, a.rk1, a.layer, h, a.pos0 + t, lane, tensor)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
     const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
     uint32_t packed = 0;
     int codes[4];
-    Df rdf[4];
-    float err = 0.f;
+    float rr[4];
+    float ferr = 0.f;
     int clamps = 0;
     const bool resid = tensor == 0 || VW;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int code = 0;
       if (s > 0.0f) {
-        const float z = __fadd_rn(__fdiv_rn(x[e], s), xs[e]);
+        const float z = __fadd_rn(div_rn_by(x[e], s, ys), xs[e]);
         float rz = rintf(z);
         if (rz < -128.f) { rz = -128.f; ++clamps; }
         if (rz > 127.f) { rz = 127.f; ++clamps; }
@@ -257,13 +329,11 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
       }
       codes[e] = code;
       if (resid) {
-        // residual x - s (code - xi) = x - s code + s xi, as exact fp32 terms (s code has at most
-        // 19 significant bits; s xi is an exact product pair)
-        const float sc = __fmul_rn(s, (float)code);
-        const Df sx = two_prod(s, xs[e]);
-        rdf[e] = residual_df(x[e], -sc, sx.hi, sx.lo);
-        err = __fadd_ru(err, __fmul_ru(0x1p-46f, __fadd_ru(__fadd_ru(fabsf(x[e]), fabsf(sc)),
-                                                           __fadd_ru(fabsf(sx.hi), fabsf(sx.lo)))));
+        // residual x - s (code - xi) = (x - s code) + s xi: s code is exact (at most 19
+        // significant bits), the difference and the FMA round once each
+        const float d = __fsub_rn(x[e], __fmul_rn(s, (float)code));
+        rr[e] = __fmaf_rn(s, xs[e], d);
+        ferr = __fadd_ru(ferr, resid_err(d, rr[e]));
       }
       const uint32_t biased = (uint32_t)(code + 128) & 0xFFu;
       if (tensor == 0) packed |= biased << (8 * e);
@@ -272,19 +342,38 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     if (clamps) atomicAdd(a.clamps, (unsigned long long)clamps);
     if ((lane & 7) == 0)
       *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS + vscale_off(r, G) : Int8Layout::KS + (r * 4 + G) * 2)) = s16;
+    // exact residual terms for the double-float path (x, -s code, and s xi as an exact product pair)
+    auto resid_df = [&](Df (&rdf)[4], float& err) {
+      err = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float sc = __fmul_rn(s, (float)codes[e]);
+        const Df sx = two_prod(s, xs[e]);
+        rdf[e] = residual_df(x[e], -sc, sx.hi, sx.lo);
+        err = __fadd_ru(err, __fmul_ru(0x1p-46f, __fadd_ru(__fadd_ru(fabsf(x[e]), fabsf(sc)),
+                                                           __fadd_ru(fabsf(sx.hi), fabsf(sx.lo)))));
+      }
+    };
+    Df rdf[4];
+    float err = 0.f;
     if (tensor == 0) {
       *reinterpret_cast<uint32_t*>(bp + Int8Layout::KC + kcode_off(r, 4 * lane)) = packed;
+      if (store_witness_fast(bp + Int8Layout::W, r, rr, ferr, lane, repaired)) continue;
+      resid_df(rdf, err);
       if (!store_witness_df(bp + Int8Layout::W, r, rdf, err, lane, repaired)) {
         double res[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
         store_witness(bp + Int8Layout::W, r, res, lane, repaired);
       }
-    } else if (VW && !store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
-      double res[4];
+    } else if (VW && !store_rownorm_fast(vwit_at(a, i, h, t), rr, ferr, lane)) {
+      resid_df(rdf, err);
+      if (!store_rownorm_df(vwit_at(a, i, h, t), rdf, err, lane)) {
+        double res[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
-      store_rownorm(vwit_at(a, i, h, t), res, lane);
+        for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)s * ((double)codes[e] - (double)xs[e]);
+        store_rownorm(vwit_at(a, i, h, t), res, lane);
+      }
     }
   }
 }
@@ -299,26 +388,36 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
     float x[4];
     load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
     uint32_t packed = 0;
-    float xhs[4];
+    float xhs[4], rr[4];
     Df rdf[4];
+    float ferr = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(x[e], __NV_SATFINITE, __NV_E4M3);
       const float xh = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
       xhs[e] = xh;
-      rdf[e] = residual_df(x[e], -xh, 0.f, 0.f);            // exact: one error-free sum
+      rr[e] = __fsub_rn(x[e], xh);
+      ferr = __fadd_ru(ferr, resid_err(rr[e], rr[e]));
       if (tensor == 0) packed |= (uint32_t)c << (8 * e);
       else bp[Fp8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)c;
     }
+    auto resid_df = [&]() {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rdf[e] = residual_df(x[e], -xhs[e], 0.f, 0.f);   // exact: one error-free sum
+      return true;
+    };
     if (tensor == 0) {
       *reinterpret_cast<uint32_t*>(bp + Fp8Layout::KC + kcode_off(r, 4 * lane)) = packed;
+      if (store_witness_fast(bp + Fp8Layout::W, r, rr, ferr, lane, repaired)) continue;
+      resid_df();
       if (!store_witness_df(bp + Fp8Layout::W, r, rdf, 0.f, lane, repaired)) {
         double res[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xhs[e];
         store_witness(bp + Fp8Layout::W, r, res, lane, repaired);
       }
-    } else if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
+    } else if (a.vwit && !store_rownorm_fast(vwit_at(a, i, h, t), rr, ferr, lane) && resid_df() &&
+               !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
       double res[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xhs[e];
@@ -341,12 +440,23 @@ __device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int 
     const __nv_bfloat162 p01 = __floats2bfloat162_rn(y[0], y[1]), p23 = __floats2bfloat162_rn(y[2], y[3]);
     const float xh[4] = {__low2float(p01), __high2float(p01), __low2float(p23), __high2float(p23)};
     Df rdf[4];
+    float rr[4], ferr = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) rdf[e] = residual_df(x[e], -xh[e], 0.f, 0.f);   // exact: one error-free sum
+    for (int e = 0; e < 4; ++e) {
+      rr[e] = __fsub_rn(x[e], xh[e]);
+      ferr = __fadd_ru(ferr, resid_err(rr[e], rr[e]));
+    }
+    auto resid_df = [&]() {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) rdf[e] = residual_df(x[e], -xh[e], 0.f, 0.f);   // exact: one error-free sum
+      return true;
+    };
     if (tensor == 0) {
       // channels 4 lane .. 4 lane + 3: registers h (e = 0, 1) and h + 2 (e = 2, 3) of one (k-step, lane) slot
       *reinterpret_cast<uint32_t*>(bp + BboxLayout::KH + kbf_off(r, 4 * lane)) = bf2_bits(p01);
       *reinterpret_cast<uint32_t*>(bp + BboxLayout::KH + kbf_off(r, 4 * lane + 2)) = bf2_bits(p23);
+      if (store_witness_fast(bp + BboxLayout::W, r, rr, ferr, lane, repaired)) continue;
+      resid_df();
       if (!store_witness_df(bp + BboxLayout::W, r, rdf, 0.f, lane, repaired)) {
         double res[4];
 #pragma unroll
@@ -359,7 +469,8 @@ __device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int 
       vh[vbf_off(r, 4 * lane + 1) / 2] = __high2bfloat16(p01);
       vh[vbf_off(r, 4 * lane + 2) / 2] = __low2bfloat16(p23);
       vh[vbf_off(r, 4 * lane + 3) / 2] = __high2bfloat16(p23);
-      if (a.vwit && !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
+      if (a.vwit && !store_rownorm_fast(vwit_at(a, i, h, t), rr, ferr, lane) && resid_df() &&
+          !store_rownorm_df(vwit_at(a, i, h, t), rdf, 0.f, lane)) {
         double res[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) res[e] = (double)x[e] - (double)xh[e];
@@ -423,9 +534,10 @@ __global__ void __launch_bounds__(128, 6) write_block_kernel(const WriteArgs a, 
 }
 
 // KIVI asymmetric 2-bit of one value against fp16 scale/zero (fp32 steps as the oracle states them).
-__device__ __forceinline__ int kivi_code(float x, float zr, float sc) {
+// ysc = RN(1 / sc): the quotient by div_rn_by, equal to the IEEE one wherever it can move a code.
+__device__ __forceinline__ int kivi_code(float x, float zr, float sc, float ysc) {
   if (!(sc > 0.0f)) return 0;
-  float v = rintf(__fdiv_rn(__fsub_rn(x, zr), sc));
+  float v = rintf(div_rn_by(__fsub_rn(x, zr), sc, ysc));
   v = fminf(fmaxf(v, 0.0f), 3.0f);
   return (int)v;
 }
@@ -441,15 +553,16 @@ __device__ __forceinline__ void kivi_v_token(const WriteArgs& a, uint8_t* bp, in
   load4f<T>(reinterpret_cast<const T*>(a.V) + row + 4 * lane, x);
   const float mn = grp_min8(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
   const float mx = grp_max8(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
-  const __half sc16 = f16_sat_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+  const __half sc16 = f16_sat_rn(div_rn_by(__fsub_rn(mx, mn), 3.0f, kInv3));
   const __half zr16 = f16_sat_rn(mn);
   const float sc = __half2float(sc16), zr = __half2float(zr16);
+  const float ysc = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
   int codes[4];
   Df rdf[4];
   float err = 0.f;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const int code = kivi_code(x[e], zr, sc);
+    const int code = kivi_code(x[e], zr, sc, ysc);
     codes[e] = code;
     int off, bit;
     kivi_v_pos(r, 4 * lane + e, off, bit);
@@ -561,19 +674,20 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int
     uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * KiviLayout::BYTES;
     __half* ksc = reinterpret_cast<__half*>(bp + KiviLayout::KP);
     __half* kzr = reinterpret_cast<__half*>(bp + KiviLayout::KP + 256);
-    float sc[4], zr[4];
+    float sc[4], zr[4], ysc[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float mn = x[0][e], mx = x[0][e];
 #pragma unroll
       for (int r = 1; r < kBlk; ++r) { mn = fminf(mn, x[r][e]); mx = fmaxf(mx, x[r][e]); }
-      const __half s16 = f16_sat_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half s16 = f16_sat_rn(div_rn_by(__fsub_rn(mx, mn), 3.0f, kInv3));
       const __half z16 = f16_sat_rn(mn);
       const int c = 4 * lane + e;
       ksc[kivi_kparam_idx(c)] = s16;
       kzr[kivi_kparam_idx(c)] = z16;
       sc[e] = __half2float(s16);
       zr[e] = __half2float(z16);
+      ysc[e] = sc[e] > 0.0f ? __frcp_rn(sc[e]) : 0.0f;
     }
 #pragma unroll
     for (int r = 0; r < kBlk; ++r) {
@@ -582,7 +696,7 @@ __global__ void __launch_bounds__(32) write_kivi_k_kernel(const WriteArgs a, int
       float err = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int code = kivi_code(x[r][e], zr[e], sc[e]);
+        const int code = kivi_code(x[r][e], zr[e], sc[e], ysc[e]);
         codes[e] = code;
         // residual x - (zero + scale code): scale code is exact (at most 13 significant bits)
         const float scc = __fmul_rn(sc[e], (float)code);
@@ -714,6 +828,58 @@ cudaError_t launch_set_lengths(const LengthArgs& u, cudaStream_t st, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, set_lengths_kernel, u);
+}
+
+namespace {
+
+// 32-bit mix of a counter (the xorshift-multiply finalizer of MurmurHash3): test inputs only.
+__device__ __forceinline__ uint32_t mix32(uint32_t h) {
+  h ^= h >> 16; h *= 0x85ebca6bu; h ^= h >> 13; h *= 0xc2b2ae35u; h ^= h >> 16;
+  return h;
+}
+
+// One CTA per positive fp16 scale (bits 1 .. 0x7BFF): every bf16 x with |x| <= 127.5 s, then
+// n_f32 fp32 x = s * u with u drawn in (-127.5, 127.5).  Two more CTAs divide by the constants
+// 127 (the INT8 scale) and 3 (the KIVI scale), every finite bf16 x and n_f32 fp32 x drawn over
+// fp32's exponent range.  Counts quotients that differ from the IEEE quotient where a code or a
+// scale can depend on them (|x / s| >= 2^-25).
+__global__ void __launch_bounds__(256) quotient_selftest_kernel(int n_f32, uint32_t seed, unsigned long long* bad) {
+  const bool konst = blockIdx.x >= 0x7BFF;
+  const float s = konst ? (blockIdx.x == 0x7BFF ? 127.0f : 3.0f) : __half2float(__ushort_as_half((unsigned short)(blockIdx.x + 1)));
+  const float y = konst ? (blockIdx.x == 0x7BFF ? kInv127 : kInv3) : __frcp_rn(s);
+  const float range = konst ? FLT_MAX : 127.5f * s;
+  unsigned long long cnt = 0;
+  for (int b = threadIdx.x; b < 65536 + n_f32; b += blockDim.x) {
+    float x;
+    if (b < 65536) {
+      x = __uint_as_float((uint32_t)b << 16);
+    } else {
+      const uint32_t h = mix32(seed ^ mix32((uint32_t)(blockIdx.x * 0x9E3779B9u) ^ (uint32_t)b));
+      if (konst) x = __uint_as_float(h);                         // any bit pattern; inf and NaN skipped
+      else x = __fmul_rn(s, __fmul_rn((float)(int)(h >> 8) - 8388608.0f, 0x1.fep-17f));   // u = 127.5 (m - 2^23) / 2^23
+    }
+    if (!(fabsf(x) <= range)) continue;
+    const float want = __fdiv_rn(x, s);
+    if (fabsf(want) >= 0x1p-25f && __float_as_uint(div_rn_by(x, s, y)) != __float_as_uint(want)) ++cnt;
+  }
+  if (cnt) atomicAdd(bad, cnt);
+}
+
+}  // namespace
+
+cudaError_t run_quotient_selftest(int n_f32, uint64_t seed, unsigned long long* mismatches, cudaStream_t st) {
+  unsigned long long* d = nullptr;
+  cudaError_t e = cudaMalloc(&d, sizeof(unsigned long long));
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(d, 0, sizeof(unsigned long long), st);
+  if (e == cudaSuccess) {
+    quotient_selftest_kernel<<<0x7BFF + 2, 256, 0, st>>>(n_f32, (uint32_t)(seed ^ (seed >> 32)), d);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(mismatches, d, sizeof(unsigned long long), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  cudaFree(d);
+  return e;
 }
 
 void philox_round_keys(uint64_t seed, uint32_t (&rk0)[10], uint32_t (&rk1)[10]) {

@@ -9,10 +9,12 @@ from kv_cache_quantization_witcert_gb300 import _lib
 from oracle import OracleCache, meter, quant
 from oracle.philox import dither
 
-# Meters: GPU >= oracle (one fp32 ulp of slack for rounding the oracle's value to fp32)
-# and GPU <= oracle * (1 + 1e-4); a GPU NaN where the oracle has a number fails.
+# Meters: GPU >= oracle with no relative slack (the library rounds every meter up) and
+# GPU <= oracle * (1 + 1e-4); a GPU NaN where the oracle has a number fails.  The one absolute
+# allowance, 2^-99, is for values below fp32's range: the meters are fp32, terms whose weights
+# fall under 2^-126 are dropped, and the library adds 2^-100 to every positive meter and risk.
 METER_REL = 1e-4
-FP32_ULP = 2.0 ** -23
+METER_ABS = 2.0 ** -99
 
 
 def torch_dtype(w):
@@ -61,8 +63,8 @@ def write_both(gpu, ref, layer, K, V, w, seed=0):
 def check_meter(gpu, ref, rel=METER_REL, what=""):
     g = np.asarray(gpu, np.float64)
     r = np.asarray(ref, np.float64)
-    low = g < r * (1 - FP32_ULP)
-    high = g > r * (1 + rel) + 1e-30
+    low = g < r - METER_ABS
+    high = g > r * (1 + rel) + METER_ABS
     nan = np.isnan(g) & ~np.isnan(r)          # a NaN bounds nothing and fails both comparisons
     if low.any() or high.any() or nan.any():
         idx = np.argwhere(low | high | nan)[:5]
@@ -166,3 +168,64 @@ def oracle_group(w, layer, K, V, q, i, h, scheme, dloc, k_pos0=0):
         kscales = None
     wst = quant.witness_stored(quant.witness(K - kh)).astype(np.float64)
     return meter.decode_ref(q, kh, vh, wst, kscales, None, dloc)
+
+
+# Block risks: as the meters, GPU >= oracle and <= oracle * (1 + 1e-4) up to METER_ABS.
+RISK_ABS = METER_ABS
+
+
+def check_risk(gpu, ref, rel=METER_REL, what="risk"):
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    low = g < r - RISK_ABS
+    high = g > r * (1 + rel) + RISK_ABS
+    nan = np.isnan(g)
+    if low.any() or high.any() or nan.any():
+        idx = np.argwhere(low | high | nan)[:5]
+        detail = [(tuple(ix), g[tuple(ix)], r[tuple(ix)]) for ix in idx]
+        raise AssertionError(f"{what}: {low.sum()} below, {high.sum()} above tolerance, {nan.sum()} NaN: {detail}")
+
+
+def gate_tie_zone(risk_row, repaired, tau, rel=METER_REL):
+    """True when the oracle's decision for one cell could change under a relative change of
+    `rel` in its risks: its total, or the remaining risk just before or after its cut, within
+    rel of D*, or the last taken and first untaken blocks within rel of each other."""
+    import math
+    from oracle.gate import canonical_risk, d_star, select_cell
+    r = [canonical_risk(x) for x in np.asarray(risk_row, np.float32)]
+    cand = [b for b in range(len(r)) if not repaired[b]]
+    order = sorted(cand, key=lambda b: (-r[b], b))
+    ds = d_star(tau)
+    near = lambda x: abs(x - ds) <= rel * max(ds, x)
+    if near(math.fsum(r[b] for b in cand)):
+        return True
+    k = len(select_cell(risk_row, repaired, tau))
+    if k == 0:
+        return False
+    rem = math.fsum(r[b] for b in order[k:])
+    if near(rem) or near(rem + r[order[k - 1]]):
+        return True
+    return k < len(order) and abs(r[order[k - 1]] - r[order[k]]) <= rel * r[order[k - 1]]
+
+
+def check_gate_end_to_end(oracle_risk, repaired_before, tau, gpu_repaired_after, g):
+    """The oracle gate fed the oracle's OWN risks [B, Hq, nblk] must pick exactly the blocks
+    the GPU repaired, outside the tie zone; returns the number of tie-zone cells (expected 0)."""
+    from oracle.gate import select_cell
+    B, Hq, nblk = oracle_risk.shape
+    ties = 0
+    for i in range(B):
+        for h in range(Hq // g):
+            want = np.asarray(repaired_before[i, h, :nblk], bool).copy()
+            tie = False
+            for j in range(h * g, (h + 1) * g):
+                if gate_tie_zone(oracle_risk[i, j], repaired_before[i, h, :nblk], tau):
+                    tie = True
+                for b in select_cell(oracle_risk[i, j], repaired_before[i, h, :nblk], tau):
+                    want[b] = True
+            if tie:
+                ties += 1
+                continue
+            np.testing.assert_array_equal(np.asarray(gpu_repaired_after[i, h, :nblk], bool), want,
+                                          err_msg=f"end-to-end gate, sequence {i} KV head {h}")
+    return ties

@@ -92,3 +92,23 @@ def test_new_entry_points_reject_bad_arguments_without_the_gpu(lib_path):
     assert lib.witcert_merge_partials(None, 1, 1, 1, 0, None, None, None, None, None, None, None) == _lib.EINVAL
     fake = ctypes.c_void_p(1)
     assert lib.witcert_merge_partials(fake, 1, 1, 1, 7, fake, None, None, None, None, None, None) == _lib.EINVAL
+
+
+def test_gate_shapes_and_fault_injection_are_checked_without_the_gpu(lib_path):
+    """A gated cache whose sequences would hold more blocks than the gate ranks is refused at
+    create; the selection call and the fault injection check their arguments first."""
+    import ctypes
+
+    import kv_cache_quantization_witcert_gb300 as w
+    from kv_cache_quantization_witcert_gb300 import _lib
+    lib = w.load()
+    h = ctypes.c_void_p()
+    too_long = _lib.witcert_config(1, 4, 2, 128, 1, 262144 + 16, 1, _lib.BF16, 0, 1, 0, 64, 0, 0, 0)
+    assert lib.witcert_create(ctypes.byref(too_long), ctypes.byref(h)) == _lib.EINVAL
+    assert b"gate" in lib.witcert_last_error()
+    fake = ctypes.c_void_p(16)
+    assert lib.witcert_gate_select(fake, None, 1, 4, 2, 16385, 1.0, fake, None) == _lib.EINVAL
+    assert lib.witcert_gate_select(fake, None, 1, 3, 2, 16, 1.0, fake, None) == _lib.EINVAL
+    assert lib.witcert_gate_select(fake, None, 1, 4, 2, 16, -1.0, fake, None) == _lib.EINVAL
+    assert lib.witcert_gate_select(None, None, 1, 4, 2, 16, 1.0, fake, None) == _lib.EINVAL
+    assert lib.witcert_inject_fault(None, _lib.FAULT_BACKING_LOST, 0) == _lib.EINVAL

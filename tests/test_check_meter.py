@@ -3,21 +3,27 @@ from above within the relative tolerance (CPU only)."""
 import numpy as np
 import pytest
 
-from gpu_helpers import FP32_ULP, METER_REL, check_meter
+from gpu_helpers import METER_REL, check_meter
 
 
 def test_accepts_equal_and_slightly_above():
     r = np.array([0.0, 1e-6, 0.25, np.inf])
     check_meter(r, r)
     check_meter(r * (1 + METER_REL / 2), r)
-    check_meter(r * (1 - FP32_ULP / 2), r)
 
 
 @pytest.mark.parametrize("bad", [
     np.array([0.25 * (1 - 1e-5)]),        # below the oracle: not a bound
+    np.array([np.nextafter(0.25, 0.0)]),  # one unit below is below too: no relative slack
     np.array([0.25 * (1 + 1e-3)]),        # looser than the tolerance
     np.array([np.nan]),                   # a NaN fails both comparisons and bounds nothing
 ])
 def test_rejects_below_above_and_nan(bad):
     with pytest.raises(AssertionError):
         check_meter(bad, np.array([0.25]))
+
+
+def test_absolute_allowance_is_for_values_below_fp32_range_only():
+    check_meter(np.array([0.0]), np.array([3.5e-90]))            # a value no fp32 meter can carry
+    with pytest.raises(AssertionError):
+        check_meter(np.array([0.0]), np.array([1e-20]))

@@ -64,3 +64,33 @@ def test_gate_with_exhausted_pool_drops_and_stays_sound():
         assert np.all(wit[i, 16 * b:16 * b + 16, h] == 0)
     ref.repaired[0][:] = slots >= 0                  # the oracle on what was really repaired
     check_decode(gpu, ref, 0, gen_q(w, 0, 1), w, w.delta_req)
+
+
+def test_lost_backing_store_fails_the_gate_and_changes_nothing():
+    """A page-in that cannot complete (the layer's backing store lost its exact keys, injected on
+    the host as a failed copy would leave it): the gate returns EPAGEIN, selects, pages in and
+    zeroes nothing, and the next decode's meters still bound the oracle's on the unrepaired
+    cache; another layer's gate still works."""
+    w = WORKLOADS["qwen_1l"].with_(n_layers=2, batch=2, context=400, steps=3, scheme="fp8_e4m3")
+    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32)
+    for layer in (0, 1):
+        K, V = gen_kv(w, layer)
+        gpu.witcert_write(layer, to_dev(K, w), to_dev(V, w))
+        ref.write(layer, K, V)
+        check_decode(gpu, ref, layer, gen_q(w, layer, 0), w, w.delta_req)
+    wit0 = gpu.export(0, _lib.X_WITNESS).cpu().numpy()
+    gpu.witcert_inject_fault(_lib.FAULT_BACKING_LOST, 0)
+    with pytest.raises(wc.WitcertError) as e:
+        gpu.witcert_gate(0, 0.05)
+    assert e.value.status == _lib.EPAGEIN
+    assert np.all(gpu.export(0, _lib.X_SLOTS).cpu().numpy() < 0)
+    np.testing.assert_array_equal(gpu.export(0, _lib.X_WITNESS).cpu().numpy().view(np.uint16), wit0.view(np.uint16))
+    st = gpu.witcert_gate_stats()
+    assert st["blocks_paged_in"] == 0 and st["cells_triggered"] == 0
+    check_decode(gpu, ref, 0, gen_q(w, 0, 1), w, w.delta_req)      # unrepaired oracle: nothing moved
+    gpu.witcert_gate(1, 0.05)                                        # layer 1 keeps its backing store
+    assert gpu.witcert_gate_stats()["blocks_paged_in"] > 0
+    with pytest.raises(wc.WitcertError) as e:                        # the fault persists
+        gpu.witcert_gate(0, 0.05)
+    assert e.value.status == _lib.EPAGEIN
+    assert gpu.witcert_stats()["device_errors"] == 0

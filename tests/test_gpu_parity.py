@@ -9,7 +9,8 @@ from oracle import meter
 from oracle.philox import dither
 from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q
 
-from gpu_helpers import check_decode, check_meter, check_write, make_pair, oracle_group, to_dev, write_both
+from gpu_helpers import (check_decode, check_gate_end_to_end, check_meter, check_risk, check_write, make_pair,
+                         oracle_group, to_dev, write_both)
 
 pytestmark = pytest.mark.gpu
 
@@ -193,24 +194,31 @@ def test_empty_layer_decodes_to_zero():
     assert torch.count_nonzero(m["meter_a"]) == 0 and torch.count_nonzero(m["meter_b"]) == 0
 
 
-@pytest.mark.parametrize("scheme,v_witness", [("fp8_e4m3", False), ("blackbox", True)])
+@pytest.mark.parametrize("scheme,v_witness", [("fp8_e4m3", False), ("blackbox", True), ("int8_dither", False),
+                                              ("int8_dither", True)])
 def test_gate_decisions_bit_exact_and_repaired_decode(scheme, v_witness):
-    """Raw-cast FP8 and the black-box store: the oracle's gate, fed the GPU's block risks, picks
-    exactly the blocks the GPU pages in; the next decode matches the oracle on the repaired cache
+    """Raw-cast FP8, the black-box store and dithered INT8 (ranked by its Tier B risks): the GPU's
+    block risks match the oracle's (never below, within 1e-4); the oracle's gate, fed the GPU's
+    block risks, picks exactly the blocks the GPU pages in, and fed its own risks picks them too
+    outside the tie zone (empty here); the next decode matches the oracle on the repaired cache
     (value witnesses stay: the gate pages in keys only)."""
     w = WORKLOADS["qwen_1l"].with_(batch=2, context=400, steps=3, scheme=scheme)
     gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32, v_witness=v_witness)
     K, V = gen_kv(w, 0)
     write_both(gpu, ref, 0, K, V, w)
-    for step, tau in enumerate((0.5, 0.2, 0.05)):
+    taus = (0.5, 0.2, 0.05) if scheme != "int8_dither" else (4.0, 2.0, 1.0)
+    for step, tau in enumerate(taus):
         q = gen_q(w, 0, step)
-        check_decode(gpu, ref, 0, q, w, w.delta_req)
+        _, _, r = check_decode(gpu, ref, 0, q, w, w.delta_req)
         risk = gpu.export(0, _lib.X_BLOCK_RISK).cpu().numpy()
+        check_risk(risk, r["risk"], what=f"block risk step {step}")
+        before = ref.repaired[0].copy()
         gpu.witcert_gate(0, tau)
         picked = ref.gate(0, tau, risk)
         slots = gpu.export(0, _lib.X_SLOTS).cpu().numpy()
         np.testing.assert_array_equal(slots >= 0, ref.repaired[0])
         assert len(picked) == len(set(picked))
+        assert check_gate_end_to_end(r["risk"], before, tau, slots >= 0, w.group) == 0
     check_decode(gpu, ref, 0, gen_q(w, 0, 9), w, w.delta_req)
     st = gpu.witcert_gate_stats()
     assert st["blocks_paged_in"] == int(ref.repaired[0].sum()) > 0

@@ -18,7 +18,7 @@ from kv_cache_quantization_witcert_gb300 import _lib
 from oracle import OracleCache
 from workload import WORKLOADS, gen_kv, gen_q
 
-from gpu_helpers import METER_REL, check_meter, tensor_function, torch_dtype
+from gpu_helpers import METER_REL, check_gate_end_to_end, check_meter, check_risk, tensor_function, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
@@ -183,26 +183,33 @@ def test_ragged_kivi_appends_close_blocks_per_sequence():
 
 
 @pytest.mark.parametrize("pages", [0, 60])
-def test_ragged_gate_decisions_match_each_sequence(pages):
-    """FP8 with the gate on ragged lengths: each sequence's block risks (its own blocks; the
-    GPU's rows past its length are zero) drive that sequence's oracle gate, and the GPU pages in
-    exactly those blocks (witnesses zeroed in the page that holds each block when paged)."""
-    w = WORKLOADS["qwen_1l"].with_(batch=3, context=500, steps=3, scheme="fp8_e4m3")
-    rg = Ragged(w, "fp8_e4m3", cap=520, v_witness=False, gate_blocks=3 * 4 * 40, max_pages=pages)
+@pytest.mark.parametrize("scheme", ["fp8_e4m3", "int8_dither"])
+def test_ragged_gate_decisions_match_each_sequence(scheme, pages):
+    """FP8 (Tier A risks) and dithered INT8 (Tier B risks) with the gate on ragged lengths: each
+    sequence's block risks (its own blocks; the GPU's rows past its length are zero) match its
+    oracle's, drive that sequence's oracle gate, and the GPU pages in exactly those blocks
+    (witnesses zeroed in the page that holds each block when paged); the oracle's own risks give
+    the same blocks outside the tie zone (empty here)."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=500, steps=3, scheme=scheme)
+    rg = Ragged(w, scheme, cap=520, v_witness=False, gate_blocks=3 * 4 * 40, max_pages=pages)
     K, V = gen_kv(w, 0)
     lens = [500, 130, 257]
     rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
-    for step, tau in enumerate((0.5, 0.1)):
-        rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
+    for step, tau in enumerate((0.5, 0.1) if scheme == "fp8_e4m3" else (4.0, 2.0)):
+        _, _, oracle_risk = rg.check_decode(0, gen_q(w, 0, step), w.delta_req)
         risk = rg.gpu.export(0, _lib.X_BLOCK_RISK).cpu().numpy()
+        before = [ref.repaired[0][0].copy() for ref in rg.refs]
         rg.gpu.witcert_gate(0, tau)
         slots = rg.gpu.export(0, _lib.X_SLOTS).cpu().numpy()
         for i, ref in enumerate(rg.refs):
             nblk = (lens[i] + 15) // 16
             assert not np.any(risk[i, :, nblk:])
+            check_risk(risk[i, :, :nblk], oracle_risk[i], what=f"block risk seq {i}")
             ref.gate(0, tau, risk[i:i + 1, :, :nblk])
             np.testing.assert_array_equal(slots[i, :, :nblk] >= 0, ref.repaired[0][0])
             assert not np.any(slots[i, :, nblk:] >= 0)
+            assert check_gate_end_to_end(oracle_risk[i][None], before[i][None], tau, slots[i:i + 1, :, :nblk] >= 0,
+                                         w.group) == 0
     rg.check_decode(0, gen_q(w, 0, 7), w.delta_req)
     assert rg.gpu.witcert_gate_stats()["blocks_paged_in"] > 0
 

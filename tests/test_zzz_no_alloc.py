@@ -5,8 +5,10 @@ allocator at start-up, and hosts that forbid device allocation after start-up,
 cannot let a library call cudaMalloc on their decode path.  This entry point
 keeps its split scratch in a static device array instead.  These tests call it
 through the C ABI and compare it with witcert_decode on the same cache, on two
-calls in a row (the second reuses the array the first call left behind).
-The file is named to run last, so a failure here never hides another test.
+calls in a row (the second reuses the array the first call left behind).  Both
+run the same kernels with the same split count, so every output, meter and
+block risk must be bit-identical.  The file is named to run last, so a failure
+here never hides another test.
 """
 import numpy as np
 import pytest
@@ -16,9 +18,11 @@ import kv_cache_quantization_witcert_gb300 as wc
 from kv_cache_quantization_witcert_gb300 import _lib
 from workload import WORKLOADS, gen_kv, gen_q
 
-from gpu_helpers import METER_REL, to_dev
+from gpu_helpers import to_dev
 
 pytestmark = pytest.mark.gpu
+
+NAMES = ("meter_a", "meter_b", "raw_a", "raw_b", "meter_v")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,28 +33,70 @@ def _cuda():
     wc.load()
 
 
+def both_decodes(cache, q, delta_req, v_witness):
+    """(out, meters) of witcert_decode, then of witcert_decode_noalloc into NaN-filled buffers."""
+    res = []
+    for call in (cache.witcert_decode, cache.witcert_decode_noalloc):
+        B, Hq = q.shape[0], q.shape[1]
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        m = torch.full((5, B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+        call(0, q, delta_req, out, m[0], m[1], m[2], m[3], m[4] if v_witness else None)
+        torch.cuda.synchronize()
+        res.append((out, m))
+    return res
+
+
 @pytest.mark.parametrize("scheme", ["int8_dither", "fp8_e4m3"])
-def test_noalloc_decode_matches_decode_on_two_calls(scheme):
+def test_noalloc_decode_is_bit_identical_on_two_calls(scheme):
     w = WORKLOADS["qwen_1l"].with_(batch=5, context=1500, scheme=scheme)
     cache = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, w.context, scheme,
                      dtype=torch.bfloat16, seed=w.seed, total_steps=w.steps)
     K, V = gen_kv(w, 0)
     cache.witcert_write(0, to_dev(K, w), to_dev(V, w))
-    vmax = float(np.abs(V).max())
-    for call, step in enumerate((0, 1)):
-        q = to_dev(gen_q(w, 0, step), w)
-        ref_out, ref_m = cache.decode(0, q, w.delta_req)
-        out = torch.full_like(ref_out, float("nan"))
-        m = torch.full((4, w.batch, w.n_q_heads), float("nan"), dtype=torch.float32, device="cuda")
-        cache.witcert_decode_noalloc(0, q, w.delta_req, out, m[0], m[1], m[2], m[3])
-        torch.cuda.synchronize()
-        assert torch.isfinite(out).all()
-        assert (out - ref_out).abs().max().item() <= 2e-3 * vmax, f"call {call}"
-        for k, idx in (("meter_a", 0), ("raw_a", 2)) + ((("meter_b", 1), ("raw_b", 3)) if scheme == "int8_dither" else ()):
-            g = m[idx].cpu().numpy().astype(np.float64)
-            r = ref_m[k].cpu().numpy().astype(np.float64)
-            np.testing.assert_allclose(g, r, rtol=METER_REL, atol=0, err_msg=f"{k} call {call}")
+    calls0 = cache.witcert_stats()["decode_calls"]
+    for step in (0, 1):
+        (o1, m1), (o2, m2) = both_decodes(cache, to_dev(gen_q(w, 0, step), w), w.delta_req, False)
+        assert torch.isfinite(o2).all()
+        assert torch.equal(o1, o2), f"out, call {step}"
+        assert torch.equal(m1[:4], m2[:4]) or (scheme != "int8_dither" and torch.equal(m1[[0, 2]], m2[[0, 2]])), step
+    st = cache.witcert_stats()
+    assert st["decode_calls"] == calls0 + 4 and st["last_n_splits"] > 0
     cache.close()
+
+
+def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter():
+    """A gated, ragged cache with value witnesses: the block risks the gate reads and the value
+    meter are the same bits through either entry point, and the gate after a no-allocation
+    decode pages in the same blocks."""
+    w = WORKLOADS["qwen_1l"].with_(batch=3, context=600, scheme="int8_dither")
+    lens = [600, 75, 333]
+    runs = []
+    for noalloc in (False, True):
+        cache = wc.Cache(1, w.n_q_heads, w.n_kv_heads, w.batch, 640, "int8_dither", dtype=torch.bfloat16,
+                         seed=w.seed, total_steps=w.steps, max_repair_blocks=3 * 4 * 40, v_witness=True)
+        K, V = gen_kv(w, 0)
+        Kp = np.concatenate([K[i, :n] for i, n in enumerate(lens)])
+        Vp = np.concatenate([V[i, :n] for i, n in enumerate(lens)])
+        cache.witcert_write_ragged(0, to_dev(Kp, w), to_dev(Vp, w), lens)
+        for step in (0, 1):
+            q = to_dev(gen_q(w, 0, step), w)
+            out = torch.empty((w.batch, w.n_q_heads, 128), dtype=torch.float32, device="cuda")
+            m = torch.empty((5, w.batch, w.n_q_heads), dtype=torch.float32, device="cuda")
+            call = cache.witcert_decode_noalloc if noalloc else cache.witcert_decode
+            call(0, q, w.delta_req, out, m[0], m[1], m[2], m[3], m[4])
+            risk = cache.export(0, _lib.X_BLOCK_RISK)
+            cache.witcert_gate(0, 4.0)
+            slots = cache.export(0, _lib.X_SLOTS)
+            torch.cuda.synchronize()
+            runs.append((out.clone(), m.clone(), risk.clone(), slots.clone()))
+        cache.close()
+    n = len(runs) // 2
+    for k in range(n):
+        (o1, m1, r1, s1), (o2, m2, r2, s2) = runs[k], runs[n + k]
+        assert torch.equal(o1, o2) and torch.equal(m1, m2), f"step {k}"
+        assert torch.equal(r1, r2), f"block risks, step {k}"
+        assert torch.equal(s1 >= 0, s2 >= 0), f"repaired blocks, step {k}"
+    assert (runs[-1][3] >= 0).any()
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_array():
