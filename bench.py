@@ -1,14 +1,16 @@
 """Benchmark of the metered KV-cache decode step on GB300.
 
-Default workload: the full 28-layer Qwen2.5-7B-shaped decode (28 query / 4 KV
-heads, d = 128, batch 16 x 4096 context, bf16 synthetic K/V/q, dithered INT8
-with the Tier B certificate at delta_req = 1e-2).  One step = for every layer:
-append the step's token (write path: quantize + witness) and run the fused
-metered split-KV decode + merge.  Metric: attended-KV-tokens/s, one attended
-token being one (sequence, layer, position) read across all KV heads.
+Default workload: the long-context point of the bandwidth sweep, Mistral-7B
+shaped (32 query / 8 KV heads, d = 128, RoPE base 1e4), batch 16 x 32768
+context, 32 layers, bf16 synthetic K/V/q, dithered INT8 with the Tier B
+certificate at delta_req = 1e-2.  One step = for every layer: append the step's
+token (write path: quantize + witness) and run the fused metered split-KV
+decode + merge.  Metric: attended-KV-tokens/s, one attended token being one
+(sequence, layer, position) read across all KV heads.  The 28-layer Qwen-shaped
+decode at 4096 tokens is --workload qwen_28l.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload qwen_28l|qwen_1l|gated|sweep:<mistral|yi>:<B>:<S>] [--scheme ...]
+                  [--workload sweep:<mistral|yi>:<B>:<S>|qwen_28l|qwen_1l|gated] [--scheme ...]
 
 --impl reference times the CPU oracle (the slow float64 statement of the same
 computation) on this host's cores, on a bounded sample of the same workload.
@@ -36,7 +38,9 @@ from workload import WORKLOADS, gen_append_kv, gen_kv, gen_q, sweep_workload  # 
 BYTES_PER_TOK_HEAD = {"int8_dither": 304, "fp8_e4m3": 288, "kivi2": 144, "int8_rtn": 304, "blackbox": 544}
 V_WITNESS_BYTES = 2        # per token and KV head, with --v-witness
 CODE_KIND = {"int8_dither": "int8", "fp8_e4m3": "e4m3", "kivi2": "2-bit", "int8_rtn": "int8", "blackbox": "bf16"}
+DEFAULT_WORKLOAD = "sweep:mistral:16:32768"
 DISTINCT_LAYERS = 4        # prefill K/V sets generated on the host; layer l uses set l % 4
+BIG_SET_ELEMENTS = 1 << 28  # above this many K elements per layer one set serves every layer
 METRIC = "metered decode attended-KV-tokens/s"
 UNIT = "tokens/s"
 
@@ -47,7 +51,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen_28l")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--scheme", default=None)
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -70,6 +74,13 @@ def workload_of(name, scheme):
     if scheme:
         w = w.with_(scheme=scheme)
     return w
+
+
+def distinct_sets(w):
+    """Prefill K/V sets drawn on the host: four, or one for long contexts (drawing several
+    sets of batch x 32768 tokens would take minutes)."""
+    big = w.batch * w.context * w.n_kv_heads * 128 > BIG_SET_ELEMENTS
+    return min(1 if big else DISTINCT_LAYERS, w.n_layers)
 
 
 def tok_head_bytes(scheme, v_witness):
@@ -126,7 +137,8 @@ def config_of(w, args, n_splits, world):
             "v_witness": bool(vw),
             "l2": "inputs larger than L2: every step reads the whole cache "
                   f"({w.n_layers * w.batch * w.n_kv_heads * w.context * tok_head_bytes(w.scheme, vw) / 1e9:.2f} GB)",
-            "prefill_data": f"{DISTINCT_LAYERS} generated K/V sets reused across layers"}
+            "prefill_data": f"{distinct_sets(w)} generated K/V set(s) reused across layers (the dither and so the "
+                            "codes still differ per layer)"}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -309,7 +321,8 @@ def run_ours(args, w):
 
     # prefill every layer (outside the step timing; its write throughput is reported on its own)
     sets = {}
-    for sid in range(min(DISTINCT_LAYERS, wl.n_layers)):
+    nsets = distinct_sets(wl)
+    for sid in range(nsets):
         K, V = gen_kv(wl, sid)
         if args.ragged:      # sequence i keeps its first lens[i] tokens, packed sequence by sequence
             K = np.concatenate([K[i, :n] for i, n in enumerate(lens)])
@@ -321,7 +334,7 @@ def run_ours(args, w):
     pf0, pf1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pf0.record(stream)
     for layer in range(wl.n_layers):
-        kv = sets[layer % DISTINCT_LAYERS]
+        kv = sets[layer % nsets]
         if args.ragged:
             cache.witcert_write_ragged(layer, kv[0], kv[1], lens, *(kv[2:] if bb else ()))
         elif bb:
@@ -342,10 +355,10 @@ def run_ours(args, w):
     def step_inputs(step, device=True):
         ks, vs, qs = [], [], []
         for layer in range(wl.n_layers):
-            k, v = gen_append_kv(wl, layer % DISTINCT_LAYERS, step % 8)
+            k, v = gen_append_kv(wl, layer % nsets, step % 8)
             ks.append(k)
             vs.append(v)
-            qs.append(gen_q(wl, layer % DISTINCT_LAYERS, step % 8))
+            qs.append(gen_q(wl, layer % nsets, step % 8))
         arr = [np.stack(ks), np.stack(vs), np.stack(qs)]
         t = [torch.from_numpy(a).to(dt) for a in arr]
         if bb:     # f(K), f(V) of the appended tokens come with the step's inputs
