@@ -129,15 +129,14 @@ constexpr float kMeterMargin = 1.0f + 3.0517578125e-5f;   // 1 + 2^-15
 constexpr float kMeterFloor = 0x1p-100f;
 
 // 2^k for an integer-valued k <= 0, or k = -inf: the largest float <= 2^k (pow2_dn) and the
-// smallest float >= 2^k (pow2_up); both are 2^k itself down to 2^-149.
+// smallest float >= 2^k (pow2_up, never below 2^-149 for a finite k); both are 2^k itself down
+// to 2^-149.
 __device__ __forceinline__ float pow2_dn(float k) {
-  if (k >= -126.0f) return __int_as_float((int)(k + 127.0f) << 23);
-  if (k >= -149.0f) return __int_as_float(1 << (int)(k + 149.0f));
-  return 0.0f;
+  const int e = (int)fmaxf(k, -160.0f) + 127;              // biased exponent of 2^k
+  return e > 0 ? __int_as_float(e << 23) : (e > -23 ? __int_as_float(1 << (e + 22)) : 0.0f);
 }
 __device__ __forceinline__ float pow2_up(float k) {
-  if (k >= -149.0f) return pow2_dn(k);
-  return k == -INFINITY ? 0.0f : 0x1p-149f;
+  return k == -INFINITY ? 0.0f : fmaxf(pow2_dn(k), 0x1p-149f);
 }
 
 // Kahan's compensated summation in (hi, lo) form: hi + lo carries the running sum and lo the
@@ -705,31 +704,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         dA = f2sub(lgA, mn);
         dB = f2sub(lgB, mn);
         m2 = mn;
-        float2 sc;
-        if (kx >= -100.f && ky >= -100.f) {
-          // the usual move: exact powers of two on packed pairs.  Z holds the old maximum's
-          // weight (>= 1/2), so it stays in fp32's normal range; an S or a low part that
-          // leaves it loses less than 2^-150, inside the meters' absolute allowance.
-          sc = make_float2(__int_as_float(((int)kx + 127) << 23), __int_as_float(((int)ky + 127) << 23));
-          Zp = __fmul2_rn(Zp, sc); Zl = __fmul2_rn(Zl, sc);
-          SAp = __fmul2_rn(SAp, sc); SAl = __fmul2_rn(SAl, sc);
-          SBp = __fmul2_rn(SBp, sc); SBl = __fmul2_rn(SBl, sc);
-          if (VW) { SVp = __fmul2_rn(SVp, sc); SVl = __fmul2_rn(SVl, sc); }
-        } else {
-          // a jump of more than 100 (log2 units): factors rounded down for Z and up for the S
-          sc = make_float2(pow2_dn(kx), pow2_dn(ky));
-          const float2 su = make_float2(pow2_up(kx), pow2_up(ky));
-          Zp = make_float2(__fmul_rd(Zp.x, sc.x), __fmul_rd(Zp.y, sc.y));
-          Zl = make_float2(__fmul_rd(Zl.x, sc.x), __fmul_rd(Zl.y, sc.y));
-          SAp = make_float2(__fmul_ru(SAp.x, su.x), __fmul_ru(SAp.y, su.y));
-          SAl = make_float2(__fmul_ru(SAl.x, su.x), __fmul_ru(SAl.y, su.y));
-          SBp = make_float2(__fmul_ru(SBp.x, su.x), __fmul_ru(SBp.y, su.y));
-          SBl = make_float2(__fmul_ru(SBl.x, su.x), __fmul_ru(SBl.y, su.y));
-          if (VW) {
-            SVp = make_float2(__fmul_ru(SVp.x, su.x), __fmul_ru(SVp.y, su.y));
-            SVl = make_float2(__fmul_ru(SVl.x, su.x), __fmul_ru(SVl.y, su.y));
-          }
-        }
+        // Z and the output take 2^k or, below fp32's range, the next float under it; the S sums
+        // the next float above it (never below 2^-149).  The products round to nearest: exact
+        // while they stay in fp32's normal range, and off by less than 2^-150 below it, inside
+        // the meters' absolute allowance (Z itself, which holds the old maximum's weight, is
+        // then at most 2^-83 against the new block's weight of at least 1/2).
+        const float2 sc = make_float2(pow2_dn(kx), pow2_dn(ky)), su = make_float2(pow2_up(kx), pow2_up(ky));
+        Zp = __fmul2_rn(Zp, sc); Zl = __fmul2_rn(Zl, sc);
+        SAp = __fmul2_rn(SAp, su); SAl = __fmul2_rn(SAl, su);
+        SBp = __fmul2_rn(SBp, su); SBl = __fmul2_rn(SBl, su);
+        if (VW) { SVp = __fmul2_rn(SVp, su); SVl = __fmul2_rn(SVl, su); }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const float2 lo = __fmul2_rn(make_float2(acco[mt][0], acco[mt][1]), sc);

@@ -40,6 +40,35 @@ template <typename T> __device__ __forceinline__ void store4(T* p, const T* src)
   else *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(src);
 }
 
+// Four consecutive elements of an input row as loaded (bf16: two registers), converted when used.
+template <typename T> struct Row4;
+template <> struct Row4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ void get(float (&x)[4]) const { x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w; }
+};
+template <> struct Row4<__nv_bfloat16> {
+  uint2 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ void get(float (&x)[4]) const {
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+};
+// A lane's share of one token's inputs: K, V and, for the black-box scheme, K_hat, V_hat.
+template <typename T> struct TokIn {
+  Row4<T> k, v, kh, vh;
+  __device__ __forceinline__ void load(const WriteArgs& a, size_t row, int lane, bool hat) {
+    const size_t o = row + 4 * lane;
+    k.load(reinterpret_cast<const T*>(a.K) + o);
+    v.load(reinterpret_cast<const T*>(a.V) + o);
+    if (hat) {
+      kh.load(reinterpret_cast<const T*>(a.Kh) + o);
+      vh.load(reinterpret_cast<const T*>(a.Vh) + o);
+    }
+  }
+};
+
 __device__ __forceinline__ float grp_max8(float v) {
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
@@ -226,6 +255,12 @@ __device__ __forceinline__ float div_rn_by(float x, float s, float y) {
   const float r = __fmaf_rn(-q0, s, x);
   return __fmaf_rn(r, y, q0);
 }
+// Nearest integer (ties to even) of z, saturated to [-128, 127]: one conversion.
+__device__ __forceinline__ int rint_sat_s8(float z) {
+  int c;
+  asm("cvt.rni.s8.f32 %0, %1;" : "=r"(c) : "f"(z));
+  return (int)(signed char)(c & 0xFF);
+}
 constexpr float kInv127 = 0x1.020408p-7f;          // RN(1/127)
 constexpr float kInv3 = 0x1.555556p-2f;            // RN(1/3)
 
@@ -289,17 +324,20 @@ __device__ __forceinline__ bool exact_side(const WriteArgs& a, int i, int h, int
 }
 
 // The token at position t (row r = t mod 16 of its block) of sequence i, KV head h, whose
-// input row starts at element `row` of K and V, quantized into the block image at bp (device
-// memory or shared memory).
-template <typename T, bool DITHER, bool VW>
-__device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+// input row starts at element `row` of K and V (this lane's part already loaded in `in`),
+// quantized into the block image at bp (device memory or shared memory).  STAGED: the value
+// codes go, as one word of four channels per lane, to row r of the warp's staging area vst
+// (natural order) instead of their places in the block.
+template <typename T, bool DITHER, bool VW, bool STAGED>
+__device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, uint32_t* vst, int i, int h, int t,
+                                           size_t row, int lane, const TokIn<T>& in) {
   const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
   const int G = lane >> 3;
 #pragma unroll
   for (int tensor = 0; tensor < 2; ++tensor) {
     float x[4];
-    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
+    (tensor ? in.v : in.k).get(x);
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
     amax = grp_max8(amax);
     // s = fp16 round-up of fp32(amax / 127), at most 65504
@@ -313,33 +351,39 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
     const float xs[4] = {xi.x, xi.y, xi.z, xi.w};
     uint32_t packed = 0;
     int codes[4];
-    float rr[4];
-    float ferr = 0.f;
-    int clamps = 0;
+    float rr[4], zs[4];
+    float eacc = 0.f;
     const bool resid = tensor == 0 || VW;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      int code = 0;
-      if (s > 0.0f) {
-        const float z = __fadd_rn(div_rn_by(x[e], s, ys), xs[e]);
-        float rz = rintf(z);
-        if (rz < -128.f) { rz = -128.f; ++clamps; }
-        if (rz > 127.f) { rz = 127.f; ++clamps; }
-        code = (int)rz;
-      }
+      // an all-zero group has s = 0 and ys = 0: z = xi, whose nearest integer is 0
+      const float z = __fadd_rn(div_rn_by(x[e], s, ys), xs[e]);
+      zs[e] = z;
+      const int code = rint_sat_s8(z);
       codes[e] = code;
       if (resid) {
         // residual x - s (code - xi) = (x - s code) + s xi: s code is exact (at most 19
-        // significant bits), the difference and the FMA round once each
+        // significant bits), the difference and the FMA round once each, so the estimate is
+        // within one unit of |d| and of |rr|
         const float d = __fsub_rn(x[e], __fmul_rn(s, (float)code));
         rr[e] = __fmaf_rn(s, xs[e], d);
-        ferr = __fadd_ru(ferr, resid_err(d, rr[e]));
+        eacc = __fadd_rn(eacc, __fadd_rn(fabsf(d), fabsf(rr[e])));
       }
-      const uint32_t biased = (uint32_t)(code + 128) & 0xFFu;
-      if (tensor == 0) packed |= biased << (8 * e);
+      const uint32_t biased = (uint32_t)(code ^ 0x80) & 0xFFu;       // code + 128
+      if (tensor == 0 || STAGED) packed |= biased << (8 * e);
       else bp[Int8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)biased;
     }
-    if (clamps) atomicAdd(a.clamps, (unsigned long long)clamps);
+    // sum of the four one-unit bounds, 2^-24 (|d| + |rr|) each plus 2^-150 below fp32's normal
+    // range: the rounded sum eacc is within 2^-21 of exact, so 2^-22 eacc + 2^-146 covers them
+    const float ferr = resid ? __fmaf_ru(eacc, 0x1p-22f, 0x1p-146f) : 0.f;
+    if (STAGED && tensor == 1) vst[r * 32 + lane] = packed;
+    // clamped codes (expected none: s >= amax / 127 keeps |x / s| <= 127 unless s saturated)
+    if (fminf(fminf(zs[0], zs[1]), fminf(zs[2], zs[3])) < -128.5f || fmaxf(fmaxf(zs[0], zs[1]), fmaxf(zs[2], zs[3])) >= 127.5f) {
+      int clamps = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) clamps += (zs[e] < -128.5f) + (zs[e] >= 127.5f);
+      atomicAdd(a.clamps, (unsigned long long)clamps);
+    }
     if ((lane & 7) == 0)
       *reinterpret_cast<__half*>(bp + (tensor ? Int8Layout::VS + vscale_off(r, G) : Int8Layout::KS + (r * 4 + G) * 2)) = s16;
     // exact residual terms for the double-float path (x, -s code, and s xi as an exact product pair)
@@ -379,14 +423,15 @@ __device__ __forceinline__ void int8_token(const WriteArgs& a, uint8_t* bp, int 
 }
 
 // As int8_token, for the raw FP8 cast.
-template <typename T>
-__device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+template <typename T, bool STAGED>
+__device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, uint32_t* vst, int i, int h, int t,
+                                          size_t row, int lane, const TokIn<T>& in) {
   const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
 #pragma unroll
   for (int tensor = 0; tensor < 2; ++tensor) {
     float x[4];
-    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
+    (tensor ? in.v : in.k).get(x);
     uint32_t packed = 0;
     float xhs[4], rr[4];
     Df rdf[4];
@@ -398,9 +443,10 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
       xhs[e] = xh;
       rr[e] = __fsub_rn(x[e], xh);
       ferr = __fadd_ru(ferr, resid_err(rr[e], rr[e]));
-      if (tensor == 0) packed |= (uint32_t)c << (8 * e);
+      if (tensor == 0 || STAGED) packed |= (uint32_t)c << (8 * e);
       else bp[Fp8Layout::VC + vcode_off(r, 4 * lane + e)] = (uint8_t)c;
     }
+    if (STAGED && tensor == 1) vst[r * 32 + lane] = packed;
     auto resid_df = [&]() {
 #pragma unroll
       for (int e = 0; e < 4; ++e) rdf[e] = residual_df(x[e], -xhs[e], 0.f, 0.f);   // exact: one error-free sum
@@ -429,14 +475,15 @@ __device__ __forceinline__ void fp8_token(const WriteArgs& a, uint8_t* bp, int i
 // Black-box scheme: the caller's K_hat, V_hat rows rounded to bfloat16 (nearest even) are the
 // store; the key witness (and the value witness) are taken against those stored values.
 template <typename T>
-__device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
+__device__ __forceinline__ void bbox_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane,
+                                           const TokIn<T>& in) {
   const int r = t & 15;
   const bool repaired = exact_side<T>(a, i, h, t, lane, reinterpret_cast<const T*>(a.K) + row);
 #pragma unroll
   for (int tensor = 0; tensor < 2; ++tensor) {
     float x[4], y[4];
-    load4f<T>(reinterpret_cast<const T*>(tensor ? a.V : a.K) + row + 4 * lane, x);
-    load4f<T>(reinterpret_cast<const T*>(tensor ? a.Vh : a.Kh) + row + 4 * lane, y);
+    (tensor ? in.v : in.k).get(x);
+    (tensor ? in.vh : in.kh).get(y);
     const __nv_bfloat162 p01 = __floats2bfloat162_rn(y[0], y[1]), p23 = __floats2bfloat162_rn(y[2], y[3]);
     const float xh[4] = {__low2float(p01), __high2float(p01), __low2float(p23), __high2float(p23)};
     Df rdf[4];
@@ -486,12 +533,22 @@ __device__ __forceinline__ size_t uniform_row(const WriteArgs& a, int i, int n, 
   return (((size_t)i * a.n_tok + n) * a.Hkv + h) * kD;
 }
 
-// One token of a write into the block image at bp, by scheme (VW: with value witnesses).
+// One token of a write into the block image at bp, by scheme (VW: with value witnesses), from
+// the lane's inputs `in`; STAGED as for int8_token (the black-box store stages nothing).
+template <typename T, int SCH, bool VW, bool STAGED>
+__device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, uint32_t* vst, int i, int h, int t,
+                                            size_t row, int lane, const TokIn<T>& in) {
+  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8, VW, STAGED>(a, bp, vst, i, h, t, row, lane, in);
+  else if constexpr (SCH == kFp8) fp8_token<T, STAGED>(a, bp, vst, i, h, t, row, lane, in);
+  else bbox_token<T>(a, bp, i, h, t, row, lane, in);
+}
+// Load, then write one token straight into its block.
 template <typename T, int SCH, bool VW>
-__device__ __forceinline__ void write_token(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row, int lane) {
-  if constexpr (int8_layout(SCH)) int8_token<T, SCH == kInt8, VW>(a, bp, i, h, t, row, lane);
-  else if constexpr (SCH == kFp8) fp8_token<T>(a, bp, i, h, t, row, lane);
-  else bbox_token<T>(a, bp, i, h, t, row, lane);
+__device__ __forceinline__ void write_token_direct(const WriteArgs& a, uint8_t* bp, int i, int h, int t, size_t row,
+                                                   int lane) {
+  TokIn<T> in;
+  in.load(a, row, lane, SCH == kBbox);
+  write_token<T, SCH, VW, false>(a, bp, nullptr, i, h, t, row, lane, in);
 }
 
 
@@ -506,28 +563,54 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
   const int blk = (a.t0 + n) >> 4;
   constexpr int kBytes = block_bytes(SCH);
   uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes;
-  write_token<T, SCH, VW>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
+  write_token_direct<T, SCH, VW>(a, bp, i, h, a.t0 + n, uniform_row(a, i, n, h), lane);
 }
 
 // One warp per (sequence, KV head, block) for blocks blk0, blk0 + 1, ... that the write fills
 // completely: the warp builds the block's image in shared memory token by token and stores
 // it with 16-byte writes.
+// The next token's inputs are loaded while a token is quantized.  The INT8 and FP8 value codes
+// of the block are staged in natural order (a conflict-free word per lane and token) and then
+// packed into their fragment-order words, lane by lane: the word of channel c and lane slot t
+// holds tokens 2t, 2t + 1, 2t + 8, 2t + 9.
 template <typename T, int SCH, bool VW>
 __global__ void __launch_bounds__(128, 6) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
   const ChainEntry chain(a.late_wait != 0);
   constexpr int kBytes = block_bytes(SCH);
+  constexpr bool kStaged = SCH != kBbox;
   __shared__ __align__(16) uint8_t img[4][kBytes];
+  __shared__ uint32_t vstage[4][kStaged ? kBlk * 32 : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long unit = (long long)blockIdx.x * 4 + warp;       // (i * Hkv + h) * nblocks + b
   if (unit >= (long long)a.B * a.Hkv * nblocks) return;
   const int b = (int)(unit % nblocks), sh = (int)(unit / nblocks);
   const int i = sh / a.Hkv, h = sh % a.Hkv, blk = blk0 + b;
   uint8_t* im = img[warp];
+  uint32_t* vst = vstage[warp];
+  TokIn<T> cur, nxt;
+  cur.load(a, uniform_row(a, i, blk * kBlk - a.t0, h), lane, SCH == kBbox);
   for (int r = 0; r < kBlk; ++r) {
     const int t = blk * kBlk + r;
-    write_token<T, SCH, VW>(a, im, i, h, t, uniform_row(a, i, t - a.t0, h), lane);
+    if (r + 1 < kBlk) nxt.load(a, uniform_row(a, i, t + 1 - a.t0, h), lane, SCH == kBbox);
+    write_token<T, SCH, VW, kStaged>(a, im, vst, i, h, t, uniform_row(a, i, t - a.t0, h), lane, cur);
+    cur = nxt;
   }
   __syncwarp();
+  if constexpr (kStaged) {
+    constexpr int kVC = SCH == kFp8 ? Fp8Layout::VC : Int8Layout::VC;
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      const uint32_t w0 = vst[(2 * tt) * 32 + lane], w1 = vst[(2 * tt + 1) * 32 + lane];
+      const uint32_t w2 = vst[(2 * tt + 8) * 32 + lane], w3 = vst[(2 * tt + 9) * 32 + lane];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = __byte_perm(w0, w1, (uint32_t)(e | ((4 + e) << 4)));
+        const uint32_t hi = __byte_perm(w2, w3, (uint32_t)(e | ((4 + e) << 4)));
+        *reinterpret_cast<uint32_t*>(im + kVC + vcode_off(2 * tt, 4 * lane + e)) = __byte_perm(lo, hi, 0x5410u);
+      }
+    }
+    __syncwarp();
+  }
   uint4* dst = reinterpret_cast<uint4*>(a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, blk) * kBytes);
   const uint4* src = reinterpret_cast<const uint4*>(im);
   for (int k = lane; k < kBytes / 16; k += 32) dst[k] = src[k];
@@ -620,7 +703,7 @@ __global__ void __launch_bounds__(128) write_ragged_kernel(const WriteArgs a, co
   const size_t row = ((size_t)(g.row0[lo] + (tok - g.off[lo])) * a.Hkv + h) * kD;
   uint8_t* bp = a.blocks + block_index(a.table, a.Hkv, a.nblk_max, i, h, t >> 4) * block_bytes(SCH);
   if constexpr (SCH == kKivi) kivi_v_token<T>(a, bp, i, h, t, row, lane);
-  else write_token<T, SCH, VW>(a, bp, i, h, t, row, lane);
+  else write_token_direct<T, SCH, VW>(a, bp, i, h, t, row, lane);
 }
 
 // Per-sequence lengths on the device ([B] of one layer), set from the launch's parameters.
