@@ -76,42 +76,40 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
   }
   *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
   __syncthreads();
-  // the warps' states meet at the largest maximum: warp 0 forms the sums and the meters, the
-  // first kD threads the output channels
-  __shared__ float s_tot[2];
+  // the warps' states meet at the largest maximum.  Every thread forms Z (the same arithmetic in
+  // every thread, so the same value) and its output channel; warp 0 forms the S sums and the
+  // meters without holding up the output.
   float Mx = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kMergeWarps; ++w) Mx = fmaxf(Mx, s_hdr[w][0]);
-  float o = 0.f;
-  if (threadIdx.x < kD && Mx != -INFINITY) {
+  float fw[kMergeWarps];
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) o = fmaf(pow2_dn(s_hdr[w][0] == Mx ? 0.f : s_hdr[w][0] - Mx), s_acc[w][threadIdx.x], o);
+  for (int w = 0; w < kMergeWarps; ++w) fw[w] = Mx == -INFINITY ? 0.f : pow2_dn(s_hdr[w][0] == Mx ? 0.f : s_hdr[w][0] - Mx);
+  float Zsh = 0.f, Zsl = 0.f, o = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    pair_add(Zsh, Zsl, __fmul_rd(fw[w], s_hdr[w][1]), __fmul_rd(fw[w], s_hdr[w][2]));
+    if (threadIdx.x < kD) o = fmaf(fw[w], s_acc[w][threadIdx.x], o);
   }
-  // warp 0: lane 8q + w holds quantity q (Z, S_A, S_B, S_V) of warp w, scaled exactly to Mx (Z
-  // rounded down, the S rounded up where the scale leaves fp32's normal range); three rounds of
-  // two-sums add the warps, then the lane of each S forms its meter against Z
+  const float Zt = Zsh + Zsl, Zdn = __fadd_rd(Zsh, Zsl);
+  // warp 0: lane 8q + w (q = 1, 2, 3: S_A, S_B, S_V) holds warp w's pair of that sum, scaled exactly
+  // to Mx (rounded up where the scale leaves fp32's normal range); three rounds of two-sums add
+  // the warps, then the first lane of each sum forms its meter against Z
   if (warp == 0) {
     const int q = lane >> 3, w = lane & 7;
     const float* hw = s_hdr[w];
-    const float k = hw[0] == Mx ? 0.f : hw[0] - Mx;
+    const float fu = Mx == -INFINITY ? 0.f : pow2_up(hw[0] == Mx ? 0.f : hw[0] - Mx);
     float hi = 0.f, lo = 0.f;
-    if (Mx != -INFINITY) {
-      if (q == 0) { const float f = pow2_dn(k); hi = __fmul_rd(f, hw[1]); lo = __fmul_rd(f, hw[2]); }
-      else { const float f = pow2_up(k); hi = __fmul_ru(f, hw[2 * q + 1]); lo = __fmul_ru(f, hw[2 * q + 2]); }
-    }
+    if (q > 0) { hi = __fmul_ru(fu, hw[2 * q + 1]); lo = __fmul_ru(fu, hw[2 * q + 2]); }
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) {
       const float ohi = __shfl_xor_sync(0xffffffffu, hi, m), olo = __shfl_xor_sync(0xffffffffu, lo, m);
       pair_add(hi, lo, ohi, olo);
     }
-    const float Zhi = __shfl_sync(0xffffffffu, hi, 0), Zlo = __shfl_sync(0xffffffffu, lo, 0);
-    const float Zdn = __fadd_rd(Zhi, Zlo);
-    const float S_up = __fadd_ru(hi, lo);
-    if (lane == 0) { s_tot[0] = Zhi + Zlo; s_tot[1] = Zdn; }
     if (p.part_out) {         // context-parallel shard: the cell's combined record, unnormalized
       float* rec = p.part_out + (size_t)cell * kPartStride;
       if (lane == 0) { rec[0] = Mx; rec[1] = Zdn; rec[5] = 0.f; rec[6] = 0.f; rec[7] = 0.f; }
-      if (w == 0 && q > 0) rec[1 + q] = S_up;
+      if (w == 0 && q > 0) rec[1 + q] = __fadd_ru(hi, lo);
     } else if (p.meter && w == 0 && q > 0) {
       const float D = meter_ratio(hi, lo, Zdn);
       if (q == 3) {
@@ -127,12 +125,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const De
       }
     }
   }
-  __syncthreads();
   if (p.part_out) {
     if (threadIdx.x < kD) p.part_out[(size_t)cell * kPartStride + kPartAcc + threadIdx.x] = o;
     return;
   }
-  const float Zt = s_tot[0], Zdn = s_tot[1];
   const float inv = Zt > 0.f ? 1.0f / Zt : 0.f;
   if (threadIdx.x < kD) p.out[(size_t)cell * kD + threadIdx.x] = o * inv;
   if (!p.meter) return;

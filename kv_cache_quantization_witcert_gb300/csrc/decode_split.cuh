@@ -90,7 +90,11 @@ template <int NW, int SCHEME> struct Smem {
   // NW x NST stage barriers (one warp each), then NXI "dither slot filled" and NXI
   // "dither slot free" barriers (NW arrivals each)
   static constexpr int kBarOff = kXiOff + kXi;
-  static constexpr int kBytes = kBarOff + (NW * NST + 2 * NXI) * 8;
+  // KIVI: each lane's eight query quads (16 bytes each at most), read again every block, live in
+  // shared memory rather than in registers
+  static constexpr int kQOff = (kBarOff + (NW * NST + 2 * NXI) * 8 + 15) / 16 * 16;
+  static constexpr int kQBytes = SCHEME == kKivi ? NW * 32 * 8 * 16 : 0;
+  static constexpr int kBytes = kQOff + kQBytes;
 };
 
 // An upper bound of sqrt(x) at most one unit above the correctly rounded value: the SFU
@@ -356,6 +360,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
   // 32-channel group.  The loads are issued here and consumed after the first block's dither.
   const bool has_q = active && g < grp;
   Raw4<QT> qraw[8];
+  Raw4<QT>* qsm = reinterpret_cast<Raw4<QT>*>(smem + SM::kQOff) + warp * 8 * 32;   // KIVI only
   {
     const QT* qr = reinterpret_cast<const QT*>(p.q) + ((size_t)(has_q ? i : 0) * p.Hq + j0 + (has_q ? g : 0)) * kD + 4 * t;
 #pragma unroll
@@ -390,6 +395,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     for (int kk = 0; kk < 8; ++kk) {
       const float4 v4 = qraw[kk].get();
       const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      if constexpr (SCHEME == kKivi) qsm[kk * 32 + lane] = qraw[kk];
       __half hv[4], lv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -526,7 +532,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           if constexpr (SCHEME == kKivi) {
-            const float4 v4 = qraw[kk].get();
+            const float4 v4 = qsm[kk * 32 + lane].get();
             __half h0, h1, h2, h3, l0, l1, l2, l3;
             split_h(v4.x, h0, l0); split_h(v4.y, h1, l1); split_h(v4.z, h2, l2); split_h(v4.w, h3, l3);
             fb[kk][0] = pack_h2(h0, h1); fb[kk][1] = pack_h2(h2, h3);
@@ -635,7 +641,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int kk = 2 * kq + hf;
-            const float4 q4 = qraw[kk].get();
+            const float4 q4 = qsm[kk * 32 + lane].get();
             const float2 q01 = make_float2(q4.x, q4.y), q23 = make_float2(q4.z, q4.w);
             zq2 = __ffma2_rn(q01, __half22float2(bits_h2(zw[2 * hf])), zq2);
             zq2 = __ffma2_rn(q23, __half22float2(bits_h2(zw[2 * hf + 1])), zq2);

@@ -27,3 +27,19 @@ def test_absolute_allowance_is_for_values_below_fp32_range_only():
     check_meter(np.array([0.0]), np.array([3.5e-90]))            # a value no fp32 meter can carry
     with pytest.raises(AssertionError):
         check_meter(np.array([0.0]), np.array([1e-20]))
+
+
+def test_raw_meters_above_one_are_held_to_the_tolerance_on_d():
+    # D = 9023.25: raw = D + D^2/2; D 6e-5 above passes (raw then 1.2e-4 above), 2e-4 above does not
+    d = 9023.25
+    raw = lambda x: x + x * x / 2
+    check_meter(np.array([raw(d * (1 + 6e-5))]), np.array([raw(d)]), raw=True)
+    with pytest.raises(AssertionError):
+        check_meter(np.array([raw(d * (1 + 6e-5))]), np.array([raw(d)]))
+    with pytest.raises(AssertionError):
+        check_meter(np.array([raw(d * (1 + 2e-4))]), np.array([raw(d)]), raw=True)
+    with pytest.raises(AssertionError):                           # below stays below
+        check_meter(np.array([np.nextafter(raw(d), 0.0)]), np.array([raw(d)]), raw=True)
+    # at or below 1 the raw value is the meter: the tolerance stays on it
+    with pytest.raises(AssertionError):
+        check_meter(np.array([0.9 * (1 + 1.5e-4)]), np.array([0.9]), raw=True)

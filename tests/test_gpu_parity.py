@@ -248,8 +248,8 @@ def test_full_28_layer_config_sampled_cells(delta_req, n_splits):
             js = slice(h * w.group, (h + 1) * w.group)
             r = oracle_group(w, layer, K[i, :, h], V[i, :, h], q[i, js], i, h, w.scheme, dl)
             assert np.abs(o[i, js] - r["out"]).max() <= 2e-3 * np.abs(V[i, :, h]).max()
-            check_meter(m["raw_a"].cpu().numpy()[i, js], r["raw_a"], what="raw_a")
-            check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what="raw_b")
+            check_meter(m["raw_a"].cpu().numpy()[i, js], r["raw_a"], what="raw_a", raw=True)
+            check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what="raw_b", raw=True)
 
 
 def test_errors_are_reported_not_raised_on_device():

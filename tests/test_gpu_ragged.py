@@ -95,9 +95,9 @@ class Ragged:
             r = ref.decode(layer, q[i:i + 1], delta_req)
             vmax = np.abs(ref.v[layer]).max() if S else 1.0
             assert np.abs(o[i] - r["out"][0]).max() <= 2e-3 * vmax, f"sequence {i} (S={S})"
-            check_meter(mm["raw_a"][i], r["raw_a"][0], METER_REL, f"raw_a seq {i}")
+            check_meter(mm["raw_a"][i], r["raw_a"][0], METER_REL, f"raw_a seq {i}", raw=True)
             if self.scheme == "int8_dither":
-                check_meter(mm["raw_b"][i], r["raw_b"][0], METER_REL, f"raw_b seq {i}")
+                check_meter(mm["raw_b"][i], r["raw_b"][0], METER_REL, f"raw_b seq {i}", raw=True)
             if self.gpu.v_witness:
                 check_meter(mm["meter_v"][i], r["meter_v"][0], METER_REL, f"meter_v seq {i}")
             if S == 0:
@@ -212,6 +212,67 @@ def test_ragged_gate_decisions_match_each_sequence(scheme, pages):
                                          w.group) == 0
     rg.check_decode(0, gen_q(w, 0, 7), w.delta_req)
     assert rg.gpu.witcert_gate_stats()["blocks_paged_in"] > 0
+
+
+def _gate_check(rg, layer, tau, lens, oracle_risk):
+    """The gate on every sequence: its block risks against its oracle's, the GPU's repairs equal
+    to its oracle gate's on the GPU's risks and, outside the tie zone, on the oracle's own."""
+    risk = rg.gpu.export(layer, _lib.X_BLOCK_RISK).cpu().numpy()
+    before = [ref.repaired[layer][0].copy() for ref in rg.refs]
+    rg.gpu.witcert_gate(layer, tau)
+    slots = rg.gpu.export(layer, _lib.X_SLOTS).cpu().numpy()
+    for i, ref in enumerate(rg.refs):
+        nblk = (lens[i] + 15) // 16
+        assert not np.any(risk[i, :, nblk:])
+        check_risk(risk[i, :, :nblk], oracle_risk[i], what=f"block risk seq {i}")
+        ref.gate(layer, tau, risk[i:i + 1, :, :nblk])
+        np.testing.assert_array_equal(slots[i, :, :nblk] >= 0, ref.repaired[layer][0])
+        assert check_gate_end_to_end(oracle_risk[i][None], before[i][None], tau, slots[i:i + 1, :, :nblk] >= 0,
+                                     rg.w.group) == 0
+
+
+WIDE_CASES = [
+    ("int8_dither", 20, False, 4.0),   # CTAs of 16 sequences: a full one and one of 4; gated
+    ("fp8_e4m3", 16, True, 0.5),       # one group, paged, gated
+    ("kivi2", 9, False, None),         # CTAs of 8 sequences: a full one and one of a single sequence
+    ("int8_rtn", 12, True, None),
+    ("blackbox", 8, False, None),
+]
+
+
+@pytest.mark.parametrize("scheme,B,paged,tau", WIDE_CASES)
+def test_wide_ragged_batches_match_each_sequence(scheme, B, paged, tau):
+    """Ragged bf16 batches of 8 to 20 sequences: split CTAs of 8 and 16 warps, a full group of
+    sequences and a partial one.  Lengths from 0 to 1500 (an empty sequence, a single token,
+    equal lengths, ragged tails); every sequence against its own oracle, then one-token appends
+    to every other sequence (some crossing a block boundary), a reset of the longest, and decodes
+    again."""
+    w = WORKLOADS["qwen_1l"].with_(batch=B, context=1500, steps=4, scheme=scheme)
+    rng = np.random.default_rng(B)
+    lens = [int(n) for n in rng.integers(2, 1501, B)]
+    lens[0], lens[1], lens[2] = 0, 1, 1500
+    lens[3] = lens[4] = lens[5] = lens[6] = lens[7] = 640      # ties across the first group's end
+    lens[B - 1] = 32
+    pages = sum((n + 16) // 16 + 1 for n in lens) + 8 if paged else 0
+    gate = tau is not None
+    rg = Ragged(w, scheme, cap=1536, v_witness=not gate, gate_blocks=B * 4 * 96 if gate else 0, max_pages=pages)
+    K, V = gen_kv(w, 0)
+    rg.write(0, list(zip(_split(K, lens), _split(V, lens))))
+    rg.check_store(0)
+    _, _, oracle_risk = rg.check_decode(0, gen_q(w, 0, 0), w.delta_req)
+    if gate:
+        _gate_check(rg, 0, tau, lens, oracle_risk)
+    K2, V2 = gen_kv(w.with_(context=16), 3)
+    app = [1 if i % 2 == 0 else 0 for i in range(B)]
+    rg.write(0, list(zip(_split(K2, app), _split(V2, app))))
+    lens = [n + a for n, a in zip(lens, app)]
+    _, _, oracle_risk = rg.check_decode(0, gen_q(w, 0, 1), w.delta_req)
+    if gate:
+        _gate_check(rg, 0, tau, lens, oracle_risk)
+    rg.gpu.witcert_reset_sequence(2)
+    rg.refs[2] = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, 1, scheme, w.seed, w.steps, v_witness=not gate)
+    rg.check_decode(0, gen_q(w, 0, 2), w.delta_req)
+    assert rg.gpu.witcert_stats()["device_errors"] == 0
 
 
 def test_ragged_rejects_overflow_and_partial_decode():

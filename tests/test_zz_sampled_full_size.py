@@ -39,10 +39,10 @@ def check_group(w, o, m, r, i, h, V, tier_b):
     vmax = np.abs(V[i, :, h]).max()
     d = np.abs(o[i, js] - r["out"]).max()
     assert d <= 2e-3 * vmax, f"out seq {i} head {h}: {d} > {2e-3 * vmax}"
-    check_meter(m["raw_a"].cpu().numpy()[i, js], r["raw_a"], what=f"raw_a seq {i} head {h}")
+    check_meter(m["raw_a"].cpu().numpy()[i, js], r["raw_a"], what=f"raw_a seq {i} head {h}", raw=True)
     check_meter(m["meter_a"].cpu().numpy()[i, js], r["meter_a"], what=f"meter_a seq {i} head {h}")
     if tier_b:
-        check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what=f"raw_b seq {i} head {h}")
+        check_meter(m["raw_b"].cpu().numpy()[i, js], r["raw_b"], what=f"raw_b seq {i} head {h}", raw=True)
 
 
 @pytest.mark.parametrize("model,batch,scheme,context", [("mistral", 16, "int8_dither", LONG), ("yi", 8, "fp8_e4m3", LONG),

@@ -64,16 +64,16 @@ def test_noalloc_decode_is_bit_identical_on_two_calls(scheme):
     cache.close()
 
 
-def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter():
+@pytest.mark.parametrize("lens", [[600, 75, 333], [600, 75, 333, 0, 1, 599, 16, 17, 300, 450]])
+def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter(lens):
     """A gated, ragged cache with value witnesses: the block risks the gate reads and the value
     meter are the same bits through either entry point, and the gate after a no-allocation
-    decode pages in the same blocks."""
-    w = WORKLOADS["qwen_1l"].with_(batch=3, context=600, scheme="int8_dither")
-    lens = [600, 75, 333]
+    decode pages in the same blocks.  Three sequences (split CTAs of 2 warps) and ten (8 warps)."""
+    w = WORKLOADS["qwen_1l"].with_(batch=len(lens), context=600, scheme="int8_dither")
     runs = []
     for noalloc in (False, True):
         cache = wc.Cache(1, w.n_q_heads, w.n_kv_heads, w.batch, 640, "int8_dither", dtype=torch.bfloat16,
-                         seed=w.seed, total_steps=w.steps, max_repair_blocks=3 * 4 * 40, v_witness=True)
+                         seed=w.seed, total_steps=w.steps, max_repair_blocks=w.batch * 4 * 40, v_witness=True)
         K, V = gen_kv(w, 0)
         Kp = np.concatenate([K[i, :n] for i, n in enumerate(lens)])
         Vp = np.concatenate([V[i, :n] for i, n in enumerate(lens)])
