@@ -73,8 +73,10 @@ template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 :
 
 // Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
 // warps consume, so warps may drift up to two blocks apart (one with three slots, which is
-// what two 8-warp CTAs per SM leave room for).
-template <int NW> struct XiSlots { static constexpr int value = NW == 8 ? 3 : 4; };
+// what two 8-warp CTAs per SM leave room for).  CTAs of one or two warps keep two slots and
+// regenerate one block ahead: their warps hardly drift, and the smaller footprint fits five
+// (three) CTAs on an SM instead of three (two).
+template <int NW> struct XiSlots { static constexpr int value = NW <= 2 ? 2 : NW == 8 ? 3 : 4; };
 
 // A ring stage holds one block and, behind it, the block's value witnesses.
 template <int NW, int SCHEME> struct Smem {
