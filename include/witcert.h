@@ -195,7 +195,11 @@ witcert_status witcert_reset_sequence(witcert_cache* cache, int seq, void* strea
  * of two and rounded down (Z) or up (S) where they leave their compensated pairs, and the
  * quotient, D + D^2/2 and a margin of 2^-15 on D are rounded up, so no error grows with the
  * context length; the margin covers each token's own rounding (SFU exponentials and
- * roots, tensor-core products, the expm1 series, which is itself an upper bound).
+ * roots, tensor-core products, the expm1 series, which is itself an upper bound) for
+ * per-token bounds c_t up to 5 and logits accurate to a few 1e-6.  KIVI2 caches of keys
+ * with large outlier channels reach c_t near 30 and logits of tens of units, where the
+ * tensor cores' fp32 accumulation of eps_t and of the logits is covered by the margin as
+ * measured, not by a worst-case bound.
  * Any meter pointer may be NULL; if all five are NULL the meter work is
  * compiled out and `out` is bit-identical to the metered run's.
  * With the gate enabled, per-16-token-block risks of the gate's tier

@@ -86,7 +86,12 @@ template <int NW, int SCHEME> struct Smem {
   static constexpr int XD = NXI > 2 ? NXI - 2 : 1;
   static constexpr int STB = Lay<SCHEME>::BYTES + kVwBytes;
   static constexpr int kRing = NW * NST * STB;
-  static constexpr int kXi = NXI * kXiBytes;
+  // A single-warp CTA forms its key dither in registers where it uses it (each lane's operand
+  // fragment is one item of the generator); its slots hold the value dither only.
+  static constexpr bool XREG = SCHEME == kInt8 && NW == 1;
+  static constexpr int XSLOT = XREG ? kXiBytes - kXiV : kXiBytes;
+  static constexpr int XV = XREG ? 0 : kXiV;            // value dither within a slot
+  static constexpr int kXi = NXI * XSLOT;
   static constexpr int kRingOff = 0;
   static constexpr int kXiOff = (kRing + 127) / 128 * 128;
   // NW x NST stage barriers (one warp each), then NXI "dither slot filled" and NXI
@@ -177,31 +182,40 @@ __device__ __forceinline__ float2 meter_term2(float2 pe, float2 d, float2 c) {
   return make_float2(c.x < 0.125f ? poly.x : big.x, c.y < 0.125f ? poly.y : big.y);
 }
 
+// The key dither of k-step kk for lane L = 4g + tq of the block whose first token is at
+// position tb: tokens g and g + 8, channels 16kk + 4tq .. 16kk + 4tq + 3, as the lane's QK A
+// operand, negated, in fp16 hi and lo pieces.  Registers R0 = (g, ch +0,+1), R1 = (g + 8,
+// ch +0,+1), R2 = (g, ch +2,+3), R3 = (g + 8, ch +2,+3).
+__device__ __forceinline__ void xi_key_frag(const DecodeArgs& p, int h, int tb, int kk, int L, uint32_t (&hw)[4],
+                                            uint32_t (&lw)[4]) {
+  const int g = L >> 2, quad = 4 * kk + (L & 3);
+  const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g, quad, 0);
+  const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g + 8, quad, 0);
+  const float2 v[4] = {make_float2(x0.x, x0.y), make_float2(x1.x, x1.y), make_float2(x0.z, x0.w),
+                       make_float2(x1.z, x1.w)};
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    // hi = fp16(-xi), lo = fp16(-xi - hi), two values per conversion
+    const __half2 hh = __floats2half2_rn(v[r].x, v[r].y);
+    const float2 f = __half22float2(hh);
+    hw[r] = h2_bits(hh);
+    lw[r] = h2_bits(__floats2half2_rn(v[r].x - f.x, v[r].y - f.y));
+  }
+}
+
 // Regenerate the dither of block `blk` of KV head h into shared memory, in the
 // fragment order of the QK operands (negated, fp16 hi + lo) and of the PV operand
 // (negated, fp16): each lane's four A registers are contiguous, so one 16-byte load
 // fills an MMA operand.  Items 0..255 fill the QK operands, one (k-step, lane) each, with
-// 16-byte stores; items 256..511 fill the PV operand, one (token pair, channel quad) each.
-__device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads) {
+// 16-byte stores; items 256..511 fill the PV operand, one (token pair, channel quad) each,
+// at offset xv.  VONLY: the value items only (the CTA forms its key dither in registers).
+template <bool VONLY>
+__device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, int blk, int nthreads, int xv) {
   const int tb = p.pos0 + blk * kBlk;
-  for (int idx = threadIdx.x; idx < 512; idx += nthreads) {
-    if (idx < 256) {
-      // k-step kk, lane L = 4g + tq: tokens g and g + 8, channels 16kk + 4tq .. 16kk + 4tq + 3.
-      // Registers R0 = (g, ch +0,+1), R1 = (g + 8, ch +0,+1), R2 = (g, ch +2,+3), R3 = (g + 8, ch +2,+3).
-      const int kk = idx >> 5, L = idx & 31, g = L >> 2, quad = 4 * kk + (L & 3);
-      const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g, quad, 0);
-      const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + g + 8, quad, 0);
-      const float2 v[4] = {make_float2(x0.x, x0.y), make_float2(x1.x, x1.y), make_float2(x0.z, x0.w),
-                           make_float2(x1.z, x1.w)};
+  for (int idx = (VONLY ? 256 : 0) + threadIdx.x; idx < 512; idx += nthreads) {
+    if (!VONLY && idx < 256) {
       uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        // hi = fp16(-xi), lo = fp16(-xi - hi), two values per conversion
-        const __half2 hh = __floats2half2_rn(v[r].x, v[r].y);
-        const float2 f = __half22float2(hh);
-        hw[r] = h2_bits(hh);
-        lw[r] = h2_bits(__floats2half2_rn(v[r].x - f.x, v[r].y - f.y));
-      }
+      xi_key_frag(p, h, tb, idx >> 5, idx & 31, hw, lw);
       *reinterpret_cast<uint4*>(xb + kXiKHi + idx * 16) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4*>(xb + kXiKLo + idx * 16) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     } else {
@@ -214,7 +228,7 @@ __device__ __forceinline__ void gen_xi(uint8_t* xb, const DecodeArgs& p, int h, 
       const float4 x0 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + r0, q, 1);
       const float4 x1 = neg_dither4_rk(p.rk0, p.rk1, p.layer, h, tb + r0 + 1, q, 1);
       const float a0[4] = {x0.x, x0.y, x0.z, x0.w}, a1[4] = {x1.x, x1.y, x1.z, x1.w};
-      uint32_t* vb = reinterpret_cast<uint32_t*>(xb + kXiV);
+      uint32_t* vb = reinterpret_cast<uint32_t*>(xb + xv);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int c = 4 * q + e;
@@ -379,7 +393,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
       if (!fault && lane == 0) atomicAdd(p.err, 1);
       fault = true;
     }
-    gen_xi(xib + ps * kXiBytes, p, h, b_begin + m, NW * 32);
+    gen_xi<SM::XREG>(xib + ps * SM::XSLOT, p, h, b_begin + m, NW * 32, SM::XV);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&xfull[ps]));
   };
@@ -503,7 +517,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
     const int blk = b_begin + n, stage = n % NST;
     const uint32_t par = (uint32_t)((n / NST) & 1);
     const int xs = SCHEME == kInt8 ? n % SM::NXI_DIV : 0;
-    const uint8_t* xb = xib + xs * kXiBytes;
+    const uint8_t* xb = xib + xs * SM::XSLOT;
     // The dither XD blocks ahead: half of the warps (two per scheduler) make their share before
     // this block's logits, the other half between its softmax and its P.V product, so that the
     // integer work of the one overlaps the tensor and FP32 work of the other.
@@ -563,10 +577,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             mma16816(acc[G], a, qb[kk]);
             if (QLO) mma16816(acc[G], a, qbl[kk]);
             if constexpr (SCHEME != kInt8) continue;                 // no dither to subtract
-            const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
-            const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
-            const uint32_t ah[4] = {xh.x, xh.y, xh.z, xh.w};
-            const uint32_t al[4] = {xl.x, xl.y, xl.z, xl.w};
+            uint32_t ah[4], al[4];
+            if constexpr (SM::XREG) {
+              xi_key_frag(p, h, p.pos0 + blk * kBlk, kk, lane, ah, al);
+            } else {
+              const uint4 xh = *reinterpret_cast<const uint4*>(xb + kXiKHi + (kk * 32 + lane) * 16);
+              const uint4 xl = *reinterpret_cast<const uint4*>(xb + kXiKLo + (kk * 32 + lane) * 16);
+              ah[0] = xh.x; ah[1] = xh.y; ah[2] = xh.z; ah[3] = xh.w;
+              al[0] = xl.x; al[1] = xl.y; al[2] = xl.z; al[3] = xl.w;
+            }
             mma16816(acc[G], ah, qb[kk]);
             mma16816(acc[G], al, qb[kk]);
             if (QLO) mma16816(acc[G], ah, qbl[kk]);
@@ -819,7 +838,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             const uint32_t a[4] = {i8x2_lo(w0), i8x2_lo(w1), i8x2_hi(w0), i8x2_hi(w1)};
             mma16816(acco[mt], a, bfr);
             if constexpr (SCHEME == kInt8) {
-              const uint4 xv = *reinterpret_cast<const uint4*>(xb + kXiV + (mt * 32 + lane) * 16);
+              const uint4 xv = *reinterpret_cast<const uint4*>(xb + SM::XV + (mt * 32 + lane) * 16);
               const uint32_t ax[4] = {xv.x, xv.y, xv.z, xv.w};
               mma16816(acco[mt], ax, bfr);
             }
