@@ -25,12 +25,12 @@ def to_dev(x, w):
     return torch.from_numpy(np.ascontiguousarray(x)).to(device="cuda").to(torch_dtype(w))
 
 
-def make_pair(w, scheme=None, n_splits=None, extra_tokens=None, gate_blocks=0, v_witness=False):
+def make_pair(w, scheme=None, n_splits=None, extra_tokens=None, gate_blocks=0, v_witness=False, max_pages=0):
     scheme = scheme or w.scheme
     cap = w.context + (w.steps if extra_tokens is None else extra_tokens)
     gpu = wc.Cache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, cap, scheme, dtype=torch_dtype(w),
                    seed=w.seed, total_steps=w.steps, n_splits=w.n_splits if n_splits is None else n_splits,
-                   max_repair_blocks=gate_blocks, v_witness=v_witness)
+                   max_repair_blocks=gate_blocks, v_witness=v_witness, max_pages=max_pages)
     ref = OracleCache(w.n_layers, w.n_q_heads, w.n_kv_heads, w.batch, scheme, w.seed, w.steps, v_witness=v_witness)
     return gpu, ref
 

@@ -194,16 +194,19 @@ def test_empty_layer_decodes_to_zero():
     assert torch.count_nonzero(m["meter_a"]) == 0 and torch.count_nonzero(m["meter_b"]) == 0
 
 
-@pytest.mark.parametrize("scheme,v_witness", [("fp8_e4m3", False), ("blackbox", True), ("int8_dither", False),
-                                              ("int8_dither", True)])
-def test_gate_decisions_bit_exact_and_repaired_decode(scheme, v_witness):
+@pytest.mark.parametrize("scheme,v_witness,batch,pages", [
+    ("fp8_e4m3", False, 2, 0), ("blackbox", True, 2, 0), ("int8_dither", False, 2, 0), ("int8_dither", True, 2, 0),
+    ("int8_dither", True, 1, 0),         # one sequence: single-warp CTAs, key dither in registers
+    ("int8_dither", False, 1, 40),       # the same, paged
+])
+def test_gate_decisions_bit_exact_and_repaired_decode(scheme, v_witness, batch, pages):
     """Raw-cast FP8, the black-box store and dithered INT8 (ranked by its Tier B risks): the GPU's
     block risks match the oracle's (never below, within 1e-4); the oracle's gate, fed the GPU's
     block risks, picks exactly the blocks the GPU pages in, and fed its own risks picks them too
     outside the tie zone (empty here); the next decode matches the oracle on the repaired cache
     (value witnesses stay: the gate pages in keys only)."""
-    w = WORKLOADS["qwen_1l"].with_(batch=2, context=400, steps=3, scheme=scheme)
-    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32, v_witness=v_witness)
+    w = WORKLOADS["qwen_1l"].with_(batch=batch, context=400, steps=3, scheme=scheme)
+    gpu, ref = make_pair(w, gate_blocks=2 * 4 * 32, v_witness=v_witness, max_pages=pages)
     K, V = gen_kv(w, 0)
     write_both(gpu, ref, 0, K, V, w)
     taus = (0.5, 0.2, 0.05) if scheme != "int8_dither" else (4.0, 2.0, 1.0)
