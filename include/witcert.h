@@ -191,7 +191,7 @@ witcert_status witcert_reset_sequence(witcert_cache* cache, int seq, void* strea
  *   meter_v [batch][n_q_heads]       value meter E_V = sum_t p~_t wv_t (v_witness caches;
  *                                    EINVAL if non-NULL on a cache without value witnesses)
  * Meters are upper bounds of the formula's value on the stored cache: the sums over
- * tokens, splits and warps are compensated (Kahan, two-sums), rescaled only by exact powers
+ * tokens, splits and warps are compensated (hi/lo pairs, two-sums), rescaled only by exact powers
  * of two and rounded down (Z) or up (S) where they leave their compensated pairs, and the
  * quotient, D + D^2/2 and a margin of 2^-15 on D are rounded up, so no error grows with the
  * context length; the margin covers each token's own rounding (SFU exponentials and

@@ -126,9 +126,10 @@ __device__ __forceinline__ float2 f2sub(float2 a, float2 b) { return __ffma2_rn(
 // the length of the sums and the pattern of their roundings:
 //  * the running maximum m (log2 units) is kept integer-valued, so every rescale of the sums
 //    is a multiplication by an exact power of two;
-//  * a lane adds its per-block terms to Z and S with Kahan's compensated summation (a
-//    relative error of at most 2u + O(n u^2), u = 2^-24, for n non-negative terms, instead
-//    of the n u of a plain running sum);
+//  * a lane adds its per-block terms to Z and S in compensated (hi, lo) pairs, moving the
+//    low word into the high one by an error-free two-sum every eight blocks (a relative
+//    error of at most 8u + O(n u^2), u = 2^-24, for n non-negative terms, instead of the
+//    n u of a plain running sum);
 //  * lanes, splits and warps are combined with error-free two-sums, and whenever a sum
 //    leaves its (hi, lo) pair it is rounded down (Z) or up (S);
 //  * the quotient, the margin and D + D^2/2 are rounded up.
@@ -150,13 +151,19 @@ __device__ __forceinline__ float pow2_up(float k) {
   return k == -INFINITY ? 0.0f : fmaxf(pow2_dn(k), 0x1p-149f);
 }
 
-// Kahan's compensated summation in (hi, lo) form: hi + lo carries the running sum and lo the
-// rounding error hi has accumulated; two query heads at once.
-__device__ __forceinline__ void kahan_add2(float2& hi, float2& lo, float2 x) {
-  const float2 y = __fadd2_rn(x, lo);
-  const float2 t = __fadd2_rn(hi, y);
-  lo = f2sub(y, f2sub(t, hi));
-  hi = t;
+// Compensated running sum of non-negative terms in (hi, lo) form, two query heads at once: each
+// block's term goes into lo with one add, and every kRenorm blocks an error-free two-sum
+// (Knuth's, valid for either order of the operands) moves lo's value into hi and leaves its
+// rounding error in lo.  An add's error is at most one unit of lo, which holds at most kRenorm
+// terms of the current period plus the last two-sum's error, so the errors of a period stay
+// below kRenorm u times its sum and the relative error below kRenorm u + O(n u^2) whatever the
+// number of blocks n (u = 2^-24).
+constexpr int kRenorm = 8;
+__device__ __forceinline__ void renorm2(float2& hi, float2& lo) {
+  const float2 s = __fadd2_rn(hi, lo);
+  const float2 bb = f2sub(s, hi);
+  lo = __fadd2_rn(f2sub(hi, f2sub(s, bb)), f2sub(lo, bb));
+  hi = s;
 }
 // (hi, lo) += (ohi, olo) with an error-free two-sum of the high parts (Knuth).
 __device__ __forceinline__ void pair_add(float& hi, float& lo, float ohi, float olo) {
@@ -485,7 +492,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
 
   // ---------------------------------------------------------------- state
   // per lane: heads 2t (.x) and 2t+1 (.y); A = token g, B = token g+8 of the block.  m2 is
-  // integer-valued; the sums are Kahan pairs (hi, lo).
+  // integer-valued; the sums are compensated pairs (hi, lo), renormalized every kRenorm blocks.
   float2 m2 = f2(-INFINITY), Zp = f2(0.f), SAp = f2(0.f), SBp = f2(0.f), SVp = f2(0.f);
   float2 Zl = f2(0.f), SAl = f2(0.f), SBl = f2(0.f), SVl = f2(0.f);
   float acco[8][4];
@@ -756,19 +763,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
         }
       }
       const float2 peA = ex2x2(dA), peB = ex2x2(dB);
-      kahan_add2(Zp, Zl, __fadd2_rn(peA, peB));
+      Zl = __fadd2_rn(Zl, __fadd2_rn(peA, peB));
       if (METER) {
         const float2 taA = meter_term2(peA, dA, epsA), taB = meter_term2(peB, dB, epsB);
-        kahan_add2(SAp, SAl, __fadd2_rn(taA, taB));
+        SAl = __fadd2_rn(SAl, __fadd2_rn(taA, taB));
         if (VW) {       // value witnesses of tokens g and g + 8 (zero past the context, where p is 0)
           const __half* wv = reinterpret_cast<const __half*>(sb + L::BYTES);
-          kahan_add2(SVp, SVl, __ffma2_rn(peA, f2(__half2float(wv[g])), __fmul2_rn(peB, f2(__half2float(wv[g + 8])))));
+          SVl = __fadd2_rn(SVl, __ffma2_rn(peA, f2(__half2float(wv[g])), __fmul2_rn(peB, f2(__half2float(wv[g + 8])))));
         }
         float2 tbA = f2(0.f), tbB = f2(0.f);
         if (SCHEME == kInt8) {
           tbA = meter_term2(peA, dA, ubA);
           tbB = meter_term2(peB, dB, ubB);
-          kahan_add2(SBp, SBl, __fadd2_rn(tbA, tbB));
+          SBl = __fadd2_rn(SBl, __fadd2_rn(tbA, tbB));
         }
         if (RISK) {
           float2 r = SCHEME == kInt8 ? __fadd2_rn(tbA, tbB) : __fadd2_rn(taA, taB);
@@ -781,6 +788,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) decode_split_ke
             if (2 * t < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t) * p.nblk_max + blk] = make_float2(m2.x, r.x);
             if (2 * t + 1 < grp) p.risk_raw[((size_t)i * p.Hq + j0 + 2 * t + 1) * p.nblk_max + blk] = make_float2(m2.y, r.y);
           }
+        }
+      }
+      if ((n & (kRenorm - 1)) == kRenorm - 1) {      // warp-uniform
+        renorm2(Zp, Zl);
+        if (METER) {
+          renorm2(SAp, SAl);
+          if (SCHEME == kInt8) renorm2(SBp, SBl);
+          if (VW) renorm2(SVp, SVl);
         }
       }
 
