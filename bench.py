@@ -122,6 +122,18 @@ def timed_launches(scheme, n_layers, lens0, steps, ragged, paged):
     return n
 
 
+L2_BYTES = 129e6          # GB300's L2
+
+
+def l2_note(cache_bytes):
+    """How the timed steps relate to L2: a cache of more than twice L2 is read from HBM every step
+    (layers are decoded in turn, so a layer's blocks have left L2 before its next step)."""
+    if cache_bytes > 2 * L2_BYTES:
+        return f"inputs larger than L2: every step reads the whole cache ({cache_bytes / 1e9:.2f} GB)"
+    return (f"cache of {cache_bytes / 1e9:.3f} GB within twice L2 ({L2_BYTES / 1e6:.0f} MB): steps may be "
+            "served partly from L2; use more layers for an HBM figure")
+
+
 def config_of(w, args, n_splits, world):
     vw = getattr(args, "v_witness", False)
     rg = getattr(args, "ragged", None)
@@ -135,8 +147,7 @@ def config_of(w, args, n_splits, world):
             "scheme": w.scheme, "delta_req": w.delta_req, "n_splits": n_splits,
             "parallelism": f"replicas x{world} (independent sequence shards)",
             "v_witness": bool(vw),
-            "l2": "inputs larger than L2: every step reads the whole cache "
-                  f"({w.n_layers * w.batch * w.n_kv_heads * w.context * tok_head_bytes(w.scheme, vw) / 1e9:.2f} GB)",
+            "l2": l2_note(w.n_layers * w.batch * w.n_kv_heads * w.context * tok_head_bytes(w.scheme, vw)),
             "prefill_data": f"{distinct_sets(w)} generated K/V set(s) reused across layers (the dither and so the "
                             "codes still differ per layer)"}
 
