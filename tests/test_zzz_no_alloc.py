@@ -64,15 +64,19 @@ def test_noalloc_decode_is_bit_identical_on_two_calls(scheme):
     cache.close()
 
 
-@pytest.mark.parametrize("lens", [[600, 75, 333], [600, 75, 333, 0, 1, 599, 16, 17, 300, 450]])
-def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter(lens):
+TEN = [600, 75, 333, 0, 1, 599, 16, 17, 300, 450]
+
+
+@pytest.mark.parametrize("scheme,lens", [("int8_dither", [600, 75, 333]), ("int8_dither", TEN), ("fp8_e4m3", TEN)])
+def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter(scheme, lens):
     """A gated, ragged cache with value witnesses: the block risks the gate reads and the value
     meter are the same bits through either entry point, and the gate after a no-allocation
-    decode pages in the same blocks.  Three sequences (split CTAs of 2 warps) and ten (8 warps)."""
-    w = WORKLOADS["qwen_1l"].with_(batch=len(lens), context=600, scheme="int8_dither")
+    decode pages in the same blocks.  Three sequences (split CTAs of 2 warps), ten (8 warps), and
+    ten of the raw-cast FP8 scheme (one warp per sequence and block range)."""
+    w = WORKLOADS["qwen_1l"].with_(batch=len(lens), context=600, scheme=scheme)
     runs = []
     for noalloc in (False, True):
-        cache = wc.Cache(1, w.n_q_heads, w.n_kv_heads, w.batch, 640, "int8_dither", dtype=torch.bfloat16,
+        cache = wc.Cache(1, w.n_q_heads, w.n_kv_heads, w.batch, 640, scheme, dtype=torch.bfloat16,
                          seed=w.seed, total_steps=w.steps, max_repair_blocks=w.batch * 4 * 40, v_witness=True)
         K, V = gen_kv(w, 0)
         Kp = np.concatenate([K[i, :n] for i, n in enumerate(lens)])
@@ -85,7 +89,7 @@ def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter(lens):
             call = cache.witcert_decode_noalloc if noalloc else cache.witcert_decode
             call(0, q, w.delta_req, out, m[0], m[1], m[2], m[3], m[4])
             risk = cache.export(0, _lib.X_BLOCK_RISK)
-            cache.witcert_gate(0, 4.0)
+            cache.witcert_gate(0, 4.0 if scheme == "int8_dither" else 0.5)
             slots = cache.export(0, _lib.X_SLOTS)
             torch.cuda.synchronize()
             runs.append((out.clone(), m.clone(), risk.clone(), slots.clone()))
@@ -93,7 +97,9 @@ def test_noalloc_keeps_the_gate_risks_and_ragged_value_meter(lens):
     n = len(runs) // 2
     for k in range(n):
         (o1, m1, r1, s1), (o2, m2, r2, s2) = runs[k], runs[n + k]
-        assert torch.equal(o1, o2) and torch.equal(m1, m2), f"step {k}"
+        assert torch.equal(o1, o2), f"step {k}"
+        # the same bits, NaN where the scheme has no Tier B (FP8: meter_b and raw_b)
+        torch.testing.assert_close(m1, m2, rtol=0, atol=0, equal_nan=True, msg=f"meters, step {k}")
         assert torch.equal(r1, r2), f"block risks, step {k}"
         assert torch.equal(s1 >= 0, s2 >= 0), f"repaired blocks, step {k}"
     assert (runs[-1][3] >= 0).any()
