@@ -573,15 +573,21 @@ __global__ void __launch_bounds__(128) write_token_kernel(const WriteArgs a) {
 // of the block are staged in natural order (a conflict-free word per lane and token) and then
 // packed into their fragment-order words, lane by lane: the word of channel c and lane slot t
 // holds tokens 2t, 2t + 1, 2t + 8, 2t + 9.
+// Four warps a CTA.  The INT8 and FP8 writers are held to 64 registers a thread, so that the
+// shared-memory images, not the registers, bound an SM at seven CTAs (28 warps; 24 at 80
+// registers): INT8 bulk writes 0.198 -> 0.214 of HBM at 32k.  Six-warp CTAs (30 warps, the most
+// that 48 KB of static shared memory per CTA allows) measured a little slower, and the
+// black-box writer is faster at six CTAs of up to 85 registers than at eight of 64.
+constexpr int kBlockWriterWarps = 4;
 template <typename T, int SCH, bool VW>
-__global__ void __launch_bounds__(128, 6) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
+__global__ void __launch_bounds__(kBlockWriterWarps * 32, SCH == kBbox ? 6 : 8) write_block_kernel(const WriteArgs a, int blk0, int nblocks) {
   const ChainEntry chain(a.late_wait != 0);
   constexpr int kBytes = block_bytes(SCH);
   constexpr bool kStaged = SCH != kBbox;
-  __shared__ __align__(16) uint8_t img[4][kBytes];
-  __shared__ uint32_t vstage[4][kStaged ? kBlk * 32 : 1];
+  __shared__ __align__(16) uint8_t img[kBlockWriterWarps][kBytes];
+  __shared__ uint32_t vstage[kBlockWriterWarps][kStaged ? kBlk * 32 : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long unit = (long long)blockIdx.x * 4 + warp;       // (i * Hkv + h) * nblocks + b
+  const long long unit = (long long)blockIdx.x * kBlockWriterWarps + warp;   // (i * Hkv + h) * nblocks + b
   if (unit >= (long long)a.B * a.Hkv * nblocks) return;
   const int b = (int)(unit % nblocks), sh = (int)(unit / nblocks);
   const int i = sh / a.Hkv, h = sh % a.Hkv, blk = blk0 + b;
@@ -855,15 +861,16 @@ cudaError_t launch_t(int scheme, const WriteArgs& a, cudaStream_t st, bool pdl) 
     cudaError_t e = tokens(0, lo_full - a.t0);
     if (e != cudaSuccess) return e;
     const int nblocks = (hi_full - lo_full) / kBlk;
-    const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + 3) / 4));
+    const dim3 g((unsigned)(((long long)a.B * a.Hkv * nblocks + kBlockWriterWarps - 1) / kBlockWriterWarps));
+    const dim3 wb(kBlockWriterWarps * 32);
     const int b0 = lo_full / kBlk;
     const bool vw = a.vwit != nullptr;
-    e = scheme == kInt8  ? (vw ? launch_pdl(write_block_kernel<T, kInt8, true>, g, dim3(128), st, pdl, a, b0, nblocks)
-                               : launch_pdl(write_block_kernel<T, kInt8, false>, g, dim3(128), st, pdl, a, b0, nblocks))
-        : scheme == kRtn ? (vw ? launch_pdl(write_block_kernel<T, kRtn, true>, g, dim3(128), st, pdl, a, b0, nblocks)
-                               : launch_pdl(write_block_kernel<T, kRtn, false>, g, dim3(128), st, pdl, a, b0, nblocks))
-        : scheme == kFp8 ? launch_pdl(write_block_kernel<T, kFp8, false>, g, dim3(128), st, pdl, a, b0, nblocks)
-                         : launch_pdl(write_block_kernel<T, kBbox, false>, g, dim3(128), st, pdl, a, b0, nblocks);
+    e = scheme == kInt8  ? (vw ? launch_pdl(write_block_kernel<T, kInt8, true>, g, wb, st, pdl, a, b0, nblocks)
+                               : launch_pdl(write_block_kernel<T, kInt8, false>, g, wb, st, pdl, a, b0, nblocks))
+        : scheme == kRtn ? (vw ? launch_pdl(write_block_kernel<T, kRtn, true>, g, wb, st, pdl, a, b0, nblocks)
+                               : launch_pdl(write_block_kernel<T, kRtn, false>, g, wb, st, pdl, a, b0, nblocks))
+        : scheme == kFp8 ? launch_pdl(write_block_kernel<T, kFp8, false>, g, wb, st, pdl, a, b0, nblocks)
+                         : launch_pdl(write_block_kernel<T, kBbox, false>, g, wb, st, pdl, a, b0, nblocks);
     if (e != cudaSuccess) return e;
     return tokens(hi_full - a.t0, t_end - hi_full);
   }
