@@ -59,3 +59,12 @@ def test_timed_launch_count_follows_the_write_path(bench):
     # step 12, which takes one push
     assert t("int8_dither", 1, [4096], 20, False, True) == 3 * 20 + 2
     assert t("int8_dither", 1, [4100, 4100], 20, True, True) == 4 * 20 + 1
+
+
+def test_l2_note_says_when_a_cache_can_stay_in_l2(bench):
+    """Below twice L2 the bench line says the steps may hit L2; above it that they read HBM."""
+    assert bench.l2_note(40e6).startswith("cache of 0.040 GB within twice L2")
+    assert bench.l2_note(2 * bench.L2_BYTES + 1).startswith("inputs larger than L2")
+    from workload import sweep_workload
+    w = sweep_workload("mistral", 16, 32768)
+    assert w.batch * w.n_kv_heads * w.context * 304 * 32 > 2 * bench.L2_BYTES     # the default line
