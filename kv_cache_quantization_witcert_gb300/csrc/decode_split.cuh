@@ -68,15 +68,15 @@ template <> struct Lay<kFp8> : Fp8Layout {};
 template <> struct Lay<kKivi> : KiviLayout {};
 template <> struct Lay<kBbox> : BboxLayout {};
 
-template <int NW> struct Stages { static constexpr int value = NW >= 8 ? 2 : NW == 4 ? 3 : 4; };
-template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : 2; };
+template <int NW> struct Stages { static constexpr int value = NW >= 4 ? 2 : 4; };
+template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : NW == 4 ? 3 : 2; };
 
 // Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
 // warps consume, so warps may drift up to two blocks apart (one with three slots, which is
 // what two 8-warp CTAs per SM leave room for).  CTAs of one or two warps keep two slots and
 // regenerate one block ahead: their warps hardly drift, and the smaller footprint fits five
 // (three) CTAs on an SM instead of three (two).
-template <int NW> struct XiSlots { static constexpr int value = NW <= 2 ? 2 : NW == 8 ? 3 : 4; };
+template <int NW> struct XiSlots { static constexpr int value = NW <= 4 ? 2 : NW == 8 ? 3 : 4; };
 
 // A ring stage holds one block and, behind it, the block's value witnesses.
 template <int NW, int SCHEME> struct Smem {
