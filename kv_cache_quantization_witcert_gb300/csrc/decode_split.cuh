@@ -68,7 +68,7 @@ template <> struct Lay<kFp8> : Fp8Layout {};
 template <> struct Lay<kKivi> : KiviLayout {};
 template <> struct Lay<kBbox> : BboxLayout {};
 
-template <int NW> struct Stages { static constexpr int value = NW >= 4 ? 2 : 4; };
+template <int NW> struct Stages { static constexpr int value = 2; };
 template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : NW == 4 ? 3 : 2; };
 
 // Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
