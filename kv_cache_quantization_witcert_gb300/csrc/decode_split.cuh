@@ -68,14 +68,17 @@ template <> struct Lay<kFp8> : Fp8Layout {};
 template <> struct Lay<kKivi> : KiviLayout {};
 template <> struct Lay<kBbox> : BboxLayout {};
 
+// Ring stages per warp, and resident CTAs per SM the compiler plans registers for (four-warp
+// CTAs: three, at most 170 registers a thread).
 template <int NW> struct Stages { static constexpr int value = 2; };
 template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : NW == 4 ? 3 : 2; };
 
 // Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
 // warps consume, so warps may drift up to two blocks apart (one with three slots, which is
-// what two 8-warp CTAs per SM leave room for).  CTAs of one or two warps keep two slots and
-// regenerate one block ahead: their warps hardly drift, and the smaller footprint fits five
-// (three) CTAs on an SM instead of three (two).
+// what two 8-warp CTAs per SM leave room for).  CTAs of up to four warps keep two slots and
+// regenerate one block ahead (a warp then waits for every warp to finish the block before the
+// one it fills, so they drift at most one block apart): the smaller footprint fits more CTAs
+// on an SM.
 template <int NW> struct XiSlots { static constexpr int value = NW <= 4 ? 2 : NW == 8 ? 3 : 4; };
 
 // A ring stage holds one block and, behind it, the block's value witnesses.
