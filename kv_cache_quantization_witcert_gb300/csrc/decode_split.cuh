@@ -69,9 +69,9 @@ template <> struct Lay<kKivi> : KiviLayout {};
 template <> struct Lay<kBbox> : BboxLayout {};
 
 // Ring stages per warp, and resident CTAs per SM the compiler plans registers for (four-warp
-// CTAs: three, at most 170 registers a thread).
+// CTAs: three, at most 170 registers a thread; single-warp CTAs: twelve, at most 168).
 template <int NW> struct Stages { static constexpr int value = 2; };
-template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : NW == 4 ? 3 : 2; };
+template <int NW> struct MinBlocks { static constexpr int value = NW >= 16 ? 1 : NW == 4 ? 3 : NW == 1 ? 12 : 2; };
 
 // Dither slots: the CTA regenerates the dither XD = NXI - 2 blocks ahead of the block its
 // warps consume, so warps may drift up to two blocks apart (one with three slots, which is
